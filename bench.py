@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE-layer forward on B300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one whole layer forward (route, dispatch, expert up/down GEMMs,
+combine, aux loss) over one batch of seeded synthetic tokens already resident
+in HBM.  Default workload: bf16, T=4096 tokens, d=4096, 8 experts, top-2,
+SwiGLU d_ff=14336, capacity factor 1.25.
+
+Timing: W untimed warm-up steps; then K steps, each preceded (outside the
+timed events) by a 512 MB write that flushes the 126 MB L2; CUDA events on
+the launching stream around every step and around every call inside it;
+barrier + synchronize on both sides; max over ranks.  SM clocks and
+clock-event reasons are sampled through NVML during the timed steps.
+
+``e2e``: the same metric through the public API with host buffers: each step
+copies x from pinned host memory, runs the layer and reads y and the loss
+back, all inside the timed region.
+
+``roofline``: the dominant kernel (the expert up-projection GEMM) -- its
+algorithmic FLOPs (2 * kept slots * d * N1) over its CUDA-event duration,
+against the measured dense bf16 peak.
+
+``cpu_baseline`` (rank 0, N=1): the CPU oracle timed on a bounded sample of
+the same workload (its first S tokens, capacity recomputed for S tokens).
+
+``--impl reference``: the CPU oracle alone on the host cores (the method has
+no other runnable implementation); rank 0 only.
+
+With torchrun (N>1) every rank runs its own independent batch (seed + rank):
+the layer forward needs no exchange between GPUs, so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from top_routing_expert_02_b300 import synth  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s and grouped-GEMM TFLOP/s (% BF16 peak) on 1 B300"
+L2_FLUSH_BYTES = 512 << 20
+KERNELS_PER_STEP = {"route": 2, "dispatch": 3, "expert_up": 1, "expert_down": 1, "combine": 1, "aux_loss": 1}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j["bf16_tflops_sustained"]), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """NVML samples of SM clock and clock-event reasons (read only)."""
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.samples, self.reasons, self.max_mhz, self.ok = [], set(), None, False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            phys = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(phys)
+            self._nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:   # no NVML: report what is known
+            self.ok = False
+        self._period = period_s
+        self._t = None
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                    nv.nvmlDeviceGetCurrentClocksThrottleReasons
+                bits = fn(self._h)
+                for b, name in self.BITS.items():
+                    if bits & b:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self._period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        reasons = sorted(self.reasons - {"gpu_idle"})
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------- CPU oracle --
+def oracle_sample(cfg: synth.MoEConfig, ri, w1, w2, budget_s: float = 15.0):
+    """Time the CPU oracle on the first S tokens (S grown until ~budget_s)."""
+    import oracle
+    w1h, w2h = w1.cpu(), w2.cpu()
+
+    def run(S):
+        sub = ri.x[:S].contiguous()
+        cap = oracle.capacity(S, cfg.E, cfg.cf)
+        t0 = time.perf_counter()
+        oracle.forward(sub, ri.W, ri.b, w1h, w2h, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
+                       alpha=cfg.alpha)
+        return time.perf_counter() - t0
+
+    S = min(cfg.T, 8)
+    t = run(S)
+    if t < budget_s / 4 and S < cfg.T:
+        S = int(min(cfg.T, max(S + 1, S * (budget_s / max(t, 1e-3)))))
+        t = run(S)
+    return {"value": S / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {S} of {cfg.T} tokens of the workload, whole layer (routing, capacity for {S} "
+                      f"tokens, expert FFN, combine, aux loss) in fp64, {t:.1f} s"}, S, t
+
+
+def reference_arm(args, cfg):
+    """--impl reference: the oracle on the host cores, rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    ri = synth.make_routing_inputs(cfg)
+    w1, w2 = synth.make_expert_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    cb, S, t = oracle_sample(cfg, ri, w1, w2, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    # warm-up and timed steps: each step is the bounded sample
+    import oracle
+    w1h, w2h = w1.cpu(), w2.cpu()
+    sub = ri.x[:S].contiguous()
+    cap = oracle.capacity(S, cfg.E, cfg.cf)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(sub, ri.W, ri.b, w1h, w2h, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
+                       alpha=cfg.alpha)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1000.0 * statistics.mean(times)
+    value = S / (ms / 1000.0)
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(cfg), "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg):
+    return {"workload": cfg.name, "description": cfg.describe(), "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
+            "F": cfg.F, "act": cfg.act, "cf": cfg.cf, "renorm": cfg.renorm, "alpha": cfg.alpha,
+            "l2": "flushed before every timed step (512 MB write); weights exceed L2"}
+
+
+def traffic_from_profile(kernel_src: str):
+    """DRAM bytes per launch of the up-projection GEMM from the committed ncu
+    summary, only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "expert_up_gemm_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(kernel_src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    vals = {}
+    for line in open(p):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------------- ours --
+def our_arm(args, cfg):
+    import top_routing_expert_02_b300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    moe.lib()
+
+    rcfg = cfg.replace(seed=cfg.seed + rank)
+    ri = synth.make_routing_inputs(rcfg)
+    w1, w2 = synth.make_expert_weights(cfg, device=dev)
+    x = ri.x.to(dev)
+    W = ri.W.to(dev)
+    b = None if ri.b is None else ri.b.to(dev)
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    cap = moe.capacity(cfg.T, cfg.E, cfg.cf)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    D = plan.disp
+
+    def step(evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record(stream)
+        mark(0)
+        moe.route(x, W, b, plan.k, plan.renorm, topk_idx=plan.topk_idx, topk_gate=plan.topk_gate,
+                  prob_sum=plan.prob_sum, ws=plan.ws_route)
+        mark(1)
+        moe.dispatch(plan.topk_idx, plan.topk_gate, x, plan.E, plan.cap, out=D, ws=plan.ws_dispatch)
+        mark(2)
+        moe.expert_up(D.x_perm, D.offsets, D.kept, w1, plan.F, plan.act, plan.rows_max, h=plan.h)
+        mark(3)
+        moe.expert_down(plan.h, D.offsets, D.kept, w2, D.row_gate, plan.rows_max, y_perm=plan.y_perm)
+        mark(4)
+        moe.combine(plan.y_perm, D.slot_row, y=plan.y)
+        moe.aux_loss(D.counts, plan.prob_sum, plan.T, plan.alpha, loss=plan.loss)
+        mark(5)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    moe.check()
+    A = int(D.offsets[plan.E].item())
+    n_drop = int(D.n_dropped.item())
+    counts = D.counts.cpu()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier()
+    with sampler:
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        barrier()
+    moe.check()
+    part = {n: [] for n in ("route", "dispatch", "expert_up", "expert_down", "combine_aux", "step")}
+    for e in evs:
+        part["route"].append(e[0].elapsed_time(e[1]))
+        part["dispatch"].append(e[1].elapsed_time(e[2]))
+        part["expert_up"].append(e[2].elapsed_time(e[3]))
+        part["expert_down"].append(e[3].elapsed_time(e[4]))
+        part["combine_aux"].append(e[4].elapsed_time(e[5]))
+        part["step"].append(e[0].elapsed_time(e[5]))
+    ms_step = sum(part["step"]) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * cfg.T / (ms_step / 1000.0)
+
+    # end to end through the public API: pinned host x in, y + loss out
+    x_host = ri.x.pin_memory()
+    y_host = torch.empty((cfg.T, cfg.d), dtype=tdt).pin_memory()
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        if i >= args.warmup:
+            e_start[i - args.warmup].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        plan.run(x_dev, W, b, w1, w2)
+        y_host.copy_(plan.y, non_blocking=True)
+        loss_host.copy_(plan.loss, non_blocking=True)
+        if i >= args.warmup:
+            e_end[i - args.warmup].record(stream)
+    torch.cuda.synchronize(dev)
+    moe.check()
+    ms_e2e = sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    esz = 2 if tdt == torch.bfloat16 else 4
+
+    hbm, bf16_peak, bf16_sust, peak_src = peaks()
+    N1 = cfg.N1
+    up_flops = 2.0 * A * cfg.d * N1
+    down_flops = 2.0 * A * cfg.F * cfg.d
+    up_ms = statistics.mean(part["expert_up"])
+    down_ms = statistics.mean(part["expert_down"])
+    achieved = up_flops / (up_ms * 1e-3) / 1e12
+    gemm_tflops = (up_flops + down_flops) / ((up_ms + down_ms) * 1e-3) / 1e12
+    traffic = traffic_from_profile(os.path.join(ROOT, "top_routing_expert_02_b300", "csrc", "ffn_tc.cuh"))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded; weights random-init)",
+        "config": config_dict(cfg),
+        "clocks": sampler.summary(),
+        "e2e": {"value": world * cfg.T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": cfg.T * cfg.d * esz, "d2h_bytes_per_step": cfg.T * cfg.d * esz + 4},
+        "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
+        "roofline": {"kernel": "expert_up (tcgen05 grouped GEMM + activation)", "bound": "tensor",
+                     "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                     "peak_source": f"{peak_src} bf16 dense burst", "traffic": traffic,
+                     "algorithmic_flops_per_launch": up_flops},
+        "gemm_tflops": gemm_tflops, "gemm_frac_of_peak": gemm_tflops / bf16_peak,
+        "kernel_ms": {k: statistics.mean(v) for k, v in part.items()},
+        "routing": {"kept_slots": A, "dropped_slots": n_drop, "max_over_mean_load":
+                    float(counts.max()) / (cfg.T * cfg.k / cfg.E)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb, _, _ = oracle_sample(cfg, ri, w1, w2)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="e8_swiglu", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
+    args.steps = max(args.steps, 1)
+    cfg = synth.workload(args.workload)
+    if args.impl == "reference":
+        reference_arm(args, cfg)
+    else:
+        our_arm(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

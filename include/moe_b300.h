@@ -1,0 +1,220 @@
+/*
+ * moe_b300.h -- C ABI of the single-GPU MoE-layer forward for B300 (sm_103a).
+ *
+ * The forward pass is cut into the five steps that the expert-parallelism
+ * tutorial "专家并行：混合专家模型的分布式训练方案" states in §2.1 (gate
+ * decision, dispatch plan, token exchange, local expert compute, token
+ * return), with the capacity rule of its §2.2 and the auxiliary loss of its
+ * §5.1; the fine-grained EP deployment guide "细粒度专家并行部署实践与优化指南"
+ * gives the same steps as pseudo-code in §七 (top-k of the gate
+ * probabilities, dispatch, per-expert compute, gather back).  On one GPU the
+ * two All-to-All exchanges become a row permutation and un-permutation in HBM.
+ *
+ *   moe_route      router linear layer, softmax over E, top-k     (§1.1, §2.1 step 1)
+ *   moe_dispatch   capacity, slot ranks, drops, row permutation   (§2.1 steps 2-3, §2.2)
+ *   moe_expert_ffn per-expert w1 -> activation -> w2, gate scale  (§2.1 step 4)
+ *   moe_combine    gate-weighted sum back into token order        (§2.1 step 5)
+ *   moe_aux_loss   L_aux = alpha * E * sum_i f_i * P_i            (§5.1)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership   The caller allocates and owns every buffer (inputs, outputs,
+ *             intermediates and workspaces).  The library never allocates
+ *             device or host memory and never synchronises the stream on the
+ *             compute calls.
+ * Pointers    Every array argument is a DEVICE pointer, row-major, 16-byte
+ *             aligned (torch allocations are).  Sizes are element counts.
+ * Streams     Work is enqueued on `stream` and runs asynchronously.
+ * Errors      Bad arguments and launch failures come back synchronously as a
+ *             moe_status; nothing is enqueued when a call returns an error.
+ *             Problems found on the device (an expert id out of range, a
+ *             pipeline wait that ran past its time limit) set a sticky device
+ *             status word that moe_check() reads and clears.  No kernel traps.
+ * Indices     int32: T*k < 2^31, E <= 256, 1 <= k <= min(E, 16).
+ * Shapes      d % 64 == 0 and F % 64 == 0 (16-byte rows for the vector
+ *             moves, 64-element K blocks for the tensor-core GEMMs).
+ * Dtypes      x, w1, w2, h, y_perm and y share one dtype (MOE_F32 or
+ *             MOE_BF16); the router weight, bias, gates and prob sums are
+ *             fp32.  bf16 data is accumulated in fp32 and rounded once per
+ *             stored tensor; the fp32 path uses no TF32 and no bf16.
+ * Residual    Adding the layer input back (the residual path that dropped
+ *             tokens take, §2.2) is the caller's job: a dropped slot
+ *             contributes zero to y.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA
+ * headers.  NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, size out of range, bad enum */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented (shape rule, dtype) */
+    MOE_ERR_WORKSPACE = 3,     /* ws NULL or ws_bytes below moe_workspace_bytes() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+    MOE_ERR_TIMEOUT = 5        /* (moe_check) a device-side wait hit its limit */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+    MOE_ACT_GELU = 0,      /* exact erf GELU: z * (1 + erf(z / sqrt 2)) / 2        */
+    MOE_ACT_SWIGLU = 1,    /* silu(z[0:F]) * z[F:2F]; w1[e] rows 0..F-1 gate, F..2F-1 up */
+    MOE_ACT_IDENTITY = 2   /* h = z; for checks (identity experts)                 */
+} moe_act;
+
+typedef enum { MOE_CALL_ROUTE = 0, MOE_CALL_DISPATCH = 1, MOE_CALL_FFN = 2 } moe_call;
+
+/* ---------------------------------------------------------------- host --- */
+
+/* Expert capacity of the tutorial's §2.2: round((T / E) * cf), rounded half
+ * away from zero in double precision, no minimum.  cf <= 0 selects dropless
+ * routing and returns T.  Returns -1 when T < 0 or E < 1. */
+int64_t moe_capacity(int64_t T, int E, double cf);
+
+/* Rows of the permuted buffers (x_perm, h, y_perm, row_token, row_gate):
+ * the largest possible number of kept slots, min(T * k, E * cap).
+ * Returns -1 on invalid arguments. */
+int64_t moe_perm_rows_max(int64_t T, int k, int E, int64_t cap);
+
+/* Bytes of device workspace the given call needs at these sizes (0 = none;
+ * pass ws = NULL then).  Returns 0 for an unknown call. */
+size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F,
+                           moe_act act, moe_dtype dtype);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status s);
+
+/* ABI revision of this header (bumped on any incompatible change). */
+int moe_abi_version(void);
+#define MOE_ABI_VERSION 1
+
+/* ------------------------------------------------------------- compute --- */
+
+/* Router: tutorial §1.1 (a lightweight linear layer scores every expert),
+ * §2.1 step 1 (each token picks its Top-K experts); guide §七 takes top-k of
+ * the softmaxed gate probabilities.
+ *   x          [T, d]  xdt (F32 or BF16)
+ *   w_router   [E, d]  fp32;  b_router [E] fp32 or NULL
+ *   logits l[t,e] = sum_c x[t,c] w_router[e,c] + b[e]  (fp32 accumulation)
+ *   p[t,:]     = softmax over all E experts
+ * Outputs (all written, caller-owned):
+ *   topk_idx   [T, k]  int32: experts ordered by (logit desc, index asc);
+ *                      ties go to the lower expert index; j is the k-rank
+ *   topk_gate  [T, k]  fp32: p[t, idx]; divided by sum_j p[t, idx[t,j]] when
+ *                      renorm != 0
+ *   prob_sum   [E]     fp32: sum_t p[t,e], reduced in a fixed order
+ *                      (bitwise reproducible run to run)
+ *   ws         >= moe_workspace_bytes(MOE_CALL_ROUTE, T, d, E, k, ...) bytes
+ * T == 0 is allowed (prob_sum becomes zeros). */
+moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const float* b_router,
+                     int64_t T, int d, int E, int k, int renorm,
+                     int32_t* topk_idx, float* topk_gate, float* prob_sum,
+                     void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch: tutorial §2.1 steps 2-3 (dispatch plan, token exchange) and
+ * §2.2 (capacity, overflow tokens dropped).  Assignments (t, j) are granted
+ * expert slots in k-rank-then-token order -- every first choice in token
+ * order, then every second choice, ... -- and an assignment whose place in
+ * its expert's queue is >= cap is dropped.  The exchange becomes a gather of
+ * x rows into expert-contiguous segments.
+ *   topk_idx [T,k] int32, topk_gate [T,k] fp32 (from moe_route)
+ *   x        [T, d] xdt
+ * Outputs:
+ *   counts   [E]    assignments per expert before drops
+ *   kept     [E]    min(counts, cap)
+ *   offsets  [E+1]  exclusive prefix sum of kept; offsets[E] = kept slots A
+ *   slot_row [T,k]  row of x_perm holding (t, j), or -1 when dropped;
+ *                   slot_row - offsets[e] is the place in expert e's queue
+ *   row_token[rows_max], row_gate[rows_max], x_perm[rows_max, d]: rows
+ *                   0..A-1 filled (token id, gate, copy of x[token]); rows
+ *                   A..rows_max-1 are left untouched
+ *   n_dropped[1]    sum_e max(0, counts[e] - cap)
+ *   rows_max = moe_perm_rows_max(T, k, E, cap); cap >= 0.
+ * An expert id outside [0, E) in topk_idx sets the device status (the
+ * assignment is ignored). */
+moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t T, int k, int E,
+                        int64_t cap, const void* x, moe_dtype xdt, int d,
+                        int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
+                        int32_t* row_token, float* row_gate, void* x_perm, int32_t* n_dropped,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Expert up-projection: tutorial §2.1 step 4 (each expert is an FFN run on
+ * the tokens it received); the expert shape d -> d_ff -> d with w1
+ * column-split and w2 row-split is the one the ETP page
+ * "ETP专家并行加速MoE模型：ms-swift中稀疏架构的极致优化" describes.
+ * For every expert e and row r in [offsets[e], offsets[e] + kept[e]):
+ *   z = w1[e] . x_perm[r]        (w1 [E, N1, d], nn.Linear layout; N1 = 2F for
+ *                                 SwiGLU, F otherwise)
+ *   h[r, :F] = act(z)            fp32 accumulate, one rounding to dtype
+ * BF16 runs on the tcgen05 tensor cores (TMA-fed, TMEM accumulators); F32 on
+ * CUDA cores in true fp32.  rows_max is the row count of x_perm and h.
+ * Rows outside the kept segments are not written. */
+moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32_t* kept,
+                         int E, int d, int F, moe_act act, moe_dtype dtype, const void* w1,
+                         int64_t rows_max, void* h, moe_stream_t stream);
+
+/* Expert down-projection with the gate scale of the combine folded in:
+ *   y_perm[r, :] = row_gate[r] * (w2[e] . h[r, :F])     (w2 [E, d, F])
+ * fp32 accumulate and gate product, one rounding to dtype.  Same segment
+ * rules as moe_expert_up. */
+moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t* kept,
+                           int E, int d, int F, moe_dtype dtype, const void* w2,
+                           const float* row_gate, int64_t rows_max, void* y_perm,
+                           moe_stream_t stream);
+
+/* moe_expert_up followed by moe_expert_down on the same stream.
+ * ws may be NULL (moe_workspace_bytes(MOE_CALL_FFN, ...) is 0). */
+moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const int32_t* kept,
+                          int E, int d, int F, moe_act act, moe_dtype dtype,
+                          const void* w1, const void* w2, const float* row_gate,
+                          int64_t rows_max, void* h, void* y_perm,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine: tutorial §2.1 step 5 (outputs return to their original token
+ * positions) with the guide's §七 gather-back.  The gate weights are already
+ * inside y_perm, so
+ *   y[t] = sum_{j : slot_row[t,j] >= 0} y_perm[slot_row[t,j]]
+ * summed in j order in fp32 and rounded once; a token with every slot
+ * dropped gets a zero row.  y [T, d] has dtype `dtype`. */
+moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d,
+                       moe_dtype dtype, void* y, moe_stream_t stream);
+
+/* Auxiliary load-balance loss, tutorial §5.1:
+ *   L = alpha * E * sum_e f_e * P_e,  f_e = counts[e] / T,  P_e = prob_sum[e] / T
+ * (f counts every choice before capacity drops).  Computed in fp64 on the
+ * device, stored as fp32 to loss[0] (device pointer).  T must be >= 1. */
+moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T, int E,
+                        float alpha, float* loss, moe_stream_t stream);
+
+/* ---------------------------------------------------------- diagnostics --- */
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device: MOE_OK, MOE_ERR_TIMEOUT (a pipeline wait ran past its
+ * limit), MOE_ERR_INVALID_ARG (an out-of-range expert id reached dispatch),
+ * or MOE_ERR_CUDA (the stream reported an error). */
+moe_status moe_check(moe_stream_t stream);
+
+/* Time limit of every device-side wait, in SM clock cycles (default 4e9,
+ * about two seconds).  A wait that runs past it records MOE_ERR_TIMEOUT and
+ * its kernel winds down cleanly.  0 restores the default. */
+void moe_set_wait_limit(uint64_t cycles);
+
+/* Launches one block that waits, under the current limit, on a barrier that
+ * nothing ever completes, so that a test can watch the time-limit path end
+ * in MOE_ERR_TIMEOUT from moe_check() with the context still usable. */
+moe_status moe_selftest_wait_timeout(moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

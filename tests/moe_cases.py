@@ -1,0 +1,100 @@
+"""Shared helpers of the GPU parity tests: build a seeded case, run the CUDA
+path through the C ABI, run the oracle, compare.
+
+Bars (written here once, used by every parity test):
+  routing indices, counts, kept, offsets, slot places, drops: bit-exact
+  gates, prob sums, aux loss:         relative error <= 1e-5
+  layer output y:                     relative Frobenius error <= 1e-5 (fp32 layer),
+                                      <= 2e-2 (bf16 layer)
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import top_routing_expert_02_b300 as moe
+from top_routing_expert_02_b300 import synth
+
+GATE_RTOL = 1e-5
+Y_TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def make_case(cfg: synth.MoEConfig, device="cuda", condition=True, routing=None):
+    """Inputs of one workload: host copies for the oracle, device copies for the kernels."""
+    ri = routing if routing is not None else synth.make_routing_inputs(cfg)
+    if condition:
+        ri = synth.condition_near_ties(cfg, ri, oracle.router_logits)
+    w1, w2 = synth.make_expert_weights(cfg, device=device)
+    cap = moe.capacity(cfg.T, cfg.E, cfg.cf)
+    return dict(cfg=cfg, cap=cap, x_h=ri.x, W_h=ri.W, b_h=ri.b, x=ri.x.to(device), W=ri.W.to(device),
+                b=None if ri.b is None else ri.b.to(device), w1=w1, w2=w2)
+
+
+def run_gpu(case, plan=None):
+    cfg = case["cfg"]
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    if plan is None:
+        plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, case["cap"], case["x"].device,
+                           cfg.alpha, cfg.renorm)
+    plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+    moe.check()
+    return plan
+
+
+def run_oracle(case, tokens=None, w_host=None):
+    cfg = case["cfg"]
+    if w_host is None:
+        w_host = (case["w1"].cpu(), case["w2"].cpu())
+    return oracle.forward(case["x_h"], case["W_h"], case["b_h"], w_host[0], w_host[1], k=cfg.k, cap=case["cap"],
+                          act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha, tokens=tokens)
+
+
+def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+def compare_routing(plan, ref):
+    idx = plan.topk_idx.cpu().numpy()
+    assert np.array_equal(idx, ref["idx"]), "top-k indices differ"
+    g = plan.topk_gate.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(g, ref["gate"], rtol=GATE_RTOL, atol=0)
+    np.testing.assert_allclose(plan.prob_sum.cpu().numpy().astype(np.float64), ref["prob_sum"], rtol=GATE_RTOL,
+                               atol=1e-30)
+
+
+def compare_dispatch(plan, ref, x_h=None, check_rows=256):
+    D = plan.disp
+    counts, kept = D.counts.cpu().numpy(), D.kept.cpu().numpy()
+    offsets, slot = D.offsets.cpu().numpy(), D.slot_row.cpu().numpy()
+    assert np.array_equal(counts, ref["counts"])
+    assert np.array_equal(kept, ref["kept"])
+    assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(ref["kept"])]))
+    assert int(D.n_dropped.item()) == ref["n_dropped"]
+    idx = ref["idx"]
+    pos = np.where(slot >= 0, slot - offsets[idx], -1)
+    assert np.array_equal(pos, ref["pos"]), "slot places differ"
+    A = int(offsets[-1])
+    if A:
+        row_token = D.row_token[:A].cpu().numpy()
+        row_gate = D.row_gate[:A].cpu().numpy()
+        t, j = np.nonzero(slot >= 0)
+        rows = slot[t, j]
+        assert np.array_equal(np.sort(rows), np.arange(A))        # bijection onto 0..A-1
+        assert np.array_equal(row_token[rows], t)
+        assert np.array_equal(row_gate[rows], plan.topk_gate.cpu().numpy()[t, j])
+        if x_h is not None:
+            sel = np.linspace(0, A - 1, num=min(A, check_rows)).astype(np.int64)
+            xp = D.x_perm[torch.from_numpy(sel).to(D.x_perm.device)].cpu()
+            assert torch.equal(xp, x_h[torch.from_numpy(row_token[sel]).long()])
+
+
+def compare_output(plan, ref, dtype: str):
+    toks = torch.from_numpy(ref["tokens"]).long().to(plan.y.device)
+    y = plan.y[toks].float().cpu().numpy().astype(np.float64)
+    err = rel_fro(y, ref["y"])
+    assert err <= Y_TOL[dtype], f"relative Frobenius error {err:.3e} > {Y_TOL[dtype]}"
+    loss = float(plan.loss.item())
+    assert abs(loss - ref["loss"]) <= GATE_RTOL * abs(ref["loss"]) + 1e-12, (loss, ref["loss"])
+    return err

@@ -1,0 +1,116 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/moe_b300.h declares, its host-side functions are right, and
+argument errors come back synchronously before any CUDA work is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import top_routing_expert_02_b300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_b300.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "capacity.txt")
+
+FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: every call below fails validation first
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_aux_loss"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function():
+    L = moe.lib()
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    assert L.moe_abi_version() == 1
+
+
+def _golden_caps():
+    rows = []
+    for line in open(GOLDEN):
+        if line.strip() and not line.startswith("#"):
+            T, E, cf, cap = line.split()
+            rows.append((int(T), int(E), float(cf), int(cap)))
+    return rows
+
+
+@pytest.mark.parametrize("T,E,cf,cap", _golden_caps())
+def test_capacity_matches_golden_table(T, E, cf, cap):
+    assert moe.capacity(T, E, cf) == cap
+
+
+def test_perm_rows_and_workspace():
+    assert moe.perm_rows_max(4096, 2, 8, 640) == 5120
+    assert moe.perm_rows_max(512, 8, 128, 512) == 4096
+    assert moe.perm_rows_max(0, 2, 8, 10) == 0
+    assert moe.perm_rows_max(10, 2, 8, -1) == -1
+    assert moe.workspace_bytes("ffn", 4096, 4096, 8, 2, 14336) == 0
+    assert moe.workspace_bytes("route", 4096, 4096, 8, 2, 14336) > 0
+    assert moe.workspace_bytes("dispatch", 4096, 4096, 8, 2, 14336) >= 8 * 4 * 8
+    assert moe.workspace_bytes("route", 0, 4096, 8, 2, 14336) == 0
+
+
+def test_status_strings():
+    L = moe.lib()
+    for code in range(6):
+        assert L.moe_status_string(code)
+    assert L.moe_status_string(5) == b"device wait timed out"
+
+
+def _route(L, **over):
+    a = dict(x=FAKE, xdt=1, w=FAKE, b=None, T=16, d=128, E=8, k=2, renorm=1, idx=FAKE, gate=FAKE, ps=FAKE,
+             ws=FAKE, ws_bytes=1 << 20)
+    a.update(over)
+    return L.moe_route(a["x"], a["xdt"], a["w"], a["b"], a["T"], a["d"], a["E"], a["k"], a["renorm"], a["idx"],
+                       a["gate"], a["ps"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(E=0), 1), (dict(E=257), 1), (dict(k=0), 1), (dict(k=9, E=8), 1), (dict(k=17, E=64), 1),
+    (dict(T=-1), 1), (dict(xdt=7), 1), (dict(x=None), 1), (dict(ps=None), 1),
+    (dict(d=100), 2), (dict(ws=None), 3), (dict(ws_bytes=4), 3),
+])
+def test_route_argument_errors(over, code):
+    assert _route(moe.lib(), **over) == code
+
+
+def test_dispatch_ffn_combine_aux_argument_errors():
+    L = moe.lib()
+    F_ = FAKE
+    # dispatch: negative capacity, null outputs, bad d, small workspace
+    args = [F_, F_, 16, 2, 8, 4, F_, 1, 128, F_, F_, F_, F_, F_, F_, F_, F_, F_, 1 << 20, None]
+    bad = list(args); bad[5] = -1
+    assert L.moe_dispatch(*bad) == 1
+    bad = list(args); bad[9] = None
+    assert L.moe_dispatch(*bad) == 1
+    bad = list(args); bad[8] = 96
+    assert L.moe_dispatch(*bad) == 2
+    bad = list(args); bad[18] = 8
+    assert L.moe_dispatch(*bad) == 3
+    # ffn: F not a multiple of 64, bad act, null weights
+    assert L.moe_expert_up(F_, F_, F_, 8, 128, 96, 0, 1, F_, 10, F_, None) == 2
+    assert L.moe_expert_up(F_, F_, F_, 8, 128, 128, 9, 1, F_, 10, F_, None) == 1
+    assert L.moe_expert_down(F_, F_, F_, 8, 128, 128, 1, None, F_, 10, F_, None) == 1
+    assert L.moe_expert_ffn(F_, None, F_, 8, 128, 128, 0, 1, F_, F_, F_, 10, F_, F_, None, 0, None) == 1
+    # combine / aux
+    assert L.moe_combine(F_, F_, 16, 0, 128, 1, F_, None) == 1
+    assert L.moe_combine(F_, F_, 16, 2, 120, 1, F_, None) == 2
+    assert L.moe_aux_loss(F_, F_, 0, 8, ctypes.c_float(0.01), F_, None) == 1
+    assert L.moe_aux_loss(F_, F_, 16, 8, ctypes.c_float(0.01), None, None) == 1
+
+
+def test_binding_rejects_unsupported_dtype():
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        moe.route(x, torch.zeros(8, 64), None, 2)

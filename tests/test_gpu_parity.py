@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.  Sizes span several tiles with ragged tails in M
+(expert segments), N and K; bars are in moe_cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import top_routing_expert_02_b300 as moe
+from top_routing_expert_02_b300 import synth
+
+from moe_cases import compare_dispatch, compare_output, compare_routing, make_case, rel_fro, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+C = synth.MoEConfig
+
+SMALL = {
+    # ragged M tiles (cap 313 = 128+128+57), 4 K blocks, 3 SwiGLU N tiles
+    "swiglu_e8": C("swiglu_e8", 2000, 256, 8, 2, 384, "swiglu", 1.25, "bf16"),
+    # GELU with a half N tile (F=320), 3 K blocks, two hot experts over capacity
+    "gelu_e16_hot": C("gelu_e16_hot", 1500, 192, 16, 2, 320, "gelu", 1.0, "bf16", bias="hot2"),
+    # 64 experts, Zipf skew: many empty or tiny segments; SwiGLU half N tile
+    "swiglu_e64_zipf": C("swiglu_e64_zipf", 3000, 128, 64, 2, 192, "swiglu", 1.25, "bf16", bias="zipf"),
+    # 128 experts, top-8, dropless
+    "swiglu_e128_top8": C("swiglu_e128_top8", 300, 256, 128, 8, 128, "swiglu", 0.0, "bf16"),
+    # router without renormalisation, E=32 (one expert per lane)
+    "gelu_e32_norenorm": C("gelu_e32_norenorm", 900, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False),
+    # fp32 x with E=200 (8 experts per lane), through the fp32 FFN
+    "f32_e200": C("f32_e200", 400, 128, 200, 3, 128, "swiglu", 2.0, "f32"),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "these tests need a CUDA device"
+    moe.lib()
+    yield
+
+
+def test_tiny_fp32_layer_full():
+    case = make_case(synth.workload("tiny_fp32"))
+    plan = run_gpu(case)
+    ref = run_oracle(case)
+    compare_routing(plan, ref)
+    compare_dispatch(plan, ref, case["x_h"])
+    assert ref["n_dropped"] > 0
+    compare_output(plan, ref, "f32")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_layers_full(name):
+    cfg = SMALL[name]
+    case = make_case(cfg)
+    plan = run_gpu(case)
+    ref = run_oracle(case)
+    compare_routing(plan, ref)
+    compare_dispatch(plan, ref, case["x_h"])
+    compare_output(plan, ref, cfg.dtype)
+
+
+def test_expert_up_and_down_against_torch():
+    """The two grouped GEMMs alone, against CPU torch fp32 per expert."""
+    cfg = SMALL["swiglu_e8"]
+    case = make_case(cfg)
+    plan = run_gpu(case)
+    D = plan.disp
+    kept, offs = D.kept.cpu().numpy(), D.offsets.cpu().numpy()
+    xp = D.x_perm.float().cpu()
+    h = plan.h.float().cpu()
+    yp = plan.y_perm.float().cpu()
+    rg = D.row_gate.cpu()
+    w1, w2 = case["w1"].float().cpu(), case["w2"].float().cpu()
+    F = cfg.F
+    for e in range(cfg.E):
+        r0, r1 = offs[e], offs[e] + kept[e]
+        z = xp[r0:r1] @ w1[e].T
+        href = torch.nn.functional.silu(z[:, :F]) * z[:, F:]
+        assert rel_fro(h[r0:r1].numpy(), href.numpy()) < 1e-2
+        yref = rg[r0:r1, None] * (h[r0:r1] @ w2[e].T)
+        assert rel_fro(yp[r0:r1].numpy(), yref.numpy()) < 1e-2
+
+
+def test_identity_experts_return_x_bf16():
+    """w1 = w2 = I, act = identity, renormalised gates, dropless: y = x up to
+    the bf16 roundings of y_perm and y."""
+    T, d, E, k = 700, 128, 8, 2
+    cfg = C("ident", T, d, E, k, d, "identity", 0.0, "bf16")
+    ri = synth.make_routing_inputs(cfg)
+    case = make_case(cfg, routing=ri)
+    eye = torch.eye(d, dtype=torch.bfloat16, device="cuda").expand(E, d, d).contiguous()
+    case["w1"], case["w2"] = eye, eye
+    plan = run_gpu(case)
+    y = plan.y.float().cpu().numpy()
+    x = case["x_h"].float().numpy()
+    assert rel_fro(y, x) < 8e-3
+    assert int(plan.disp.n_dropped.item()) == 0
+
+
+def test_capacity_zero_drops_everything():
+    cfg = C("cap0", 256, 128, 8, 2, 128, "swiglu", 0.001, "bf16")
+    case = make_case(cfg)
+    assert case["cap"] == 0
+    plan = run_gpu(case)
+    assert int(plan.disp.n_dropped.item()) == cfg.T * cfg.k
+    assert (plan.disp.kept.cpu() == 0).all() and (plan.disp.slot_row.cpu() == -1).all()
+    assert torch.count_nonzero(plan.y).item() == 0
+    ref = run_oracle(case, tokens=[0])
+    assert abs(plan.loss.item() - ref["loss"]) <= 1e-5 * ref["loss"]
+
+
+def test_single_expert_dense_layer():
+    cfg = C("dense", 300, 128, 1, 1, 256, "gelu", 0.0, "bf16")
+    case = make_case(cfg)
+    plan = run_gpu(case)
+    ref = run_oracle(case)
+    compare_routing(plan, ref)
+    compare_dispatch(plan, ref)
+    compare_output(plan, ref, "bf16")
+
+
+@pytest.mark.parametrize("xdtype", ["f32", "bf16"])
+def test_exact_ties_go_to_lower_index(xdtype):
+    """One-hot x rows make every logit an exact table entry; the table repeats
+    values on purpose, so GPU and oracle must both break ties by index."""
+    T, d, E, k = 96, 64, 16, 4
+    rng = np.random.default_rng(5)
+    table = (rng.integers(-6, 7, size=(E, d)) / 8.0).astype(np.float32)
+    table[5] = table[3]
+    table[11] = table[2]
+    x = np.zeros((T, d), dtype=np.float32)
+    x[np.arange(T), np.arange(T) % d] = 1.0
+    cfg = C("ties", T, d, E, k, 128, "swiglu", 0.0, xdtype)
+    xt = torch.from_numpy(x)
+    ri = synth.RoutingInputs(x=xt.to(torch.bfloat16) if xdtype == "bf16" else xt, W=torch.from_numpy(table), b=None)
+    case = make_case(cfg, condition=False, routing=ri)
+    idx, gate, ps = moe.route(case["x"], case["W"], None, k)
+    ref_idx, ref_gate, ref_ps = oracle.route(oracle.router_logits(ri.x, ri.W), k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_allclose(gate.cpu().numpy(), ref_gate, rtol=1e-5)
+    np.testing.assert_allclose(ps.cpu().numpy(), ref_ps, rtol=1e-5)
+
+
+def test_run_to_run_bitwise_determinism():
+    cfg = SMALL["swiglu_e64_zipf"]
+    case = make_case(cfg)
+    p1 = run_gpu(case)
+    snap = [t.clone() for t in (p1.topk_idx, p1.topk_gate, p1.prob_sum, p1.disp.slot_row, p1.y, p1.loss)]
+    p2 = run_gpu(case, plan=p1)
+    for a, b in zip(snap, (p2.topk_idx, p2.topk_gate, p2.prob_sum, p2.disp.slot_row, p2.y, p2.loss)):
+        assert torch.equal(a, b)
+
+
+def test_empty_batch():
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    W = torch.randn(8, 128, device="cuda")
+    idx, gate, ps = moe.route(x, W, None, 2)
+    torch.cuda.synchronize()
+    assert idx.shape == (0, 2) and torch.count_nonzero(ps).item() == 0
+    D = moe.dispatch(idx, gate, x, 8, 4)
+    torch.cuda.synchronize()
+    assert (D.counts.cpu() == 0).all() and (D.offsets.cpu() == 0).all() and D.n_dropped.item() == 0
+    moe.check()
+
+
+def test_bad_expert_id_is_reported_not_trapped():
+    T, k, E, d = 64, 2, 8, 128
+    idx = torch.zeros(T, k, dtype=torch.int32, device="cuda")
+    idx[3, 1] = 99
+    gate = torch.full((T, k), 0.5, device="cuda")
+    x = torch.zeros(T, d, dtype=torch.bfloat16, device="cuda")
+    D = moe.dispatch(idx, gate, x, E, T)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.check()
+    assert ei.value.code == 1
+    assert D.slot_row[3, 1].item() == -1
+    moe.check()   # status was cleared
+
+
+def test_wait_time_limit_path_reports_timeout():
+    """A barrier nothing completes, under a ~1 ms limit: the kernel records a
+    timeout and returns; the context stays usable."""
+    moe.set_wait_limit(2_000_000)
+    try:
+        moe.selftest_wait_timeout()
+        with pytest.raises(moe.MoEError) as ei:
+            moe.check()
+        assert ei.value.code == 5
+    finally:
+        moe.set_wait_limit(0)
+    moe.check()
+    test_tiny_fp32_layer_full()

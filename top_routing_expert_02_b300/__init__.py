@@ -1,0 +1,302 @@
+"""B300-native MoE-layer forward (router, capacity dispatch, expert FFN,
+combine, aux loss) for sm_103a.
+
+This module is the Python binding of ``libmoe_b300.so``: it only marshals
+torch tensors (device pointers, sizes, the current CUDA stream) into the C ABI
+declared in ``include/moe_b300.h`` and turns status codes into exceptions.
+Every step of the layer runs in the library's CUDA kernels; there is no
+fallback.  PyTorch provides device memory and streams.
+
+Entry points (same names as the C ABI, without the ``moe_`` prefix):
+``route``, ``dispatch``, ``expert_up``, ``expert_down``, ``expert_ffn``,
+``combine``, ``aux_loss``, plus ``capacity``, ``perm_rows_max``,
+``workspace_bytes``, ``check``.  :class:`MoEPlan` holds preallocated buffers
+for one layer shape and enqueues the five calls; :func:`moe_forward` is the
+one-shot form.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "dispatch", "expert_up",
+    "expert_down", "expert_ffn", "combine", "aux_loss", "check", "set_wait_limit", "selftest_wait_timeout",
+    "MoEPlan", "moe_forward", "ACT", "CALL",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
+
+ACT = {"gelu": 0, "swiglu": 1, "identity": 2}
+CALL = {"route": 0, "dispatch": 1, "ffn": 2}
+_DT = {torch.float32: 0, torch.bfloat16: 1}
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({_lib.moe_status_string(code).decode()})")
+
+
+_lib = None
+
+_P, _I64, _I32, _D, _F, _SZ, _U64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
+                                     ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64)
+_SIGS = {
+    "moe_capacity": (_I64, [_I64, _I32, _D]),
+    "moe_perm_rows_max": (_I64, [_I64, _I32, _I32, _I64]),
+    "moe_workspace_bytes": (_SZ, [_I32, _I64, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "moe_status_string": (ctypes.c_char_p, [_I32]),
+    "moe_abi_version": (_I32, []),
+    "moe_route": (_I32, [_P, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                            _P, _SZ, _P]),
+    "moe_expert_up": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_expert_down": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P]),
+    "moe_expert_ffn": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P, _P, _SZ,
+                              _P]),
+    "moe_combine": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P]),
+    "moe_aux_loss": (_I32, [_P, _P, _I64, _I32, _F, _P, _P]),
+    "moe_check": (_I32, [_P]),
+    "moe_set_wait_limit": (None, [_U64]),
+    "moe_selftest_wait_timeout": (_I32, [_P]),
+}
+
+
+def lib():
+    """The loaded CUDA library (built in-tree first if missing or stale)."""
+    global _lib
+    if _lib is None:
+        from . import build as _build
+        if _build.needs_build():
+            _build.build_library()
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"CUDA library {LIB_PATH} is missing; run python -m top_routing_expert_02_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16") from None
+
+
+def _ok(fn: str, code: int):
+    if code != 0:
+        raise MoEError(fn, code)
+
+
+def _empty_ws(nbytes: int, device):
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ host ---
+
+def capacity(T: int, E: int, cf: float) -> int:
+    return int(lib().moe_capacity(T, E, float(cf)))
+
+
+def perm_rows_max(T: int, k: int, E: int, cap: int) -> int:
+    return int(lib().moe_perm_rows_max(T, k, E, cap))
+
+
+def workspace_bytes(call: str, T: int, d: int, E: int, k: int, F: int, act: str = "swiglu",
+                    dtype: torch.dtype = torch.bfloat16) -> int:
+    return int(lib().moe_workspace_bytes(CALL[call], T, d, E, k, F, ACT[act], _DT[dtype]))
+
+
+def check(stream=None):
+    """Synchronise the stream and raise if a kernel recorded a device error."""
+    _ok("moe_check", lib().moe_check(_stream(stream)))
+
+
+def set_wait_limit(cycles: int):
+    lib().moe_set_wait_limit(int(cycles))
+
+
+def selftest_wait_timeout(stream=None):
+    _ok("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(_stream(stream)))
+
+
+# --------------------------------------------------------------- compute ---
+
+def route(x, w_router, b_router, k: int, renorm: bool = True, *, topk_idx=None, topk_gate=None, prob_sum=None,
+          ws=None, stream=None):
+    """Router (moe_route): returns (topk_idx [T,k] int32, topk_gate [T,k] f32, prob_sum [E] f32)."""
+    T, d = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_gate = torch.empty((T, k), dtype=torch.float32, device=dev) if topk_gate is None else topk_gate
+    prob_sum = torch.empty(E, dtype=torch.float32, device=dev) if prob_sum is None else prob_sum
+    need = workspace_bytes("route", T, d, E, k, 64)
+    ws = _empty_ws(need, dev) if ws is None else ws
+    _ok("moe_route", lib().moe_route(_ptr(x), _dt(x), _ptr(w_router), _ptr(b_router), T, d, E, k, int(renorm),
+                                     _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(ws), ws.numel(),
+                                     _stream(stream)))
+    return topk_idx, topk_gate, prob_sum
+
+
+@dataclass
+class Dispatched:
+    counts: torch.Tensor
+    kept: torch.Tensor
+    offsets: torch.Tensor
+    slot_row: torch.Tensor
+    row_token: torch.Tensor
+    row_gate: torch.Tensor
+    x_perm: torch.Tensor
+    n_dropped: torch.Tensor
+    rows_max: int
+
+
+def dispatch(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatched] = None, ws=None,
+             stream=None) -> Dispatched:
+    """Capacity dispatch + row permutation (moe_dispatch)."""
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    dev = x.device
+    R = perm_rows_max(T, k, E, cap)
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = Dispatched(torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                         torch.empty((T, k), **i32), torch.empty(max(R, 1), **i32),
+                         torch.empty(max(R, 1), dtype=torch.float32, device=dev),
+                         torch.empty((max(R, 1), d), dtype=x.dtype, device=dev), torch.empty(1, **i32), R)
+    need = workspace_bytes("dispatch", T, d, E, k, 64)
+    ws = _empty_ws(need, dev) if ws is None else ws
+    _ok("moe_dispatch", lib().moe_dispatch(_ptr(topk_idx), _ptr(topk_gate), T, k, E, cap, _ptr(x), _dt(x), d,
+                                           _ptr(out.counts), _ptr(out.kept), _ptr(out.offsets), _ptr(out.slot_row),
+                                           _ptr(out.row_token), _ptr(out.row_gate), _ptr(out.x_perm),
+                                           _ptr(out.n_dropped), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def expert_up(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None, stream=None):
+    E, _, d = w1.shape
+    h = torch.empty((max(rows_max, 1), F), dtype=x_perm.dtype, device=x_perm.device) if h is None else h
+    _ok("moe_expert_up", lib().moe_expert_up(_ptr(x_perm), _ptr(offsets), _ptr(kept), E, d, F, ACT[act],
+                                             _dt(x_perm), _ptr(w1), rows_max, _ptr(h), _stream(stream)))
+    return h
+
+
+def expert_down(h, offsets, kept, w2, row_gate, rows_max: int, *, y_perm=None, stream=None):
+    E, d, F = w2.shape
+    y_perm = torch.empty((max(rows_max, 1), d), dtype=h.dtype, device=h.device) if y_perm is None else y_perm
+    _ok("moe_expert_down", lib().moe_expert_down(_ptr(h), _ptr(offsets), _ptr(kept), E, d, F, _dt(h), _ptr(w2),
+                                                 _ptr(row_gate), rows_max, _ptr(y_perm), _stream(stream)))
+    return y_perm
+
+
+def expert_ffn(x_perm, offsets, kept, w1, w2, row_gate, act: str, rows_max: int, *, h=None, y_perm=None,
+               stream=None):
+    E, d, F = w2.shape
+    dev = x_perm.device
+    h = torch.empty((max(rows_max, 1), F), dtype=x_perm.dtype, device=dev) if h is None else h
+    y_perm = torch.empty((max(rows_max, 1), d), dtype=x_perm.dtype, device=dev) if y_perm is None else y_perm
+    _ok("moe_expert_ffn", lib().moe_expert_ffn(_ptr(x_perm), _ptr(offsets), _ptr(kept), E, d, F, ACT[act],
+                                               _dt(x_perm), _ptr(w1), _ptr(w2), _ptr(row_gate), rows_max, _ptr(h),
+                                               _ptr(y_perm), None, 0, _stream(stream)))
+    return h, y_perm
+
+
+def combine(y_perm, slot_row, *, y=None, stream=None):
+    T, k = slot_row.shape
+    d = y_perm.shape[1]
+    y = torch.empty((T, d), dtype=y_perm.dtype, device=y_perm.device) if y is None else y
+    _ok("moe_combine", lib().moe_combine(_ptr(y_perm), _ptr(slot_row), T, k, d, _dt(y_perm), _ptr(y),
+                                         _stream(stream)))
+    return y
+
+
+def aux_loss(counts, prob_sum, T: int, alpha: float, *, loss=None, stream=None):
+    E = counts.shape[0]
+    loss = torch.empty(1, dtype=torch.float32, device=counts.device) if loss is None else loss
+    _ok("moe_aux_loss", lib().moe_aux_loss(_ptr(counts), _ptr(prob_sum), T, E, float(alpha), _ptr(loss),
+                                           _stream(stream)))
+    return loss
+
+
+# ------------------------------------------------------------ whole layer ---
+
+class MoEPlan:
+    """Preallocated device buffers for one layer shape.
+
+    ``run(x, w_router, b_router, w1, w2)`` enqueues route, dispatch, the
+    expert FFN, combine and the aux loss on the current stream (no host
+    synchronisation; safe to capture in a CUDA graph) and returns ``y``.
+    Every intermediate stays readable as an attribute afterwards.
+    """
+
+    def __init__(self, T: int, d: int, E: int, k: int, F: int, act: str, dtype: torch.dtype, cap: int,
+                 device="cuda", alpha: float = 0.01, renorm: bool = True):
+        self.T, self.d, self.E, self.k, self.F, self.act = T, d, E, k, F, act
+        self.dtype, self.cap, self.alpha, self.renorm = dtype, int(cap), float(alpha), bool(renorm)
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.rows_max = R = perm_rows_max(T, k, E, cap)
+        Rb = max(R, 1)
+        self.topk_idx = torch.empty((T, k), **i32)
+        self.topk_gate = torch.empty((T, k), **f32)
+        self.prob_sum = torch.empty(E, **f32)
+        self.disp = Dispatched(torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                               torch.empty((T, k), **i32), torch.empty(Rb, **i32), torch.empty(Rb, **f32),
+                               torch.empty((Rb, d), dtype=dtype, device=dev), torch.empty(1, **i32), R)
+        self.h = torch.empty((Rb, F), dtype=dtype, device=dev)
+        self.y_perm = torch.empty((Rb, d), dtype=dtype, device=dev)
+        self.y = torch.empty((T, d), dtype=dtype, device=dev)
+        self.loss = torch.empty(1, **f32)
+        self.ws_route = _empty_ws(workspace_bytes("route", T, d, E, k, F), dev)
+        self.ws_dispatch = _empty_ws(workspace_bytes("dispatch", T, d, E, k, F), dev)
+
+    def run(self, x, w_router, b_router, w1, w2, stream=None) -> torch.Tensor:
+        route(x, w_router, b_router, self.k, self.renorm, topk_idx=self.topk_idx, topk_gate=self.topk_gate,
+              prob_sum=self.prob_sum, ws=self.ws_route, stream=stream)
+        dispatch(self.topk_idx, self.topk_gate, x, self.E, self.cap, out=self.disp, ws=self.ws_dispatch,
+                 stream=stream)
+        D = self.disp
+        expert_ffn(D.x_perm, D.offsets, D.kept, w1, w2, D.row_gate, self.act, self.rows_max, h=self.h,
+                   y_perm=self.y_perm, stream=stream)
+        combine(self.y_perm, D.slot_row, y=self.y, stream=stream)
+        if self.T > 0:
+            aux_loss(D.counts, self.prob_sum, self.T, self.alpha, loss=self.loss, stream=stream)
+        return self.y
+
+
+def moe_forward(x, w_router, b_router, w1, w2, *, k: int, cf: float, act: str, renorm: bool = True,
+                alpha: float = 0.01):
+    """One MoE-layer forward; returns (y, loss, plan) with every intermediate on ``plan``."""
+    T, d = x.shape
+    E, N1, _ = w1.shape
+    F = w2.shape[2]
+    plan = MoEPlan(T, d, E, k, F, act, x.dtype, capacity(T, E, cf), x.device, alpha, renorm)
+    y = plan.run(x, w_router, b_router, w1, w2)
+    return y, plan.loss, plan

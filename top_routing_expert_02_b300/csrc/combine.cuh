@@ -1,0 +1,81 @@
+// Combine (the return All-to-All of expert parallelism, here an
+// un-permutation in HBM) and the auxiliary load-balance loss.
+//
+// Expert-parallelism tutorial "专家并行：混合专家模型的分布式训练方案" §2.1 step 5:
+// expert outputs go back to their tokens' original positions; the
+// deployment guide "细粒度专家并行部署实践与优化指南" §七 gathers them back the same
+// way.  The gate product already sits inside y_perm (expert down-projection
+// epilogue), so the combine is a plain sum over the k slots of a token.
+// Aux loss: §5.1 of the tutorial, L = alpha * num_experts * sum_i f_i P_i.
+#pragma once
+#include "common.cuh"
+
+namespace combine {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+
+// One warp per token; each lane sums 16-byte vectors of the token's k rows
+// in j order (fp32) and rounds once.  Dropped slots (-1) are skipped; a token
+// with none kept gets zeros.
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS)
+combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ slot_row, int T, int k,
+               int vec16, uint4* __restrict__ y)
+{
+    const int lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * WARPS;
+    for (int t = blockIdx.x * WARPS + (threadIdx.x >> 5); t < T; t += warps_total) {
+        int rows[16];
+        int nk = 0;
+        for (int j = 0; j < k; ++j) {
+            const int r = __ldg(slot_row + (size_t)t * k + j);
+            if (r >= 0) rows[nk++] = r;
+        }
+        for (int v = lane; v < vec16; v += 32) {
+            if (BF16) {
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                for (int q = 0; q < nk; ++q) {
+                    float f[8];
+                    unpack_bf16x8(ldg_nc_v4(y_perm + (size_t)rows[q] * vec16 + v), f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+                }
+                uint4 o;
+                o.x = pack_bf16x2(acc[0], acc[1]);
+                o.y = pack_bf16x2(acc[2], acc[3]);
+                o.z = pack_bf16x2(acc[4], acc[5]);
+                o.w = pack_bf16x2(acc[6], acc[7]);
+                y[(size_t)t * vec16 + v] = o;
+            } else {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int q = 0; q < nk; ++q) {
+                    const uint4 u = ldg_nc_v4(y_perm + (size_t)rows[q] * vec16 + v);
+                    acc[0] += __uint_as_float(u.x);
+                    acc[1] += __uint_as_float(u.y);
+                    acc[2] += __uint_as_float(u.z);
+                    acc[3] += __uint_as_float(u.w);
+                }
+                y[(size_t)t * vec16 + v] = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                                      __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+            }
+        }
+    }
+}
+
+// One warp: f_e = counts[e] / T, P_e = prob_sum[e] / T, fixed-order fp64 sum.
+__global__ void aux_loss_kernel(const int32_t* __restrict__ counts, const float* __restrict__ prob_sum,
+                                long long T, int E, float alpha, float* __restrict__ loss)
+{
+    const int lane = threadIdx.x;
+    double s = 0.0;
+    for (int e = lane; e < E; e += 32)
+        s += ((double)counts[e] / (double)T) * ((double)prob_sum[e] / (double)T);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) *loss = (float)((double)alpha * (double)E * s);
+}
+
+}  // namespace combine

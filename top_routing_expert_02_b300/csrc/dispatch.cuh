@@ -1,0 +1,167 @@
+// Dispatch: capacity-limited slot assignment and the row permutation that
+// replaces the All-to-All token exchange on one GPU.
+//
+// Expert-parallelism tutorial "专家并行：混合专家模型的分布式训练方案" §2.1 steps
+// 2-3 (mark each token with its target expert, exchange the tokens) and §2.2
+// (expert capacity; tokens beyond it are dropped and take the residual path);
+// §5.3 of the same page packs and sorts tokens so each expert's rows are
+// contiguous.
+//
+// Assignments are numbered a = j*T + t (k-rank major, token minor): that is
+// the order in which slots are granted.  Three kernels:
+//   hist    per chunk of 1024 assignments, a histogram over experts
+//   rank    per chunk: base of every expert from the earlier chunks, then the
+//           stable rank of each assignment inside the chunk (warp match +
+//           per-warp counts), giving its place in the expert's queue; kept
+//           slots get a row of the permuted buffer
+//   gather  x_perm[row] = x[row_token[row]] with 16-byte vector moves
+#pragma once
+#include "common.cuh"
+
+namespace dispatch {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+constexpr int CHUNK = 1024;
+constexpr int MAX_E = 256;
+
+__global__ void __launch_bounds__(THREADS)
+hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int* __restrict__ hist)
+{
+    __shared__ int h[MAX_E];
+    for (int e = threadIdx.x; e < E; e += THREADS) h[e] = 0;
+    __syncthreads();
+    const long long n = (long long)T * k;
+    const long long a0 = (long long)blockIdx.x * CHUNK;
+    bool bad = false;
+    for (int i = threadIdx.x; i < CHUNK; i += THREADS) {
+        const long long a = a0 + i;
+        if (a >= n) break;
+        const int j = (int)(a / T), t = (int)(a - (long long)j * T);
+        const int e = __ldg(idx + (size_t)t * k + j);
+        if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+        else bad = true;
+    }
+    if (bad) moe_flag(MOE_DEV_BAD_EXPERT);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += THREADS) hist[(size_t)blockIdx.x * E + e] = h[e];
+}
+
+__global__ void __launch_bounds__(THREADS)
+rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int k, int E, int cap,
+            const int* __restrict__ hist, int nchunk, int32_t* __restrict__ counts, int32_t* __restrict__ kept,
+            int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row, int32_t* __restrict__ row_token,
+            float* __restrict__ row_gate, int32_t* __restrict__ n_dropped)
+{
+    __shared__ int base[MAX_E], off[MAX_E + 1], running[MAX_E], scan[MAX_E];
+    __shared__ int wcnt[WARPS][MAX_E];
+    __shared__ int drop_part[THREADS];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk = blockIdx.x;
+
+    // 1. place of this chunk in every expert's queue, and the totals
+    int my_drop = 0;
+    for (int e = tid; e < E; e += THREADS) {
+        int before = 0, total = 0;
+        for (int c = 0; c < nchunk; ++c) {
+            const int v = __ldg(hist + (size_t)c * E + e);
+            if (c < chunk) before += v;
+            total += v;
+        }
+        base[e] = before;
+        running[e] = 0;
+        const int kp = total < cap ? total : cap;
+        scan[e] = kp;
+        if (chunk == 0) {
+            counts[e] = total;
+            kept[e] = kp;
+        }
+        my_drop += total - kp;
+    }
+    drop_part[tid] = my_drop;
+    __syncthreads();
+    // 2. exclusive scan of kept over experts (E <= 256, one pass per thread)
+    if (tid == 0) {
+        int s = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = s;
+            s += scan[e];
+        }
+        off[E] = s;
+        if (chunk == 0) {
+            int dsum = 0;
+            for (int i = 0; i < THREADS; ++i) dsum += drop_part[i];
+            *n_dropped = dsum;
+        }
+    }
+    __syncthreads();
+    if (chunk == 0)
+        for (int e = tid; e <= E; e += THREADS) offsets[e] = off[e];
+
+    // 3. stable rank inside the chunk, THREADS assignments per round
+    const long long n = (long long)T * k;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int r = 0; r < CHUNK / THREADS; ++r) {
+        for (int v = tid; v < WARPS * E; v += THREADS) wcnt[v / E][v % E] = 0;
+        __syncthreads();
+        const long long a = (long long)chunk * CHUNK + (long long)r * THREADS + tid;
+        int e = -1, t = 0, j = 0;
+        if (a < n) {
+            j = (int)(a / T);
+            t = (int)(a - (long long)j * T);
+            e = __ldg(idx + (size_t)t * k + j);
+            if (e < 0 || e >= E) e = -2;   // flagged by hist_kernel; the slot is dropped
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int intra = __popc(peers & lt_mask);
+        if (e >= 0 && intra == 0) wcnt[warp][e] = __popc(peers);
+        __syncthreads();
+        if (a < n) {
+            int32_t row = -1;
+            if (e >= 0) {
+                int pos = base[e] + running[e] + intra;
+                for (int w = 0; w < warp; ++w) pos += wcnt[w][e];
+                if (pos < cap) {
+                    row = off[e] + pos;
+                    row_token[row] = t;
+                    row_gate[row] = __ldg(gate + (size_t)t * k + j);
+                }
+            }
+            slot_row[(size_t)t * k + j] = row;
+        }
+        __syncthreads();
+        for (int v = tid; v < E; v += THREADS) {
+            int s = 0;
+            for (int w = 0; w < WARPS; ++w) s += wcnt[w][v];
+            running[v] += s;
+        }
+        __syncthreads();
+    }
+}
+
+// One warp per row, rows strided over the grid; vec16 = 16-byte vectors per row.
+__global__ void __launch_bounds__(THREADS)
+gather_rows_kernel(const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets, int E,
+                   const uint4* __restrict__ x, uint4* __restrict__ x_perm, int vec16)
+{
+    const int lane = threadIdx.x & 31;
+    const int A = __ldg(offsets + E);
+    const int warps_total = gridDim.x * WARPS;
+    for (int row = blockIdx.x * WARPS + (threadIdx.x >> 5); row < A; row += warps_total) {
+        const int t = __ldg(row_token + row);
+        const uint4* src = x + (size_t)t * vec16;
+        uint4* dst = x_perm + (size_t)row * vec16;
+        int v = lane;
+        for (; v + 96 < vec16; v += 128) {
+            const uint4 a0 = ldg_nc_v4(src + v), a1 = ldg_nc_v4(src + v + 32);
+            const uint4 a2 = ldg_nc_v4(src + v + 64), a3 = ldg_nc_v4(src + v + 96);
+            dst[v] = a0;
+            dst[v + 32] = a1;
+            dst[v + 64] = a2;
+            dst[v + 96] = a3;
+        }
+        for (; v < vec16; v += 32) dst[v] = ldg_nc_v4(src + v);
+    }
+}
+
+}  // namespace dispatch

@@ -1,0 +1,278 @@
+// bf16 grouped expert GEMMs on the 5th-generation tensor cores (tcgen05).
+//
+// Expert-parallelism tutorial "专家并行：混合专家模型的分布式训练方案" §2.1 step 4
+// (every expert runs its FFN on the rows it received) with the two-matrix
+// expert d -> d_ff -> d of the ETP page "ETP专家并行加速MoE模型：ms-swift中稀疏架构的
+// 极致优化".  Up:   h[r] = act(w1[e] . x_perm[r]);  down: y_perm[r] = row_gate[r]
+// * (w2[e] . h[r]).  The activation lives in the up epilogue and the gate
+// product in the down epilogue, so neither needs a pass of its own.
+//
+// One persistent block per SM, 6 warps:
+//   warp 0     TMA producer: A tile 128x64 and B tile 256x64 (two 128-row
+//              boxes) per stage, 128-byte swizzle, STAGES-deep ring
+//   warp 1     MMA issuer: tcgen05.mma M=128 N=256 K=16, fp32 accumulator in
+//              TMEM, two accumulators (512 columns) so the epilogue of one
+//              tile overlaps the main loop of the next
+//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, activation or
+//              gate scale in fp32, one rounding to bf16, masked stores
+// Tiles never straddle experts: M-tile m of expert e starts at row
+// offsets[e] + 128 m; rows past kept[e] are computed (they belong to the next
+// expert or to the zero fill past the buffer) but never stored.  Tiles run
+// M-fastest inside (expert, N-tile), so the blocks working at the same time
+// share one weight tile through L2.  For SwiGLU the B tile pairs gate rows
+// n..n+127 with up rows F+n..F+n+127, so accumulator columns [0,128) are the
+// gate and [128,256) the up projection of the same 128 outputs.
+//
+// Every wait is bounded by a cycle limit; a wait that runs out records
+// MOE_DEV_TIMEOUT and its role stops, the other roles then run out too, and
+// the block still drains its copies and frees TMEM before it exits.
+#pragma once
+#include "common.cuh"
+#include "ptx_sm103.cuh"
+#include "tiles.cuh"
+
+namespace tcg {
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;              // 16 KB
+constexpr int BH_BYTES = 128 * BK * 2;            // one 128-row half of B
+constexpr int STAGE_BYTES = A_BYTES + 2 * BH_BYTES;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int THREADS = 192;
+constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, 256);
+
+enum { EPI_GELU = 0, EPI_SWIGLU = 1, EPI_IDENT = 2, EPI_GATE = 3 };
+
+struct Args {
+    const int32_t* offsets;
+    const int32_t* kept;
+    int E;
+    int K;             // reduction length (d for up, F for down)
+    int n_tiles;       // N-tiles per expert
+    int b_rows;        // rows of one expert's weight in the 2-D view [E*b_rows, K]
+    int half_off;      // row offset of the second 128-row box of a B tile
+    int n_step;        // output columns per tile: 128 (SwiGLU) or 256
+    int out_cols;      // columns of the output (F for up, d for down)
+    uint16_t* out;     // bf16 [rows_max, out_cols]
+    const float* row_gate;
+    unsigned long long wait_limit;
+};
+
+__device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tiles, int tile, int& e, int& m,
+                                            int& n)
+{
+    e = find_expert(mstart, E, tile / n_tiles);
+    const int local = tile - mstart[e] * n_tiles;
+    const int mt = mstart[e + 1] - mstart[e];
+    n = local / mt;
+    m = local - n * mt;
+}
+
+__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const Args g)
+{
+    extern __shared__ uint8_t dsmem[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int mstart[257];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t smem0 = (ptx::smem_u32(dsmem) + 1023u) & ~1023u;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(ptx::smem_u32(&tfull_bar[a]), 1);
+            ptx::mbar_init(ptx::smem_u32(&tempty_bar[a]), 128);
+        }
+        ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+        ptx::fence_mbar_init();
+        ptx::tma_prefetch_desc(&tmA);
+        ptx::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 2) build_mtile_prefix<BM>(g.kept, g.E, mstart, lane);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem_base = tmem_base_sh;
+    const int total_tiles = mstart[g.E] * g.n_tiles;
+    const int nk = (g.K + BK - 1) / BK;
+    const uint64_t limit = g.wait_limit;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                int e, m, n;
+                decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+                const int rowA = __ldg(g.offsets + e) + m * BM;
+                const int rowB0 = e * g.b_rows + n * g.n_step;
+                const int rowB1 = rowB0 + g.half_off;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
+                    const uint32_t sa = smem0 + stage * STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    ptx::tma_load_2d(sa, &tmA, fb, kb * BK, rowA);
+                    ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, rowB0);
+                    ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kb * BK, rowB1);
+                    ++fills;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) moe_flag(MOE_DEV_TIMEOUT);
+            // drain: the last fill of every stage must have landed before exit
+            for (long long f = fills - 1; f >= 0 && f >= fills - STAGES; --f) {
+                const int s = (int)(f % STAGES);
+                const uint32_t par = (uint32_t)((f / STAGES) & 1);
+                if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), par, limit)) {
+                    moe_flag(MOE_DEV_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aphase ^ 1u, limit)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = smem0 + stage * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32),
+                                      ptx::sdesc_kmajor_sw128(sb + kk * 32), IDESC, (kb | kk) != 0);
+                    ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_u32(&tfull_bar[acc]));
+                acc ^= 1;
+                if (acc == 0) aphase ^= 1u;
+            }
+            if (!ok) moe_flag(MOE_DEV_TIMEOUT);
+            // no MMA may still write TMEM when the block frees it
+            ptx::mma_commit(ptx::smem_u32(&drain_bar));
+            if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, limit)) moe_flag(MOE_DEV_TIMEOUT);
+        }
+    } else {
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int r_in = q * 32 + lane;    // row of the tile owned by this thread
+        int acc = 0;
+        uint32_t aphase = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            int e, m, n;
+            decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+            const int rows_valid = __ldg(g.kept + e) - m * BM;
+            const int row = __ldg(g.offsets + e) + m * BM + r_in;
+            const bool rv = r_in < rows_valid;
+            const bool waited = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aphase, limit);
+            if (!__all_sync(0xffffffffu, waited)) {
+                moe_flag(MOE_DEV_TIMEOUT);
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            if (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t gv[32], uv[32];
+                    ptx::tmem_ld32(tb + c, gv);
+                    ptx::tmem_ld32(tb + 128 + c, uv);
+                    ptx::tmem_ld_wait();
+                    const int col = n * 128 + c;
+                    if (rv && col < g.out_cols) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(silu_f32(f32(gv[2 * i])) * f32(uv[2 * i]),
+                                                silu_f32(f32(gv[2 * i + 1])) * f32(uv[2 * i + 1]));
+                        uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.out_cols + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            } else {
+                const float gate = (EPI == EPI_GATE && rv) ? __ldg(g.row_gate + row) : 0.f;
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 32) {
+                    uint32_t av[32];
+                    ptx::tmem_ld32(tb + c, av);
+                    ptx::tmem_ld_wait();
+                    const int col = n * 256 + c;
+                    if (rv && col < g.out_cols) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float z0 = f32(av[2 * i]), z1 = f32(av[2 * i + 1]);
+                            if (EPI == EPI_GELU) {
+                                z0 = gelu_f32(z0);
+                                z1 = gelu_f32(z1);
+                            } else if (EPI == EPI_GATE) {
+                                z0 *= gate;
+                                z1 *= gate;
+                            }
+                            pk[i] = pack_bf16x2(z0, z1);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.out_cols + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[acc]));
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace tcg

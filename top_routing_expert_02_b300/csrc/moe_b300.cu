@@ -1,0 +1,408 @@
+// C ABI of the MoE-layer forward (see include/moe_b300.h for the contract).
+//
+// One translation unit: the kernels live in the headers included below and
+// share the device status word defined in common.cuh.  This file validates
+// arguments, encodes TMA tensor maps, picks launch shapes and enqueues the
+// kernels; it allocates nothing.
+#include <atomic>
+#include <climits>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "combine.cuh"
+#include "dispatch.cuh"
+#include "ffn_simt.cuh"
+#include "ffn_tc.cuh"
+#include "route.cuh"
+
+namespace {
+
+constexpr int MAX_E = 256;
+constexpr int MAX_K = 16;
+constexpr unsigned long long DEFAULT_WAIT_LIMIT = 4000000000ull;   // ~2 s of SM cycles
+std::atomic<unsigned long long> g_wait_limit{DEFAULT_WAIT_LIMIT};
+
+inline bool dtype_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+inline int esize(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+inline moe_status launch_status()
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "moe_b300: CUDA error: %s\n", cudaGetErrorString(e));
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+// Router block shape: experts per lane and tokens per warp.
+inline int route_epl(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8; }
+inline int route_tw(int E) { return route_epl(E) == 1 ? 2 : 4; }
+inline int route_tokens_per_block(int E) { return route::WARPS * route_tw(E); }
+inline size_t route_ws_bytes(long long T, int E)
+{
+    const long long nblk = (T + route_tokens_per_block(E) - 1) / route_tokens_per_block(E);
+    return (size_t)nblk * E * sizeof(float);
+}
+inline long long dispatch_chunks(long long T, int k) { return (T * k + dispatch::CHUNK - 1) / dispatch::CHUNK; }
+inline size_t dispatch_ws_bytes(long long T, int k, int E) { return (size_t)dispatch_chunks(T, k) * E * sizeof(int); }
+
+// ---------------------------------------------------------- TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 matrix [rows, cols] (cols contiguous), boxes of 64 columns x 128 rows,
+// 128-byte swizzle, zero fill outside.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+moe_status launch_tc(const void* A, long long rows_max, int K, const void* W, long long w_rows_total,
+                     const tcg::Args& args, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    if (!make_tmap_bf16(&ta, A, (unsigned long long)rows_max, (unsigned long long)K)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K)) return MOE_ERR_CUDA;
+    // per-device attribute; cheap, so set on every launch
+    if (cudaFuncSetAttribute(tcg::grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tcg::SMEM_DYN) != cudaSuccess)
+        return launch_status();
+    const long long max_mtiles = (rows_max + tcg::BM - 1) / tcg::BM + args.E;
+    const long long max_tiles = max_mtiles * args.n_tiles;
+    const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
+    if (grid <= 0) return MOE_OK;
+    tcg::grouped_gemm_kernel<EPI><<<grid, tcg::THREADS, tcg::SMEM_DYN, stream>>>(ta, tb, args);
+    return launch_status();
+}
+
+template <int ACT>
+moe_status launch_simt(const float* A, const int32_t* offsets, const int32_t* kept, int E, int K, int N, int F,
+                       const float* W, const float* gate, float* out, long long rows_max, cudaStream_t stream)
+{
+    const long long max_mtiles = (rows_max + simt::BM - 1) / simt::BM + E;
+    if (max_mtiles > 65535) return MOE_ERR_UNSUPPORTED;
+    dim3 grid(N / simt::BN, (unsigned)max_mtiles);
+    simt::ffn_simt_kernel<ACT><<<grid, simt::THREADS, 0, stream>>>(A, offsets, kept, E, K, N, F, W, gate, out);
+    return launch_status();
+}
+
+template <int EPL, int TW>
+void launch_route(bool bf16, int nblk, const void* x, const float* W, const float* b, int T, int d, int E, int k,
+                  int renorm, int32_t* idx, float* gate, float* partial, cudaStream_t s)
+{
+    if (bf16)
+        route::route_kernel<EPL, TW, true><<<nblk, route::THREADS, 0, s>>>(x, W, b, T, d, E, k, renorm, idx, gate,
+                                                                           partial);
+    else
+        route::route_kernel<EPL, TW, false><<<nblk, route::THREADS, 0, s>>>(x, W, b, T, d, E, k, renorm, idx, gate,
+                                                                            partial);
+}
+
+__global__ void selftest_wait_kernel(unsigned long long limit)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::fence_mbar_init();
+        // nothing ever arrives on this barrier: the wait must run out
+        if (!ptx::mbar_wait(ptx::smem_u32(&bar), 0, limit)) moe_flag(MOE_DEV_TIMEOUT);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status s)
+{
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int64_t moe_capacity(int64_t T, int E, double cf)
+{
+    if (T < 0 || E < 1) return -1;
+    if (cf <= 0.0) return T;
+    return (int64_t)llround(((double)T / (double)E) * cf);
+}
+
+int64_t moe_perm_rows_max(int64_t T, int k, int E, int64_t cap)
+{
+    if (T < 0 || k < 1 || E < 1 || cap < 0) return -1;
+    const int64_t all = T * k, lim = (int64_t)E * cap;
+    return all < lim ? all : lim;
+}
+
+size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F, moe_act act, moe_dtype dtype)
+{
+    (void)d;
+    (void)F;
+    (void)act;
+    (void)dtype;
+    if (T < 0 || E < 1 || E > MAX_E || k < 1) return 0;
+    switch (call) {
+    case MOE_CALL_ROUTE: return route_ws_bytes(T, E);
+    case MOE_CALL_DISPATCH: return dispatch_ws_bytes(T, k, E);
+    case MOE_CALL_FFN: return 0;
+    }
+    return 0;
+}
+
+moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const float* b_router, int64_t T, int d,
+                     int E, int k, int renorm, int32_t* topk_idx, float* topk_gate, float* prob_sum, void* ws,
+                     size_t ws_bytes, moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (T < 0 || d <= 0 || E < 1 || E > MAX_E || k < 1 || k > MAX_K || k > E || !dtype_ok(xdt))
+        return MOE_ERR_INVALID_ARG;
+    if (T * k >= INT_MAX || (long long)T * d >= (1LL << 40)) return MOE_ERR_INVALID_ARG;
+    if (!prob_sum || (T > 0 && (!x || !w_router || !topk_idx || !topk_gate))) return MOE_ERR_INVALID_ARG;
+    if (d % 64) return MOE_ERR_UNSUPPORTED;
+    const size_t need = route_ws_bytes(T, E);
+    if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+    const int tpb = route_tokens_per_block(E);
+    const int nblk = (int)((T + tpb - 1) / tpb);
+    float* partial = (float*)ws;
+    if (nblk > 0) {
+        const bool bf = xdt == MOE_BF16;
+        const int Ti = (int)T;
+        switch (route_epl(E)) {
+        case 1: launch_route<1, 2>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
+        case 2: launch_route<2, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
+        case 4: launch_route<4, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
+        default: launch_route<8, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
+        }
+        const moe_status st = launch_status();
+        if (st != MOE_OK) return st;
+    }
+    route::route_finalize<<<1, route::FIN_THREADS, 0, stream>>>(partial, nblk, E, prob_sum);
+    return launch_status();
+}
+
+moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t T, int k, int E, int64_t cap,
+                        const void* x, moe_dtype xdt, int d, int32_t* counts, int32_t* kept, int32_t* offsets,
+                        int32_t* slot_row, int32_t* row_token, float* row_gate, void* x_perm, int32_t* n_dropped,
+                        void* ws, size_t ws_bytes, moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (T < 0 || k < 1 || k > MAX_K || E < 1 || E > MAX_E || k > E || cap < 0 || d <= 0 || !dtype_ok(xdt))
+        return MOE_ERR_INVALID_ARG;
+    if (T * k >= INT_MAX) return MOE_ERR_INVALID_ARG;
+    if (!counts || !kept || !offsets || !n_dropped) return MOE_ERR_INVALID_ARG;
+    const int64_t rows_max = moe_perm_rows_max(T, k, E, cap);
+    if (T > 0 && (!topk_idx || !topk_gate || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
+    if (rows_max > 0 && (!row_token || !row_gate || !x_perm)) return MOE_ERR_INVALID_ARG;
+    if (d % 64) return MOE_ERR_UNSUPPORTED;
+    const size_t need = dispatch_ws_bytes(T, k, E);
+    if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+    const int nchunk = (int)dispatch_chunks(T, k);
+    const int cap32 = cap > INT_MAX ? INT_MAX : (int)cap;
+    int* hist = (int*)ws;
+    if (nchunk > 0) {
+        dispatch::hist_kernel<<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T, k, E, hist);
+        const moe_status st = launch_status();
+        if (st != MOE_OK) return st;
+    }
+    dispatch::rank_kernel<<<nchunk > 0 ? nchunk : 1, dispatch::THREADS, 0, stream>>>(
+        topk_idx, topk_gate, (int)T, k, E, cap32, hist, nchunk, counts, kept, offsets, slot_row, row_token, row_gate,
+        n_dropped);
+    moe_status st = launch_status();
+    if (st != MOE_OK || rows_max == 0) return st;
+    const int vec16 = d * esize(xdt) / 16;
+    long long grid = (rows_max + dispatch::WARPS - 1) / dispatch::WARPS;
+    if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
+    dispatch::gather_rows_kernel<<<(int)grid, dispatch::THREADS, 0, stream>>>(row_token, offsets, E, (const uint4*)x,
+                                                                              (uint4*)x_perm, vec16);
+    return launch_status();
+}
+
+static moe_status ffn_common_checks(const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                                    moe_dtype dtype, int64_t rows_max)
+{
+    if (E < 1 || E > MAX_E || d <= 0 || F <= 0 || rows_max < 0 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+    if (!offsets || !kept) return MOE_ERR_INVALID_ARG;
+    if (d % 64 || F % 64) return MOE_ERR_UNSUPPORTED;
+    if (rows_max >= INT_MAX) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                         moe_act act, moe_dtype dtype, const void* w1, int64_t rows_max, void* h,
+                         moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    moe_status st = ffn_common_checks(offsets, kept, E, d, F, dtype, rows_max);
+    if (st != MOE_OK) return st;
+    if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
+    if (!w1 || (rows_max > 0 && (!x_perm || !h))) return MOE_ERR_INVALID_ARG;
+    if (rows_max == 0) return MOE_OK;
+    const int N1 = act == MOE_ACT_SWIGLU ? 2 * F : F;
+    if (dtype == MOE_F32) {
+        const float* A = (const float*)x_perm;
+        const float* W = (const float*)w1;
+        float* out = (float*)h;
+        switch (act) {
+        case MOE_ACT_GELU: return launch_simt<simt::ACT_GELU>(A, offsets, kept, E, d, F, F, W, nullptr, out, rows_max, stream);
+        case MOE_ACT_SWIGLU: return launch_simt<simt::ACT_SWIGLU>(A, offsets, kept, E, d, F, F, W, nullptr, out, rows_max, stream);
+        default: return launch_simt<simt::ACT_IDENT>(A, offsets, kept, E, d, F, F, W, nullptr, out, rows_max, stream);
+        }
+    }
+    tcg::Args a{};
+    a.offsets = offsets;
+    a.kept = kept;
+    a.E = E;
+    a.K = d;
+    a.b_rows = N1;
+    a.out_cols = F;
+    a.out = (uint16_t*)h;
+    a.row_gate = nullptr;
+    a.wait_limit = g_wait_limit.load();
+    if (act == MOE_ACT_SWIGLU) {
+        a.n_step = 128;
+        a.half_off = F;
+        a.n_tiles = (F + 127) / 128;
+        return launch_tc<tcg::EPI_SWIGLU>(x_perm, rows_max, d, w1, (long long)E * N1, a, stream);
+    }
+    a.n_step = 256;
+    a.half_off = 128;
+    a.n_tiles = (F + 255) / 256;
+    if (act == MOE_ACT_GELU) return launch_tc<tcg::EPI_GELU>(x_perm, rows_max, d, w1, (long long)E * N1, a, stream);
+    return launch_tc<tcg::EPI_IDENT>(x_perm, rows_max, d, w1, (long long)E * N1, a, stream);
+}
+
+moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                           moe_dtype dtype, const void* w2, const float* row_gate, int64_t rows_max, void* y_perm,
+                           moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    moe_status st = ffn_common_checks(offsets, kept, E, d, F, dtype, rows_max);
+    if (st != MOE_OK) return st;
+    if (!w2 || (rows_max > 0 && (!h || !row_gate || !y_perm))) return MOE_ERR_INVALID_ARG;
+    if (rows_max == 0) return MOE_OK;
+    if (dtype == MOE_F32)
+        return launch_simt<simt::ACT_GATE>((const float*)h, offsets, kept, E, F, d, F, (const float*)w2, row_gate,
+                                           (float*)y_perm, rows_max, stream);
+    tcg::Args a{};
+    a.offsets = offsets;
+    a.kept = kept;
+    a.E = E;
+    a.K = F;
+    a.b_rows = d;
+    a.out_cols = d;
+    a.out = (uint16_t*)y_perm;
+    a.row_gate = row_gate;
+    a.wait_limit = g_wait_limit.load();
+    a.n_step = 256;
+    a.half_off = 128;
+    a.n_tiles = (d + 255) / 256;
+    return launch_tc<tcg::EPI_GATE>(h, rows_max, F, w2, (long long)E * d, a, stream);
+}
+
+moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                          moe_act act, moe_dtype dtype, const void* w1, const void* w2, const float* row_gate,
+                          int64_t rows_max, void* h, void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    (void)ws;
+    (void)ws_bytes;
+    moe_status st = moe_expert_up(x_perm, offsets, kept, E, d, F, act, dtype, w1, rows_max, h, stream);
+    if (st != MOE_OK) return st;
+    return moe_expert_down(h, offsets, kept, E, d, F, dtype, w2, row_gate, rows_max, y_perm, stream);
+}
+
+moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d, moe_dtype dtype, void* y,
+                       moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (T < 0 || k < 1 || k > MAX_K || d <= 0 || !dtype_ok(dtype) || T * k >= INT_MAX) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!slot_row || !y || !y_perm)) return MOE_ERR_INVALID_ARG;
+    if (d % 64) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    const int vec16 = d * esize(dtype) / 16;
+    long long grid = (T + combine::WARPS - 1) / combine::WARPS;
+    if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
+    if (dtype == MOE_BF16)
+        combine::combine_kernel<true><<<(int)grid, combine::THREADS, 0, stream>>>((const uint4*)y_perm, slot_row,
+                                                                                  (int)T, k, vec16, (uint4*)y);
+    else
+        combine::combine_kernel<false><<<(int)grid, combine::THREADS, 0, stream>>>((const uint4*)y_perm, slot_row,
+                                                                                   (int)T, k, vec16, (uint4*)y);
+    return launch_status();
+}
+
+moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T, int E, float alpha, float* loss,
+                        moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (T < 1 || E < 1 || E > MAX_E || !counts || !prob_sum || !loss) return MOE_ERR_INVALID_ARG;
+    combine::aux_loss_kernel<<<1, 32, 0, stream>>>(counts, prob_sum, (long long)T, E, alpha, loss);
+    return launch_status();
+}
+
+moe_status moe_check(moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    unsigned int st = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&st, g_moe_status, sizeof st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (st && cudaMemcpyToSymbol(g_moe_status, &zero, sizeof zero) != cudaSuccess) return MOE_ERR_CUDA;
+    if (st & MOE_DEV_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (st & MOE_DEV_BAD_EXPERT) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+void moe_set_wait_limit(uint64_t cycles) { g_wait_limit.store(cycles ? cycles : DEFAULT_WAIT_LIMIT); }
+
+moe_status moe_selftest_wait_timeout(moe_stream_t stream_)
+{
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream_>>>(g_wait_limit.load());
+    return launch_status();
+}
+
+}  // extern "C"
