@@ -70,21 +70,30 @@ class ClockSampler:
             0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
 
     def __init__(self, device_index: int, period_s: float = 0.01):
-        self.samples, self.reasons, self.max_mhz, self.ok = [], set(), None, False
+        self.samples, self.reasons, self.max_mhz, self.ok, self.err = [], set(), None, False, None
         self._stop = threading.Event()
+        self._period = period_s
+        self._t = None
+        self._smi = None
         try:
             import pynvml
             pynvml.nvmlInit()
-            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-            phys = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(phys)
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            try:
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid.encode())
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
             self._nv = pynvml
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
             self.ok = True
-        except Exception:   # no NVML: report what is known
-            self.ok = False
-        self._period = period_s
-        self._t = None
+        except Exception as e:   # fall back to nvidia-smi sampling
+            self.err = f"nvml: {type(e).__name__}: {e}"
+            self._uuid = None
+            try:
+                self._uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            except Exception:
+                pass
 
     def _run(self):
         nv = self._nv
@@ -101,10 +110,33 @@ class ClockSampler:
                 pass
             time.sleep(self._period)
 
+    def _run_smi(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        sel = ["-i", "GPU-" + self._uuid if self._uuid and not self._uuid.startswith("GPU-") else self._uuid] \
+            if self._uuid else []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", *sel, f"--query-gpu={q}", "--format=csv,noheader,nounits"],
+                                     capture_output=True, text=True, timeout=5).stdout.strip().splitlines()
+                f = [v.strip() for v in out[0].split(",")]
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+                for name, v in zip(names, f[2:]):
+                    if v.lower().startswith("active"):
+                        self.reasons.add(name)
+                self.ok = True
+            except Exception as e:
+                self.err = f"{self.err}; nvidia-smi: {type(e).__name__}: {e}"
+                return
+            time.sleep(0.05)
+
     def __enter__(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        target = self._run if self.ok else self._run_smi
+        self._t = threading.Thread(target=target, daemon=True)
+        self._t.start()
         return self
 
     def __exit__(self, *a):
@@ -113,11 +145,12 @@ class ClockSampler:
             self._t.join()
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "error": self.err}
         reasons = sorted(self.reasons - {"gpu_idle"})
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(self.samples)}
+        d = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+             "samples": len(self.samples), "source": "nvml" if self.err is None else "nvidia-smi"}
+        return d
 
 
 # ------------------------------------------------------------- CPU oracle --
@@ -151,7 +184,7 @@ def reference_arm(args, cfg):
         return
     ri = synth.make_routing_inputs(cfg)
     w1, w2 = synth.make_expert_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
-    cb, S, t = oracle_sample(cfg, ri, w1, w2, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    cb, S, t = oracle_sample(cfg, ri, w1, w2, budget_s=max(0.2, 120.0 / max(1, args.steps + args.warmup)))
     # warm-up and timed steps: each step is the bounded sample
     import oracle
     w1h, w2h = w1.cpu(), w2.cpu()
@@ -350,7 +383,7 @@ def our_arm(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="e8_swiglu", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
