@@ -196,6 +196,37 @@ moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, i
 moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T, int E,
                         float alpha, float* loss, moe_stream_t stream);
 
+/* ------------------------------------------------- no-allocation variant --- */
+
+/* moe_dispatch without a caller workspace.  The pages have no counterpart to
+ * this entry point: it exists for callers that cannot allocate device memory
+ * where they run the layer -- a plugin enqueue callback of an inference
+ * engine that must not call cudaMalloc, a process whose device memory is all
+ * handed out by its own pool, a latency-critical loop that cannot take the
+ * device-wide synchronisation an allocation may cause.
+ *
+ * Same arguments, outputs and errors as moe_dispatch, minus ws / ws_bytes.
+ * Its scratch (the per-chunk expert histograms) is a fixed 256 KiB array in
+ * the library's device memory, which every GPU that loads the library holds
+ * until the process exits.  Limit: moe_workspace_bytes(MOE_CALL_DISPATCH,
+ * T, d, E, k, ...) <= 262144, i.e. ceil(T*k / 1024) * E <= 65536 (for
+ * example T*k <= 262144 at E = 256); larger calls return MOE_ERR_WORKSPACE
+ * with a message on stderr and enqueue nothing.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (once per device); make that first call before any stream
+ * capture.  Every call shares the one array and the array keeps the last
+ * call's contents: each call overwrites every histogram cell it reads, so
+ * nothing needs clearing, but calls that overlap on the GPU (different
+ * streams, or different host threads, with no ordering between them) race on
+ * the array and must not be issued. */
+moe_status moe_dispatch_noalloc(const int32_t* topk_idx, const float* topk_gate, int64_t T, int k, int E,
+                                int64_t cap, const void* x, moe_dtype xdt, int d,
+                                int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* slot_row,
+                                int32_t* row_token, float* row_gate, void* x_perm, int32_t* n_dropped,
+                                moe_stream_t stream);
+
 /* ---------------------------------------------------------- diagnostics --- */
 
 /* Synchronises `stream`, then reads and clears the device status word of the

@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "dispatch", "expert_up",
-    "expert_down", "expert_ffn", "combine", "aux_loss", "check", "set_wait_limit", "selftest_wait_timeout",
+    "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
@@ -63,6 +63,8 @@ _SIGS = {
                               _P]),
     "moe_combine": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P]),
     "moe_aux_loss": (_I32, [_P, _P, _I64, _I32, _F, _P, _P]),
+    "moe_dispatch_noalloc": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P]),
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
     "moe_selftest_wait_timeout": (_I32, [_P]),
@@ -196,6 +198,29 @@ def dispatch(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatch
                                            _ptr(out.counts), _ptr(out.kept), _ptr(out.offsets), _ptr(out.slot_row),
                                            _ptr(out.row_token), _ptr(out.row_gate), _ptr(out.x_perm),
                                            _ptr(out.n_dropped), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def dispatch_noalloc(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatched] = None,
+                     stream=None) -> Dispatched:
+    """moe_dispatch_noalloc: dispatch with the library's built-in scratch
+    instead of a workspace (for callers that cannot allocate device memory
+    where they run the layer).  Outputs are allocated here only when ``out``
+    is None; pass ``out`` to allocate nothing."""
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    dev = x.device
+    R = perm_rows_max(T, k, E, cap)
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = Dispatched(torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                         torch.empty((T, k), **i32), torch.empty(max(R, 1), **i32),
+                         torch.empty(max(R, 1), dtype=torch.float32, device=dev),
+                         torch.empty((max(R, 1), d), dtype=x.dtype, device=dev), torch.empty(1, **i32), R)
+    _ok("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
+        _ptr(topk_idx), _ptr(topk_gate), T, k, E, cap, _ptr(x), _dt(x), d, _ptr(out.counts), _ptr(out.kept),
+        _ptr(out.offsets), _ptr(out.slot_row), _ptr(out.row_token), _ptr(out.row_gate), _ptr(out.x_perm),
+        _ptr(out.n_dropped), _stream(stream)))
     return out
 
 

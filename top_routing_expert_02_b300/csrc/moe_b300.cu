@@ -406,3 +406,67 @@ moe_status moe_selftest_wait_timeout(moe_stream_t stream_)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- dispatch without allocation
+// Some callers cannot allocate device memory at the point where they run the
+// layer: an inference engine's plugin enqueue callback that must not call
+// cudaMalloc, a process whose device memory is handed out entirely by its
+// own pool, or a latency-critical loop that cannot afford the device-wide
+// synchronisation cudaMalloc may cause.  moe_dispatch_noalloc gives them the
+// dispatch step with its scratch (the per-chunk expert histograms) in the
+// fixed array below instead of a caller-provided workspace.
+namespace {
+constexpr size_t NOALLOC_SCRATCH_BYTES = 256u * 1024u;   // 64 Ki int32 histogram cells
+constexpr int NOALLOC_MAX_DEVICES = 64;
+// Every GPU that loads this library holds these 256 KiB until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+
+// Device address of the array on the current device, looked up once per device
+// with that device current.  (In host code the array's name is only a host-side
+// stand-in, not a device address.)
+moe_status noalloc_scratch(void** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return launch_status();
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            std::fprintf(stderr, "moe_dispatch_noalloc: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(e));
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+extern "C" moe_status moe_dispatch_noalloc(const int32_t* topk_idx, const float* topk_gate, int64_t T, int k, int E,
+                                           int64_t cap, const void* x, moe_dtype xdt, int d, int32_t* counts,
+                                           int32_t* kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+                                           float* row_gate, void* x_perm, int32_t* n_dropped, moe_stream_t stream)
+{
+    if (T < 0 || T > INT_MAX || k < 1 || k > MAX_K || E < 1 || E > MAX_E) return MOE_ERR_INVALID_ARG;
+    const size_t need = dispatch_ws_bytes(T, k, E);
+    if (need > NOALLOC_SCRATCH_BYTES) {
+        std::fprintf(stderr,
+                     "moe_dispatch_noalloc: T*k = %lld assignments over E = %d experts need %zu bytes of "
+                     "scratch; the built-in scratch holds %zu bytes (use moe_dispatch with a workspace)\n",
+                     (long long)T * k, E, need, NOALLOC_SCRATCH_BYTES);
+        return MOE_ERR_WORKSPACE;
+    }
+    void* scratch = nullptr;
+    if (need > 0) {
+        const moe_status st = noalloc_scratch(&scratch);
+        if (st != MOE_OK) return st;
+    }
+    return moe_dispatch(topk_idx, topk_gate, T, k, E, cap, x, xdt, d, counts, kept, offsets, slot_row, row_token,
+                        row_gate, x_perm, n_dropped, scratch, NOALLOC_SCRATCH_BYTES, stream);
+}
