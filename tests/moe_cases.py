@@ -3,7 +3,11 @@ path through the C ABI, run the oracle, compare.
 
 Bars (written here once, used by every parity test):
   routing indices, counts, kept, offsets, slot places, drops: bit-exact
-  gates, prob sums, aux loss:         relative error <= 1e-5
+  gates, prob sums, aux loss:         relative error <= 1e-5 for fp32 x (router logits are
+                                      one fp32 FMA chain each), <= 2e-4 for bf16 x (tensor-core
+                                      router: d/16 accumulation steps of at most 2^-23 relative
+                                      error each, about 1e-4 absolute on a logit of size ~1.5 at
+                                      d = 4096; a gate inherits at most twice that relatively)
   layer output y:                     relative Frobenius error <= 1e-5 (fp32 layer),
                                       <= 2e-2 (bf16 layer)
 """
@@ -16,7 +20,7 @@ import oracle
 import top_routing_expert_02_b300 as moe
 from top_routing_expert_02_b300 import synth
 
-GATE_RTOL = 1e-5
+GATE_RTOL = {"f32": 1e-5, "bf16": 2e-4}
 Y_TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
@@ -55,13 +59,15 @@ def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
 
 
-def compare_routing(plan, ref):
+def compare_routing(plan, ref, dtype: str):
     idx = plan.topk_idx.cpu().numpy()
     assert np.array_equal(idx, ref["idx"]), "top-k indices differ"
     g = plan.topk_gate.cpu().numpy().astype(np.float64)
-    np.testing.assert_allclose(g, ref["gate"], rtol=GATE_RTOL, atol=0)
-    np.testing.assert_allclose(plan.prob_sum.cpu().numpy().astype(np.float64), ref["prob_sum"], rtol=GATE_RTOL,
-                               atol=1e-30)
+    ps = plan.prob_sum.cpu().numpy().astype(np.float64)
+    print(f"[parity] gate max rel err {np.max(np.abs(g - ref['gate']) / np.abs(ref['gate'])):.3e}, "
+          f"prob_sum max rel err {np.max(np.abs(ps - ref['prob_sum']) / np.maximum(np.abs(ref['prob_sum']), 1e-300)):.3e}")
+    np.testing.assert_allclose(g, ref["gate"], rtol=GATE_RTOL[dtype], atol=0)
+    np.testing.assert_allclose(ps, ref["prob_sum"], rtol=GATE_RTOL[dtype], atol=1e-30)
 
 
 def compare_dispatch(plan, ref, x_h=None, check_rows=256):
@@ -94,7 +100,9 @@ def compare_output(plan, ref, dtype: str):
     toks = torch.from_numpy(ref["tokens"]).long().to(plan.y.device)
     y = plan.y[toks].float().cpu().numpy().astype(np.float64)
     err = rel_fro(y, ref["y"])
+    print(f"[parity] y rel Frobenius err {err:.3e} over {len(ref['tokens'])} tokens; "
+          f"loss {float(plan.loss.item()):.7f} vs {ref['loss']:.7f}")
     assert err <= Y_TOL[dtype], f"relative Frobenius error {err:.3e} > {Y_TOL[dtype]}"
     loss = float(plan.loss.item())
-    assert abs(loss - ref["loss"]) <= GATE_RTOL * abs(ref["loss"]) + 1e-12, (loss, ref["loss"])
+    assert abs(loss - ref["loss"]) <= GATE_RTOL[dtype] * abs(ref["loss"]) + 1e-12, (loss, ref["loss"])
     return err

@@ -28,6 +28,12 @@ SMALL = {
     "gelu_e32_norenorm": C("gelu_e32_norenorm", 900, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False),
     # fp32 x with E=200 (8 experts per lane), through the fp32 FFN
     "f32_e200": C("f32_e200", 400, 128, 200, 3, 128, "swiglu", 2.0, "f32"),
+    # bf16 x with E=200: above the tensor-core router's 160 experts -> CUDA-core router
+    "bf16_e200": C("bf16_e200", 257, 128, 200, 2, 128, "gelu", 0.0, "bf16"),
+    # bf16, E=160 (largest tensor-core router: two 240-column MMAs), top-16
+    "bf16_e160_top16": C("bf16_e160_top16", 300, 192, 160, 16, 128, "swiglu", 0.0, "bf16", renorm=False),
+    # fewer tokens than one 128-row tile, and fewer kept rows than one GEMM tile
+    "small_T": C("small_T", 50, 128, 8, 2, 128, "swiglu", 1.25, "bf16"),
 }
 
 
@@ -42,7 +48,7 @@ def test_tiny_fp32_layer_full():
     case = make_case(synth.workload("tiny_fp32"))
     plan = run_gpu(case)
     ref = run_oracle(case)
-    compare_routing(plan, ref)
+    compare_routing(plan, ref, "f32")
     compare_dispatch(plan, ref, case["x_h"])
     assert ref["n_dropped"] > 0
     compare_output(plan, ref, "f32")
@@ -54,7 +60,7 @@ def test_small_layers_full(name):
     case = make_case(cfg)
     plan = run_gpu(case)
     ref = run_oracle(case)
-    compare_routing(plan, ref)
+    compare_routing(plan, ref, cfg.dtype)
     compare_dispatch(plan, ref, case["x_h"])
     compare_output(plan, ref, cfg.dtype)
 
@@ -106,7 +112,7 @@ def test_capacity_zero_drops_everything():
     assert (plan.disp.kept.cpu() == 0).all() and (plan.disp.slot_row.cpu() == -1).all()
     assert torch.count_nonzero(plan.y).item() == 0
     ref = run_oracle(case, tokens=[0])
-    assert abs(plan.loss.item() - ref["loss"]) <= 1e-5 * ref["loss"]
+    assert abs(plan.loss.item() - ref["loss"]) <= 2e-4 * ref["loss"]
 
 
 def test_single_expert_dense_layer():
@@ -114,7 +120,7 @@ def test_single_expert_dense_layer():
     case = make_case(cfg)
     plan = run_gpu(case)
     ref = run_oracle(case)
-    compare_routing(plan, ref)
+    compare_routing(plan, ref, "bf16")
     compare_dispatch(plan, ref)
     compare_output(plan, ref, "bf16")
 
@@ -137,6 +143,7 @@ def test_exact_ties_go_to_lower_index(xdtype):
     idx, gate, ps = moe.route(case["x"], case["W"], None, k)
     ref_idx, ref_gate, ref_ps = oracle.route(oracle.router_logits(ri.x, ri.W), k)
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    # one-hot x: every logit is an exact table entry on both paths
     np.testing.assert_allclose(gate.cpu().numpy(), ref_gate, rtol=1e-5)
     np.testing.assert_allclose(ps.cpu().numpy(), ref_ps, rtol=1e-5)
 

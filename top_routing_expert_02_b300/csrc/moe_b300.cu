@@ -15,6 +15,7 @@
 #include "ffn_simt.cuh"
 #include "ffn_tc.cuh"
 #include "route.cuh"
+#include "route_tc.cuh"
 
 namespace {
 
@@ -48,10 +49,48 @@ int sm_count()
 inline int route_epl(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8; }
 inline int route_tw(int E) { return route_epl(E) == 1 ? 2 : 4; }
 inline int route_tokens_per_block(int E) { return route::WARPS * route_tw(E); }
-inline size_t route_ws_bytes(long long T, int E)
+inline size_t route_ws_bytes_simt(long long T, int E)
 {
     const long long nblk = (T + route_tokens_per_block(E) - 1) / route_tokens_per_block(E);
     return (size_t)nblk * E * sizeof(float);
+}
+
+// Tensor-core router shape: E_pad experts per weight part, one or two MMAs of nb_rows.
+struct RouteTcShape {
+    int E_pad, nb_chunks, nb_rows;
+    uint32_t tmem_cols;
+};
+inline bool route_tc_shape(int E, RouteTcShape* s)
+{
+    if (E > rtc::MAX_EPAD) return false;
+    int ep = (E + 15) / 16 * 16;
+    if (3 * ep <= 256) {
+        s->E_pad = ep;
+        s->nb_chunks = 1;
+        s->nb_rows = 3 * ep;
+    } else {
+        ep = (E + 31) / 32 * 32;
+        s->E_pad = ep;
+        s->nb_chunks = 2;
+        s->nb_rows = 3 * ep / 2;
+    }
+    uint32_t c = 32;
+    while (c < (uint32_t)(3 * s->E_pad)) c <<= 1;
+    s->tmem_cols = c;
+    return true;
+}
+inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+inline size_t route_ws_bytes_tc(long long T, int d, int E)
+{
+    RouteTcShape sh;
+    if (T <= 0 || !route_tc_shape(E, &sh)) return 0;
+    const long long nblk = (T + rtc::BM - 1) / rtc::BM;
+    return align256((size_t)3 * sh.E_pad * d * 2) + (size_t)nblk * E * sizeof(float);
+}
+inline size_t route_ws_bytes(long long T, int d, int E)
+{
+    const size_t a = route_ws_bytes_simt(T, E), b = route_ws_bytes_tc(T, d, E);
+    return a > b ? a : b;
 }
 inline long long dispatch_chunks(long long T, int k) { return (T * k + dispatch::CHUNK - 1) / dispatch::CHUNK; }
 inline size_t dispatch_ws_bytes(long long T, int k, int E) { return (size_t)dispatch_chunks(T, k) * E * sizeof(int); }
@@ -76,19 +115,35 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// bf16 matrix [rows, cols] (cols contiguous), boxes of 64 columns x 128 rows,
-// 128-byte swizzle, zero fill outside.
-bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols)
+// bf16 matrix [rows, cols] (cols contiguous), boxes of 64 columns x box_rows
+// rows, 128-byte swizzle, zero fill outside.
+bool make_tmap_bf16_box(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols,
+                        unsigned box_rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols)
+{
+    return make_tmap_bf16_box(m, base, rows, cols, 128);
+}
+
+template <int KMAX>
+moe_status launch_route_tc(int nblk, int smem, const CUtensorMap& tx, const CUtensorMap& tw, const rtc::Args& a,
+                           cudaStream_t stream)
+{
+    if (cudaFuncSetAttribute(rtc::route_tc_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return launch_status();
+    rtc::route_tc_kernel<KMAX><<<nblk, rtc::THREADS, smem, stream>>>(tx, tw, a);
+    return launch_status();
 }
 
 template <int EPI>
@@ -179,13 +234,12 @@ int64_t moe_perm_rows_max(int64_t T, int k, int E, int64_t cap)
 
 size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F, moe_act act, moe_dtype dtype)
 {
-    (void)d;
     (void)F;
     (void)act;
     (void)dtype;
-    if (T < 0 || E < 1 || E > MAX_E || k < 1) return 0;
+    if (T < 0 || E < 1 || E > MAX_E || k < 1 || d < 0) return 0;
     switch (call) {
-    case MOE_CALL_ROUTE: return route_ws_bytes(T, E);
+    case MOE_CALL_ROUTE: return route_ws_bytes(T, d, E);
     case MOE_CALL_DISPATCH: return dispatch_ws_bytes(T, k, E);
     case MOE_CALL_FFN: return 0;
     }
@@ -202,8 +256,58 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
     if (T * k >= INT_MAX || (long long)T * d >= (1LL << 40)) return MOE_ERR_INVALID_ARG;
     if (!prob_sum || (T > 0 && (!x || !w_router || !topk_idx || !topk_gate))) return MOE_ERR_INVALID_ARG;
     if (d % 64) return MOE_ERR_UNSUPPORTED;
-    const size_t need = route_ws_bytes(T, E);
+    const size_t need = route_ws_bytes(T, d, E);
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+    RouteTcShape sh;
+    if (xdt == MOE_BF16 && T > 0 && route_tc_shape(E, &sh)) {
+        // tensor-core router: split weights, then one block per 128 tokens
+        uint16_t* Ws = (uint16_t*)ws;
+        float* partial = (float*)((char*)ws + align256((size_t)3 * sh.E_pad * d * 2));
+        const int nblk = (int)((T + rtc::BM - 1) / rtc::BM);
+        const long long nsplit = (long long)sh.E_pad * d;
+        int sgrid = (int)((nsplit + 255) / 256);
+        if (sgrid > sm_count() * 4) sgrid = sm_count() * 4;
+        rtc::split_weight_kernel<<<sgrid, 256, 0, stream>>>(w_router, E, sh.E_pad, d, Ws);
+        moe_status st = launch_status();
+        if (st != MOE_OK) return st;
+        CUtensorMap tx, tw;
+        if (!make_tmap_bf16_box(&tx, x, (unsigned long long)T, (unsigned long long)d, 128)) return MOE_ERR_CUDA;
+        if (!make_tmap_bf16_box(&tw, Ws, (unsigned long long)(3 * sh.E_pad), (unsigned long long)d,
+                                (unsigned)sh.nb_rows))
+            return MOE_ERR_CUDA;
+        rtc::Args a{};
+        a.bias = b_router;
+        a.T = (int)T;
+        a.E = E;
+        a.E_pad = sh.E_pad;
+        a.k = k;
+        a.renorm = renorm;
+        a.nk = d / rtc::BK;
+        a.nb_chunks = sh.nb_chunks;
+        a.nb_rows = sh.nb_rows;
+        a.stage_bytes = rtc::A_BYTES + 3 * sh.E_pad * 128;
+        const int budget = (nblk <= sm_count() ? 200 : 100) * 1024;
+        int stages = budget / a.stage_bytes;
+        if (stages > rtc::MAX_STAGES) stages = rtc::MAX_STAGES;
+        if (stages > a.nk) stages = a.nk;
+        if (stages < 2) stages = 2;
+        a.stages = stages;
+        a.tmem_cols = sh.tmem_cols;
+        a.idx = topk_idx;
+        a.gate = topk_gate;
+        a.partial = partial;
+        a.wait_limit = g_wait_limit.load();
+        const int smem = stages * a.stage_bytes + 1024;
+        switch (k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16) {
+        case 2: st = launch_route_tc<2>(nblk, smem, tx, tw, a, stream); break;
+        case 4: st = launch_route_tc<4>(nblk, smem, tx, tw, a, stream); break;
+        case 8: st = launch_route_tc<8>(nblk, smem, tx, tw, a, stream); break;
+        default: st = launch_route_tc<16>(nblk, smem, tx, tw, a, stream); break;
+        }
+        if (st != MOE_OK) return st;
+        route::route_finalize<<<1, route::FIN_THREADS, 0, stream>>>(partial, nblk, E, prob_sum);
+        return launch_status();
+    }
     const int tpb = route_tokens_per_block(E);
     const int nblk = (int)((T + tpb - 1) / tpb);
     float* partial = (float*)ws;
