@@ -154,6 +154,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             }
         }
+        __syncwarp();   // reconverge before the block-wide barrier below
     } else if (warp == 1) {
         if (lane == 0) {
             int stage = 0, acc = 0;
@@ -193,6 +194,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ptx::mma_commit(ptx::smem_u32(&drain_bar));
             if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, limit)) moe_flag(MOE_DEV_TIMEOUT);
         }
+        __syncwarp();   // reconverge before the block-wide barrier below
     } else {
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int r_in = q * 32 + lane;    // row of the tile owned by this thread

@@ -80,12 +80,44 @@ inline bool route_tc_shape(int E, RouteTcShape* s)
     return true;
 }
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+// Blocks per 128-token tile: split d so that small batches still fill the GPU
+// (148 SMs), at most 16 ways and never below one K block of 64 per split.
+inline int route_tc_splits(long long ntiles, int d)
+{
+    const int nk = d / rtc::BK;
+    long long S = (148 + ntiles - 1) / (ntiles > 0 ? ntiles : 1);
+    if (S > rtc::MAX_SPLITS) S = rtc::MAX_SPLITS;
+    if (S > nk) S = nk;
+    return S < 1 ? 1 : (int)S;
+}
+// Blocks of the finishing kernel: one lane per token for E <= 32, else one warp
+// per token; up to four blocks per SM (many warps hide the shuffle latency).
+inline int route_fin_blocks(long long T, int E)
+{
+    const long long per_block = E <= 32 ? rtc::FIN_THREADS : rtc::FIN_WARPS;
+    const long long b = (T + per_block - 1) / per_block;
+    return (int)(b < 592 ? (b > 0 ? b : 1) : 592);
+}
+struct RouteTcWs {
+    size_t ws_off, part_off, psum_off, cnt_off, total;
+};
+inline RouteTcWs route_tc_ws(long long T, int d, int E, const RouteTcShape& sh)
+{
+    const long long ntiles = (T + rtc::BM - 1) / rtc::BM;
+    const int S = route_tc_splits(ntiles, d);
+    RouteTcWs w;
+    w.ws_off = 0;
+    w.part_off = align256((size_t)3 * sh.E_pad * d * 2);
+    w.psum_off = w.part_off + align256((size_t)S * T * sh.E_pad * sizeof(float));
+    w.cnt_off = w.psum_off + align256((size_t)route_fin_blocks(T, E) * E * sizeof(float));
+    w.total = w.cnt_off;
+    return w;
+}
 inline size_t route_ws_bytes_tc(long long T, int d, int E)
 {
     RouteTcShape sh;
     if (T <= 0 || !route_tc_shape(E, &sh)) return 0;
-    const long long nblk = (T + rtc::BM - 1) / rtc::BM;
-    return align256((size_t)3 * sh.E_pad * d * 2) + (size_t)nblk * E * sizeof(float);
+    return route_tc_ws(T, d, E, sh).total;
 }
 inline size_t route_ws_bytes(long long T, int d, int E)
 {
@@ -94,6 +126,34 @@ inline size_t route_ws_bytes(long long T, int d, int E)
 }
 inline long long dispatch_chunks(long long T, int k) { return (T * k + dispatch::CHUNK - 1) / dispatch::CHUNK; }
 inline size_t dispatch_ws_bytes(long long T, int k, int E) { return (size_t)dispatch_chunks(T, k) * E * sizeof(int); }
+
+
+// Opt a kernel into `bytes` of dynamic shared memory once per device (the
+// attribute is per device; setting it again on every launch is wasted host time).
+bool ensure_dyn_smem(const void* kernel, int bytes)
+{
+    struct Entry {
+        const void* k;
+        int dev;
+        int bytes;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int n_done = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].k == kernel && done[i].dev == dev && done[i].bytes >= bytes) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].k == kernel && done[i].dev == dev) {
+            done[i].bytes = bytes;
+            return true;
+        }
+    if (n_done < 256) done[n_done++] = Entry{kernel, dev, bytes};
+    return true;
+}
 
 // ---------------------------------------------------------- TMA descriptors
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -135,17 +195,6 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, u
     return make_tmap_bf16_box(m, base, rows, cols, 128);
 }
 
-template <int KMAX>
-moe_status launch_route_tc(int nblk, int smem, const CUtensorMap& tx, const CUtensorMap& tw, const rtc::Args& a,
-                           cudaStream_t stream)
-{
-    if (cudaFuncSetAttribute(rtc::route_tc_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return launch_status();
-    rtc::route_tc_kernel<KMAX><<<nblk, rtc::THREADS, smem, stream>>>(tx, tw, a);
-    return launch_status();
-}
-
 template <int EPI>
 moe_status launch_tc(const void* A, long long rows_max, int K, const void* W, long long w_rows_total,
                      const tcg::Args& args, cudaStream_t stream)
@@ -153,10 +202,7 @@ moe_status launch_tc(const void* A, long long rows_max, int K, const void* W, lo
     CUtensorMap ta, tb;
     if (!make_tmap_bf16(&ta, A, (unsigned long long)rows_max, (unsigned long long)K)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K)) return MOE_ERR_CUDA;
-    // per-device attribute; cheap, so set on every launch
-    if (cudaFuncSetAttribute(tcg::grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tcg::SMEM_DYN) != cudaSuccess)
-        return launch_status();
+    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI>, tcg::SMEM_DYN)) return launch_status();
     const long long max_mtiles = (rows_max + tcg::BM - 1) / tcg::BM + args.E;
     const long long max_tiles = max_mtiles * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
@@ -260,10 +306,14 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
     RouteTcShape sh;
     if (xdt == MOE_BF16 && T > 0 && route_tc_shape(E, &sh)) {
-        // tensor-core router: split weights, then one block per 128 tokens
-        uint16_t* Ws = (uint16_t*)ws;
-        float* partial = (float*)((char*)ws + align256((size_t)3 * sh.E_pad * d * 2));
-        const int nblk = (int)((T + rtc::BM - 1) / rtc::BM);
+        // tensor-core router: split weights, partial logits, softmax / top-k per token
+        // with per-block probability sums, then the sums over blocks
+        const RouteTcWs wl = route_tc_ws(T, d, E, sh);
+        uint16_t* Ws = (uint16_t*)((char*)ws + wl.ws_off);
+        float* part = (float*)((char*)ws + wl.part_off);
+        float* psum = (float*)((char*)ws + wl.psum_off);
+        const int ntiles = (int)((T + rtc::BM - 1) / rtc::BM);
+        const int S = route_tc_splits(ntiles, d);
         const long long nsplit = (long long)sh.E_pad * d;
         int sgrid = (int)((nsplit + 255) / 256);
         if (sgrid > sm_count() * 4) sgrid = sm_count() * 4;
@@ -276,36 +326,56 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
                                 (unsigned)sh.nb_rows))
             return MOE_ERR_CUDA;
         rtc::Args a{};
-        a.bias = b_router;
         a.T = (int)T;
-        a.E = E;
         a.E_pad = sh.E_pad;
-        a.k = k;
-        a.renorm = renorm;
         a.nk = d / rtc::BK;
+        a.S = S;
         a.nb_chunks = sh.nb_chunks;
         a.nb_rows = sh.nb_rows;
         a.stage_bytes = rtc::A_BYTES + 3 * sh.E_pad * 128;
-        const int budget = (nblk <= sm_count() ? 200 : 100) * 1024;
+        const int grid = ntiles * S;
+        const int budget = (grid <= sm_count() ? 200 : 100) * 1024;
         int stages = budget / a.stage_bytes;
         if (stages > rtc::MAX_STAGES) stages = rtc::MAX_STAGES;
-        if (stages > a.nk) stages = a.nk;
         if (stages < 2) stages = 2;
         a.stages = stages;
         a.tmem_cols = sh.tmem_cols;
-        a.idx = topk_idx;
-        a.gate = topk_gate;
-        a.partial = partial;
+        a.part = part;
         a.wait_limit = g_wait_limit.load();
         const int smem = stages * a.stage_bytes + 1024;
-        switch (k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16) {
-        case 2: st = launch_route_tc<2>(nblk, smem, tx, tw, a, stream); break;
-        case 4: st = launch_route_tc<4>(nblk, smem, tx, tw, a, stream); break;
-        case 8: st = launch_route_tc<8>(nblk, smem, tx, tw, a, stream); break;
-        default: st = launch_route_tc<16>(nblk, smem, tx, tw, a, stream); break;
-        }
+        if (!ensure_dyn_smem((const void*)rtc::route_logits_kernel, smem)) return launch_status();
+        rtc::route_logits_kernel<<<grid, rtc::THREADS, smem, stream>>>(tx, tw, a);
+        st = launch_status();
         if (st != MOE_OK) return st;
-        route::route_finalize<<<1, route::FIN_THREADS, 0, stream>>>(partial, nblk, E, prob_sum);
+        const int fgrid = route_fin_blocks(T, E);
+        const int Ti = (int)T;
+        const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16;
+#define MOE_FIN_LANE(EM, KM) rtc::route_finish_lane_kernel<EM, KM><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
+    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum)
+#define MOE_FIN_WARP(EP) rtc::route_finish_warp_kernel<EP><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
+    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum)
+        if (E <= 16) {
+            if (kmax == 2) MOE_FIN_LANE(16, 2);
+            else if (kmax == 4) MOE_FIN_LANE(16, 4);
+            else if (kmax == 8) MOE_FIN_LANE(16, 8);
+            else MOE_FIN_LANE(16, 16);
+        } else if (E <= 32) {
+            if (kmax == 2) MOE_FIN_LANE(32, 2);
+            else if (kmax == 4) MOE_FIN_LANE(32, 4);
+            else if (kmax == 8) MOE_FIN_LANE(32, 8);
+            else MOE_FIN_LANE(32, 16);
+        } else if (E <= 64) {
+            MOE_FIN_WARP(2);
+        } else if (E <= 128) {
+            MOE_FIN_WARP(4);
+        } else {
+            MOE_FIN_WARP(8);
+        }
+#undef MOE_FIN_LANE
+#undef MOE_FIN_WARP
+        st = launch_status();
+        if (st != MOE_OK) return st;
+        rtc::prob_sum_kernel<<<E, 256, 0, stream>>>(psum, fgrid, E, prob_sum);
         return launch_status();
     }
     const int tpb = route_tokens_per_block(E);

@@ -13,14 +13,18 @@
 // accuracy at tensor-core speed, and the router stays bound by the HBM read
 // of x at every E (on CUDA cores it is FP32-bound from E of about 16 up).
 //
-// One block per 128 tokens, 6 warps: TMA producer (x tile 128x64 + the
-// stacked weight), one MMA-issuing thread (M=128, N = 3*E_pad in one or two
-// MMAs), 4 epilogue warps with one token per thread: the thread reads its
-// token's accumulator row from TMEM, forms l = (a0 + a1) + a2 + b, and keeps
-// the running max and a sorted top-k list in registers; a second pass sums
-// exp(l - max); a third forms p = exp(l - max) / sum, reduces it over the 128
-// tokens (warp shuffles, then the 4 warps in a fixed order) into this block's
-// row of partial sums.  route_finalize then adds the rows in block order.
+// route_logits_kernel: S blocks per 128-token tile (S > 1 splits d when there
+// are too few tiles to fill the GPU), 6 warps each: TMA producer (x tile
+// 128x64 + the stacked weight), one MMA-issuing thread (M=128, N = 3*E_pad in
+// one or two MMAs), 4 epilogue warps that turn the accumulator row of each
+// token into its partial logits (a0 + a1) + a2 and store them.
+// route_finish_*_kernel: adds each token's S partial rows in split order plus
+// the bias, takes the softmax and the top-k on (logit desc, index asc), and
+// sums the probabilities per block; prob_sum_kernel then adds the block rows
+// with one fixed-shape tree per expert.  E <= 32: one lane per token (all E logits in
+// registers, sorted top-k insertion); larger E: one warp per token (lane l
+// owns experts l, l+32, ...; k rounds of warp argmax).
+// Every sum runs in a fixed order, so the result is the same bits on every run.
 #pragma once
 #include "common.cuh"
 #include "ptx_sm103.cuh"
@@ -30,19 +34,18 @@ namespace rtc {
 constexpr int BM = 128, BK = 64, THREADS = 192, MAX_STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int MAX_EPAD = 160;   // 3 * E_pad <= 480 TMEM columns
+constexpr int MAX_SPLITS = 16;  // blocks per 128-token tile
 
 struct Args {
-    const float* bias;
-    int T, E, E_pad, k, renorm;
-    int nk;          // K blocks of 64
+    int T, E_pad;
+    int nk;          // K blocks of 64 in d
+    int S;           // K splits: blocks per 128-token tile
     int nb_chunks;   // MMAs per K step (1 or 2)
     int nb_rows;     // N of each MMA (rows of one weight box)
     int stages;
     int stage_bytes;
     uint32_t tmem_cols;
-    int32_t* idx;
-    float* gate;
-    float* partial;  // [gridDim.x, E]
+    float* part;     // [S, T, E_pad] partial logits
     unsigned long long wait_limit;
 };
 
@@ -53,7 +56,9 @@ __global__ void split_weight_kernel(const float* __restrict__ W, int E, int E_pa
                                     uint16_t* __restrict__ Ws)
 {
     const long long n = (long long)E_pad * d;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = i0; i < n; i += stride) {
         const int e = (int)(i / d);
         float w = e < E ? __ldg(W + i) : 0.f;
         __nv_bfloat16 b0 = __float2bfloat16_rn(w);
@@ -67,40 +72,20 @@ __global__ void split_weight_kernel(const float* __restrict__ W, int E, int E_pa
     }
 }
 
-// Insert (v, e) into the descending list tv/ti of KMAX entries; an equal
-// value already present stays ahead (it has the lower expert index).
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float v, int e)
-{
-    if (!(v > tv[KMAX - 1])) return;
-#pragma unroll
-    for (int j = KMAX - 1; j > 0; --j) {
-        if (v > tv[j - 1]) {
-            tv[j] = tv[j - 1];
-            ti[j] = ti[j - 1];
-        } else if (v > tv[j]) {
-            tv[j] = v;
-            ti[j] = e;
-        }
-    }
-    if (v > tv[0]) {
-        tv[0] = v;
-        ti[0] = e;
-    }
-}
-
-template <int KMAX>
+// Block (tile, s): tile = blockIdx.x / S covers tokens [128*tile, 128*tile + 128),
+// split s covers K blocks [s*nk/S, (s+1)*nk/S).
 __global__ void __launch_bounds__(THREADS, 1)
-route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Args g)
+route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Args g)
 {
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES], acc_bar;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float red[4][MAX_EPAD];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem0 = (ptx::smem_u32(dsmem) + 1023u) & ~1023u;
-    const int t0 = blockIdx.x * BM;
+    const int tile = blockIdx.x / g.S, split = blockIdx.x - tile * g.S;
+    const int t0 = tile * BM;
+    const int kb0 = (int)((long long)split * g.nk / g.S), kb1 = (int)((long long)(split + 1) * g.nk / g.S);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < g.stages; ++s) {
@@ -129,7 +114,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             uint32_t phase = 0;
             int fills = 0;
             bool ok = true;
-            for (int kb = 0; kb < g.nk; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit)) {
                     ok = false;
                     break;
@@ -153,13 +138,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     break;
                 }
         }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_bf16_f32(128, g.nb_rows);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int kb = 0; kb < g.nk; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, limit)) {
                     ok = false;
                     break;
@@ -171,7 +157,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     for (int c = 0; c < g.nb_chunks; ++c)
                         ptx::mma_bf16(tmem_base + (uint32_t)(c * g.nb_rows), ptx::sdesc_kmajor_sw128(sa + kk * 32),
                                       ptx::sdesc_kmajor_sw128(sb + c * b_box_bytes + kk * 32), idesc,
-                                      (kb | kk) != 0);
+                                      (kb > kb0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
                 if (++stage == g.stages) {
                     stage = 0;
@@ -182,100 +168,35 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             // arrives once every MMA issued above has completed (also on the error path)
             ptx::mma_commit(ptx::smem_u32(&acc_bar));
         }
+        __syncwarp();
     } else {
         const int q = warp & 3;
         const int r = q * 32 + lane;
         const int t = t0 + r;
-        const bool valid = t < g.T;
+        const int Ep = g.E_pad;
         const bool waited = ptx::mbar_wait(ptx::smem_u32(&acc_bar), 0, limit);
-        const bool all_ok = __all_sync(0xffffffffu, waited);
-        if (!all_ok) moe_flag(MOE_DEV_TIMEOUT);
+        if (!__all_sync(0xffffffffu, waited)) moe_flag(MOE_DEV_TIMEOUT);
         ptx::tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
-        const int E = g.E, Ep = g.E_pad;
-
-        float tv[KMAX];
-        int ti[KMAX];
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            tv[j] = -INFINITY;
-            ti[j] = 0x7fffffff;
-        }
-        float mx = -INFINITY;
-        // pass 1: running max and top-k
+        float* row = g.part + ((size_t)split * g.T + t) * Ep;
         for (int e0 = 0; e0 < Ep; e0 += 16) {
             uint32_t a0[16], a1[16], a2[16];
             ptx::tmem_ld16(tb + e0, a0);
             ptx::tmem_ld16(tb + Ep + e0, a1);
             ptx::tmem_ld16(tb + 2 * Ep + e0, a2);
             ptx::tmem_ld_wait();
+            if (t < g.T) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int e = e0 + i;
-                if (e < E) {
-                    const float l = (__uint_as_float(a0[i]) + __uint_as_float(a1[i])) + __uint_as_float(a2[i]) +
-                                    (g.bias ? __ldg(g.bias + e) : 0.f);
-                    mx = fmaxf(mx, l);
-                    topk_insert<KMAX>(tv, ti, l, e);
+                for (int i = 0; i < 16; i += 4) {
+                    float4 v;
+                    v.x = (__uint_as_float(a0[i]) + __uint_as_float(a1[i])) + __uint_as_float(a2[i]);
+                    v.y = (__uint_as_float(a0[i + 1]) + __uint_as_float(a1[i + 1])) + __uint_as_float(a2[i + 1]);
+                    v.z = (__uint_as_float(a0[i + 2]) + __uint_as_float(a1[i + 2])) + __uint_as_float(a2[i + 2]);
+                    v.w = (__uint_as_float(a0[i + 3]) + __uint_as_float(a1[i + 3])) + __uint_as_float(a2[i + 3]);
+                    *reinterpret_cast<float4*>(row + e0 + i) = v;
                 }
             }
         }
-        // pass 2: softmax denominator
-        float s = 0.f;
-        for (int e0 = 0; e0 < Ep; e0 += 16) {
-            uint32_t a0[16], a1[16], a2[16];
-            ptx::tmem_ld16(tb + e0, a0);
-            ptx::tmem_ld16(tb + Ep + e0, a1);
-            ptx::tmem_ld16(tb + 2 * Ep + e0, a2);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int e = e0 + i;
-                if (e < E) {
-                    const float l = (__uint_as_float(a0[i]) + __uint_as_float(a1[i])) + __uint_as_float(a2[i]) +
-                                    (g.bias ? __ldg(g.bias + e) : 0.f);
-                    s += expf(l - mx);
-                }
-            }
-        }
-        // pass 3: probabilities, summed over this block's tokens per expert
-        for (int e0 = 0; e0 < Ep; e0 += 16) {
-            uint32_t a0[16], a1[16], a2[16];
-            ptx::tmem_ld16(tb + e0, a0);
-            ptx::tmem_ld16(tb + Ep + e0, a1);
-            ptx::tmem_ld16(tb + 2 * Ep + e0, a2);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int e = e0 + i;
-                float p = 0.f;
-                if (e < E && valid) {
-                    const float l = (__uint_as_float(a0[i]) + __uint_as_float(a1[i])) + __uint_as_float(a2[i]) +
-                                    (g.bias ? __ldg(g.bias + e) : 0.f);
-                    p = expf(l - mx) / s;
-                }
-#pragma unroll
-                for (int o = 16; o; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                if (lane == 0) red[q][e] = p;
-            }
-        }
-        if (valid) {
-            float chosen = 0.f;
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < g.k) chosen += expf(tv[j] - mx) / s;
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < g.k) {
-                    const float pj = expf(tv[j] - mx) / s;
-                    g.idx[(size_t)t * g.k + j] = ti[j];
-                    g.gate[(size_t)t * g.k + j] = g.renorm ? pj / chosen : pj;
-                }
-        }
-        ptx::tc_fence_before();
-        ptx::named_bar_sync(1, 128);
-        for (int e = r; e < E; e += 128)
-            g.partial[(size_t)blockIdx.x * E + e] = ((red[0][e] + red[1][e]) + red[2][e]) + red[3][e];
     }
 
     ptx::tc_fence_before();
@@ -284,6 +205,241 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, g.tmem_cols);
     }
+}
+
+constexpr int FIN_THREADS = 256;
+constexpr int FIN_WARPS = FIN_THREADS / 32;
+
+// Sum of the S partial logits of token t, expert e, in split order (loads first).
+__device__ __forceinline__ float sum_splits(const float* __restrict__ part, int S, int T, int E_pad, int t, int e)
+{
+    float v[MAX_SPLITS];
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s)
+        if (s < S) v[s] = __ldcg(part + ((size_t)s * T + t) * E_pad + e);
+    float acc = v[0];
+#pragma unroll
+    for (int s = 1; s < MAX_SPLITS; ++s)
+        if (s < S) acc += v[s];
+    return acc;
+}
+
+// Per-block probability sums (rows in warp order) -> psum[block].
+__device__ __forceinline__ void block_prob_sums(float (*red)[256], int E, float* __restrict__ psum)
+{
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += FIN_THREADS) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < FIN_WARPS; ++w) v += red[w][e];
+        psum[(size_t)blockIdx.x * E + e] = v;
+    }
+}
+
+// prob_sum[e] = sum over the R block rows of psum[:, e]: one block per expert,
+// a fixed-shape tree (strided fp64 partial sums, then a shared-memory tree).
+__global__ void __launch_bounds__(256) prob_sum_kernel(const float* __restrict__ psum, int R, int E,
+                                                       float* __restrict__ prob_sum)
+{
+    __shared__ double sh[256];
+    const int e = blockIdx.x;
+    double acc = 0.0;
+    for (int b = threadIdx.x; b < R; b += 256) acc += (double)__ldg(psum + (size_t)b * E + e);
+    sh[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) prob_sum[e] = (float)sh[0];
+}
+
+// E <= 32: one lane per token, its E logits in registers.
+template <int EMAX, int KMAX>
+__global__ void __launch_bounds__(FIN_THREADS)
+route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, int E_pad, int k, int renorm,
+                         const float* __restrict__ bias, int32_t* __restrict__ idx_out,
+                         float* __restrict__ gate_out, float* __restrict__ psum)
+{
+    __shared__ float red[FIN_WARPS][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float bia[EMAX], acc_p[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        bia[e] = (bias && e < E) ? __ldg(bias + e) : 0.f;
+        acc_p[e] = 0.f;
+    }
+    for (int t = (blockIdx.x * FIN_WARPS + warp) * 32 + lane; t < T; t += gridDim.x * FIN_THREADS) {
+        float l[EMAX];
+#pragma unroll
+        for (int e4 = 0; e4 < EMAX; e4 += 4) {
+            float4 v[MAX_SPLITS];
+#pragma unroll
+            for (int s = 0; s < MAX_SPLITS; ++s)
+                if (s < S && e4 < E_pad)
+                    v[s] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)s * T + t) * E_pad + e4));
+            float4 a = v[0];
+#pragma unroll
+            for (int s = 1; s < MAX_SPLITS; ++s)
+                if (s < S) {
+                    a.x += v[s].x;
+                    a.y += v[s].y;
+                    a.z += v[s].z;
+                    a.w += v[s].w;
+                }
+            l[e4] = a.x;
+            l[e4 + 1] = a.y;
+            l[e4 + 2] = a.z;
+            l[e4 + 3] = a.w;
+        }
+        float tv[KMAX];
+        int ti[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            tv[j] = -INFINITY;
+            ti[j] = 0x7fffffff;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            l[e] = (e < E) ? l[e] + bia[e] : -INFINITY;
+            mx = fmaxf(mx, l[e]);
+            if (e < E) {
+                // insert into the descending top list; equal values keep the lower index ahead
+                const float v = l[e];
+                if (v > tv[KMAX - 1]) {
+#pragma unroll
+                    for (int j = KMAX - 1; j > 0; --j) {
+                        if (v > tv[j - 1]) {
+                            tv[j] = tv[j - 1];
+                            ti[j] = ti[j - 1];
+                        } else if (v > tv[j]) {
+                            tv[j] = v;
+                            ti[j] = e;
+                        }
+                    }
+                    if (v > tv[0]) {
+                        tv[0] = v;
+                        ti[0] = e;
+                    }
+                }
+            }
+        }
+        float p[EMAX], s = 0.f;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            p[e] = (e < E) ? expf(l[e] - mx) : 0.f;
+            s += p[e];
+        }
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc_p[e] += p[e] / s;
+        float chosen = 0.f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            if (j < k) chosen += expf(tv[j] - mx) / s;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            if (j < k) {
+                const float pj = expf(tv[j] - mx) / s;
+                idx_out[(size_t)t * k + j] = ti[j];
+                gate_out[(size_t)t * k + j] = renorm ? pj / chosen : pj;
+            }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        float v = acc_p[e];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[warp][e] = v;
+    }
+    block_prob_sums(red, E, psum);
+}
+
+// E > 32: one warp per token, lane l owns experts l, l+32, ...
+template <int EPL>
+__global__ void __launch_bounds__(FIN_THREADS)
+route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, int E_pad, int k, int renorm,
+                         const float* __restrict__ bias, int32_t* __restrict__ idx_out,
+                         float* __restrict__ gate_out, float* __restrict__ psum)
+{
+    __shared__ float red[FIN_WARPS][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float bia[EPL], acc_p[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        bia[i] = (bias && e < E) ? __ldg(bias + e) : 0.f;
+        acc_p[i] = 0.f;
+    }
+    for (int t = blockIdx.x * FIN_WARPS + warp; t < T; t += gridDim.x * FIN_WARPS) {
+        float l[EPL];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            l[i] = (e < E) ? sum_splits(part, S, T, E_pad, t, e) + bia[i] : -INFINITY;
+            mx = fmaxf(mx, l[i]);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float p[EPL], s = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            p[i] = (lane + 32 * i < E) ? expf(l[i] - mx) : 0.f;
+            s += p[i];
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            p[i] = p[i] / s;
+            acc_p[i] += p[i];
+        }
+        unsigned taken = 0;
+        int my_e = 0;
+        float my_p = 0.f, chosen = 0.f;
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u) && (l[i] > bv || (l[i] == bv && e < bi))) {
+                    bv = l[i];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            float pv = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (lane + 32 * i == bi) {
+                    pv = p[i];
+                    taken |= 1u << i;
+                }
+            const float pw = __shfl_sync(0xffffffffu, pv, bi & 31);
+            chosen += pw;
+            if (lane == j) {
+                my_e = bi;
+                my_p = pw;
+            }
+        }
+        if (lane < k) {
+            idx_out[(size_t)t * k + lane] = my_e;
+            gate_out[(size_t)t * k + lane] = renorm ? my_p / chosen : my_p;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) red[warp][lane + 32 * i] = acc_p[i];
+    block_prob_sums(red, E, psum);
 }
 
 }  // namespace rtc

@@ -100,6 +100,10 @@ WORKLOADS = {
 # small profiling case of the e8 SwiGLU layer (d_ff 2048): weights 400 MB, still
 # larger than L2, short kernels, so a full ncu capture stays small
 WORKLOADS["prof_e8_swiglu_F2048"] = _mk("prof_e8_swiglu_F2048", 4096, 4096, 8, 2, 2048, "swiglu", 1.25, "bf16")
+# router profiling cases: x above L2 (134 / 268 MB), small experts
+WORKLOADS["prof_route_e8_T32768"] = _mk("prof_route_e8_T32768", 32768, 4096, 8, 2, 128, "swiglu", 1.25, "bf16")
+WORKLOADS["prof_route_e128_T16384"] = _mk("prof_route_e128_T16384", 16384, 4096, 128, 8, 128, "swiglu", 1.25,
+                                          "bf16")
 for _T in (512, 2048, 8192, 32768):
     WORKLOADS[f"e128_top8_T{_T}"] = _mk(f"e128_top8_T{_T}", _T, 4096, 128, 8, 1536,
                                         "swiglu", 0.0, "bf16")
