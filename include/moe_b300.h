@@ -240,6 +240,18 @@ moe_status moe_check(moe_stream_t stream);
  * its kernel winds down cleanly.  0 restores the default. */
 void moe_set_wait_limit(uint64_t cycles);
 
+/* Kernel family of the bf16 expert GEMMs: 0 (default) automatic, 1 one SM
+ * per 128-token x 256-column tile, 2 CTA pairs (two SMs per 256-weight-row x
+ * up-to-256-token tile).  Process-wide; for tests and tuning.
+ * MOE_ERR_INVALID_ARG for any other value. */
+moe_status moe_set_gemm_kernel(int kind);
+
+/* Output-tile width of the one-SM bf16 expert GEMMs: 128, 192 or 256 columns, or 0
+ * (the default) to pick per call the width whose tiles best fill whole waves
+ * of the SMs.  Process-wide; for tests and tuning.  MOE_ERR_INVALID_ARG for
+ * any other value. */
+moe_status moe_set_gemm_tile_n(int bn);
+
 /* Launches one block that waits, under the current limit, on a barrier that
  * nothing ever completes, so that a test can watch the time-limit path end
  * in MOE_ERR_TIMEOUT from moe_check() with the context still usable. */

@@ -109,6 +109,13 @@ def test_dispatch_ffn_combine_aux_argument_errors():
     assert L.moe_aux_loss(F_, F_, 16, 8, ctypes.c_float(0.01), None, None) == 1
 
 
+def test_gemm_tile_width_setter_validates():
+    L = moe.lib()
+    assert L.moe_set_gemm_tile_n(100) == 1
+    assert L.moe_set_gemm_tile_n(192) == 0
+    assert L.moe_set_gemm_tile_n(0) == 0
+
+
 def test_binding_rejects_unsupported_dtype():
     import torch
     x = torch.zeros(4, 64, dtype=torch.float16)

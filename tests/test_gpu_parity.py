@@ -87,6 +87,44 @@ def test_expert_up_and_down_against_torch():
         assert rel_fro(yp[r0:r1].numpy(), yref.numpy()) < 1e-2
 
 
+@pytest.mark.parametrize("bn", [128, 192, 256])
+@pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot"])
+def test_every_gemm_tile_width(name, bn):
+    """Each output-tile width of the tensor-core GEMMs, forced, on layers with
+    ragged M, N and K tails."""
+    cfg = SMALL[name]
+    case = make_case(cfg)
+    moe.set_gemm_tile_n(bn)
+    try:
+        plan = run_gpu(case)
+    finally:
+        moe.set_gemm_tile_n(0)
+    ref = run_oracle(case)
+    compare_routing(plan, ref, cfg.dtype)
+    compare_dispatch(plan, ref)
+    compare_output(plan, ref, cfg.dtype)
+
+
+@pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot", "swiglu_e64_zipf", "swiglu_e128_top8", "small_T",
+                                  "gelu_e32_norenorm"])
+def test_cta_pair_gemm_kernel(name):
+    """The CTA-pair (2-SM) grouped GEMMs, forced, against the oracle.  A short
+    wait limit turns any pipeline stall into a reported timeout."""
+    cfg = SMALL[name]
+    case = make_case(cfg)
+    moe.set_gemm_kernel(2)
+    moe.set_wait_limit(400_000_000)
+    try:
+        plan = run_gpu(case)
+    finally:
+        moe.set_gemm_kernel(0)
+        moe.set_wait_limit(0)
+    ref = run_oracle(case)
+    compare_routing(plan, ref, cfg.dtype)
+    compare_dispatch(plan, ref)
+    compare_output(plan, ref, cfg.dtype)
+
+
 def test_identity_experts_return_x_bf16():
     """w1 = w2 = I, act = identity, renormalised gates, dropless: y = x up to
     the bf16 roundings of y_perm and y."""

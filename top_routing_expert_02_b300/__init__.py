@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "dispatch", "expert_up",
-    "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "selftest_wait_timeout",
+    "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
@@ -67,6 +67,8 @@ _SIGS = {
                                     _P, _P, _P]),
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
+    "moe_set_gemm_tile_n": (_I32, [_I32]),
+    "moe_set_gemm_kernel": (_I32, [_I32]),
     "moe_selftest_wait_timeout": (_I32, [_P]),
 }
 
@@ -141,6 +143,16 @@ def check(stream=None):
 
 def set_wait_limit(cycles: int):
     lib().moe_set_wait_limit(int(cycles))
+
+
+def set_gemm_tile_n(bn: int):
+    """Force the bf16 expert GEMM tile width (128, 192, 256) or 0 for automatic."""
+    _ok("moe_set_gemm_tile_n", lib().moe_set_gemm_tile_n(int(bn)))
+
+
+def set_gemm_kernel(kind: int):
+    """Force the bf16 expert GEMM kernel: 1 one-SM tiles, 2 CTA-pair tiles, 0 automatic."""
+    _ok("moe_set_gemm_kernel", lib().moe_set_gemm_kernel(int(kind)))
 
 
 def selftest_wait_timeout(stream=None):

@@ -7,12 +7,14 @@
 // * (w2[e] . h[r]).  The activation lives in the up epilogue and the gate
 // product in the down epilogue, so neither needs a pass of its own.
 //
-// One persistent block per SM, 6 warps:
-//   warp 0     TMA producer: A tile 128x64 and B tile 256x64 (two 128-row
-//              boxes) per stage, 128-byte swizzle, STAGES-deep ring
-//   warp 1     MMA issuer: tcgen05.mma M=128 N=256 K=16, fp32 accumulator in
-//              TMEM, two accumulators (512 columns) so the epilogue of one
-//              tile overlaps the main loop of the next
+// One persistent block per SM, 6 warps (BN = 128, 192 or 256 output-tile
+// columns, chosen per call for the best wave balance over the SMs):
+//   warp 0     TMA producer: A tile 128x64 and B tile BNx64 (two BN/2-row
+//              boxes) per stage, 128-byte swizzle, a ring as deep as shared
+//              memory allows (6 / 5 / 4 stages)
+//   warp 1     MMA issuer: tcgen05.mma M=128 N=BN K=16, fp32 accumulator in
+//              TMEM, two accumulators so the epilogue of one tile overlaps
+//              the main loop of the next
 //   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, activation or
 //              gate scale in fp32, one rounding to bf16, masked stores
 // Tiles never straddle experts: M-tile m of expert e starts at row
@@ -20,8 +22,8 @@
 // expert or to the zero fill past the buffer) but never stored.  Tiles run
 // M-fastest inside (expert, N-tile), so the blocks working at the same time
 // share one weight tile through L2.  For SwiGLU the B tile pairs gate rows
-// n..n+127 with up rows F+n..F+n+127, so accumulator columns [0,128) are the
-// gate and [128,256) the up projection of the same 128 outputs.
+// n..n+BN/2-1 with up rows F+n..F+n+BN/2-1, so accumulator columns [0,BN/2)
+// are the gate and [BN/2,BN) the up projection of the same BN/2 outputs.
 //
 // Every wait is bounded by a cycle limit; a wait that runs out records
 // MOE_DEV_TIMEOUT and its role stops, the other roles then run out too, and
@@ -33,15 +35,22 @@
 
 namespace tcg {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;              // 16 KB
-constexpr int BH_BYTES = 128 * BK * 2;            // one 128-row half of B
-constexpr int STAGE_BYTES = A_BYTES + 2 * BH_BYTES;
-constexpr int ACC_COLS = 256;
-constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int THREADS = 192;
-constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;   // + slack for 1024-B alignment
-constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, 256);
+
+template <int BN>
+struct Shape {
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int BH_BYTES = B_BYTES / 2;                       // one BN/2-row box
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 6 ? 6 : (200 * 1024) / STAGE_BYTES;
+    static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;       // + slack for 1024-B alignment
+    static constexpr int ACC_COLS = BN;
+    static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
+};
+constexpr int MAX_STAGES = 6;
 
 enum { EPI_GELU = 0, EPI_SWIGLU = 1, EPI_IDENT = 2, EPI_GATE = 3 };
 
@@ -52,8 +61,8 @@ struct Args {
     int K;             // reduction length (d for up, F for down)
     int n_tiles;       // N-tiles per expert
     int b_rows;        // rows of one expert's weight in the 2-D view [E*b_rows, K]
-    int half_off;      // row offset of the second 128-row box of a B tile
-    int n_step;        // output columns per tile: 128 (SwiGLU) or 256
+    int half_off;      // row offset of the second BN/2-row box of a B tile
+    int n_step;        // output columns per tile: BN/2 (SwiGLU) or BN
     int out_cols;      // columns of the output (F for up, d for down)
     uint16_t* out;     // bf16 [rows_max, out_cols]
     const float* row_gate;
@@ -72,13 +81,17 @@ __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tile
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
-template <int EPI>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const Args g)
 {
+    using SH = Shape<BN>;
+    constexpr int STAGES = SH::STAGES, STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
+    constexpr int ACC_COLS = SH::ACC_COLS, TMEM_COLS = SH::TMEM_COLS;
+    constexpr uint32_t IDESC = SH::IDESC;
     extern __shared__ uint8_t dsmem[];
-    __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int mstart[257];
 
@@ -215,12 +228,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
+                for (int c = 0; c < BN / 2; c += 32) {
                     uint32_t gv[32], uv[32];
                     ptx::tmem_ld32(tb + c, gv);
-                    ptx::tmem_ld32(tb + 128 + c, uv);
+                    ptx::tmem_ld32(tb + BN / 2 + c, uv);
                     ptx::tmem_ld_wait();
-                    const int col = n * 128 + c;
+                    const int col = n * (BN / 2) + c;
                     if (rv && col < g.out_cols) {
                         uint32_t pk[16];
 #pragma unroll
@@ -236,11 +249,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else {
                 const float gate = (EPI == EPI_GATE && rv) ? __ldg(g.row_gate + row) : 0.f;
 #pragma unroll 1
-                for (int c = 0; c < 256; c += 32) {
+                for (int c = 0; c < BN; c += 32) {
                     uint32_t av[32];
                     ptx::tmem_ld32(tb + c, av);
                     ptx::tmem_ld_wait();
-                    const int col = n * 256 + c;
+                    const int col = n * BN + c;
                     if (rv && col < g.out_cols) {
                         uint32_t pk[16];
 #pragma unroll

@@ -14,6 +14,7 @@
 #include "dispatch.cuh"
 #include "ffn_simt.cuh"
 #include "ffn_tc.cuh"
+#include "ffn_tc2.cuh"
 #include "route.cuh"
 #include "route_tc.cuh"
 
@@ -23,6 +24,8 @@ constexpr int MAX_E = 256;
 constexpr int MAX_K = 16;
 constexpr unsigned long long DEFAULT_WAIT_LIMIT = 4000000000ull;   // ~2 s of SM cycles
 std::atomic<unsigned long long> g_wait_limit{DEFAULT_WAIT_LIMIT};
+std::atomic<int> g_forced_bn{0};   // 0: pick the GEMM tile width per call
+std::atomic<int> g_gemm_kind{0};   // 0 auto, 1 one-SM tiles, 2 CTA-pair tiles
 
 inline bool dtype_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
 inline int esize(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
@@ -195,20 +198,82 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, u
     return make_tmap_bf16_box(m, base, rows, cols, 128);
 }
 
-template <int EPI>
-moe_status launch_tc(const void* A, long long rows_max, int K, const void* W, long long w_rows_total,
-                     const tcg::Args& args, cudaStream_t stream)
+template <int EPI, int BN>
+moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W, long long w_rows_total,
+                        tcg::Args args, cudaStream_t stream)
 {
+    using SH = tcg::Shape<BN>;
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16(&ta, A, (unsigned long long)rows_max, (unsigned long long)K)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K)) return MOE_ERR_CUDA;
-    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI>, tcg::SMEM_DYN)) return launch_status();
+    if (!make_tmap_bf16_box(&ta, A, (unsigned long long)rows_max, (unsigned long long)K, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2))
+        return MOE_ERR_CUDA;
+    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN>, SH::SMEM_DYN)) return launch_status();
     const long long max_mtiles = (rows_max + tcg::BM - 1) / tcg::BM + args.E;
     const long long max_tiles = max_mtiles * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
-    tcg::grouped_gemm_kernel<EPI><<<grid, tcg::THREADS, tcg::SMEM_DYN, stream>>>(ta, tb, args);
+    tcg::grouped_gemm_kernel<EPI, BN><<<grid, tcg::THREADS, SH::SMEM_DYN, stream>>>(ta, tb, args);
     return launch_status();
+}
+
+// Output-tile width of the tensor-core GEMMs.  Measured in SM cycles on the
+// B300 for the e8 / e16 / e128 layers, 256 columns beats 192 and 128 on
+// every GEMM, even where narrower tiles balance the waves better: the wider
+// tile reuses each A row block over more output columns per byte loaded.
+int choose_bn(long long, int, bool) { return 256; }
+
+template <int EPI>
+moe_status launch_tc(const void* A, long long rows_max, int K, const void* W, long long w_rows_total, tcg::Args a,
+                     int n_out, cudaStream_t stream)
+{
+    const bool sw = EPI == tcg::EPI_SWIGLU;
+    const int forced = g_forced_bn.load();
+    const int bn = forced ? forced : choose_bn(rows_max, n_out, sw);
+    a.n_step = sw ? bn / 2 : bn;
+    a.half_off = sw ? n_out : bn / 2;
+    a.n_tiles = (n_out + a.n_step - 1) / a.n_step;
+    switch (bn) {
+    case 128: return launch_tc_bn<EPI, 128>(A, rows_max, K, W, w_rows_total, a, stream);
+    case 192: return launch_tc_bn<EPI, 192>(A, rows_max, K, W, w_rows_total, a, stream);
+    default: return launch_tc_bn<EPI, 256>(A, rows_max, K, W, w_rows_total, a, stream);
+    }
+}
+
+// CTA-pair (2-SM) grouped GEMM, weights on the 256-row side.
+template <int EPI>
+moe_status launch_tc2(const void* W, long long w_rows_total, const void* X, long long rows_max, int K, tc2::Args a,
+                      cudaStream_t stream)
+{
+    CUtensorMap tw, tx;
+    if (!make_tmap_bf16_box(&tw, W, (unsigned long long)w_rows_total, (unsigned long long)K, 64)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_box(&tx, X, (unsigned long long)rows_max, (unsigned long long)K, 128)) return MOE_ERR_CUDA;
+    if (!ensure_dyn_smem((const void*)tc2::grouped_gemm_2sm_kernel<EPI>, tc2::SMEM_DYN)) return launch_status();
+    const long long max_tok_tiles = (rows_max + tc2::BNT - 1) / tc2::BNT + a.E;
+    const long long max_pairs = max_tok_tiles * a.n_wtiles;
+    long long npairs = sm_count() / 2;
+    if (npairs > max_pairs) npairs = max_pairs;
+    if (npairs <= 0) return MOE_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * npairs), 1, 1);
+    cfg.blockDim = dim3(tc2::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = tc2::SMEM_DYN;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tc2::grouped_gemm_2sm_kernel<EPI>, tw, tx, a) != cudaSuccess) return launch_status();
+    return launch_status();
+}
+
+// 1-SM or CTA-pair kernel for this call.
+bool use_pair_kernel()
+{
+    const int kind = g_gemm_kind.load();
+    return kind == 2;
 }
 
 template <int ACT>
@@ -465,6 +530,24 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
         default: return launch_simt<simt::ACT_IDENT>(A, offsets, kept, E, d, F, F, W, nullptr, out, rows_max, stream);
         }
     }
+    if (use_pair_kernel()) {
+        tc2::Args b{};
+        b.offsets = offsets;
+        b.kept = kept;
+        b.E = E;
+        b.K = d;
+        b.w_rows = N1;
+        b.F = F;
+        b.out_cols = F;
+        b.out = (uint16_t*)h;
+        b.row_gate = nullptr;
+        b.wait_limit = g_wait_limit.load();
+        b.n_wtiles = act == MOE_ACT_SWIGLU ? (F + 127) / 128 : (F + 255) / 256;
+        const long long wr = (long long)E * N1;
+        if (act == MOE_ACT_SWIGLU) return launch_tc2<tc2::EPI_SWIGLU>(w1, wr, x_perm, rows_max, d, b, stream);
+        if (act == MOE_ACT_GELU) return launch_tc2<tc2::EPI_GELU>(w1, wr, x_perm, rows_max, d, b, stream);
+        return launch_tc2<tc2::EPI_IDENT>(w1, wr, x_perm, rows_max, d, b, stream);
+    }
     tcg::Args a{};
     a.offsets = offsets;
     a.kept = kept;
@@ -475,17 +558,10 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
     a.out = (uint16_t*)h;
     a.row_gate = nullptr;
     a.wait_limit = g_wait_limit.load();
-    if (act == MOE_ACT_SWIGLU) {
-        a.n_step = 128;
-        a.half_off = F;
-        a.n_tiles = (F + 127) / 128;
-        return launch_tc<tcg::EPI_SWIGLU>(x_perm, rows_max, d, w1, (long long)E * N1, a, stream);
-    }
-    a.n_step = 256;
-    a.half_off = 128;
-    a.n_tiles = (F + 255) / 256;
-    if (act == MOE_ACT_GELU) return launch_tc<tcg::EPI_GELU>(x_perm, rows_max, d, w1, (long long)E * N1, a, stream);
-    return launch_tc<tcg::EPI_IDENT>(x_perm, rows_max, d, w1, (long long)E * N1, a, stream);
+    if (act == MOE_ACT_SWIGLU)
+        return launch_tc<tcg::EPI_SWIGLU>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
+    if (act == MOE_ACT_GELU) return launch_tc<tcg::EPI_GELU>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
+    return launch_tc<tcg::EPI_IDENT>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
 }
 
 moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
@@ -500,6 +576,21 @@ moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t*
     if (dtype == MOE_F32)
         return launch_simt<simt::ACT_GATE>((const float*)h, offsets, kept, E, F, d, F, (const float*)w2, row_gate,
                                            (float*)y_perm, rows_max, stream);
+    if (use_pair_kernel()) {
+        tc2::Args b{};
+        b.offsets = offsets;
+        b.kept = kept;
+        b.E = E;
+        b.K = F;
+        b.w_rows = d;
+        b.F = F;
+        b.out_cols = d;
+        b.out = (uint16_t*)y_perm;
+        b.row_gate = row_gate;
+        b.wait_limit = g_wait_limit.load();
+        b.n_wtiles = (d + 255) / 256;
+        return launch_tc2<tc2::EPI_GATE>(w2, (long long)E * d, h, rows_max, F, b, stream);
+    }
     tcg::Args a{};
     a.offsets = offsets;
     a.kept = kept;
@@ -510,10 +601,7 @@ moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t*
     a.out = (uint16_t*)y_perm;
     a.row_gate = row_gate;
     a.wait_limit = g_wait_limit.load();
-    a.n_step = 256;
-    a.half_off = 128;
-    a.n_tiles = (d + 255) / 256;
-    return launch_tc<tcg::EPI_GATE>(h, rows_max, F, w2, (long long)E * d, a, stream);
+    return launch_tc<tcg::EPI_GATE>(h, rows_max, F, w2, (long long)E * d, a, d, stream);
 }
 
 moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
@@ -572,6 +660,20 @@ moe_status moe_check(moe_stream_t stream_)
 }
 
 void moe_set_wait_limit(uint64_t cycles) { g_wait_limit.store(cycles ? cycles : DEFAULT_WAIT_LIMIT); }
+
+moe_status moe_set_gemm_kernel(int kind)
+{
+    if (kind < 0 || kind > 2) return MOE_ERR_INVALID_ARG;
+    g_gemm_kind.store(kind);
+    return MOE_OK;
+}
+
+moe_status moe_set_gemm_tile_n(int bn)
+{
+    if (bn != 0 && bn != 128 && bn != 192 && bn != 256) return MOE_ERR_INVALID_ARG;
+    g_forced_bn.store(bn);
+    return MOE_OK;
+}
 
 moe_status moe_selftest_wait_timeout(moe_stream_t stream_)
 {
