@@ -196,6 +196,26 @@ def test_run_to_run_bitwise_determinism():
         assert torch.equal(a, b)
 
 
+def test_cuda_graph_replay_matches_eager():
+    """The five calls captured once into a CUDA graph and replayed on new data
+    in the same input tensors give the same bits as eager runs."""
+    cfg = SMALL["swiglu_e8"]
+    case = make_case(cfg)
+    eager = run_gpu(case)
+    ref = [t.clone() for t in (eager.topk_idx, eager.topk_gate, eager.prob_sum, eager.disp.slot_row, eager.y,
+                               eager.loss)]
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], "cuda",
+                       cfg.alpha, cfg.renorm)
+    x = torch.zeros_like(case["x"])
+    graph = plan.capture(x, case["W"], case["b"], case["w1"], case["w2"])
+    x.copy_(case["x"])
+    graph.replay()
+    moe.check()
+    got = (plan.topk_idx, plan.topk_gate, plan.prob_sum, plan.disp.slot_row, plan.y, plan.loss)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+
+
 def test_empty_batch():
     x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
     W = torch.randn(8, 128, device="cuda")
