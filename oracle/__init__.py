@@ -39,20 +39,26 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
-        P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        L.orc_capacity.restype = I64
-        L.orc_capacity.argtypes = [I64, I32, D]
-        L.orc_router_logits.argtypes = [P, I32, P, P, I64, I32, I32, P]
-        L.orc_route.argtypes = [P, I64, I32, I32, I32, P, P, P, P]
-        L.orc_dispatch.argtypes = [P, I64, I32, I32, I64, P, P, P, P]
-        L.orc_expert_ffn_row.argtypes = [P, I32, P, P, I32, I32, I32, I32, I32, P, P]
-        L.orc_combine.argtypes = [P, I32, P, I64, P, P, P, I32, P, P, I32, I32, I32, I32, P]
-        L.orc_aux_loss.restype = D
-        L.orc_aux_loss.argtypes = [P, P, I64, I32, D]
-        L.orc_num_threads.restype = I32
-        _lib = L
+        _lib = load(build())
     return _lib
+
+
+def load(path: str):
+    """A ctypes handle on an oracle library built from this source (the tests
+    also load deliberately broken copies to check that the pins catch them)."""
+    L = ctypes.CDLL(path)
+    P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    L.orc_capacity.restype = I64
+    L.orc_capacity.argtypes = [I64, I32, D]
+    L.orc_router_logits.argtypes = [P, I32, P, P, I64, I32, I32, P]
+    L.orc_route.argtypes = [P, I64, I32, I32, I32, P, P, P, P]
+    L.orc_dispatch.argtypes = [P, I64, I32, I32, I64, P, P, P, P]
+    L.orc_expert_ffn_row.argtypes = [P, I32, P, P, I32, I32, I32, I32, I32, P, P]
+    L.orc_combine.argtypes = [P, I32, P, I64, P, P, P, I32, P, P, I32, I32, I32, I32, P]
+    L.orc_aux_loss.restype = D
+    L.orc_aux_loss.argtypes = [P, P, I64, I32, D]
+    L.orc_num_threads.restype = I32
+    return L
 
 
 def _host(a):
