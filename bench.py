@@ -158,6 +158,8 @@ class ClockSampler:
         reasons = sorted(self.reasons - {"gpu_idle"})
         d = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
              "samples": len(self.samples), "source": "nvml" if self.err is None else "nvidia-smi"}
+        if self.err:
+            d["nvml_error"] = self.err[:200]
         return d
 
 
@@ -421,6 +423,7 @@ def our_arm(args, cfg):
         "roofline": {"kernel": "expert_up (tcgen05 grouped GEMM + activation)", "bound": "tensor",
                      "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s", "frac": achieved / bf16_peak,
                      "peak_source": f"{peak_src} bf16 dense burst", "traffic": traffic,
+                     "frac_of_sustained": achieved / bf16_sust,
                      "algorithmic_flops_per_launch": up_flops},
         "gemm_tflops": gemm_tflops, "gemm_frac_of_peak": gemm_tflops / bf16_peak,
         "graph_ms_per_step": ms_graph, "graph_tokens_per_s": world * cfg.T / (ms_graph / 1000.0),
