@@ -137,7 +137,9 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
  *                   slot_row - offsets[e] is the place in expert e's queue
  *   row_token[rows_max], row_gate[rows_max], x_perm[rows_max, d]: rows
  *                   0..A-1 filled (token id, gate, copy of x[token]); rows
- *                   A..rows_max-1 are left untouched
+ *                   A..rows_max-1 are left untouched.  x_perm may be NULL:
+ *                   then no rows are copied (for moe_expert_up_gathered,
+ *                   which reads x through row_token itself)
  *   n_dropped[1]    sum_e max(0, counts[e] - cap)
  *   rows_max = moe_perm_rows_max(T, k, E, cap); cap >= 0.
  * An expert id outside [0, E) in topk_idx sets the device status (the
@@ -162,6 +164,16 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
 moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32_t* kept,
                          int E, int d, int F, moe_act act, moe_dtype dtype, const void* w1,
                          int64_t rows_max, void* h, moe_stream_t stream);
+
+/* moe_expert_up reading its A rows straight from x: row r of the permuted
+ * order is x[row_token[r]] (row_token from moe_dispatch), so the dispatch can
+ * skip materialising x_perm (the tutorial's §5.3 packs tokens for contiguous
+ * transfer; here TMA four-row gathers read them in place).
+ *   x [T, d] bf16; row_token [rows_max]; other arguments as moe_expert_up.
+ * BF16 only (MOE_ERR_UNSUPPORTED otherwise). */
+moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_token, const int32_t* offsets,
+                                  const int32_t* kept, int E, int d, int F, moe_act act, moe_dtype dtype,
+                                  const void* w1, int64_t rows_max, void* h, moe_stream_t stream);
 
 /* Expert down-projection with the gate scale of the combine folded in:
  *   y_perm[r, :] = row_gate[r] * (w2[e] . h[r, :F])     (w2 [E, d, F])

@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import top_routing_expert_02_b300 as moe
 from top_routing_expert_02_b300 import synth
 
 from moe_cases import compare_dispatch, compare_output, compare_routing, make_case, run_gpu, run_oracle
@@ -36,6 +37,23 @@ def test_full_size_workload(name):
     ref = run_oracle(case, tokens=toks)
     compare_routing(plan, ref, cfg.dtype)
     compare_dispatch(plan, ref, case["x_h"])
+    compare_output(plan, ref, cfg.dtype)
+    del plan, case
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["e8_swiglu", "e128_top8_T32768"])
+def test_full_size_gathered_up_projection(name):
+    """The fused-gather layer (no x_perm) at full size: same checks."""
+    cfg = synth.workload(name)
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], case["x"].device,
+                       cfg.alpha, cfg.renorm, gather=True)
+    run_gpu(case, plan)
+    toks = sample_tokens(plan.disp.slot_row.cpu().numpy())
+    ref = run_oracle(case, tokens=toks)
+    compare_routing(plan, ref, cfg.dtype)
+    compare_dispatch(plan, ref)
     compare_output(plan, ref, cfg.dtype)
     del plan, case
     torch.cuda.empty_cache()

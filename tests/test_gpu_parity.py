@@ -125,6 +125,33 @@ def test_cta_pair_gemm_kernel(name):
     compare_output(plan, ref, cfg.dtype)
 
 
+@pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot", "swiglu_e64_zipf", "swiglu_e128_top8", "small_T",
+                                  "gelu_e32_norenorm", "bf16_e160_top16"])
+def test_gathered_up_projection(name):
+    """MoEPlan(gather=True): no permuted copy of x; the up GEMM reads x rows
+    through row_token with TMA four-row gathers.  Against the oracle, and
+    bitwise against the materialised-x_perm path (same operands, same
+    accumulation order)."""
+    cfg = SMALL[name]
+    case = make_case(cfg)
+    moe.set_wait_limit(400_000_000)
+    try:
+        plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"],
+                           case["x"].device, cfg.alpha, cfg.renorm, gather=True)
+        run_gpu(case, plan)
+    finally:
+        moe.set_wait_limit(0)
+    assert plan.disp.x_perm is None
+    ref = run_oracle(case)
+    compare_routing(plan, ref, cfg.dtype)
+    compare_dispatch(plan, ref)
+    compare_output(plan, ref, cfg.dtype)
+    base = run_gpu(case)
+    A = int(plan.disp.offsets[-1].item())
+    assert torch.equal(plan.h[:A], base.h[:A])
+    assert torch.equal(plan.y, base.y)
+
+
 def test_identity_experts_return_x_bf16():
     """w1 = w2 = I, act = identity, renormalised gates, dropless: y = x up to
     the bf16 roundings of y_perm and y."""

@@ -8,7 +8,7 @@ Every step of the layer runs in the library's CUDA kernels; there is no
 fallback.  PyTorch provides device memory and streams.
 
 Entry points (same names as the C ABI, without the ``moe_`` prefix):
-``route``, ``dispatch``, ``expert_up``, ``expert_down``, ``expert_ffn``,
+``route``, ``dispatch``, ``expert_up``, ``expert_up_gathered``, ``expert_down``, ``expert_ffn``,
 ``combine``, ``aux_loss``, plus ``capacity``, ``perm_rows_max``,
 ``workspace_bytes``, ``check``.  :class:`MoEPlan` holds preallocated buffers
 for one layer shape and enqueues the five calls; :func:`moe_forward` is the
@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "dispatch", "expert_up",
-    "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
+    "expert_up_gathered", "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
@@ -58,6 +58,7 @@ _SIGS = {
     "moe_dispatch": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                             _P, _SZ, _P]),
     "moe_expert_up": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_expert_up_gathered": (_I32, [_P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
     "moe_expert_down": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P]),
     "moe_expert_ffn": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P, _P, _SZ,
                               _P]),
@@ -192,18 +193,20 @@ class Dispatched:
 
 
 def dispatch(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatched] = None, ws=None,
-             stream=None) -> Dispatched:
-    """Capacity dispatch + row permutation (moe_dispatch)."""
+             stream=None, copy_rows: bool = True) -> Dispatched:
+    """Capacity dispatch + row permutation (moe_dispatch).  With
+    ``copy_rows=False`` (or ``out.x_perm`` None) no permuted copy of x is
+    written: :func:`expert_up_gathered` reads x through ``row_token``."""
     T, k = topk_idx.shape
     d = x.shape[1]
     dev = x.device
     R = perm_rows_max(T, k, E, cap)
     if out is None:
         i32 = dict(dtype=torch.int32, device=dev)
+        xp = torch.empty((max(R, 1), d), dtype=x.dtype, device=dev) if copy_rows else None
         out = Dispatched(torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
                          torch.empty((T, k), **i32), torch.empty(max(R, 1), **i32),
-                         torch.empty(max(R, 1), dtype=torch.float32, device=dev),
-                         torch.empty((max(R, 1), d), dtype=x.dtype, device=dev), torch.empty(1, **i32), R)
+                         torch.empty(max(R, 1), dtype=torch.float32, device=dev), xp, torch.empty(1, **i32), R)
     need = workspace_bytes("dispatch", T, d, E, k, 64)
     ws = _empty_ws(need, dev) if ws is None else ws
     _ok("moe_dispatch", lib().moe_dispatch(_ptr(topk_idx), _ptr(topk_gate), T, k, E, cap, _ptr(x), _dt(x), d,
@@ -241,6 +244,18 @@ def expert_up(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=N
     h = torch.empty((max(rows_max, 1), F), dtype=x_perm.dtype, device=x_perm.device) if h is None else h
     _ok("moe_expert_up", lib().moe_expert_up(_ptr(x_perm), _ptr(offsets), _ptr(kept), E, d, F, ACT[act],
                                              _dt(x_perm), _ptr(w1), rows_max, _ptr(h), _stream(stream)))
+    return h
+
+
+def expert_up_gathered(x, row_token, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None,
+                       stream=None):
+    """moe_expert_up with the A rows read from x at row_token (no x_perm)."""
+    E, _, d = w1.shape
+    T = x.shape[0]
+    h = torch.empty((max(rows_max, 1), F), dtype=x.dtype, device=x.device) if h is None else h
+    _ok("moe_expert_up_gathered", lib().moe_expert_up_gathered(
+        _ptr(x), T, _ptr(row_token), _ptr(offsets), _ptr(kept), E, d, F, ACT[act], _dt(x), _ptr(w1), rows_max,
+        _ptr(h), _stream(stream)))
     return h
 
 
@@ -290,12 +305,19 @@ class MoEPlan:
     expert FFN, combine and the aux loss on the current stream (no host
     synchronisation; safe to capture in a CUDA graph) and returns ``y``.
     Every intermediate stays readable as an attribute afterwards.
+
+    ``gather=True`` (bf16 only) skips the permuted copy of x: the dispatch
+    writes only the row maps and the up-projection gathers its rows from x
+    (``disp.x_perm`` is then None).
     """
 
     def __init__(self, T: int, d: int, E: int, k: int, F: int, act: str, dtype: torch.dtype, cap: int,
-                 device="cuda", alpha: float = 0.01, renorm: bool = True):
+                 device="cuda", alpha: float = 0.01, renorm: bool = True, gather: bool = False):
         self.T, self.d, self.E, self.k, self.F, self.act = T, d, E, k, F, act
         self.dtype, self.cap, self.alpha, self.renorm = dtype, int(cap), float(alpha), bool(renorm)
+        if gather and dtype != torch.bfloat16:
+            raise ValueError("the gathered up-projection is bf16 only")
+        self.gather = bool(gather)
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
@@ -306,7 +328,8 @@ class MoEPlan:
         self.prob_sum = torch.empty(E, **f32)
         self.disp = Dispatched(torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
                                torch.empty((T, k), **i32), torch.empty(Rb, **i32), torch.empty(Rb, **f32),
-                               torch.empty((Rb, d), dtype=dtype, device=dev), torch.empty(1, **i32), R)
+                               None if self.gather else torch.empty((Rb, d), dtype=dtype, device=dev),
+                               torch.empty(1, **i32), R)
         self.h = torch.empty((Rb, F), dtype=dtype, device=dev)
         self.y_perm = torch.empty((Rb, d), dtype=dtype, device=dev)
         self.y = torch.empty((T, d), dtype=dtype, device=dev)
@@ -338,8 +361,14 @@ class MoEPlan:
         dispatch(self.topk_idx, self.topk_gate, x, self.E, self.cap, out=self.disp, ws=self.ws_dispatch,
                  stream=stream)
         D = self.disp
-        expert_ffn(D.x_perm, D.offsets, D.kept, w1, w2, D.row_gate, self.act, self.rows_max, h=self.h,
-                   y_perm=self.y_perm, stream=stream)
+        if self.gather:
+            expert_up_gathered(x, D.row_token, D.offsets, D.kept, w1, self.F, self.act, self.rows_max, h=self.h,
+                               stream=stream)
+            expert_down(self.h, D.offsets, D.kept, w2, D.row_gate, self.rows_max, y_perm=self.y_perm,
+                        stream=stream)
+        else:
+            expert_ffn(D.x_perm, D.offsets, D.kept, w1, w2, D.row_gate, self.act, self.rows_max, h=self.h,
+                       y_perm=self.y_perm, stream=stream)
         combine(self.y_perm, D.slot_row, y=self.y, stream=stream)
         if self.T > 0:
             aux_loss(D.counts, self.prob_sum, self.T, self.alpha, loss=self.loss, stream=stream)
@@ -347,11 +376,11 @@ class MoEPlan:
 
 
 def moe_forward(x, w_router, b_router, w1, w2, *, k: int, cf: float, act: str, renorm: bool = True,
-                alpha: float = 0.01):
+                alpha: float = 0.01, gather: bool = False):
     """One MoE-layer forward; returns (y, loss, plan) with every intermediate on ``plan``."""
     T, d = x.shape
     E, N1, _ = w1.shape
     F = w2.shape[2]
-    plan = MoEPlan(T, d, E, k, F, act, x.dtype, capacity(T, E, cf), x.device, alpha, renorm)
+    plan = MoEPlan(T, d, E, k, F, act, x.dtype, capacity(T, E, cf), x.device, alpha, renorm, gather)
     y = plan.run(x, w_router, b_router, w1, w2)
     return y, plan.loss, plan

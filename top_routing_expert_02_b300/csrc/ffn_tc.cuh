@@ -66,6 +66,7 @@ struct Args {
     int out_cols;      // columns of the output (F for up, d for down)
     uint16_t* out;     // bf16 [rows_max, out_cols]
     const float* row_gate;
+    const int32_t* row_token;   // gathered A: row r of the tile is x[row_token[r]]
     unsigned long long wait_limit;
 };
 
@@ -81,7 +82,10 @@ __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tile
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
-template <int EPI, int BN>
+// GATHER: the A rows are read straight from x at row_token[] (the dispatch
+// permutation) with TMA four-row gathers issued by the 32 lanes of the
+// producer warp, so no permuted copy of x is materialised.
+template <int EPI, int BN, bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const Args g)
@@ -127,7 +131,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint64_t limit = g.wait_limit;
 
     if (warp == 0) {
-        if (lane == 0) {
+        if (GATHER || lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             long long fills = 0;
@@ -138,17 +142,39 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int rowA = __ldg(g.offsets + e) + m * BM;
                 const int rowB0 = e * g.b_rows + n * g.n_step;
                 const int rowB1 = rowB0 + g.half_off;
+                int gr[4] = {0, 0, 0, 0};
+                if (GATHER) {
+                    // lane l gathers tile rows 4l..4l+3; rows past the segment repeat a valid token
+                    const int rows_valid = __ldg(g.kept + e) - m * BM;
+                    const int first = __ldg(g.row_token + rowA);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 4 * lane + i;
+                        gr[i] = r < rows_valid ? __ldg(g.row_token + rowA + r) : first;
+                    }
+                }
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit)) {
+                    bool got = true;
+                    if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit);
+                    if (GATHER) got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
                     const uint32_t sa = smem0 + stage * STAGE_BYTES;
-                    ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    ptx::tma_load_2d(sa, &tmA, fb, kb * BK, rowA);
-                    ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, rowB0);
-                    ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kb * BK, rowB1);
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kb * BK, rowA);
+                        ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, rowB0);
+                        ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kb * BK, rowB1);
+                    }
+                    if (GATHER) {
+                        __syncwarp();   // the expect_tx above is posted before any lane's bytes land
+                        // four 128-byte rows per lane at 512-byte steps: the 128B swizzle follows the
+                        // shared-memory address, so the tile ends up as one 128-row box load would leave it
+                        ptx::tma_gather4_2d(sa + lane * 512, &tmA, fb, kb * BK, gr[0], gr[1], gr[2], gr[3]);
+                    }
                     ++fills;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -156,14 +182,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             }
-            if (!ok) moe_flag(MOE_DEV_TIMEOUT);
-            // drain: the last fill of every stage must have landed before exit
-            for (long long f = fills - 1; f >= 0 && f >= fills - STAGES; --f) {
-                const int s = (int)(f % STAGES);
-                const uint32_t par = (uint32_t)((f / STAGES) & 1);
-                if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), par, limit)) {
-                    moe_flag(MOE_DEV_TIMEOUT);
-                    break;
+            if (lane == 0) {
+                if (!ok) moe_flag(MOE_DEV_TIMEOUT);
+                // drain: the last fill of every stage must have landed before exit
+                for (long long f = fills - 1; f >= 0 && f >= fills - STAGES; --f) {
+                    const int s = (int)(f % STAGES);
+                    const uint32_t par = (uint32_t)((f / STAGES) & 1);
+                    if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), par, limit)) {
+                        moe_flag(MOE_DEV_TIMEOUT);
+                        break;
+                    }
                 }
             }
         }

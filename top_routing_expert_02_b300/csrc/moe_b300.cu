@@ -198,21 +198,24 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, u
     return make_tmap_bf16_box(m, base, rows, cols, 128);
 }
 
-template <int EPI, int BN>
+// A_rows: rows of the A tensor (rows_max of x_perm, or T of x when gathering).
+template <int EPI, int BN, bool GATHER = false>
 moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W, long long w_rows_total,
-                        tcg::Args args, cudaStream_t stream)
+                        tcg::Args args, cudaStream_t stream, long long A_rows = -1)
 {
     using SH = tcg::Shape<BN>;
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16_box(&ta, A, (unsigned long long)rows_max, (unsigned long long)K, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_box(&ta, A, (unsigned long long)(A_rows >= 0 ? A_rows : rows_max), (unsigned long long)K,
+                            GATHER ? 1 : 128))
+        return MOE_ERR_CUDA;
     if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2))
         return MOE_ERR_CUDA;
-    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN>, SH::SMEM_DYN)) return launch_status();
+    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, GATHER>, SH::SMEM_DYN)) return launch_status();
     const long long max_mtiles = (rows_max + tcg::BM - 1) / tcg::BM + args.E;
     const long long max_tiles = max_mtiles * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
-    tcg::grouped_gemm_kernel<EPI, BN><<<grid, tcg::THREADS, SH::SMEM_DYN, stream>>>(ta, tb, args);
+    tcg::grouped_gemm_kernel<EPI, BN, GATHER><<<grid, tcg::THREADS, SH::SMEM_DYN, stream>>>(ta, tb, args);
     return launch_status();
 }
 
@@ -474,7 +477,7 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     if (!counts || !kept || !offsets || !n_dropped) return MOE_ERR_INVALID_ARG;
     const int64_t rows_max = moe_perm_rows_max(T, k, E, cap);
     if (T > 0 && (!topk_idx || !topk_gate || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
-    if (rows_max > 0 && (!row_token || !row_gate || !x_perm)) return MOE_ERR_INVALID_ARG;
+    if (rows_max > 0 && (!row_token || !row_gate)) return MOE_ERR_INVALID_ARG;
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     const size_t need = dispatch_ws_bytes(T, k, E);
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
@@ -490,7 +493,7 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
         topk_idx, topk_gate, (int)T, k, E, cap32, hist, nchunk, counts, kept, offsets, slot_row, row_token, row_gate,
         n_dropped);
     moe_status st = launch_status();
-    if (st != MOE_OK || rows_max == 0) return st;
+    if (st != MOE_OK || rows_max == 0 || !x_perm) return st;   // x_perm NULL: the up GEMM gathers from x
     const int vec16 = d * esize(xdt) / 16;
     long long grid = (rows_max + dispatch::WARPS - 1) / dispatch::WARPS;
     if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
@@ -562,6 +565,39 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
         return launch_tc<tcg::EPI_SWIGLU>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
     if (act == MOE_ACT_GELU) return launch_tc<tcg::EPI_GELU>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
     return launch_tc<tcg::EPI_IDENT>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
+}
+
+moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_token, const int32_t* offsets,
+                                  const int32_t* kept, int E, int d, int F, moe_act act, moe_dtype dtype,
+                                  const void* w1, int64_t rows_max, void* h, moe_stream_t stream_)
+{
+    cudaStream_t stream = (cudaStream_t)stream_;
+    moe_status st = ffn_common_checks(offsets, kept, E, d, F, dtype, rows_max);
+    if (st != MOE_OK) return st;
+    if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || T >= INT_MAX || !w1 || (rows_max > 0 && (!x || !row_token || !h))) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (rows_max == 0 || T == 0) return MOE_OK;
+    const int N1 = act == MOE_ACT_SWIGLU ? 2 * F : F;
+    tcg::Args a{};
+    a.offsets = offsets;
+    a.kept = kept;
+    a.E = E;
+    a.K = d;
+    a.b_rows = N1;
+    a.out_cols = F;
+    a.out = (uint16_t*)h;
+    a.row_gate = nullptr;
+    a.row_token = row_token;
+    a.wait_limit = g_wait_limit.load();
+    const bool sw = act == MOE_ACT_SWIGLU;
+    a.n_step = sw ? 128 : 256;
+    a.half_off = sw ? F : 128;
+    a.n_tiles = (F + a.n_step - 1) / a.n_step;
+    const long long wr = (long long)E * N1;
+    if (sw) return launch_tc_bn<tcg::EPI_SWIGLU, 256, true>(x, rows_max, d, w1, wr, a, stream, T);
+    if (act == MOE_ACT_GELU) return launch_tc_bn<tcg::EPI_GELU, 256, true>(x, rows_max, d, w1, wr, a, stream, T);
+    return launch_tc_bn<tcg::EPI_IDENT, 256, true>(x, rows_max, d, w1, wr, a, stream, T);
 }
 
 moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
