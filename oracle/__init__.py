@@ -58,6 +58,10 @@ def load(path: str):
     L.orc_aux_loss.restype = D
     L.orc_aux_loss.argtypes = [P, P, I64, I32, D]
     L.orc_num_threads.restype = I32
+    L.orc_route_grouped.argtypes = [P, I64, I32, I32, I32, I32, I32, P, P, P, P]
+    L.orc_logsumexp.argtypes = [P, I64, I32, P]
+    L.orc_z_loss.restype = D
+    L.orc_z_loss.argtypes = [P, I64, D]
     return L
 
 
@@ -117,6 +121,64 @@ def route(L: np.ndarray, k: int, renorm: bool = True, want_prob: bool = False):
     return (idx, gate, ps, prob) if want_prob else (idx, gate, ps)
 
 
+def route_grouped(L: np.ndarray, k: int, n_group: int, topk_group: int, renorm: bool = True,
+                  want_prob: bool = False):
+    """Group-limited routing: top-k among the experts of the topk_group best
+    of n_group contiguous expert groups (group score = its largest logit)."""
+    L = np.ascontiguousarray(L, dtype=np.float64)
+    T, E = L.shape
+    if n_group < 1 or E % n_group or not 1 <= topk_group <= n_group or k > topk_group * (E // n_group):
+        raise ValueError("need E % n_group == 0, 1 <= topk_group <= n_group, k <= topk_group * E / n_group")
+    idx = np.empty((T, k), dtype=np.int32)
+    gate = np.empty((T, k), dtype=np.float64)
+    ps = np.empty(E, dtype=np.float64)
+    prob = np.empty((T, E), dtype=np.float64) if want_prob else None
+    lib().orc_route_grouped(_ptr(L), T, E, k, int(bool(renorm)), int(n_group), int(topk_group), _ptr(idx),
+                            _ptr(gate), _ptr(prob), _ptr(ps))
+    return (idx, gate, ps, prob) if want_prob else (idx, gate, ps)
+
+
+def logsumexp(L: np.ndarray) -> np.ndarray:
+    """lse [T] = log sum_e exp(L[t, e])."""
+    L = np.ascontiguousarray(L, dtype=np.float64)
+    T, E = L.shape
+    out = np.empty(T, dtype=np.float64)
+    lib().orc_logsumexp(_ptr(L), T, E, _ptr(out))
+    return out
+
+
+def z_loss(lse: np.ndarray, beta: float) -> float:
+    """Router z-loss beta * mean_t lse[t]^2."""
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    return float(lib().orc_z_loss(_ptr(lse), lse.size, float(beta)))
+
+
+def decision_gaps(L: np.ndarray, k: int, n_group: int = 1, topk_group: int = 1) -> np.ndarray:
+    """Smallest logit gap, per token, among the comparisons that decide the
+    routing: the top k+1 logits (ungrouped), or, with groups, the best
+    topk_group+1 group scores and the top k+1 logits inside the kept groups.
+    Input conditioning uses it to keep every choice far from a tie."""
+    L = np.asarray(L, dtype=np.float64)
+    T, E = L.shape
+
+    def top_gaps(v, m):
+        top = -np.sort(-v, axis=1)[:, :m]
+        return (top[:, :-1] - top[:, 1:]).min(axis=1) if top.shape[1] > 1 else np.full(v.shape[0], np.inf)
+
+    if n_group <= 1:
+        return top_gaps(L, min(k + 1, E))
+    gsz = E // n_group
+    score = L.reshape(T, n_group, gsz).max(axis=2)
+    gap = top_gaps(score, min(topk_group + 1, n_group))
+    ranked = np.argsort(-score, axis=1, kind="stable")[:, :topk_group]
+    keep = np.zeros((T, n_group), dtype=bool)
+    np.put_along_axis(keep, ranked, True, axis=1)
+    Lm = np.where(np.repeat(keep, gsz, axis=1), L, -np.inf)
+    m = min(k + 1, topk_group * gsz)
+    inner = top_gaps(Lm, m)
+    return np.minimum(gap, inner)
+
+
 def dispatch(idx: np.ndarray, E: int, cap: int):
     """(counts [E], kept [E], pos [T,k] (-1 = dropped), n_dropped)."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
@@ -170,14 +232,22 @@ def aux_loss(counts, prob_sum, T: int, alpha: float) -> float:
 
 
 def forward(x, W, b, w1, w2, *, k: int, cap: int, act: str, renorm: bool = True,
-            alpha: float = 0.01, tokens: Optional[Sequence[int]] = None) -> dict:
+            alpha: float = 0.01, tokens: Optional[Sequence[int]] = None, n_group: int = 1,
+            topk_group: int = 1, z_beta: float = 0.0, aux_post_drop: bool = False) -> dict:
     """The whole layer: routing and dispatch for every token, y for ``tokens``
-    (all tokens when None), and the aux loss."""
+    (all tokens when None), the aux loss (f_i before drops, or after them with
+    ``aux_post_drop``), the per-token log-sum-exp of the logits and the router
+    z-loss with coefficient ``z_beta``."""
     L = router_logits(x, W, b)
     T, E = L.shape
-    idx, gate, ps = route(L, k, renorm)
+    if n_group > 1:
+        idx, gate, ps = route_grouped(L, k, n_group, topk_group, renorm)
+    else:
+        idx, gate, ps = route(L, k, renorm)
     counts, kept, pos, nd = dispatch(idx, E, cap)
     toks = np.arange(T, dtype=np.int32) if tokens is None else np.asarray(tokens, dtype=np.int32)
     y = combine(x, toks, idx, gate, pos, w1, w2, act)
+    lse = logsumexp(L)
     return dict(logits=L, idx=idx, gate=gate, prob_sum=ps, counts=counts, kept=kept, pos=pos,
-                n_dropped=nd, tokens=toks, y=y, loss=aux_loss(counts, ps, T, alpha))
+                n_dropped=nd, tokens=toks, y=y, loss=aux_loss(kept if aux_post_drop else counts, ps, T, alpha),
+                lse=lse, z_loss=z_loss(lse, z_beta))

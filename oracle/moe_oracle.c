@@ -20,6 +20,16 @@
  *   [EP-guide]     "细粒度专家并行部署实践与优化指南" (fine-grained EP
  *                  deployment guide): §七 forward pseudo-code (top-k of the
  *                  gate probabilities, dispatch, per-expert compute, return).
+ * and, for the routing variants:
+ *   [swift-EP]     "ms-swift MoE模型加速：Megatron并行实测提速10倍" §3.2, the
+ *                  EP bullet: route a token to an expert group, then Top-k
+ *                  inside the group (16 experts split into 2 groups of 8).
+ *   [swift-ETP]    "ETP专家并行加速MoE模型：ms-swift中稀疏架构的极致优化",
+ *                  section on dynamic routing: a routing z-loss spreads the
+ *                  router's choices.  The page gives no formula; the one
+ *                  used is the router z-loss of Zoph et al., "ST-MoE:
+ *                  Designing Stable and Transferable Sparse Expert Models"
+ *                  (2022), eq. 5: mean over tokens of (log sum_e exp l[t,e])^2.
  *
  * Readings where the pages are silent (each is stated where it is used):
  *   softmax over all E experts, then top-k; ties -> lower expert index;
@@ -101,10 +111,30 @@ void orc_router_logits(const void* x, int xdt, const float* W, const float* b,
  *   gate[t,j]  p[t, idx[t,j]], divided by sum_j p[t, idx[t,j]] when renorm
  *   prob[t,e]  full softmax (optional, may be NULL)
  *   prob_sum[e] = sum_t p[t,e]                                           */
+void orc_route_grouped(const double* L, int64_t T, int E, int k, int renorm, int n_group, int topk_group,
+                       int32_t* idx, double* gate, double* prob, double* prob_sum);
+
 void orc_route(const double* L, int64_t T, int E, int k, int renorm,
                int32_t* idx, double* gate, double* prob, double* prob_sum)
 {
+    /* one group holding every expert: the choice is unrestricted */
+    orc_route_grouped(L, T, E, k, renorm, 1, 1, idx, gate, prob, prob_sum);
+}
+
+/* [swift-EP] §3.2: group-limited routing.  The page says only that the
+ * router picks the token's expert group and then runs Top-k inside it.
+ * Readings: the E experts form n_group contiguous groups of E/n_group (the
+ * placement the same section describes); a group's score is the largest
+ * logit among its experts; the topk_group groups of highest score are kept
+ * (equal scores: lower group index first); then the k experts are chosen
+ * among the kept groups' experts in (logit desc, index asc) order.  The
+ * softmax, the gates and prob_sum are those of orc_route (over all E
+ * experts): only the choice is restricted.  n_group = 1 is orc_route.     */
+void orc_route_grouped(const double* L, int64_t T, int E, int k, int renorm, int n_group, int topk_group,
+                       int32_t* idx, double* gate, double* prob, double* prob_sum)
+{
     double* P = prob ? prob : (double*)malloc(sizeof(double) * (size_t)(T * E));
+    const int gsz = E / n_group;
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         const double* l = L + t * E;
@@ -119,11 +149,34 @@ void orc_route(const double* L, int64_t T, int E, int k, int renorm,
         }
         for (int e = 0; e < E; ++e) p[e] /= z;
 
-        /* k-rank order: insertion sort of 0..E-1 by (l desc, e asc); the
-         * insertion is stable, so equal logits keep ascending indices. */
+        /* group scores, and the groups in (score desc, group asc) order */
+        double score[256];
+        int gorder[256];
+        for (int g = 0; g < n_group; ++g) {
+            score[g] = l[g * gsz];
+            for (int e = g * gsz + 1; e < (g + 1) * gsz; ++e)
+                if (l[e] > score[g]) score[g] = l[e];
+        }
+        for (int g = 0; g < n_group; ++g) {
+            int pos = g;
+            while (pos > 0 && score[gorder[pos - 1]] < score[g]) {
+                gorder[pos] = gorder[pos - 1];
+                --pos;
+            }
+            gorder[pos] = g;
+        }
+        int allowed[256];
+        for (int g = 0; g < n_group; ++g) allowed[g] = 0;
+        for (int r = 0; r < topk_group; ++r) allowed[gorder[r]] = 1;
+
+        /* k-rank order: insertion sort of the kept groups' experts by
+         * (l desc, e asc); the insertion is stable, so equal logits keep
+         * ascending indices. */
         int order[1024];
+        int n = 0;
         for (int e = 0; e < E; ++e) {
-            int pos = e;
+            if (!allowed[e / gsz]) continue;
+            int pos = n++;
             while (pos > 0 && l[order[pos - 1]] < l[e]) {
                 order[pos] = order[pos - 1];
                 --pos;
@@ -141,6 +194,31 @@ void orc_route(const double* L, int64_t T, int E, int k, int renorm,
     for (int64_t t = 0; t < T; ++t)
         for (int e = 0; e < E; ++e) prob_sum[e] += P[t * E + e];
     if (!prob) free(P);
+}
+
+/* lse[t] = log sum_e exp(L[t,e]), evaluated as m + log sum_e exp(L[t,e] - m)
+ * with m the row maximum (the same value, without overflow). */
+void orc_logsumexp(const double* L, int64_t T, int E, double* lse)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* l = L + t * E;
+        double mx = l[0];
+        for (int e = 1; e < E; ++e)
+            if (l[e] > mx) mx = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += exp(l[e] - mx);
+        lse[t] = mx + log(z);
+    }
+}
+
+/* [swift-ETP] routing z-loss, in the ST-MoE form:
+ * L_z = beta * (1/T) * sum_t lse[t]^2. */
+double orc_z_loss(const double* lse, int64_t T, double beta)
+{
+    double s = 0.0;
+    for (int64_t t = 0; t < T; ++t) s += lse[t] * lse[t];
+    return beta * s / (double)T;
 }
 
 /* [EP-tutorial] §2.1 step 2 (dispatch plan) and §2.2 (capacity, dropping).
@@ -251,7 +329,9 @@ void orc_combine(const void* x, int xdt, const int32_t* tokens, int64_t n_tok,
 
 /* [EP-tutorial] §5.1: L_aux = alpha * num_experts * sum_i f_i * P_i with
  * f_i = counts[i] / T (fraction of tokens sent to expert i, every choice,
- * before drops) and P_i = prob_sum[i] / T (mean gate probability). */
+ * before drops) and P_i = prob_sum[i] / T (mean gate probability).
+ * The post-drop variant of f_i (only the slots that survived the capacity
+ * cut) is the same formula with kept[] passed as counts. */
 double orc_aux_loss(const int32_t* counts, const double* prob_sum, int64_t T, int E, double alpha)
 {
     double s = 0.0;

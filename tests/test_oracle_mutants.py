@@ -38,6 +38,15 @@ MUTANTS = {
     "aux loss without the E factor": ("return alpha * (double)E * s;", "return alpha * s;"),
     "P_i not divided by T": ("((double)counts[e] / (double)T) * (prob_sum[e] / (double)T)",
                              "((double)counts[e] / (double)T) * prob_sum[e]"),
+    "group score is the group's sum": ("if (l[e] > score[g]) score[g] = l[e];", "score[g] += l[e];"),
+    "group ties go to the higher index": ("while (pos > 0 && score[gorder[pos - 1]] < score[g]) {",
+                                          "while (pos > 0 && score[gorder[pos - 1]] <= score[g]) {"),
+    "groups strided instead of contiguous": ("if (!allowed[e / gsz]) continue;",
+                                             "if (!allowed[e % n_group]) continue;"),
+    "one group too many kept": ("for (int r = 0; r < topk_group; ++r) allowed[gorder[r]] = 1;",
+                                "for (int r = 0; r <= topk_group && r < n_group; ++r) allowed[gorder[r]] = 1;"),
+    "log-sum-exp without the shift back": ("lse[t] = mx + log(z);", "lse[t] = log(z);"),
+    "z-loss of lse, not lse squared": ("s += lse[t] * lse[t];", "s += lse[t];"),
 }
 
 
@@ -62,6 +71,13 @@ def _pins():
         ("aux uniform", lambda: [P.test_aux_loss_uniform_router_is_alpha_k(c) for c in (None, 0)]),
         ("aux circulant", lambda: P.test_aux_loss_circulant_router_is_alpha_k(8, 2)),
         ("aux concentration", P.test_aux_loss_one_hot_concentration),
+        ("grouped brute force", lambda: [P.test_grouped_topk_brute_force_with_exact_ties(*a)
+                                         for a in [(6, 3, 1, 2), (8, 4, 2, 2), (8, 4, 3, 5)]]),
+        ("grouped worked example", P.test_grouped_routing_worked_example),
+        ("grouped first choice", P.test_grouped_routing_keeps_first_choice_and_stays_in_kept_groups),
+        ("lse", P.test_logsumexp_against_library_and_closed_forms),
+        ("z-loss", P.test_z_loss_closed_forms),
+        ("post-drop aux", lambda: [P.test_post_drop_aux_loss_uniform_router(c) for c in (0, 3)]),
     ]
 
 

@@ -301,3 +301,120 @@ def test_aux_loss_one_hot_concentration():
     idx, _, ps = oracle.route(oracle.router_logits(x, W), 1)
     counts, _, _, _ = oracle.dispatch(idx, E, T)
     assert math.isclose(oracle.aux_loss(counts, ps, T, 0.5), 0.5 * E, rel_tol=1e-12)
+
+
+# ------------------------------------------------ group-limited routing ---
+
+@pytest.mark.parametrize("E,G,M,k", [(4, 2, 1, 2), (6, 3, 1, 2), (6, 3, 2, 3), (8, 4, 2, 2), (8, 2, 1, 4),
+                                     (8, 4, 3, 5)])
+def test_grouped_topk_brute_force_with_exact_ties(E, G, M, k):
+    """Enumerate every M-subset of groups and every ordered k-tuple of the
+    kept experts.  The kept subset is the one whose groups, listed best
+    first by (score desc, index asc), compare lexicographically best; the
+    chosen tuple is the lexicographic maximum of ((logit, -index), ...)
+    over the kept experts.  Integer logits make ties between group scores
+    and between experts common."""
+    rng = np.random.default_rng(1000 * E + 10 * G + M)
+    T = 30
+    L = rng.integers(-2, 3, size=(T, E)).astype(np.float64)
+    idx, gate, ps = oracle.route_grouped(L, k, G, M, renorm=False)
+    gsz = E // G
+    for t in range(T):
+        lt = L[t]
+        score = [max(lt[g * gsz:(g + 1) * gsz]) for g in range(G)]
+        best_set = max(itertools.combinations(range(G), M),
+                       key=lambda S: sorted(((score[g], -g) for g in S), reverse=True))
+        allowed = [e for e in range(E) if e // gsz in best_set]
+        best = max(itertools.permutations(allowed, k), key=lambda tup: tuple((lt[e], -e) for e in tup))
+        assert tuple(idx[t]) == best, (t, lt, idx[t], best)
+        np.testing.assert_allclose(gate[t], scipy.special.softmax(lt)[list(best)], rtol=1e-13, atol=0)
+    np.testing.assert_allclose(ps, scipy.special.softmax(L, axis=1).sum(0), rtol=1e-12)
+
+
+def test_grouped_routing_worked_example():
+    """Hand-worked: 8 experts in 4 groups of 2.  Row 0 has its best expert (2)
+    in group 1, whose other expert (3) is weak: one kept group gives (2, 3),
+    two kept groups (1 and 0) give (2, 0), as plain top-2 does.  Row 1 has
+    three groups tied at score 3: the lowest (0) wins, giving (1, 0); with
+    two groups (0 and 1) the tie 1 vs 2 goes to the lower index."""
+    L = np.array([[5, 4.9, 6, 0, 1, 1, 0, 0], [1, 3, 3, 2, 0, 0, 3, 1]], dtype=np.float64)
+    assert oracle.route_grouped(L, 2, 4, 1)[0].tolist() == [[2, 3], [1, 0]]
+    assert oracle.route_grouped(L, 2, 4, 2)[0].tolist() == [[2, 0], [1, 2]]
+    assert oracle.route_grouped(L, 3, 4, 2)[0].tolist() == [[2, 0, 1], [1, 2, 3]]
+    assert oracle.route_grouped(L, 2, 2, 1)[0].tolist() == [[2, 0], [1, 2]]   # groups {0..3}, {4..7}
+
+
+@pytest.mark.parametrize("G,M", [(1, 1), (4, 4), (8, 8)])
+def test_grouped_routing_reduces_to_plain_topk(G, M):
+    """One group, or every group kept: the restriction is void."""
+    rng = np.random.default_rng(7)
+    L = rng.standard_normal((200, 16))
+    for renorm in (True, False):
+        a = oracle.route(L, 3, renorm)
+        b = oracle.route_grouped(L, 3, G, M, renorm)
+        assert np.array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+        np.testing.assert_array_equal(a[2], b[2])
+
+
+def test_grouped_routing_keeps_first_choice_and_stays_in_kept_groups():
+    """With one kept group the overall best expert is always chosen first
+    (its group has the top score), and every choice lies in its group."""
+    rng = np.random.default_rng(8)
+    L = rng.standard_normal((300, 32))
+    idx, gate, _ = oracle.route_grouped(L, 4, 8, 1)
+    assert np.array_equal(idx[:, 0], np.argmax(L, axis=1))
+    assert np.all(idx // 4 == (idx[:, :1] // 4))
+    np.testing.assert_allclose(gate.sum(1), 1.0, rtol=1e-14)
+
+
+def test_grouped_routing_rejects_bad_shapes():
+    L = np.zeros((2, 8))
+    for args in [(2, 3, 1), (2, 4, 0), (2, 4, 5), (5, 4, 2)]:
+        with pytest.raises(ValueError):
+            oracle.route_grouped(L, *args)
+
+
+# --------------------------------------------------------- router z-loss ---
+
+def test_logsumexp_against_library_and_closed_forms():
+    rng = np.random.default_rng(9)
+    L = rng.standard_normal((50, 24)) * 3
+    np.testing.assert_allclose(oracle.logsumexp(L), scipy.special.logsumexp(L, axis=1), rtol=1e-14)
+    np.testing.assert_allclose(oracle.logsumexp(np.zeros((3, 8))), math.log(8), rtol=1e-15)
+    # shift invariance, and no overflow for large logits
+    np.testing.assert_allclose(oracle.logsumexp(L + 1000.0), oracle.logsumexp(L) + 1000.0, rtol=1e-14)
+    # two experts: lse(0, ln 3) = ln 4
+    np.testing.assert_allclose(oracle.logsumexp(np.array([[0.0, math.log(3.0)]])), math.log(4.0), rtol=1e-15)
+
+
+def test_z_loss_closed_forms():
+    """Zero router: every lse is ln E, so L_z = beta (ln E)^2.  In general
+    L_z = beta * mean(lse^2), checked on lse values given directly."""
+    E, T = 16, 64
+    x = torch.randn(T, 32)
+    L = oracle.router_logits(x, torch.zeros(E, 32), torch.zeros(E))
+    lse = oracle.logsumexp(L)
+    assert oracle.z_loss(lse, 1e-3) == pytest.approx(1e-3 * math.log(E) ** 2, rel=1e-14)
+    v = np.array([1.0, -2.0, 3.0, 0.5])
+    assert oracle.z_loss(v, 0.5) == pytest.approx(0.5 * (1 + 4 + 9 + 0.25) / 4, rel=1e-15)
+    assert oracle.z_loss(v, 0.0) == 0.0
+
+
+# ------------------------------------------------- post-drop f_i variant ---
+
+@pytest.mark.parametrize("cap", [0, 3, 7, 10**6])
+def test_post_drop_aux_loss_uniform_router(cap):
+    """Zero router (P_i = 1/E): with f_i = kept_i / T the loss is
+    alpha * (T k - n_dropped) / T; dropless it equals the pre-drop loss."""
+    E, k, T, alpha = 8, 2, 40, 0.01
+    rng = np.random.default_rng(cap)
+    x = torch.randn(T, 16)
+    L = oracle.router_logits(x, torch.zeros(E, 16), None)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)   # any routing
+    _, _, ps = oracle.route(L, k)
+    counts, kept, pos, nd = oracle.dispatch(idx, E, cap)
+    post = oracle.aux_loss(kept, ps, T, alpha)
+    assert post == pytest.approx(alpha * (T * k - nd) / T, rel=1e-13)
+    if cap >= T:
+        assert post == oracle.aux_loss(counts, ps, T, alpha)

@@ -66,3 +66,17 @@ def test_zipf_skew_is_heavy():
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
     assert counts.argmax() == 0
     assert counts.max() / counts.mean() > 10
+
+
+def test_near_tie_conditioning_for_group_limited_routing():
+    """With a routing variant's own gap function, every decision it takes
+    (group scores, then the logits inside the kept groups) clears the margin."""
+    cfg = synth.MoEConfig("grp", 512, 128, 32, 4, 128, "swiglu", 1.25, "bf16")
+    gaps = lambda L: oracle.decision_gaps(L, cfg.k, 8, 2)
+    ri = synth.condition_near_ties(cfg, synth.make_routing_inputs(cfg), oracle.router_logits, gaps_fn=gaps)
+    L = oracle.router_logits(ri.x, ri.W, ri.b)
+    assert (gaps(L) >= 1e-3).all()
+    assert ri.redrawn > 0
+    # decision_gaps without groups is the plain top-(k+1) test
+    top = -np.sort(-L, axis=1)[:, :cfg.k + 1]
+    np.testing.assert_array_equal(oracle.decision_gaps(L, cfg.k), np.diff(-top, axis=1).min(axis=1))

@@ -179,15 +179,19 @@ def make_expert_weights(cfg: MoEConfig, device="cpu"):
 
 def condition_near_ties(cfg: MoEConfig, ri: RoutingInputs,
                         logits_fn: Callable[[torch.Tensor, torch.Tensor, Optional[torch.Tensor]], np.ndarray],
-                        margin: float = 1e-3, max_passes: int = 100) -> RoutingInputs:
+                        margin: float = 1e-3, max_passes: int = 100,
+                        gaps_fn: Optional[Callable[[np.ndarray], np.ndarray]] = None) -> RoutingInputs:
     """Redraw x rows whose top-(k+1) router logits are closer than ``margin``.
 
     ``logits_fn(x_rows, W, b)`` returns the float64 logits [rows, E] of the
-    given rows; the caller supplies it.  Rows are redrawn in ascending token
-    order from the resample stream, and only redrawn rows are re-checked, so
-    the result depends on the seed alone.  With the margin in place every
-    top-k choice and every k-rank is decided by more than 1e-3, far above the
-    rounding error of an fp32 logit.
+    given rows; the caller supplies it.  ``gaps_fn(logits)``, when given,
+    replaces the top-(k+1) test: it returns each row's smallest gap among the
+    comparisons that decide its routing (a routing variant knows which those
+    are).  Rows are redrawn in ascending token order from the resample
+    stream, and only redrawn rows are re-checked, so the result depends on
+    the seed alone.  With the margin in place every top-k choice and every
+    k-rank is decided by more than 1e-3, far above the rounding error of an
+    fp32 logit.
     """
     m = min(cfg.k + 1, cfg.E)
     rows = np.arange(cfg.T)
@@ -195,8 +199,11 @@ def condition_near_ties(cfg: MoEConfig, ri: RoutingInputs,
         if rows.size == 0:
             return ri
         L = np.asarray(logits_fn(ri.x[torch.from_numpy(rows)], ri.W, ri.b), dtype=np.float64)
-        top = -np.sort(-L, axis=1)[:, :m]
-        bad = rows[((top[:, :-1] - top[:, 1:]) < margin).any(axis=1)] if m > 1 else rows[:0]
+        if gaps_fn is not None:
+            bad = rows[np.asarray(gaps_fn(L)) < margin]
+        else:
+            top = -np.sort(-L, axis=1)[:, :m]
+            bad = rows[((top[:, :-1] - top[:, 1:]) < margin).any(axis=1)] if m > 1 else rows[:0]
         for t in bad:
             fresh = ri._resample.standard_normal((1, cfg.d), dtype=np.float32)
             ri.x[int(t)] = _to_dtype(fresh, cfg.dtype)[0]
