@@ -16,6 +16,9 @@
  *   moe_combine    gate-weighted sum back into token order        (§2.1 step 5)
  *   moe_aux_loss   L_aux = alpha * E * sum_i f_i * P_i            (§5.1)
  *
+ * Routing variants from the ms-swift pages: moe_route_ex (group-limited
+ * top-k, per-token log-sum-exp) and moe_z_loss (router z-loss).
+ *
  * Conventions shared by every call
  * --------------------------------
  * Ownership   The caller allocates and owns every buffer (inputs, outputs,
@@ -121,6 +124,26 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
                      int32_t* topk_idx, float* topk_gate, float* prob_sum,
                      void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route with the routing variants.
+ * Group-limited routing, from "ms-swift MoE模型加速：Megatron并行实测提速10倍"
+ * §3.2 (EP bullet): the router first picks the token's expert group, then
+ * runs Top-k inside it.  That page fixes no more; the readings taken: the E
+ * experts form n_group contiguous groups of E / n_group (the EP placement of
+ * the same section); a group's score is its largest logit; the topk_group
+ * groups of highest score are kept (equal scores: lower group index); the k
+ * experts are then chosen among the kept groups' experts exactly as
+ * moe_route orders them.  The softmax, the gates (and their renormalisation)
+ * and prob_sum stay those over all E experts.  n_group = 1 is moe_route.
+ *   n_group     1..32, dividing E;  topk_group 1..n_group;
+ *               k <= topk_group * E / n_group (else MOE_ERR_INVALID_ARG)
+ *   lse         [T] fp32 or NULL: log sum_e exp(l[t,e]) per token, the
+ *               input of moe_z_loss
+ * Other arguments, outputs and workspace as moe_route. */
+moe_status moe_route_ex(const void* x, moe_dtype xdt, const float* w_router, const float* b_router,
+                        int64_t T, int d, int E, int k, int renorm, int n_group, int topk_group,
+                        int32_t* topk_idx, float* topk_gate, float* prob_sum, float* lse,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Dispatch: tutorial §2.1 steps 2-3 (dispatch plan, token exchange) and
  * §2.2 (capacity, overflow tokens dropped).  Assignments (t, j) are granted
  * expert slots in k-rank-then-token order -- every first choice in token
@@ -204,9 +227,20 @@ moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, i
 /* Auxiliary load-balance loss, tutorial §5.1:
  *   L = alpha * E * sum_e f_e * P_e,  f_e = counts[e] / T,  P_e = prob_sum[e] / T
  * (f counts every choice before capacity drops).  Computed in fp64 on the
- * device, stored as fp32 to loss[0] (device pointer).  T must be >= 1. */
+ * device, stored as fp32 to loss[0] (device pointer).  T must be >= 1.
+ * Passing kept[] (from moe_dispatch) as counts gives the post-drop variant,
+ * where f_e counts only the slots that survived the capacity cut. */
 moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T, int E,
                         float alpha, float* loss, moe_stream_t stream);
+
+/* Router z-loss.  "ETP专家并行加速MoE模型：ms-swift中稀疏架构的极致优化", section
+ * on dynamic routing, names a routing z-loss that spreads the router's
+ * choices but gives no formula; this is the router z-loss of ST-MoE (Zoph et
+ * al. 2022, eq. 5):
+ *   loss = beta * (1/T) * sum_t lse[t]^2,   lse from moe_route_ex
+ * Summed in fp64 in a fixed order on the device, stored as fp32 to loss[0]
+ * (device pointer).  T must be >= 1. */
+moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_stream_t stream);
 
 /* ------------------------------------------------- no-allocation variant --- */
 

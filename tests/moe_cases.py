@@ -10,6 +10,8 @@ Bars (written here once, used by every parity test):
                                       d = 4096; a gate inherits at most twice that relatively)
   layer output y:                     relative Frobenius error <= 1e-5 (fp32 layer),
                                       <= 2e-2 (bf16 layer)
+  per-token log-sum-exp:              as the gates (it carries the same logit error, atol 1e-6)
+  router z-loss:                      twice the gates' bar (it squares the log-sum-exp)
 """
 from __future__ import annotations
 
@@ -24,11 +26,13 @@ GATE_RTOL = {"f32": 1e-5, "bf16": 2e-4}
 Y_TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
-def make_case(cfg: synth.MoEConfig, device="cuda", condition=True, routing=None):
-    """Inputs of one workload: host copies for the oracle, device copies for the kernels."""
+def make_case(cfg: synth.MoEConfig, device="cuda", condition=True, routing=None, n_group=1, topk_group=1):
+    """Inputs of one workload: host copies for the oracle, device copies for the
+    kernels.  With groups, the near-tie margin covers the group decisions too."""
     ri = routing if routing is not None else synth.make_routing_inputs(cfg)
     if condition:
-        ri = synth.condition_near_ties(cfg, ri, oracle.router_logits)
+        gaps = None if n_group == 1 else (lambda L: oracle.decision_gaps(L, cfg.k, n_group, topk_group))
+        ri = synth.condition_near_ties(cfg, ri, oracle.router_logits, gaps_fn=gaps)
     w1, w2 = synth.make_expert_weights(cfg, device=device)
     cap = moe.capacity(cfg.T, cfg.E, cfg.cf)
     return dict(cfg=cfg, cap=cap, x_h=ri.x, W_h=ri.W, b_h=ri.b, x=ri.x.to(device), W=ri.W.to(device),
@@ -46,12 +50,14 @@ def run_gpu(case, plan=None):
     return plan
 
 
-def run_oracle(case, tokens=None, w_host=None):
+def run_oracle(case, tokens=None, w_host=None, **variant):
+    """The oracle's layer on the case's inputs; ``variant`` passes the routing
+    variants (n_group, topk_group, z_beta, aux_post_drop) through."""
     cfg = case["cfg"]
     if w_host is None:
         w_host = (case["w1"].cpu(), case["w2"].cpu())
     return oracle.forward(case["x_h"], case["W_h"], case["b_h"], w_host[0], w_host[1], k=cfg.k, cap=case["cap"],
-                          act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha, tokens=tokens)
+                          act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha, tokens=tokens, **variant)
 
 
 def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
@@ -106,3 +112,14 @@ def compare_output(plan, ref, dtype: str):
     loss = float(plan.loss.item())
     assert abs(loss - ref["loss"]) <= GATE_RTOL[dtype] * abs(ref["loss"]) + 1e-12, (loss, ref["loss"])
     return err
+
+
+def compare_z_loss(plan, ref, dtype: str):
+    """Per-token log-sum-exp and the router z-loss against the oracle."""
+    T = plan.T
+    lse = plan.lse[:T].cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(lse - ref["lse"]) / np.maximum(np.abs(ref["lse"]), 1e-30)) if T else 0.0
+    z = float(plan.z_loss.item())
+    print(f"[parity] lse max rel err {err:.3e}; z-loss {z:.8f} vs {ref['z_loss']:.8f}")
+    np.testing.assert_allclose(lse, ref["lse"], rtol=GATE_RTOL[dtype], atol=1e-6)
+    assert abs(z - ref["z_loss"]) <= 2 * GATE_RTOL[dtype] * abs(ref["z_loss"]) + 1e-12, (z, ref["z_loss"])

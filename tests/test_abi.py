@@ -121,3 +121,21 @@ def test_binding_rejects_unsupported_dtype():
     x = torch.zeros(4, 64, dtype=torch.float16)
     with pytest.raises(TypeError):
         moe.route(x, torch.zeros(8, 64), None, 2)
+
+
+def test_route_ex_and_z_loss_argument_errors():
+    L = moe.lib()
+
+    def rex(E=8, k=2, G=4, M=2, T=16):
+        return L.moe_route_ex(FAKE, 1, FAKE, None, T, 128, E, k, 1, G, M, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
+                              None)
+
+    assert rex(G=3) == 1            # 3 does not divide 8
+    assert rex(G=0) == 1
+    assert rex(E=64, G=64, M=1, k=1) == 1   # more than 32 groups
+    assert rex(M=0) == 1
+    assert rex(M=5) == 1            # more groups kept than exist
+    assert rex(G=4, M=1, k=3) == 1  # one group of 2 cannot hold 3 choices
+    assert L.moe_z_loss(FAKE, 0, ctypes.c_float(1e-3), FAKE, None) == 1
+    assert L.moe_z_loss(None, 16, ctypes.c_float(1e-3), FAKE, None) == 1
+    assert L.moe_z_loss(FAKE, 16, ctypes.c_float(1e-3), None, None) == 1

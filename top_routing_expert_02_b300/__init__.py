@@ -24,7 +24,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "dispatch", "expert_up",
+    "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
     "expert_up_gathered", "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
@@ -66,6 +66,9 @@ _SIGS = {
     "moe_aux_loss": (_I32, [_P, _P, _I64, _I32, _F, _P, _P]),
     "moe_dispatch_noalloc": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P]),
+    "moe_route_ex": (_I32, [_P, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ,
+                            _P]),
+    "moe_z_loss": (_I32, [_P, _I64, _F, _P, _P]),
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
     "moe_set_gemm_tile_n": (_I32, [_I32]),
@@ -163,8 +166,12 @@ def selftest_wait_timeout(stream=None):
 # --------------------------------------------------------------- compute ---
 
 def route(x, w_router, b_router, k: int, renorm: bool = True, *, topk_idx=None, topk_gate=None, prob_sum=None,
-          ws=None, stream=None):
-    """Router (moe_route): returns (topk_idx [T,k] int32, topk_gate [T,k] f32, prob_sum [E] f32)."""
+          ws=None, stream=None, n_group: int = 1, topk_group: int = 1, lse=None):
+    """Router (moe_route): returns (topk_idx [T,k] int32, topk_gate [T,k] f32, prob_sum [E] f32).
+
+    ``n_group`` > 1 selects group-limited routing (moe_route_ex): top-k among
+    the experts of the ``topk_group`` best of ``n_group`` contiguous groups.
+    ``lse`` ([T] f32) receives each token's log-sum-exp of the logits."""
     T, d = x.shape
     E = w_router.shape[0]
     dev = x.device
@@ -173,9 +180,14 @@ def route(x, w_router, b_router, k: int, renorm: bool = True, *, topk_idx=None, 
     prob_sum = torch.empty(E, dtype=torch.float32, device=dev) if prob_sum is None else prob_sum
     need = workspace_bytes("route", T, d, E, k, 64)
     ws = _empty_ws(need, dev) if ws is None else ws
-    _ok("moe_route", lib().moe_route(_ptr(x), _dt(x), _ptr(w_router), _ptr(b_router), T, d, E, k, int(renorm),
-                                     _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(ws), ws.numel(),
-                                     _stream(stream)))
+    if n_group == 1 and lse is None:
+        _ok("moe_route", lib().moe_route(_ptr(x), _dt(x), _ptr(w_router), _ptr(b_router), T, d, E, k, int(renorm),
+                                         _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    else:
+        _ok("moe_route_ex", lib().moe_route_ex(
+            _ptr(x), _dt(x), _ptr(w_router), _ptr(b_router), T, d, E, k, int(renorm), int(n_group), int(topk_group),
+            _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
     return topk_idx, topk_gate, prob_sum
 
 
@@ -296,6 +308,13 @@ def aux_loss(counts, prob_sum, T: int, alpha: float, *, loss=None, stream=None):
     return loss
 
 
+def z_loss(lse, beta: float, *, loss=None, stream=None):
+    """Router z-loss beta * mean_t lse[t]^2 (moe_z_loss); lse from route(..., lse=)."""
+    loss = torch.empty(1, dtype=torch.float32, device=lse.device) if loss is None else loss
+    _ok("moe_z_loss", lib().moe_z_loss(_ptr(lse), lse.shape[0], float(beta), _ptr(loss), _stream(stream)))
+    return loss
+
+
 # ------------------------------------------------------------ whole layer ---
 
 class MoEPlan:
@@ -309,12 +328,22 @@ class MoEPlan:
     ``gather=True`` (bf16 only) skips the permuted copy of x: the dispatch
     writes only the row maps and the up-projection gathers its rows from x
     (``disp.x_perm`` is then None).
+
+    Routing variants: ``n_group``/``topk_group`` (group-limited top-k),
+    ``z_beta`` (router z-loss into ``z_loss``, with the per-token
+    log-sum-exp in ``lse``; None skips it) and ``aux_post_drop`` (f_i from
+    the kept slots instead of every choice).
     """
 
     def __init__(self, T: int, d: int, E: int, k: int, F: int, act: str, dtype: torch.dtype, cap: int,
-                 device="cuda", alpha: float = 0.01, renorm: bool = True, gather: bool = False):
+                 device="cuda", alpha: float = 0.01, renorm: bool = True, gather: bool = False, *,
+                 n_group: int = 1, topk_group: int = 1, z_beta: Optional[float] = None,
+                 aux_post_drop: bool = False):
         self.T, self.d, self.E, self.k, self.F, self.act = T, d, E, k, F, act
         self.dtype, self.cap, self.alpha, self.renorm = dtype, int(cap), float(alpha), bool(renorm)
+        self.n_group, self.topk_group = int(n_group), int(topk_group)
+        self.z_beta = None if z_beta is None else float(z_beta)
+        self.aux_post_drop = bool(aux_post_drop)
         if gather and dtype != torch.bfloat16:
             raise ValueError("the gathered up-projection is bf16 only")
         self.gather = bool(gather)
@@ -334,6 +363,8 @@ class MoEPlan:
         self.y_perm = torch.empty((Rb, d), dtype=dtype, device=dev)
         self.y = torch.empty((T, d), dtype=dtype, device=dev)
         self.loss = torch.empty(1, **f32)
+        self.lse = torch.empty(max(T, 1), **f32) if self.z_beta is not None else None
+        self.z_loss = torch.empty(1, **f32) if self.z_beta is not None else None
         self.ws_route = _empty_ws(workspace_bytes("route", T, d, E, k, F), dev)
         self.ws_dispatch = _empty_ws(workspace_bytes("dispatch", T, d, E, k, F), dev)
 
@@ -357,7 +388,8 @@ class MoEPlan:
 
     def run(self, x, w_router, b_router, w1, w2, stream=None) -> torch.Tensor:
         route(x, w_router, b_router, self.k, self.renorm, topk_idx=self.topk_idx, topk_gate=self.topk_gate,
-              prob_sum=self.prob_sum, ws=self.ws_route, stream=stream)
+              prob_sum=self.prob_sum, ws=self.ws_route, stream=stream, n_group=self.n_group,
+              topk_group=self.topk_group, lse=self.lse)
         dispatch(self.topk_idx, self.topk_gate, x, self.E, self.cap, out=self.disp, ws=self.ws_dispatch,
                  stream=stream)
         D = self.disp
@@ -371,7 +403,10 @@ class MoEPlan:
                        y_perm=self.y_perm, stream=stream)
         combine(self.y_perm, D.slot_row, y=self.y, stream=stream)
         if self.T > 0:
-            aux_loss(D.counts, self.prob_sum, self.T, self.alpha, loss=self.loss, stream=stream)
+            aux_loss(D.kept if self.aux_post_drop else D.counts, self.prob_sum, self.T, self.alpha, loss=self.loss,
+                     stream=stream)
+            if self.z_beta is not None:
+                z_loss(self.lse, self.z_beta, loss=self.z_loss, stream=stream)
         return self.y
 
 

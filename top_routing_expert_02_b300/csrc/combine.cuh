@@ -78,4 +78,28 @@ __global__ void aux_loss_kernel(const int32_t* __restrict__ counts, const float*
     if (lane == 0) *loss = (float)((double)alpha * (double)E * s);
 }
 
+// Router z-loss (the ms-swift ETP page names a routing z-loss that spreads
+// the router's choices; its formula is the one of ST-MoE, Zoph et al. 2022,
+// eq. 5): loss = beta * (1/T) * sum_t lse[t]^2.  One block, strided fp64
+// partial sums, then a fixed shared-memory tree: the result does not depend
+// on timing.
+constexpr int ZL_THREADS = 1024;
+__global__ void __launch_bounds__(ZL_THREADS)
+z_loss_kernel(const float* __restrict__ lse, long long T, float beta, float* __restrict__ loss)
+{
+    __shared__ double sh[ZL_THREADS];
+    double s = 0.0;
+    for (long long t = threadIdx.x; t < T; t += ZL_THREADS) {
+        const double v = (double)__ldg(lse + t);
+        s += v * v;
+    }
+    sh[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = ZL_THREADS / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *loss = (float)((double)beta * sh[0] / (double)T);
+}
+
 }  // namespace combine

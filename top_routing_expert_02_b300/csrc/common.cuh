@@ -49,4 +49,54 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p)
 __device__ __forceinline__ float gelu_f32(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
+// Routing variants of the top-k step.  Group-limited routing (the ms-swift
+// Megatron acceleration page, §3.2 EP bullet: pick the token's expert group,
+// then Top-k inside it): experts form n_group contiguous groups of gsz; a
+// group scores its largest logit; the topk_group best groups (ties: lower
+// group) are kept and the k experts are chosen among theirs.  n_group = 1 is
+// plain top-k.  lse, when set, receives log sum_e exp(l[t,e]) per token for
+// the router z-loss.
+struct RouteSel {
+    int n_group;      // 1..32
+    int gsz;          // E / n_group
+    int topk_group;   // 1..n_group
+    float* lse;       // [T] or nullptr
+};
+
+// Group mask of one token (bit g set: group g kept), lane l holding the
+// logits of experts l, l+32, ...: topk_group rounds of warp argmax over the
+// experts of groups not yet kept; the winner's group is kept next.  The
+// argmax orders by (logit desc, index asc), so equal group scores go to the
+// lower group.  All ones when n_group = 1.
+template <int EPL>
+__device__ __forceinline__ unsigned keep_groups(const float* l, const int* grp, int E, const RouteSel& sel,
+                                                int lane)
+{
+    if (sel.n_group <= 1) return 0xffffffffu;
+    unsigned keep = 0;
+    for (int r = 0; r < sel.topk_group; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((keep >> grp[i]) & 1u) && (l[i] > bv || (l[i] == bv && e < bi))) {
+                bv = l[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi < E) keep |= 1u << (bi / sel.gsz);
+    }
+    return keep;
+}
+
 static inline int ceil_div_i(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -193,10 +193,6 @@ bool make_tmap_bf16_box(CUtensorMap* m, const void* base, unsigned long long row
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-bool make_tmap_bf16(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols)
-{
-    return make_tmap_bf16_box(m, base, rows, cols, 128);
-}
 
 // A_rows: rows of the A tensor (rows_max of x_perm, or T of x when gathering).
 template <int EPI, int BN, bool GATHER = false>
@@ -292,14 +288,14 @@ moe_status launch_simt(const float* A, const int32_t* offsets, const int32_t* ke
 
 template <int EPL, int TW>
 void launch_route(bool bf16, int nblk, const void* x, const float* W, const float* b, int T, int d, int E, int k,
-                  int renorm, int32_t* idx, float* gate, float* partial, cudaStream_t s)
+                  int renorm, int32_t* idx, float* gate, float* partial, RouteSel sel, cudaStream_t s)
 {
     if (bf16)
         route::route_kernel<EPL, TW, true><<<nblk, route::THREADS, 0, s>>>(x, W, b, T, d, E, k, renorm, idx, gate,
-                                                                           partial);
+                                                                           partial, sel);
     else
         route::route_kernel<EPL, TW, false><<<nblk, route::THREADS, 0, s>>>(x, W, b, T, d, E, k, renorm, idx, gate,
-                                                                            partial);
+                                                                            partial, sel);
 }
 
 __global__ void selftest_wait_kernel(unsigned long long limit)
@@ -360,11 +356,10 @@ size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F,
     return 0;
 }
 
-moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const float* b_router, int64_t T, int d,
-                     int E, int k, int renorm, int32_t* topk_idx, float* topk_gate, float* prob_sum, void* ws,
-                     size_t ws_bytes, moe_stream_t stream_)
+static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router, const float* b_router, int64_t T,
+                             int d, int E, int k, int renorm, int32_t* topk_idx, float* topk_gate, float* prob_sum,
+                             RouteSel sel, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
-    cudaStream_t stream = (cudaStream_t)stream_;
     if (T < 0 || d <= 0 || E < 1 || E > MAX_E || k < 1 || k > MAX_K || k > E || !dtype_ok(xdt))
         return MOE_ERR_INVALID_ARG;
     if (T * k >= INT_MAX || (long long)T * d >= (1LL << 40)) return MOE_ERR_INVALID_ARG;
@@ -419,9 +414,9 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
         const int Ti = (int)T;
         const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16;
 #define MOE_FIN_LANE(EM, KM) rtc::route_finish_lane_kernel<EM, KM><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
-    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum)
+    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum, sel)
 #define MOE_FIN_WARP(EP) rtc::route_finish_warp_kernel<EP><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
-    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum)
+    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum, sel)
         if (E <= 16) {
             if (kmax == 2) MOE_FIN_LANE(16, 2);
             else if (kmax == 4) MOE_FIN_LANE(16, 4);
@@ -453,15 +448,43 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
         const bool bf = xdt == MOE_BF16;
         const int Ti = (int)T;
         switch (route_epl(E)) {
-        case 1: launch_route<1, 2>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
-        case 2: launch_route<2, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
-        case 4: launch_route<4, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
-        default: launch_route<8, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, stream); break;
+        case 1: launch_route<1, 2>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, sel, stream); break;
+        case 2: launch_route<2, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, sel, stream); break;
+        case 4: launch_route<4, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, sel, stream); break;
+        default: launch_route<8, 4>(bf, nblk, x, w_router, b_router, Ti, d, E, k, renorm, topk_idx, topk_gate, partial, sel, stream); break;
         }
         const moe_status st = launch_status();
         if (st != MOE_OK) return st;
     }
     route::route_finalize<<<1, route::FIN_THREADS, 0, stream>>>(partial, nblk, E, prob_sum);
+    return launch_status();
+}
+
+moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const float* b_router, int64_t T, int d,
+                     int E, int k, int renorm, int32_t* topk_idx, float* topk_gate, float* prob_sum, void* ws,
+                     size_t ws_bytes, moe_stream_t stream)
+{
+    const RouteSel plain{1, E > 0 ? E : 1, 1, nullptr};
+    return route_impl(x, xdt, w_router, b_router, T, d, E, k, renorm, topk_idx, topk_gate, prob_sum, plain, ws,
+                      ws_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_route_ex(const void* x, moe_dtype xdt, const float* w_router, const float* b_router, int64_t T, int d,
+                        int E, int k, int renorm, int n_group, int topk_group, int32_t* topk_idx, float* topk_gate,
+                        float* prob_sum, float* lse, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (n_group < 1 || n_group > 32 || E < 1 || E % n_group || topk_group < 1 || topk_group > n_group)
+        return MOE_ERR_INVALID_ARG;
+    if ((long long)k > (long long)topk_group * (E / n_group)) return MOE_ERR_INVALID_ARG;
+    const RouteSel sel{n_group, E / n_group, topk_group, T > 0 ? lse : nullptr};
+    return route_impl(x, xdt, w_router, b_router, T, d, E, k, renorm, topk_idx, topk_gate, prob_sum, sel, ws,
+                      ws_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_stream_t stream)
+{
+    if (T <= 0 || !lse || !loss) return MOE_ERR_INVALID_ARG;
+    combine::z_loss_kernel<<<1, combine::ZL_THREADS, 0, (cudaStream_t)stream>>>(lse, (long long)T, beta, loss);
     return launch_status();
 }
 

@@ -24,7 +24,7 @@ template <int EPL, int TW, bool BF16>
 __global__ void __launch_bounds__(THREADS)
 route_kernel(const void* __restrict__ x, const float* __restrict__ W, const float* __restrict__ bias,
              int T, int d, int E, int k, int renorm, int32_t* __restrict__ idx_out,
-             float* __restrict__ gate_out, float* __restrict__ partial)
+             float* __restrict__ gate_out, float* __restrict__ partial, RouteSel sel)
 {
     constexpr int EP = 32 * EPL;
     constexpr int TM = WARPS * TW;
@@ -94,8 +94,12 @@ route_kernel(const void* __restrict__ x, const float* __restrict__ W, const floa
     }
 
     float psum[EPL];
+    int grp[EPL];   // group of each of this lane's experts
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) psum[i] = 0.f;
+    for (int i = 0; i < EPL; ++i) {
+        psum[i] = 0.f;
+        grp[i] = (lane + 32 * i) / sel.gsz;
+    }
 
 #pragma unroll
     for (int a = 0; a < TW; ++a) {
@@ -119,13 +123,15 @@ route_kernel(const void* __restrict__ x, const float* __restrict__ W, const floa
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (sel.lse && lane == 0) sel.lse[t] = mx + logf(s);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             p[i] = p[i] / s;
             psum[i] += p[i];
         }
+        const unsigned gkeep = keep_groups<EPL>(l, grp, E, sel, lane);
 
-        // k rounds of warp argmax on (logit desc, index asc)
+        // k rounds of warp argmax on (logit desc, index asc) over the kept groups
         unsigned taken = 0;
         int my_e = 0;
         float my_p = 0.f, chosen = 0.f;
@@ -135,7 +141,8 @@ route_kernel(const void* __restrict__ x, const float* __restrict__ W, const floa
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
                 const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && (l[i] > bv || (l[i] == bv && e < bi))) {
+                if (e < E && !((taken >> i) & 1u) && ((gkeep >> grp[i]) & 1u) &&
+                    (l[i] > bv || (l[i] == bv && e < bi))) {
                     bv = l[i];
                     bi = e;
                 }

@@ -259,15 +259,17 @@ template <int EMAX, int KMAX>
 __global__ void __launch_bounds__(FIN_THREADS)
 route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, int E_pad, int k, int renorm,
                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
-                         float* __restrict__ gate_out, float* __restrict__ psum)
+                         float* __restrict__ gate_out, float* __restrict__ psum, RouteSel sel)
 {
     __shared__ float red[FIN_WARPS][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float bia[EMAX], acc_p[EMAX];
+    int grp[EMAX];
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         bia[e] = (bias && e < E) ? __ldg(bias + e) : 0.f;
         acc_p[e] = 0.f;
+        grp[e] = e / sel.gsz;
     }
     for (int t = (blockIdx.x * FIN_WARPS + warp) * 32 + lane; t < T; t += gridDim.x * FIN_THREADS) {
         float l[EMAX];
@@ -299,12 +301,30 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
             tv[j] = -INFINITY;
             ti[j] = 0x7fffffff;
         }
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) l[e] = (e < E) ? l[e] + bia[e] : -INFINITY;
+        // group-limited routing: keep the topk_group groups of largest max logit
+        // (strict > scanning up the index keeps the lower group on ties)
+        unsigned gkeep = 0xffffffffu;
+        if (sel.n_group > 1) {
+            gkeep = 0;
+            for (int r = 0; r < sel.topk_group; ++r) {
+                float bv = -INFINITY;
+                int bg = -1;
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e)
+                    if (e < E && !((gkeep >> grp[e]) & 1u) && (bg < 0 || l[e] > bv)) {
+                        bv = l[e];
+                        bg = grp[e];
+                    }
+                if (bg >= 0) gkeep |= 1u << bg;
+            }
+        }
         float mx = -INFINITY;
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
-            l[e] = (e < E) ? l[e] + bia[e] : -INFINITY;
             mx = fmaxf(mx, l[e]);
-            if (e < E) {
+            if (e < E && ((gkeep >> grp[e]) & 1u)) {
                 // insert into the descending top list; equal values keep the lower index ahead
                 const float v = l[e];
                 if (v > tv[KMAX - 1]) {
@@ -331,6 +351,7 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
             p[e] = (e < E) ? expf(l[e] - mx) : 0.f;
             s += p[e];
         }
+        if (sel.lse) sel.lse[t] = mx + logf(s);
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) acc_p[e] += p[e] / s;
         float chosen = 0.f;
@@ -360,16 +381,18 @@ template <int EPL>
 __global__ void __launch_bounds__(FIN_THREADS)
 route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, int E_pad, int k, int renorm,
                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
-                         float* __restrict__ gate_out, float* __restrict__ psum)
+                         float* __restrict__ gate_out, float* __restrict__ psum, RouteSel sel)
 {
     __shared__ float red[FIN_WARPS][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float bia[EPL], acc_p[EPL];
+    int grp[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         bia[i] = (bias && e < E) ? __ldg(bias + e) : 0.f;
         acc_p[i] = 0.f;
+        grp[i] = e / sel.gsz;
     }
     for (int t = blockIdx.x * FIN_WARPS + warp; t < T; t += gridDim.x * FIN_WARPS) {
         float l[EPL];
@@ -390,11 +413,13 @@ route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, in
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (sel.lse && lane == 0) sel.lse[t] = mx + logf(s);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             p[i] = p[i] / s;
             acc_p[i] += p[i];
         }
+        const unsigned gkeep = keep_groups<EPL>(l, grp, E, sel, lane);
         unsigned taken = 0;
         int my_e = 0;
         float my_p = 0.f, chosen = 0.f;
@@ -404,7 +429,8 @@ route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, in
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
                 const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && (l[i] > bv || (l[i] == bv && e < bi))) {
+                if (e < E && !((taken >> i) & 1u) && ((gkeep >> grp[i]) & 1u) &&
+                    (l[i] > bv || (l[i] == bv && e < bi))) {
                     bv = l[i];
                     bi = e;
                 }
