@@ -2,6 +2,7 @@
 """Benchmark of the MoE-layer forward on B300: one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--n-group G --topk-group M] [--z-beta B] [--aux-post-drop] [--gather]
 
 A step is one whole layer forward (route, dispatch, expert up/down GEMMs,
 combine, aux loss) over one batch of seeded synthetic tokens already resident
@@ -29,6 +30,12 @@ the same workload (its first S tokens, capacity recomputed for S tokens).
 ``--impl reference``: the CPU oracle alone on the host cores (the method has
 no other runnable implementation); rank 0 only.
 
+Variants (same step, same JSON line; ``config.variant`` names them):
+group-limited routing (``--n-group``/``--topk-group``), the router z-loss
+(``--z-beta``), the post-drop f_i aux loss (``--aux-post-drop``) and the
+up-projection that gathers x rows itself instead of a permuted copy
+(``--gather``).
+
 With torchrun (N>1) every rank runs its own independent batch (seed + rank):
 the layer forward needs no exchange between GPUs, so scaling is weak (a
 global aux loss over all ranks' tokens would add one all-reduce of 2E + 1
@@ -54,12 +61,26 @@ from top_routing_expert_02_b300 import synth  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s and grouped-GEMM TFLOP/s (% BF16 peak) on 1 B300"
 L2_FLUSH_BYTES = 512 << 20
-def KERNELS_PER_STEP_TOTAL(cfg) -> int:
+def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     """Library kernels launched by one layer forward of this workload (the
     device-timed region launches exactly these, K times)."""
     tc_router = cfg.dtype == "bf16" and cfg.E <= 160
     route = 4 if tc_router else 2          # split + logits + finish + prob sums | router + sums
-    return route + 3 + 1 + 1 + 1 + 1      # dispatch (3), up, down, combine, aux
+    gather = bool(args and args.gather)
+    dispatch = 2 if gather else 3          # histogram, ranks (+ row copy)
+    z = 1 if (args and args.z_beta is not None) else 0
+    return route + dispatch + 1 + 1 + 1 + 1 + z   # up, down, combine, aux (+ z-loss)
+
+
+def plan_kwargs(args) -> dict:
+    return dict(gather=args.gather, n_group=args.n_group, topk_group=args.topk_group, z_beta=args.z_beta,
+                aux_post_drop=args.aux_post_drop)
+
+
+def variant_dict(args) -> dict:
+    return {"n_group": args.n_group, "topk_group": args.topk_group, "z_beta": args.z_beta,
+            "aux_f": "kept slots (post-drop)" if args.aux_post_drop else "every choice (pre-drop)",
+            "up_projection": "gathers x rows (no x_perm)" if args.gather else "reads x_perm"}
 
 
 def peaks():
@@ -164,17 +185,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU oracle --
-def oracle_sample(cfg: synth.MoEConfig, ri, w1, w2, budget_s: float = 15.0):
+def oracle_variant(args) -> dict:
+    """The routing variant's switches in the oracle's terms."""
+    return dict(n_group=args.n_group, topk_group=args.topk_group, z_beta=args.z_beta or 0.0,
+                aux_post_drop=args.aux_post_drop)
+
+
+def oracle_sample(cfg: synth.MoEConfig, ri, w1, w2, budget_s: float = 15.0, variant=None):
     """Time the CPU oracle on the first S tokens (S grown until ~budget_s)."""
     import oracle
     w1h, w2h = w1.cpu(), w2.cpu()
+    variant = variant or {}
 
     def run(S):
         sub = ri.x[:S].contiguous()
         cap = oracle.capacity(S, cfg.E, cfg.cf)
         t0 = time.perf_counter()
         oracle.forward(sub, ri.W, ri.b, w1h, w2h, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
-                       alpha=cfg.alpha)
+                       alpha=cfg.alpha, **variant)
         return time.perf_counter() - t0
 
     S = min(cfg.T, 8)
@@ -194,7 +222,9 @@ def reference_arm(args, cfg):
         return
     ri = synth.make_routing_inputs(cfg)
     w1, w2 = synth.make_expert_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
-    cb, S, t = oracle_sample(cfg, ri, w1, w2, budget_s=max(0.2, 120.0 / max(1, args.steps + args.warmup)))
+    var = oracle_variant(args)
+    cb, S, t = oracle_sample(cfg, ri, w1, w2, budget_s=max(0.2, 120.0 / max(1, args.steps + args.warmup)),
+                             variant=var)
     # warm-up and timed steps: each step is the bounded sample
     import oracle
     w1h, w2h = w1.cpu(), w2.cpu()
@@ -204,7 +234,7 @@ def reference_arm(args, cfg):
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         oracle.forward(sub, ri.W, ri.b, w1h, w2h, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
-                       alpha=cfg.alpha)
+                       alpha=cfg.alpha, **var)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     ms = 1000.0 * statistics.mean(times)
@@ -213,14 +243,15 @@ def reference_arm(args, cfg):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_dict(cfg), "cpu_baseline": cb,
+            "config": config_dict(cfg, args), "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def config_dict(cfg):
+def config_dict(cfg, args=None):
     return {"workload": cfg.name, "description": cfg.describe(), "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
             "F": cfg.F, "act": cfg.act, "cf": cfg.cf, "renorm": cfg.renorm, "alpha": cfg.alpha,
+            **({"variant": variant_dict(args)} if args is not None else {}),
             "l2": "device-timed steps: L2 flushed before every step (512 MB write); e2e steps: x arrives by a "
                   "host-to-device copy every step, weights (GBs) exceed L2"}
 
@@ -269,7 +300,8 @@ def our_arm(args, cfg):
     b = None if ri.b is None else ri.b.to(dev)
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     cap = moe.capacity(cfg.T, cfg.E, cfg.cf)
-    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm)
+    pk = plan_kwargs(args)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm, **pk)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     D = plan.disp
@@ -280,16 +312,23 @@ def our_arm(args, cfg):
                 evs[i].record(stream)
         mark(0)
         moe.route(x, W, b, plan.k, plan.renorm, topk_idx=plan.topk_idx, topk_gate=plan.topk_gate,
-                  prob_sum=plan.prob_sum, ws=plan.ws_route)
+                  prob_sum=plan.prob_sum, ws=plan.ws_route, n_group=plan.n_group, topk_group=plan.topk_group,
+                  lse=plan.lse)
         mark(1)
         moe.dispatch(plan.topk_idx, plan.topk_gate, x, plan.E, plan.cap, out=D, ws=plan.ws_dispatch)
         mark(2)
-        moe.expert_up(D.x_perm, D.offsets, D.kept, w1, plan.F, plan.act, plan.rows_max, h=plan.h)
+        if plan.gather:
+            moe.expert_up_gathered(x, D.row_token, D.offsets, D.kept, w1, plan.F, plan.act, plan.rows_max,
+                                   h=plan.h)
+        else:
+            moe.expert_up(D.x_perm, D.offsets, D.kept, w1, plan.F, plan.act, plan.rows_max, h=plan.h)
         mark(3)
         moe.expert_down(plan.h, D.offsets, D.kept, w2, D.row_gate, plan.rows_max, y_perm=plan.y_perm)
         mark(4)
         moe.combine(plan.y_perm, D.slot_row, y=plan.y)
-        moe.aux_loss(D.counts, plan.prob_sum, plan.T, plan.alpha, loss=plan.loss)
+        moe.aux_loss(D.kept if plan.aux_post_drop else D.counts, plan.prob_sum, plan.T, plan.alpha, loss=plan.loss)
+        if plan.z_beta is not None:
+            moe.z_loss(plan.lse, plan.z_beta, loss=plan.z_loss)
         mark(5)
 
     def barrier():
@@ -328,7 +367,7 @@ def our_arm(args, cfg):
 
     # the same step as one CUDA-graph replay (removes launch gaps between the calls)
     gx = x.clone()
-    gplan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm)
+    gplan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm, **pk)
     graph = gplan.capture(gx, W, b, w1, w2)
     for _ in range(args.warmup):
         flush.zero_()
@@ -351,7 +390,8 @@ def our_arm(args, cfg):
     # end to end through the public API: pinned host x in, y + loss out, as a
     # three-stream pipeline (copy in / layer / copy out) over two buffer sets, so
     # step i+1's input copy and step i-1's output copy overlap step i's layer
-    plans = [plan, moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm)]
+    plans = [plan, moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, tdt, cap, dev, cfg.alpha, cfg.renorm,
+                               **pk)]
     x_host = ri.x.pin_memory()
     y_host = [torch.empty((cfg.T, cfg.d), dtype=tdt).pin_memory() for _ in range(2)]
     loss_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -415,11 +455,11 @@ def our_arm(args, cfg):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded; weights random-init)",
-        "config": config_dict(cfg),
+        "config": config_dict(cfg, args),
         "clocks": sampler.summary(),
         "e2e": {"value": world * cfg.T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": cfg.T * cfg.d * esz, "d2h_bytes_per_step": cfg.T * cfg.d * esz + 4},
-        "gpu_launches": KERNELS_PER_STEP_TOTAL(cfg) * args.steps,
+        "gpu_launches": KERNELS_PER_STEP_TOTAL(cfg, args) * args.steps,
         "roofline": {"kernel": "expert_up (tcgen05 grouped GEMM + activation)", "bound": "tensor",
                      "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s", "frac": achieved / bf16_peak,
                      "peak_source": f"{peak_src} bf16 dense burst", "traffic": traffic,
@@ -432,7 +472,7 @@ def our_arm(args, cfg):
                     float(counts.max()) / (cfg.T * cfg.k / cfg.E)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb, _, _ = oracle_sample(cfg, ri, w1, w2)
+        cb, _, _ = oracle_sample(cfg, ri, w1, w2, variant=oracle_variant(args))
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -448,6 +488,11 @@ def main():
     ap.add_argument("--workload", default="e8_swiglu", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-group", type=int, default=1, help="group-limited routing: contiguous expert groups")
+    ap.add_argument("--topk-group", type=int, default=1, help="groups kept per token")
+    ap.add_argument("--z-beta", type=float, default=None, help="router z-loss coefficient (off when absent)")
+    ap.add_argument("--aux-post-drop", action="store_true", help="aux loss f_i from kept slots")
+    ap.add_argument("--gather", action="store_true", help="up-projection gathers x rows (bf16 only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     args.steps = max(args.steps, 1)

@@ -191,9 +191,10 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
 /* moe_expert_up reading its A rows straight from x: row r of the permuted
  * order is x[row_token[r]] (row_token from moe_dispatch), so the dispatch can
  * skip materialising x_perm (the tutorial's §5.3 packs tokens for contiguous
- * transfer; here TMA four-row gathers read them in place).
- *   x [T, d] bf16; row_token [rows_max]; other arguments as moe_expert_up.
- * BF16 only (MOE_ERR_UNSUPPORTED otherwise). */
+ * transfer; here the GEMM's producer copies the rows in place).
+ *   x [T, d] bf16, 16-byte aligned, T * d * 2 < 2^32 bytes (else
+ *   MOE_ERR_UNSUPPORTED); row_token [rows_max]; other arguments as
+ *   moe_expert_up.  BF16 only (MOE_ERR_UNSUPPORTED otherwise). */
 moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_token, const int32_t* offsets,
                                   const int32_t* kept, int E, int d, int F, moe_act act, moe_dtype dtype,
                                   const void* w1, int64_t rows_max, void* h, moe_stream_t stream);

@@ -114,3 +114,17 @@ def test_routing_variant_full_size_e128_top8_T8192():
     compare_output(plan, ref, cfg.dtype)
     compare_z_loss(plan, ref, cfg.dtype)
     assert (slot >= 0).all()
+
+
+@pytest.mark.parametrize("T,offset", [(1, 0), (4097, 0), (4097, 1), (32768, 0), (33, 3)])
+def test_z_loss_kernel_against_oracle_on_given_values(T, offset):
+    """moe_z_loss on stored log-sum-exp values (aligned or not, any length)
+    equals the oracle's z-loss of the same fp32 values."""
+    import oracle
+    g = torch.Generator().manual_seed(T + offset)
+    host = (torch.rand(T + offset, generator=g) * 6.0 - 1.0).float()
+    dev = host.cuda()[offset:]
+    z = moe.z_loss(dev, 1e-3)
+    moe.check()
+    ref = oracle.z_loss(host[offset:].double().numpy(), 1e-3)
+    assert abs(z.item() - ref) <= 1e-6 * abs(ref)

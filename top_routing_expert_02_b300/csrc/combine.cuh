@@ -80,18 +80,37 @@ __global__ void aux_loss_kernel(const int32_t* __restrict__ counts, const float*
 
 // Router z-loss (the ms-swift ETP page names a routing z-loss that spreads
 // the router's choices; its formula is the one of ST-MoE, Zoph et al. 2022,
-// eq. 5): loss = beta * (1/T) * sum_t lse[t]^2.  One block, strided fp64
-// partial sums, then a fixed shared-memory tree: the result does not depend
-// on timing.
+// eq. 5): loss = beta * (1/T) * sum_t lse[t]^2.  One block: each thread sums
+// the squares of its elements (16-byte loads, eight in flight, when lse is
+// 16-byte aligned), then a fixed shared-memory tree in fp64; the result does
+// not depend on timing.
 constexpr int ZL_THREADS = 1024;
 __global__ void __launch_bounds__(ZL_THREADS)
 z_loss_kernel(const float* __restrict__ lse, long long T, float beta, float* __restrict__ loss)
 {
     __shared__ double sh[ZL_THREADS];
     double s = 0.0;
-    for (long long t = threadIdx.x; t < T; t += ZL_THREADS) {
-        const double v = (double)__ldg(lse + t);
-        s += v * v;
+    long long done = 0;
+    if ((reinterpret_cast<uintptr_t>(lse) & 15u) == 0) {
+        const float4* v = reinterpret_cast<const float4*>(lse);
+        const long long n4 = T / 4;
+        for (long long i0 = threadIdx.x; i0 < n4; i0 += 8 * ZL_THREADS) {
+            float4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long i = i0 + (long long)u * ZL_THREADS;
+                q[u] = i < n4 ? __ldg(v + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                s += (double)q[u].x * q[u].x + (double)q[u].y * q[u].y + (double)q[u].z * q[u].z +
+                     (double)q[u].w * q[u].w;
+        }
+        done = n4 * 4;
+    }
+    for (long long t = done + threadIdx.x; t < T; t += ZL_THREADS) {
+        const double x = (double)__ldg(lse + t);
+        s += x * x;
     }
     sh[threadIdx.x] = s;
     __syncthreads();

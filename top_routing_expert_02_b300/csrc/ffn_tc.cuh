@@ -67,6 +67,8 @@ struct Args {
     uint16_t* out;     // bf16 [rows_max, out_cols]
     const float* row_gate;
     const int32_t* row_token;   // gathered A: row r of the tile is x[row_token[r]]
+    const uint8_t* a_base;      // gathered A: x
+    uint32_t a_row_bytes;       // gathered A: bytes of one x row (x is below 4 GB)
     unsigned long long wait_limit;
 };
 
@@ -82,9 +84,33 @@ __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tile
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
+// Byte offsets in x of the 32 rows lane `lane` copies for `tile` (rows
+// 4i + lane/8, plus its 16-byte chunk lane%8); rows past the expert's segment
+// repeat a valid token (they are computed, never stored).
+template <int N>
+__device__ __forceinline__ void gather_offsets(const Args& g, const int* mstart, int tile, int lane, uint32_t (&off)[N])
+{
+    int e, m, n;
+    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+    const int rowA = __ldg(g.offsets + e) + m * BM;
+    const int rows_valid = __ldg(g.kept + e) - m * BM;
+    const int first = __ldg(g.row_token + rowA);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int r = 4 * i + (lane >> 3);
+        const int tok = r < rows_valid ? __ldg(g.row_token + rowA + r) : first;
+        off[i] = (uint32_t)tok * g.a_row_bytes + (uint32_t)(lane & 7) * 16u;
+    }
+}
+
 // GATHER: the A rows are read straight from x at row_token[] (the dispatch
-// permutation) with TMA four-row gathers issued by the 32 lanes of the
-// producer warp, so no permuted copy of x is materialised.
+// permutation), so no permuted copy of x is materialised.  The 32 lanes of
+// the producer warp copy them with 16-byte cp.async (lane l: chunk l % 8 of
+// rows 4i + l / 8, written to the 128-byte-swizzled place a TMA box load would
+// use), and each lane's copies of a stage arrive on its full barrier when they
+// land (33 arrivals: 32 lanes + lane 0's TMA transaction arrival for the B
+// tile).  Those are generic-proxy writes: the MMA thread fences them into the
+// async proxy after its wait and before its tcgen05.mma reads them.
 template <int EPI, int BN, bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -104,7 +130,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), GATHER ? 33 : 1);
             ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -136,23 +162,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
+            uint32_t roff[GATHER ? 32 : 1];   // gathered rows: this lane's 32 offsets in x
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 int e, m, n;
                 decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
                 const int rowA = __ldg(g.offsets + e) + m * BM;
                 const int rowB0 = e * g.b_rows + n * g.n_step;
                 const int rowB1 = rowB0 + g.half_off;
-                int gr[4] = {0, 0, 0, 0};
-                if (GATHER) {
-                    // lane l gathers tile rows 4l..4l+3; rows past the segment repeat a valid token
-                    const int rows_valid = __ldg(g.kept + e) - m * BM;
-                    const int first = __ldg(g.row_token + rowA);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = 4 * lane + i;
-                        gr[i] = r < rows_valid ? __ldg(g.row_token + rowA + r) : first;
-                    }
-                }
+                if (GATHER) gather_offsets(g, mstart, tile, lane, roff);
                 for (int kb = 0; kb < nk; ++kb) {
                     bool got = true;
                     if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit);
@@ -164,16 +181,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
                     const uint32_t sa = smem0 + stage * STAGE_BYTES;
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        ptx::mbar_arrive_expect_tx(fb, GATHER ? 2 * BH_BYTES : STAGE_BYTES);
                         if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kb * BK, rowA);
                         ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, rowB0);
                         ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kb * BK, rowB1);
                     }
                     if (GATHER) {
-                        __syncwarp();   // the expect_tx above is posted before any lane's bytes land
-                        // four 128-byte rows per lane at 512-byte steps: the 128B swizzle follows the
-                        // shared-memory address, so the tile ends up as one 128-row box load would leave it
-                        ptx::tma_gather4_2d(sa + lane * 512, &tmA, fb, kb * BK, gr[0], gr[1], gr[2], gr[3]);
+                        const uint8_t* src = g.a_base + (size_t)kb * (BK * 2);
+                        const int c = lane & 7;
+#pragma unroll
+                        for (int i = 0; i < (GATHER ? 32 : 1); ++i) {
+                            const int r = 4 * i + (lane >> 3);
+                            ptx::cp_async_16(sa + r * 128 + ((c ^ (r & 7)) << 4), src + roff[i]);
+                        }
+                        ptx::cp_async_mbar_arrive_noinc(fb);
                     }
                     ++fills;
                     if (++stage == STAGES) {
@@ -182,6 +203,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             }
+            if (GATHER) ptx::cp_async_wait<0>();
             if (lane == 0) {
                 if (!ok) moe_flag(MOE_DEV_TIMEOUT);
                 // drain: the last fill of every stage must have landed before exit
@@ -214,6 +236,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         break;
                     }
                     ptx::tc_fence_after();
+                    if (GATHER) ptx::fence_proxy_async_smem();   // the A tile came through the generic proxy
                     const uint32_t sa = smem0 + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)

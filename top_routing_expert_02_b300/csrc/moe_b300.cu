@@ -601,6 +601,9 @@ moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_t
     if (T < 0 || T >= INT_MAX || !w1 || (rows_max > 0 && (!x || !row_token || !h))) return MOE_ERR_INVALID_ARG;
     if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0 || T == 0) return MOE_OK;
+    // the copies address x with 32-bit row offsets and 16-byte vectors
+    if ((unsigned long long)T * (unsigned long long)d * 2ull >= (1ull << 32) || ((uintptr_t)x & 15u))
+        return MOE_ERR_UNSUPPORTED;
     const int N1 = act == MOE_ACT_SWIGLU ? 2 * F : F;
     tcg::Args a{};
     a.offsets = offsets;
@@ -612,6 +615,8 @@ moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_t
     a.out = (uint16_t*)h;
     a.row_gate = nullptr;
     a.row_token = row_token;
+    a.a_base = (const uint8_t*)x;
+    a.a_row_bytes = (uint32_t)d * 2u;
     a.wait_limit = g_wait_limit.load();
     const bool sw = act == MOE_ACT_SWIGLU;
     a.n_step = sw ? 128 : 256;

@@ -62,11 +62,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
-// Orders this thread's generic-proxy shared-memory accesses after the
-// async-proxy (TMA / tensor core) accesses it has synchronised with.
+// Orders this thread's generic-proxy shared-memory accesses against async-proxy
+// (TMA / tensor core) ones: after consuming what the async proxy wrote, and
+// before handing what this thread wrote (stores, completed cp.async copies)
+// to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16-byte asynchronous global -> shared copy through L2 (no L1 allocation).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread issued so far has landed;
+// the arrival is not pre-counted (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Wait until at most N of this thread's committed copy groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ----------------------------------------------------------------- TMA ---
@@ -84,19 +105,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(map), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// Four rows of a 2-D tensor at arbitrary row indices, columns [c0, c0 + box
-// width): the tensor map's box is one row high; the rows land one after the
-// other at dst (128-byte rows for a 64-element bf16 box).
-__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int r0,
-                                               int r1, int r2, int r3)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(map), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
         : "memory");
 }
 
