@@ -103,3 +103,63 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     finally:
         oracle._lib = saved
     assert caught, f"no pin caught the planted mistake {name!r}"
+
+
+# ---------------------------------------------------------------- backward ---
+
+import importlib.util  # noqa: E402
+
+import test_oracle_backward as PB  # noqa: E402
+
+BWD_SRC = os.path.join(os.path.dirname(oracle.__file__), "backward.py")
+
+BWD_MUTANTS = {
+    "gate left out of do": ("dO = g[:, None] * DY[ts]", "dO = DY[ts]"),
+    "softmax backward without the mean term": ("dL = P * (dP - np.sum(P * dP, axis=1, keepdims=True))",
+                                               "dL = P * dP"),
+    "renormalisation backward without the coupling term": (
+        "dP[t, sel] += (dgate[t] - np.dot(dgate[t], gate[t])) / S", "dP[t, sel] += dgate[t] / S"),
+    "silu derivative taken as the sigmoid": ("dsilu = s * (1.0 + gate * (1.0 - s))", "dsilu = s"),
+    "GELU derivative without the density term": ("return da * (cdf + z * pdf)", "return da * cdf"),
+    "z-loss gradient without the factor 2": ("(2.0 * z_beta / T)", "(z_beta / T)"),
+    "aux gradient without the 1/T of P_i": ("dP += aux_weight * alpha * E * f[None, :] / T",
+                                            "dP += aux_weight * alpha * E * f[None, :]"),
+    "expert input gradient dropped": ("np.add.at(dX, ts, dZ @ W1[e])", "pass"),
+    "w2 gradient from the ungated dy": ("dW2[e] = dO.T @ A", "dW2[e] = DY[ts].T @ A"),
+    "router input gradient dropped": ("dX += dL @ Wr", "pass"),
+}
+
+
+def _bwd_pins():
+    return [
+        ("autograd", lambda: [PB.test_backward_matches_autograd(i) for i in range(len(PB.CFGS))]),
+        ("finite differences", lambda: PB.test_backward_matches_finite_differences_of_the_c_forward(0)),
+        ("identity", PB.test_identity_experts_pass_dy_through),
+        ("uniform aux", PB.test_aux_loss_gradient_of_a_uniform_router),
+    ]
+
+
+@pytest.mark.parametrize("name", list(BWD_MUTANTS))
+def test_backward_pins_catch_planted_mistake(name, tmp_path):
+    old, new = BWD_MUTANTS[name]
+    src = open(BWD_SRC).read()
+    assert src.count(old) == 1, f"mutation site of {name!r} not found exactly once"
+    path = tmp_path / "backward_mutant.py"
+    path.write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location("oracle.backward_mutant", str(path),
+                                                  submodule_search_locations=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    spec.loader.exec_module(mod)
+    saved = PB.B
+    PB.B = mod
+    caught = []
+    try:
+        for pin, fn in _bwd_pins():
+            try:
+                fn()
+            except AssertionError:
+                caught.append(pin)
+    finally:
+        PB.B = saved
+    assert caught, f"no pin caught {name!r}"
