@@ -19,6 +19,15 @@
  * Routing variants from the ms-swift pages: moe_route_ex (group-limited
  * top-k, per-token log-sum-exp) and moe_z_loss (router z-loss).
  *
+ * Backward (the layer is trained through the same steps in reverse: the
+ * tutorial's §5.1 aux loss acts through its gradient, and the guide's 步骤三
+ * item 3 returns the gradients by the reverse exchange; the pages give no
+ * formula, so each call computes a derivative of the forward):
+ *   moe_combine_bwd, moe_act_bwd, moe_route_bwd, moe_grad_x,
+ *   moe_router_wgrad, moe_expert_wgrad (+ moe_pack_segments_t), with
+ *   moe_expert_up reused for the data-gradient GEMMs on transposed weights
+ *   (moe_transpose_experts) and for recomputing the pre-activation.
+ *
  * Conventions shared by every call
  * --------------------------------
  * Ownership   The caller allocates and owns every buffer (inputs, outputs,
@@ -75,7 +84,7 @@ typedef enum {
     MOE_ACT_IDENTITY = 2   /* h = z; for checks (identity experts)                 */
 } moe_act;
 
-typedef enum { MOE_CALL_ROUTE = 0, MOE_CALL_DISPATCH = 1, MOE_CALL_FFN = 2 } moe_call;
+typedef enum { MOE_CALL_ROUTE = 0, MOE_CALL_DISPATCH = 1, MOE_CALL_FFN = 2, MOE_CALL_ROUTER_WGRAD = 3 } moe_call;
 
 /* ---------------------------------------------------------------- host --- */
 
@@ -138,10 +147,12 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
  *               k <= topk_group * E / n_group (else MOE_ERR_INVALID_ARG)
  *   lse         [T] fp32 or NULL: log sum_e exp(l[t,e]) per token, the
  *               input of moe_z_loss
+ *   logits      [T, E] fp32 or NULL: the logits (bias included), the input
+ *               of moe_route_bwd
  * Other arguments, outputs and workspace as moe_route. */
 moe_status moe_route_ex(const void* x, moe_dtype xdt, const float* w_router, const float* b_router,
                         int64_t T, int d, int E, int k, int renorm, int n_group, int topk_group,
-                        int32_t* topk_idx, float* topk_gate, float* prob_sum, float* lse,
+                        int32_t* topk_idx, float* topk_gate, float* prob_sum, float* lse, float* logits,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Dispatch: tutorial §2.1 steps 2-3 (dispatch plan, token exchange) and
@@ -242,6 +253,91 @@ moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T,
  * Summed in fp64 in a fixed order on the device, stored as fp32 to loss[0]
  * (device pointer).  T must be >= 1. */
 moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_stream_t stream);
+
+/* ------------------------------------------------------------ backward --- */
+/* Gradients of L = <dy, y> + aux_weight * L_aux + z_weight * L_z.  The top-k
+ * choice, the capacity cut and f_e carry no gradient; a dropped slot's gate
+ * gets none either.  bf16 layers only (MOE_ERR_UNSUPPORTED otherwise); fp32
+ * results where noted.  A training step runs, after the forward (with
+ * moe_route_ex keeping logits):
+ *   do_perm, dgate   = moe_combine_bwd(dy, ...)
+ *   z                = moe_expert_up(x_perm, ..., IDENTITY, F := N1, w1)  (recompute)
+ *   da               = moe_expert_up(do_perm, ..., IDENTITY, F, w2t)      (w2t = w2 transposed)
+ *   dz               = moe_act_bwd(z, da, ...)
+ *   dx_perm          = moe_expert_up(dz, ..., d := N1, F := d, IDENTITY, w1t)
+ *   dw2[e]           = moe_expert_wgrad(pack(do_perm), pack(h), M = d, N = F)
+ *   dw1[e]           = moe_expert_wgrad(pack(dz), pack(x_perm), M = N1, N = d)
+ *   dl               = moe_route_bwd(logits, topk_idx, dgate, counts, ...)
+ *   dx               = moe_grad_x(dx_perm, slot_row, dl, w_router)
+ *   dW, db           = moe_router_wgrad(dl, x)                                */
+
+/* w [E, R, C] -> wt [E, C, R] (2-byte elements; R, C multiples of 64;
+ * 16-byte aligned). */
+moe_status moe_transpose_experts(const void* w, int E, int R, int C, moe_dtype dtype, void* wt,
+                                 moe_stream_t stream);
+
+/* Combine backward.  For every kept slot r = slot_row[t, j] (gate g_r =
+ * row_gate[r], y_perm[r] = g_r * o_r from moe_expert_down):
+ *   do_perm[r]  = g_r * dy[t]             bf16 [rows_max, d]
+ *   dgate[t, j] = <dy[t], y_perm[r]> / g_r = <dy[t], o_r>    fp32 [T, k]
+ * dgate of a dropped slot is 0.  dy [T, d] bf16; d % 64 == 0. */
+moe_status moe_combine_bwd(const void* dy, const int32_t* slot_row, const float* row_gate, const void* y_perm,
+                           int64_t T, int k, int d, moe_dtype dtype, void* do_perm, float* dgate,
+                           moe_stream_t stream);
+
+/* Activation backward over the kept rows r < offsets[E]:
+ *   GELU     dz = da * (Phi(z) + z phi(z))                        dz [rows, F]
+ *   SwiGLU   dz[:, :F] = da * z_up * silu'(z_gate), dz[:, F:] = da * silu(z_gate)   dz [rows, 2F]
+ *   IDENTITY dz = da
+ * z [rows, N1] is the pre-activation (moe_expert_up with IDENTITY on w1), da
+ * [rows, F] the gradient of the activation output.  bf16, F % 64 == 0. */
+moe_status moe_act_bwd(const void* z, const void* da, const int32_t* offsets, int E, int F, moe_act act,
+                       moe_dtype dtype, int64_t rows_max, void* dz, moe_stream_t stream);
+
+/* Columns of the packed transposed operands of moe_expert_wgrad:
+ * rows_max + 64 E rounded up to 64 (each segment is padded to 64). */
+int64_t moe_wgrad_cols(int64_t rows_max, int E);
+
+/* dst [C, ld] (2-byte elements) from the expert segments of src [rows_max, C]:
+ * expert e's row offsets[e] + i lands in column 64 * kstart[e] + i, where
+ * kstart[e] = sum over e' < e of ceil(kept[e'] / 64); the padding columns of
+ * each segment are zero.  ld >= moe_wgrad_cols(rows_max, E), ld % 64 == 0,
+ * C % 64 == 0.  Columns past the last segment are left untouched. */
+moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const int32_t* kept, int E, int C,
+                               int64_t rows_max, int64_t ld, moe_dtype dtype, void* dst, moe_stream_t stream);
+
+/* Per-expert weight gradient on the tensor cores:
+ *   dw[e] = at[:, seg_e] . bt[:, seg_e]^T      fp32 [E, M, N]
+ * at [M, ld] and bt [N, ld] come from moe_pack_segments_t (seg_e = expert e's
+ * packed, zero-padded columns); an expert with no rows gets zeros.
+ * M % 64 == 0, N % 64 == 0, ld % 64 == 0. */
+moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept, int E, int M, int N, int64_t ld,
+                            moe_dtype dtype, float* dw, moe_stream_t stream);
+
+/* Router backward to the logits, per token (logits [T, E] from moe_route_ex,
+ * topk_idx and dgate [T, k], counts [E] = f_e * T: counts for the pre-drop
+ * aux loss, kept for the post-drop one):
+ *   dp[e_j] += (dgate_j - sum_i dgate_i g_i) / S   (renorm; S = sum of the k
+ *              chosen probabilities, g = p / S)    or  dgate_j
+ *   dp[e]   += aux_coef * counts[e] / T^2          (aux_coef = aux_weight * alpha * E)
+ *   dl      = p * (dp - <p, dp>) + z_coef * (2 / T) * lse * p   (z_coef = z_weight * beta)
+ * dl fp32 [T, E]. */
+moe_status moe_route_bwd(const float* logits, const int32_t* topk_idx, const float* dgate, const int32_t* counts,
+                         int64_t T, int E, int k, int renorm, float aux_coef, float z_coef, float* dl,
+                         moe_stream_t stream);
+
+/* Input gradient: dx[t] = sum over kept j of dx_perm[slot_row[t, j]] +
+ * sum_e dl[t, e] w_router[e] (fp32 sums, one rounding to dtype).
+ * dx_perm [rows_max, d] and dx [T, d] in dtype; dl [T, E]; w_router [E, d]. */
+moe_status moe_grad_x(const void* dx_perm, const int32_t* slot_row, const float* dl, const float* w_router,
+                      int64_t T, int k, int E, int d, moe_dtype dtype, void* dx, moe_stream_t stream);
+
+/* Router weight gradient: dW[e, c] = sum_t dl[t, e] x[t, c] (fp32 [E, d]) and,
+ * when db != NULL, db[e] = sum_t dl[t, e] (fp32 [E]); token splits summed in a
+ * fixed order (bitwise reproducible).  ws >=
+ * moe_workspace_bytes(MOE_CALL_ROUTER_WGRAD, T, d, E, ...) bytes; T >= 1. */
+moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64_t T, int E, int d, float* dW,
+                            float* db, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------- no-allocation variant --- */
 

@@ -127,8 +127,8 @@ def test_route_ex_and_z_loss_argument_errors():
     L = moe.lib()
 
     def rex(E=8, k=2, G=4, M=2, T=16):
-        return L.moe_route_ex(FAKE, 1, FAKE, None, T, 128, E, k, 1, G, M, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
-                              None)
+        return L.moe_route_ex(FAKE, 1, FAKE, None, T, 128, E, k, 1, G, M, FAKE, FAKE, FAKE, None, None, FAKE,
+                              1 << 20, None)
 
     assert rex(G=3) == 1            # 3 does not divide 8
     assert rex(G=0) == 1
@@ -139,3 +139,24 @@ def test_route_ex_and_z_loss_argument_errors():
     assert L.moe_z_loss(FAKE, 0, ctypes.c_float(1e-3), FAKE, None) == 1
     assert L.moe_z_loss(None, 16, ctypes.c_float(1e-3), FAKE, None) == 1
     assert L.moe_z_loss(FAKE, 16, ctypes.c_float(1e-3), None, None) == 1
+
+
+def test_backward_argument_errors():
+    L = moe.lib()
+    f = ctypes.c_float
+    assert L.moe_wgrad_cols(5120, 8) == 5632
+    assert L.moe_wgrad_cols(-1, 8) == -1
+    assert L.moe_transpose_experts(FAKE, 2, 100, 64, 1, FAKE, None) == 2       # R not a multiple of 64
+    assert L.moe_transpose_experts(FAKE, 2, 128, 64, 0, FAKE, None) == 2       # fp32 not supported
+    assert L.moe_transpose_experts(None, 2, 128, 64, 1, FAKE, None) == 1
+    assert L.moe_combine_bwd(FAKE, FAKE, FAKE, FAKE, 16, 2, 96, 1, FAKE, FAKE, None) == 2   # d % 64
+    assert L.moe_combine_bwd(FAKE, FAKE, FAKE, FAKE, 16, 0, 128, 1, FAKE, FAKE, None) == 1
+    assert L.moe_act_bwd(FAKE, FAKE, FAKE, 8, 96, 1, 1, 10, FAKE, None) == 2       # F % 64
+    assert L.moe_act_bwd(FAKE, FAKE, FAKE, 8, 128, 7, 1, 10, FAKE, None) == 1      # bad activation
+    assert L.moe_pack_segments_t(FAKE, FAKE, FAKE, 8, 128, 5120, 5000, 1, FAKE, None) == 1   # ld too small
+    assert L.moe_expert_wgrad(FAKE, FAKE, FAKE, 8, 100, 128, 5632, 1, FAKE, None) == 2      # M % 64
+    assert L.moe_route_bwd(FAKE, FAKE, FAKE, None, 16, 8, 2, 1, f(0.1), f(0.0), FAKE, None) == 1
+    assert L.moe_route_bwd(FAKE, FAKE, FAKE, FAKE, 16, 8, 9, 1, f(0.1), f(0.0), FAKE, None) == 1
+    assert L.moe_grad_x(FAKE, FAKE, FAKE, None, 16, 2, 8, 128, 1, FAKE, None) == 1
+    assert L.moe_router_wgrad(FAKE, FAKE, 1, 0, 8, 128, FAKE, None, FAKE, 1 << 20, None) == 1
+    assert L.moe_router_wgrad(FAKE, FAKE, 1, 64, 8, 128, FAKE, None, FAKE, 8, None) == 3    # workspace

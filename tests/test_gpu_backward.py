@@ -1,0 +1,143 @@
+"""GPU parity of the layer backward against the fp64 backward oracle
+(oracle/backward.py), through the C ABI (MoEPlan.backward), on seeded
+inputs spanning several tiles with ragged expert segments, drops, empty
+experts, both activations, renormalised and raw gates, the z-loss and the
+post-drop aux loss; plus the data-movement kernels bit for bit and the
+weight-gradient GEMM against torch fp32 per expert.
+
+Bar (bf16 layers): relative Frobenius error <= 2e-2 for dx, dW, db, dw1,
+dw2, dgate and dl, the bar of the bf16 forward output.  The path rounds
+to bf16 at do, z, da, dz and dx_perm (each ~2^-9 relative), so the
+expected error is a few 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import top_routing_expert_02_b300 as moe
+from oracle import backward as OB
+from top_routing_expert_02_b300 import synth
+
+from moe_cases import make_case, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+C = synth.MoEConfig
+TOL = 2e-2
+
+# name: (config, z_beta, post-drop aux)
+CASES = {
+    "swiglu_e8": (C("swiglu_e8", 2000, 256, 8, 2, 384, "swiglu", 1.25, "bf16"), 0.0, False),
+    "gelu_e16_hot": (C("gelu_e16_hot", 1500, 192, 16, 2, 320, "gelu", 1.0, "bf16", bias="hot2"), 1e-3, True),
+    "swiglu_e64_zipf": (C("swiglu_e64_zipf", 3000, 128, 64, 2, 192, "swiglu", 1.25, "bf16", bias="zipf"), 1e-3,
+                        False),
+    "swiglu_e128_top8": (C("swiglu_e128_top8", 300, 256, 128, 8, 128, "swiglu", 0.0, "bf16"), 1e-2, False),
+    "gelu_e32_norenorm": (C("gelu_e32_norenorm", 900, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False), 0.0,
+                          True),
+    "small_T": (C("small_T", 50, 128, 8, 2, 128, "swiglu", 1.25, "bf16"), 0.0, False),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "these tests need a CUDA device"
+    moe.lib()
+    yield
+
+
+def _dy(cfg):
+    g = torch.Generator().manual_seed(1234 + cfg.T)
+    return torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16)
+
+
+def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0):
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], case["x"].device,
+                       cfg.alpha, cfg.renorm, z_beta=z_beta if z_beta else None, aux_post_drop=post, train=True)
+    moe.set_wait_limit(400_000_000)
+    try:
+        plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+        dy = _dy(cfg)
+        g = plan.backward(case["x"], case["W"], case["w1"], case["w2"], dy.cuda(), aux_weight=aux_weight,
+                          z_weight=z_weight)
+        moe.check()
+    finally:
+        moe.set_wait_limit(0)
+    ref = OB.backward(case["x_h"], case["W_h"], case["b_h"], case["w1"].cpu(), case["w2"].cpu(), dy, k=cfg.k,
+                      cap=case["cap"], act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha, aux_weight=aux_weight,
+                      z_beta=z_beta, z_weight=z_weight, aux_post_drop=post)
+    return plan, g, ref, case
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_backward_against_oracle(name):
+    cfg, z_beta, post = CASES[name]
+    plan, g, ref, _ = _run(cfg, z_beta, post)
+    errs = {}
+    for key in ("dx", "dW", "db", "dw1", "dw2", "dgate", "dl"):
+        got = g[key].float().cpu().numpy().astype(np.float64)
+        if key in ("dx", "dgate", "dl"):
+            got = got[:cfg.T]
+        errs[key] = rel_fro(got, ref[key])
+    print(f"[backward parity] {name}: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()))
+    for key, err in errs.items():
+        assert err <= TOL, (key, err)
+
+
+def test_backward_is_bitwise_reproducible():
+    cfg, z_beta, post = CASES["swiglu_e64_zipf"]
+    p1, g1, _, case = _run(cfg, z_beta, post)
+    snap = {k: v.clone() for k, v in g1.items()}
+    g2 = p1.backward(case["x"], case["W"], case["w1"], case["w2"], _dy(cfg).cuda())
+    moe.check()
+    for k in ("dx", "dW", "db", "dw1", "dw2"):
+        assert torch.equal(snap[k], g2[k]), k
+
+
+def test_transpose_and_pack_are_exact():
+    g = torch.Generator(device="cuda").manual_seed(5)
+    w = torch.randn(3, 192, 320, device="cuda", generator=g).to(torch.bfloat16)
+    wt = moe.transpose_experts(w)
+    assert torch.equal(wt, w.transpose(1, 2).contiguous())
+    # ragged segments incl. an empty one and one longer than 64
+    kept = torch.tensor([70, 0, 5, 64, 1], dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(6, dtype=torch.int32, device="cuda")
+    offsets[1:] = torch.cumsum(kept, 0)
+    R = int(offsets[-1])
+    src = torch.randn(R, 128, device="cuda", generator=g).to(torch.bfloat16)
+    ld = moe.wgrad_cols(R, 5)
+    out = torch.full((128, ld), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe.pack_segments_t(src, offsets, kept, R, ld, out=out)
+    moe.check()
+    col = 0
+    for e in range(5):
+        n = int(kept[e])
+        kp = (n + 63) // 64 * 64
+        o = int(offsets[e])
+        assert torch.equal(out[:, col:col + n], src[o:o + n].T)
+        assert torch.all(out[:, col + n:col + kp] == 0)
+        col += kp
+
+
+def test_expert_wgrad_against_torch_per_expert():
+    """dw[e] = at[:, seg] bt[:, seg]^T against torch fp32 matmul, M not a
+    multiple of 128 and N not of 256; an empty expert gets zeros."""
+    g = torch.Generator(device="cuda").manual_seed(6)
+    kept = torch.tensor([100, 0, 300, 64], dtype=torch.int32, device="cuda")
+    E, M, N = 4, 192, 320
+    ld = moe.wgrad_cols(int(kept.sum()), E)
+    at = torch.zeros(M, ld, dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros(N, ld, dtype=torch.bfloat16, device="cuda")
+    col = 0
+    for e in range(E):
+        n = int(kept[e])
+        at[:, col:col + n] = torch.randn(M, n, device="cuda", generator=g).to(torch.bfloat16)
+        bt[:, col:col + n] = torch.randn(N, n, device="cuda", generator=g).to(torch.bfloat16)
+        col += (n + 63) // 64 * 64
+    dw = moe.expert_wgrad(at, bt, kept)
+    moe.check()
+    col = 0
+    for e in range(E):
+        n = int(kept[e])
+        ref = at[:, col:col + n].float() @ bt[:, col:col + n].float().T
+        assert torch.allclose(dw[e], ref, rtol=1e-4, atol=1e-3), e
+        col += (n + 63) // 64 * 64

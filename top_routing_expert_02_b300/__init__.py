@@ -25,14 +25,15 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
-    "expert_up_gathered", "expert_down", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
+    "expert_up_gathered", "expert_down", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
+    "pack_segments_t", "expert_wgrad", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
 
 ACT = {"gelu": 0, "swiglu": 1, "identity": 2}
-CALL = {"route": 0, "dispatch": 1, "ffn": 2}
+CALL = {"route": 0, "dispatch": 1, "ffn": 2, "router_wgrad": 3}
 _DT = {torch.float32: 0, torch.bfloat16: 1}
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
@@ -66,8 +67,17 @@ _SIGS = {
     "moe_aux_loss": (_I32, [_P, _P, _I64, _I32, _F, _P, _P]),
     "moe_dispatch_noalloc": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P]),
-    "moe_route_ex": (_I32, [_P, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ,
-                            _P]),
+    "moe_route_ex": (_I32, [_P, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                            _SZ, _P]),
+    "moe_transpose_experts": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _P]),
+    "moe_combine_bwd": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _P]),
+    "moe_act_bwd": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I64, _P, _P]),
+    "moe_wgrad_cols": (_I64, [_I64, _I32]),
+    "moe_pack_segments_t": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I64, _I32, _P, _P]),
+    "moe_expert_wgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I64, _I32, _P, _P]),
+    "moe_route_bwd": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _F, _F, _P, _P]),
+    "moe_grad_x": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P]),
+    "moe_router_wgrad": (_I32, [_P, _P, _I32, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "moe_z_loss": (_I32, [_P, _I64, _F, _P, _P]),
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
@@ -166,12 +176,13 @@ def selftest_wait_timeout(stream=None):
 # --------------------------------------------------------------- compute ---
 
 def route(x, w_router, b_router, k: int, renorm: bool = True, *, topk_idx=None, topk_gate=None, prob_sum=None,
-          ws=None, stream=None, n_group: int = 1, topk_group: int = 1, lse=None):
+          ws=None, stream=None, n_group: int = 1, topk_group: int = 1, lse=None, logits=None):
     """Router (moe_route): returns (topk_idx [T,k] int32, topk_gate [T,k] f32, prob_sum [E] f32).
 
     ``n_group`` > 1 selects group-limited routing (moe_route_ex): top-k among
     the experts of the ``topk_group`` best of ``n_group`` contiguous groups.
-    ``lse`` ([T] f32) receives each token's log-sum-exp of the logits."""
+    ``lse`` ([T] f32) receives each token's log-sum-exp of the logits and
+    ``logits`` ([T, E] f32) the logits themselves (for the backward)."""
     T, d = x.shape
     E = w_router.shape[0]
     dev = x.device
@@ -180,14 +191,15 @@ def route(x, w_router, b_router, k: int, renorm: bool = True, *, topk_idx=None, 
     prob_sum = torch.empty(E, dtype=torch.float32, device=dev) if prob_sum is None else prob_sum
     need = workspace_bytes("route", T, d, E, k, 64)
     ws = _empty_ws(need, dev) if ws is None else ws
-    if n_group == 1 and lse is None:
+    if n_group == 1 and lse is None and logits is None:
         _ok("moe_route", lib().moe_route(_ptr(x), _dt(x), _ptr(w_router), _ptr(b_router), T, d, E, k, int(renorm),
                                          _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(ws), ws.numel(),
                                          _stream(stream)))
     else:
         _ok("moe_route_ex", lib().moe_route_ex(
             _ptr(x), _dt(x), _ptr(w_router), _ptr(b_router), T, d, E, k, int(renorm), int(n_group), int(topk_group),
-            _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+            _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_sum), _ptr(lse), _ptr(logits), _ptr(ws), ws.numel(),
+            _stream(stream)))
     return topk_idx, topk_gate, prob_sum
 
 
@@ -315,6 +327,96 @@ def z_loss(lse, beta: float, *, loss=None, stream=None):
     return loss
 
 
+# --------------------------------------------------------------- backward ---
+
+def transpose_experts(w, *, out=None, stream=None):
+    """w [E, R, C] -> [E, C, R] (moe_transpose_experts)."""
+    E, R, C = w.shape
+    out = torch.empty((E, C, R), dtype=w.dtype, device=w.device) if out is None else out
+    _ok("moe_transpose_experts", lib().moe_transpose_experts(_ptr(w), E, R, C, _dt(w), _ptr(out), _stream(stream)))
+    return out
+
+
+def combine_bwd(dy, slot_row, row_gate, y_perm, *, do_perm=None, dgate=None, stream=None):
+    """(do_perm [rows, d], dgate [T, k] f32) (moe_combine_bwd)."""
+    T, k = slot_row.shape
+    d = dy.shape[1]
+    do_perm = torch.empty_like(y_perm) if do_perm is None else do_perm
+    dgate = torch.empty((T, k), dtype=torch.float32, device=dy.device) if dgate is None else dgate
+    _ok("moe_combine_bwd", lib().moe_combine_bwd(_ptr(dy), _ptr(slot_row), _ptr(row_gate), _ptr(y_perm), T, k, d,
+                                                 _dt(dy), _ptr(do_perm), _ptr(dgate), _stream(stream)))
+    return do_perm, dgate
+
+
+def act_bwd(z, da, offsets, F: int, act: str, rows_max: int, *, dz=None, stream=None):
+    """dz [rows, N1] from the pre-activation z and da (moe_act_bwd)."""
+    E = offsets.shape[0] - 1
+    dz = torch.empty_like(z) if dz is None else dz
+    _ok("moe_act_bwd", lib().moe_act_bwd(_ptr(z), _ptr(da), _ptr(offsets), E, F, ACT[act], _dt(z), rows_max,
+                                         _ptr(dz), _stream(stream)))
+    return dz
+
+
+def wgrad_cols(rows_max: int, E: int) -> int:
+    return int(lib().moe_wgrad_cols(rows_max, E))
+
+
+def pack_segments_t(src, offsets, kept, rows_max: int, ld: int, *, out=None, stream=None):
+    """src [rows, C] -> [C, ld], expert segments as zero-padded column blocks (moe_pack_segments_t)."""
+    C = src.shape[1]
+    E = kept.shape[0]
+    out = torch.empty((C, ld), dtype=src.dtype, device=src.device) if out is None else out
+    _ok("moe_pack_segments_t", lib().moe_pack_segments_t(_ptr(src), _ptr(offsets), _ptr(kept), E, C, rows_max, ld,
+                                                         _dt(src), _ptr(out), _stream(stream)))
+    return out
+
+
+def expert_wgrad(at, bt, kept, *, dw=None, stream=None):
+    """dw [E, M, N] f32 = per-expert at[:, seg] bt[:, seg]^T (moe_expert_wgrad)."""
+    M, ld = at.shape
+    N = bt.shape[0]
+    E = kept.shape[0]
+    dw = torch.empty((E, M, N), dtype=torch.float32, device=at.device) if dw is None else dw
+    _ok("moe_expert_wgrad", lib().moe_expert_wgrad(_ptr(at), _ptr(bt), _ptr(kept), E, M, N, ld, _dt(at), _ptr(dw),
+                                                   _stream(stream)))
+    return dw
+
+
+def route_bwd(logits, topk_idx, dgate, counts, renorm: bool, aux_coef: float, z_coef: float, *, dl=None,
+              stream=None):
+    """dl [T, E] f32, the gradient at the router logits (moe_route_bwd)."""
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    dl = torch.empty((T, E), dtype=torch.float32, device=logits.device) if dl is None else dl
+    _ok("moe_route_bwd", lib().moe_route_bwd(_ptr(logits), _ptr(topk_idx), _ptr(dgate), _ptr(counts), T, E, k,
+                                             int(renorm), float(aux_coef), float(z_coef), _ptr(dl),
+                                             _stream(stream)))
+    return dl
+
+
+def grad_x(dx_perm, slot_row, dl, w_router, *, dx=None, stream=None):
+    """dx [T, d] (moe_grad_x)."""
+    T, k = slot_row.shape
+    E, d = w_router.shape
+    dx = torch.empty((T, d), dtype=dx_perm.dtype, device=dx_perm.device) if dx is None else dx
+    _ok("moe_grad_x", lib().moe_grad_x(_ptr(dx_perm), _ptr(slot_row), _ptr(dl), _ptr(w_router), T, k, E, d,
+                                       _dt(dx_perm), _ptr(dx), _stream(stream)))
+    return dx
+
+
+def router_wgrad(dl, x, *, dW=None, db=None, ws=None, stream=None):
+    """(dW [E, d] f32, db [E] f32) (moe_router_wgrad)."""
+    T, E = dl.shape
+    d = x.shape[1]
+    dW = torch.empty((E, d), dtype=torch.float32, device=x.device) if dW is None else dW
+    db = torch.empty(E, dtype=torch.float32, device=x.device) if db is None else db
+    need = workspace_bytes("router_wgrad", T, d, E, 1, 64)
+    ws = _empty_ws(need, x.device) if ws is None else ws
+    _ok("moe_router_wgrad", lib().moe_router_wgrad(_ptr(dl), _ptr(x), _dt(x), T, E, d, _ptr(dW), _ptr(db), _ptr(ws),
+                                                   ws.numel(), _stream(stream)))
+    return dW, db
+
+
 # ------------------------------------------------------------ whole layer ---
 
 class MoEPlan:
@@ -333,12 +435,15 @@ class MoEPlan:
     ``z_beta`` (router z-loss into ``z_loss``, with the per-token
     log-sum-exp in ``lse``; None skips it) and ``aux_post_drop`` (f_i from
     the kept slots instead of every choice).
+
+    ``train=True`` keeps the router logits so that :meth:`backward` can run
+    after :meth:`run` (bf16 layers, x_perm path).
     """
 
     def __init__(self, T: int, d: int, E: int, k: int, F: int, act: str, dtype: torch.dtype, cap: int,
                  device="cuda", alpha: float = 0.01, renorm: bool = True, gather: bool = False, *,
                  n_group: int = 1, topk_group: int = 1, z_beta: Optional[float] = None,
-                 aux_post_drop: bool = False):
+                 aux_post_drop: bool = False, train: bool = False):
         self.T, self.d, self.E, self.k, self.F, self.act = T, d, E, k, F, act
         self.dtype, self.cap, self.alpha, self.renorm = dtype, int(cap), float(alpha), bool(renorm)
         self.n_group, self.topk_group = int(n_group), int(topk_group)
@@ -363,6 +468,11 @@ class MoEPlan:
         self.y_perm = torch.empty((Rb, d), dtype=dtype, device=dev)
         self.y = torch.empty((T, d), dtype=dtype, device=dev)
         self.loss = torch.empty(1, **f32)
+        self.train = bool(train)
+        if self.train and (dtype != torch.bfloat16 or self.gather):
+            raise ValueError("the backward runs on bf16 layers with a materialised x_perm")
+        self.logits = torch.empty((max(T, 1), E), **f32) if self.train else None
+        self._bwd = None
         self.lse = torch.empty(max(T, 1), **f32) if self.z_beta is not None else None
         self.z_loss = torch.empty(1, **f32) if self.z_beta is not None else None
         self.ws_route = _empty_ws(workspace_bytes("route", T, d, E, k, F), dev)
@@ -389,7 +499,7 @@ class MoEPlan:
     def run(self, x, w_router, b_router, w1, w2, stream=None) -> torch.Tensor:
         route(x, w_router, b_router, self.k, self.renorm, topk_idx=self.topk_idx, topk_gate=self.topk_gate,
               prob_sum=self.prob_sum, ws=self.ws_route, stream=stream, n_group=self.n_group,
-              topk_group=self.topk_group, lse=self.lse)
+              topk_group=self.topk_group, lse=self.lse, logits=self.logits)
         dispatch(self.topk_idx, self.topk_gate, x, self.E, self.cap, out=self.disp, ws=self.ws_dispatch,
                  stream=stream)
         D = self.disp
@@ -408,6 +518,71 @@ class MoEPlan:
             if self.z_beta is not None:
                 z_loss(self.lse, self.z_beta, loss=self.z_loss, stream=stream)
         return self.y
+
+
+    def _bwd_buffers(self, dev):
+        if self._bwd is None:
+            T, d, E, k, F = self.T, self.d, self.E, self.k, self.F
+            R = max(self.rows_max, 1)
+            N1 = 2 * F if self.act == "swiglu" else F
+            ld = wgrad_cols(self.rows_max, E)
+            bf = dict(dtype=torch.bfloat16, device=dev)
+            f32 = dict(dtype=torch.float32, device=dev)
+            self._bwd = dict(
+                do_perm=torch.empty((R, d), **bf), dgate=torch.empty((max(T, 1), k), **f32),
+                z=torch.empty((R, N1), **bf), da=torch.empty((R, F), **bf), dz=torch.empty((R, N1), **bf),
+                dx_perm=torch.empty((R, d), **bf), ld=ld,
+                doT=torch.empty((d, ld), **bf), hT=torch.empty((F, ld), **bf), dzT=torch.empty((N1, ld), **bf),
+                xT=torch.empty((d, ld), **bf), dw1=torch.empty((E, N1, d), **f32), dw2=torch.empty((E, d, F), **f32),
+                dl=torch.empty((max(T, 1), E), **f32), dx=torch.empty((max(T, 1), d), **bf),
+                dW=torch.empty((E, d), **f32), db=torch.empty(E, **f32),
+                ws=_empty_ws(workspace_bytes("router_wgrad", max(T, 1), d, E, k, F), dev))
+        return self._bwd
+
+    def backward(self, x, w_router, w1, w2, dy, *, aux_weight: float = 1.0, z_weight: float = 1.0, w1t=None,
+                 w2t=None, stream=None) -> dict:
+        """Gradients of <dy, y> + aux_weight * loss + z_weight * z_loss after
+        :meth:`run` on the same inputs (``train=True``).  ``w1t`` / ``w2t``
+        are the transposed expert weights ([E, d, N1] / [E, F, d]); they are
+        made here when not given.  Returns dx, dW, db, dw1, dw2 (weight
+        gradients fp32) and the intermediates; all buffers belong to the plan."""
+        if not self.train:
+            raise ValueError("construct the plan with train=True")
+        B = self._bwd_buffers(x.device)
+        D = self.disp
+        R, F, E, d = self.rows_max, self.F, self.E, self.d
+        N1 = 2 * F if self.act == "swiglu" else F
+        w1t = transpose_experts(w1, stream=stream) if w1t is None else w1t
+        w2t = transpose_experts(w2, stream=stream) if w2t is None else w2t
+        combine_bwd(dy, D.slot_row, D.row_gate, self.y_perm, do_perm=B["do_perm"], dgate=B["dgate"], stream=stream)
+        # data gradients: recompute z, then da, dz, dx_perm (identity epilogues on transposed weights)
+        _ok("moe_expert_up", lib().moe_expert_up(_ptr(D.x_perm), _ptr(D.offsets), _ptr(D.kept), E, d, N1,
+                                                 ACT["identity"], _dt(D.x_perm), _ptr(w1), R, _ptr(B["z"]),
+                                                 _stream(stream)))
+        _ok("moe_expert_up", lib().moe_expert_up(_ptr(B["do_perm"]), _ptr(D.offsets), _ptr(D.kept), E, d, F,
+                                                 ACT["identity"], _dt(w2t), _ptr(w2t), R, _ptr(B["da"]),
+                                                 _stream(stream)))
+        act_bwd(B["z"], B["da"], D.offsets, F, self.act, R, dz=B["dz"], stream=stream)
+        _ok("moe_expert_up", lib().moe_expert_up(_ptr(B["dz"]), _ptr(D.offsets), _ptr(D.kept), E, N1, d,
+                                                 ACT["identity"], _dt(w1t), _ptr(w1t), R, _ptr(B["dx_perm"]),
+                                                 _stream(stream)))
+        # weight gradients on segment-packed transposes
+        ld = B["ld"]
+        pack_segments_t(B["do_perm"], D.offsets, D.kept, R, ld, out=B["doT"], stream=stream)
+        pack_segments_t(self.h, D.offsets, D.kept, R, ld, out=B["hT"], stream=stream)
+        pack_segments_t(B["dz"], D.offsets, D.kept, R, ld, out=B["dzT"], stream=stream)
+        pack_segments_t(D.x_perm, D.offsets, D.kept, R, ld, out=B["xT"], stream=stream)
+        expert_wgrad(B["doT"], B["hT"], D.kept, dw=B["dw2"], stream=stream)
+        expert_wgrad(B["dzT"], B["xT"], D.kept, dw=B["dw1"], stream=stream)
+        # router
+        counts = D.kept if self.aux_post_drop else D.counts
+        zc = z_weight * (self.z_beta or 0.0)
+        route_bwd(self.logits, self.topk_idx, B["dgate"], counts, self.renorm, aux_weight * self.alpha * E, zc,
+                  dl=B["dl"], stream=stream)
+        grad_x(B["dx_perm"], D.slot_row, B["dl"], w_router, dx=B["dx"], stream=stream)
+        router_wgrad(B["dl"], x, dW=B["dW"], db=B["db"], ws=B["ws"], stream=stream)
+        return dict(dx=B["dx"], dW=B["dW"], db=B["db"], dw1=B["dw1"], dw2=B["dw2"], dgate=B["dgate"], dl=B["dl"],
+                    do_perm=B["do_perm"], z=B["z"], da=B["da"], dz=B["dz"], dx_perm=B["dx_perm"])
 
 
 def moe_forward(x, w_router, b_router, w1, w2, *, k: int, cf: float, act: str, renorm: bool = True,

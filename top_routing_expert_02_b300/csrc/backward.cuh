@@ -1,0 +1,392 @@
+// Backward of the MoE layer: the kernels that are not grouped GEMMs.
+//
+// The pages train the layer through the same steps in reverse (the
+// expert-parallelism tutorial "专家并行：混合专家模型的分布式训练方案" §2.1 and §5.1,
+// whose auxiliary loss steers the router through its gradient; the deployment
+// guide "细粒度专家并行部署实践与优化指南" 步骤三 item 3, the reverse exchange of the
+// gradients); they give no formula, so these kernels compute the derivative of
+// the forward.  With L = <dy, y> + aux_weight L_aux + z_weight L_z:
+//   combine backward   do_r = g_r dy[t],  dgate[t,j] = <dy[t], o_r>
+//                      (o_r = y_perm_r / g_r: the down projection before the gate)
+//   activation backward dz = act'(z) da   (SwiGLU: da up silu'(gate) | da silu(gate))
+//   router backward    dp from the gates (renormalised: (dgate_j - sum_i dgate_i g_i) / S)
+//                      and from L_aux (aux_weight alpha E f_e / T); dl = p (dp - <p, dp>)
+//                      + z_weight (2 beta / T) lse p
+//   input gradient     dx[t] = sum over kept j of dx_perm[slot] + W^T dl[t]
+//   router weights     dW = dl^T x, db = sum_t dl  (fixed-order sums)
+// plus the transposes that feed the tensor-core GEMMs K-major operands.
+#pragma once
+#include "common.cuh"
+#include "tiles.cuh"
+
+namespace bwd {
+
+// ----------------------------------------------------------- transposes ---
+
+// dst[e][c][r] = src[e][r][c] for 2-byte elements, R and C multiples of 64.
+// One 64x64 tile per block: 16-byte loads along c, 16-byte stores along r.
+__global__ void __launch_bounds__(256)
+transpose_experts_kernel(const uint16_t* __restrict__ src, int R, int C, uint16_t* __restrict__ dst)
+{
+    __shared__ uint16_t tile[64][64 + 2];
+    const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+    const size_t slab = (size_t)blockIdx.z * R * C;
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int r = v >> 3, q = v & 7;
+        const uint4 u = ldg_nc_v4(src + slab + (size_t)(r0 + r) * C + c0 + q * 8);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            tile[r][q * 8 + 2 * i] = (uint16_t)(w[i] & 0xffffu);
+            tile[r][q * 8 + 2 * i + 1] = (uint16_t)(w[i] >> 16);
+        }
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int c = v >> 3, q = v & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = (uint32_t)tile[q * 8 + 2 * i][c] | ((uint32_t)tile[q * 8 + 2 * i + 1][c] << 16);
+        *reinterpret_cast<uint4*>(dst + slab + (size_t)(c0 + c) * R + r0 + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Segment-packed transpose for the weight-gradient GEMMs: expert e's rows
+// src[offsets[e] + i][0..C) become columns 64 kstart[e] + i of dst [C, ld],
+// zero for kept[e] <= i < 64 (kstart[e+1] - kstart[e]) (kstart = running sum
+// of ceil(kept / 64)).  Block (x, y): columns 64x.., K block y of all experts.
+__global__ void __launch_bounds__(256)
+pack_segments_t_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ offsets,
+                       const int32_t* __restrict__ kept, int E, int C, long long ld, uint16_t* __restrict__ dst)
+{
+    __shared__ int kstart[257];
+    __shared__ uint16_t tile[64][64 + 2];
+    if (threadIdx.x < 32) build_mtile_prefix<64>(kept, E, kstart, threadIdx.x);
+    __syncthreads();
+    const int kb = blockIdx.y;
+    if (kb >= kstart[E]) return;
+    const int e = find_expert(kstart, E, kb);
+    const int i0 = (kb - kstart[e]) * 64;        // first row of this block inside the segment
+    const int n = __ldg(kept + e) - i0;         // rows of this block that exist (<= 64 valid)
+    const int base = __ldg(offsets + e) + i0;
+    const int c0 = blockIdx.x * 64;
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int r = v >> 3, q = v & 7;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (r < n) u = ldg_nc_v4(src + (size_t)(base + r) * C + c0 + q * 8);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            tile[r][q * 8 + 2 * i] = (uint16_t)(w[i] & 0xffffu);
+            tile[r][q * 8 + 2 * i + 1] = (uint16_t)(w[i] >> 16);
+        }
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int c = v >> 3, q = v & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = (uint32_t)tile[q * 8 + 2 * i][c] | ((uint32_t)tile[q * 8 + 2 * i + 1][c] << 16);
+        *reinterpret_cast<uint4*>(dst + (size_t)(c0 + c) * ld + (size_t)kb * 64 + q * 8) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ------------------------------------------------------ combine backward ---
+
+// One warp per token.  For each kept slot r = slot_row[t, j]:
+//   do_perm[r] = g_r * dy[t]   (bf16),   dgate[t, j] = <dy[t], y_perm[r]> / g_r
+// (y_perm holds g_r o_r); a dropped slot gets dgate 0 and no row.
+constexpr int CB_THREADS = 256;
+__global__ void __launch_bounds__(CB_THREADS)
+combine_bwd_kernel(const uint4* __restrict__ dy, const int32_t* __restrict__ slot_row,
+                   const float* __restrict__ row_gate, const uint4* __restrict__ y_perm, int T, int k, int vec16,
+                   uint4* __restrict__ do_perm, float* __restrict__ dgate)
+{
+    const int lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * (CB_THREADS / 32);
+    for (int t = blockIdx.x * (CB_THREADS / 32) + (threadIdx.x >> 5); t < T; t += warps_total) {
+        int rows[16];
+        float g[16], dot[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            rows[j] = (j < k) ? __ldg(slot_row + (size_t)t * k + j) : -1;
+            g[j] = rows[j] >= 0 ? __ldg(row_gate + rows[j]) : 0.f;
+            dot[j] = 0.f;
+        }
+        for (int v = lane; v < vec16; v += 32) {
+            float f[8];
+            unpack_bf16x8(ldg_nc_v4(dy + (size_t)t * vec16 + v), f);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (rows[j] < 0) continue;
+                float o[8];
+                unpack_bf16x8(ldg_nc_v4(y_perm + (size_t)rows[j] * vec16 + v), o);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dot[j] = fmaf(f[i], o[i], dot[j]);
+                uint4 w;
+                w.x = pack_bf16x2(g[j] * f[0], g[j] * f[1]);
+                w.y = pack_bf16x2(g[j] * f[2], g[j] * f[3]);
+                w.z = pack_bf16x2(g[j] * f[4], g[j] * f[5]);
+                w.w = pack_bf16x2(g[j] * f[6], g[j] * f[7]);
+                do_perm[(size_t)rows[j] * vec16 + v] = w;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= k) break;
+            float s = dot[j];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == j) dgate[(size_t)t * k + j] = rows[j] >= 0 ? s / g[j] : 0.f;
+        }
+    }
+}
+
+// --------------------------------------------------- activation backward ---
+
+// dz from z (pre-activation, bf16 [A, N1]) and da (bf16 [A, F]) over the kept
+// rows A = offsets[E]; eight columns per thread step.
+template <int ACT>
+__global__ void __launch_bounds__(256)
+act_bwd_kernel(const uint16_t* __restrict__ z, const uint16_t* __restrict__ da, const int32_t* __restrict__ offsets,
+               int E, int F, uint16_t* __restrict__ dz)
+{
+    const long long A = __ldg(offsets + E);
+    const int fv = F / 8;
+    const int N1 = ACT == MOE_ACT_SWIGLU ? 2 * F : F;
+    const long long total = A * fv;
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
+        const long long r = i / fv;
+        const int c = (int)(i - r * fv) * 8;
+        float a[8], zg[8];
+        unpack_bf16x8(ldg_nc_v4(da + r * F + c), a);
+        unpack_bf16x8(ldg_nc_v4(z + r * N1 + c), zg);
+        float o[8];
+        if (ACT == MOE_ACT_SWIGLU) {
+            float zu[8], ou[8];
+            unpack_bf16x8(ldg_nc_v4(z + r * N1 + F + c), zu);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float s = 1.0f / (1.0f + expf(-zg[q]));
+                const float silu = zg[q] * s;
+                o[q] = a[q] * zu[q] * (s * (1.0f + zg[q] * (1.0f - s)));
+                ou[q] = a[q] * silu;
+            }
+            *reinterpret_cast<uint4*>(dz + r * N1 + F + c) =
+                make_uint4(pack_bf16x2(ou[0], ou[1]), pack_bf16x2(ou[2], ou[3]), pack_bf16x2(ou[4], ou[5]),
+                           pack_bf16x2(ou[6], ou[7]));
+        } else if (ACT == MOE_ACT_GELU) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float cdf = 0.5f * (1.0f + erff(zg[q] * 0.70710678118654752f));
+                const float pdf = 0.39894228040143268f * expf(-0.5f * zg[q] * zg[q]);
+                o[q] = a[q] * (cdf + zg[q] * pdf);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] = a[q];
+        }
+        *reinterpret_cast<uint4*>(dz + r * N1 + c) =
+            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                       pack_bf16x2(o[6], o[7]));
+    }
+}
+
+// ------------------------------------------------------- router backward ---
+
+// One warp per token, lane l owns experts l, l+32, ...  logits [T, E] are the
+// forward's (bias included); counts are the f_e numerators (counts or kept).
+//   aux_coef = aux_weight * alpha * E  (the kernel divides by T twice: f_e and P_e)
+//   z_coef   = z_weight * beta         (the kernel applies 2 / T)
+template <int EPL>
+__global__ void __launch_bounds__(256)
+route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx, const float* __restrict__ dgate,
+                 const int32_t* __restrict__ counts, int T, int E, int k, int renorm, float aux_coef, float z_coef,
+                 float* __restrict__ dl)
+{
+    const int lane = threadIdx.x & 31;
+    const float invT = 1.0f / (float)T;
+    float daux[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        daux[i] = e < E ? aux_coef * ((float)__ldg(counts + e) * invT) * invT : 0.f;
+    }
+    for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+        float l[EPL], p[EPL], dp[EPL];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            l[i] = e < E ? __ldg(logits + (size_t)t * E + e) : -INFINITY;
+            mx = fmaxf(mx, l[i]);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            p[i] = (lane + 32 * i < E) ? expf(l[i] - mx) : 0.f;
+            s += p[i];
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float lse = mx + logf(s);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            p[i] = p[i] / s;
+            dp[i] = daux[i];
+        }
+        // the k gates: probabilities of the chosen experts, their sum, sum_j dgate_j g_j
+        float S = 0.f, dsum = 0.f;
+        int ej[16];
+        float pj[16], dgj[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= k) break;
+            ej[j] = __ldg(idx + (size_t)t * k + j);
+            dgj[j] = __ldg(dgate + (size_t)t * k + j);
+            float v = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (lane + 32 * i == ej[j]) v = p[i];
+            pj[j] = __shfl_sync(0xffffffffu, v, ej[j] & 31);
+            S += pj[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= k) break;
+            dsum += dgj[j] * (pj[j] / S);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j >= k) break;
+            const float add = renorm ? (dgj[j] - dsum) / S : dgj[j];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (lane + 32 * i == ej[j]) dp[i] += add;
+        }
+        float pdp = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) pdp += p[i] * dp[i];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) pdp += __shfl_xor_sync(0xffffffffu, pdp, o);
+        const float zc = z_coef * 2.0f * invT * lse;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) dl[(size_t)t * E + e] = p[i] * (dp[i] - pdp) + zc * p[i];
+        }
+    }
+}
+
+// ------------------------------------------------------- input gradient ---
+
+// dx[t][c] = sum_e dl[t,e] W[e,c] + sum over kept j of dx_perm[slot_row[t,j]][c].
+// Block: 32 tokens x 256 columns; dl rows and slot rows staged in shared memory,
+// each W element read once per block; fp32 sums, one rounding.
+constexpr int GX_TOK = 32;
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot_row, const float* __restrict__ dl,
+              const float* __restrict__ W, int T, int k, int E, int d, void* __restrict__ dx)
+{
+    __shared__ float dls[GX_TOK][257];
+    __shared__ int rows[GX_TOK][16];
+    const int t0 = blockIdx.y * GX_TOK;
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    for (int v = threadIdx.x; v < GX_TOK * E; v += 256) {
+        const int tk = v / E, e = v - tk * E;
+        dls[tk][e] = (t0 + tk < T) ? __ldg(dl + (size_t)(t0 + tk) * E + e) : 0.f;
+    }
+    for (int v = threadIdx.x; v < GX_TOK * k; v += 256) {
+        const int tk = v / k, j = v - tk * k;
+        rows[tk][j] = (t0 + tk < T) ? __ldg(slot_row + (size_t)(t0 + tk) * k + j) : -1;
+    }
+    __syncthreads();
+    if (c >= d) return;
+    float acc[GX_TOK];
+#pragma unroll
+    for (int tk = 0; tk < GX_TOK; ++tk) acc[tk] = 0.f;
+    for (int e = 0; e < E; ++e) {
+        const float w = __ldg(W + (size_t)e * d + c);
+#pragma unroll
+        for (int tk = 0; tk < GX_TOK; ++tk) acc[tk] = fmaf(dls[tk][e], w, acc[tk]);
+    }
+#pragma unroll
+    for (int tk = 0; tk < GX_TOK; ++tk) {
+        if (t0 + tk >= T) continue;
+        float a = acc[tk];
+        for (int j = 0; j < k; ++j) {
+            const int r = rows[tk][j];
+            if (r < 0) continue;
+            a += BF16 ? bf16_bits_to_f32(__ldg((const uint16_t*)dx_perm + (size_t)r * d + c))
+                      : __ldg((const float*)dx_perm + (size_t)r * d + c);
+        }
+        if (BF16) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(a);
+            ((__nv_bfloat16*)dx)[(size_t)(t0 + tk) * d + c] = h;
+        } else {
+            ((float*)dx)[(size_t)(t0 + tk) * d + c] = a;
+        }
+    }
+}
+
+// ------------------------------------------------------ router weights ---
+
+// partial[s][e][c] = sum over tokens t of split s of dl[t,e] x[t,c].
+// Block (x, y, s): 256 columns, 16 experts, token split s; dl staged 32
+// tokens at a time.  The splits are summed in order by router_wgrad_sum_kernel.
+constexpr int RW_EXP = 16;
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+router_wgrad_kernel(const float* __restrict__ dl, const void* __restrict__ x, int T, int E, int d, int tok_per_split,
+                    float* __restrict__ partial)
+{
+    __shared__ float dls[32][RW_EXP];
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    const int e0 = blockIdx.y * RW_EXP;
+    const int s = blockIdx.z;
+    const int ta = s * tok_per_split;
+    const int tb = min(T, ta + tok_per_split);
+    float acc[RW_EXP];
+#pragma unroll
+    for (int i = 0; i < RW_EXP; ++i) acc[i] = 0.f;
+    for (int t0 = ta; t0 < tb; t0 += 32) {
+        __syncthreads();
+        for (int v = threadIdx.x; v < 32 * RW_EXP; v += 256) {
+            const int tk = v / RW_EXP, i = v - tk * RW_EXP;
+            dls[tk][i] = (t0 + tk < tb && e0 + i < E) ? __ldg(dl + (size_t)(t0 + tk) * E + e0 + i) : 0.f;
+        }
+        __syncthreads();
+        if (c < d) {
+            const int n = min(32, tb - t0);
+            for (int tk = 0; tk < n; ++tk) {
+                const float xv = BF16 ? bf16_bits_to_f32(__ldg((const uint16_t*)x + (size_t)(t0 + tk) * d + c))
+                                      : __ldg((const float*)x + (size_t)(t0 + tk) * d + c);
+#pragma unroll
+                for (int i = 0; i < RW_EXP; ++i) acc[i] = fmaf(dls[tk][i], xv, acc[i]);
+            }
+        }
+    }
+    if (c < d) {
+#pragma unroll
+        for (int i = 0; i < RW_EXP; ++i)
+            if (e0 + i < E) partial[((size_t)s * E + e0 + i) * d + c] = acc[i];
+    }
+}
+
+__global__ void __launch_bounds__(256)
+router_wgrad_sum_kernel(const float* __restrict__ partial, int S, long long n, float* __restrict__ dW)
+{
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
+        float a = 0.f;
+        for (int s = 0; s < S; ++s) a += __ldg(partial + (size_t)s * n + i);
+        dW[i] = a;
+    }
+}
+
+}  // namespace bwd

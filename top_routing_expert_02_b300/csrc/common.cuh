@@ -55,12 +55,13 @@ __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)
 // group scores its largest logit; the topk_group best groups (ties: lower
 // group) are kept and the k experts are chosen among theirs.  n_group = 1 is
 // plain top-k.  lse, when set, receives log sum_e exp(l[t,e]) per token for
-// the router z-loss.
+// the router z-loss; logits, when set, receives the logits themselves.
 struct RouteSel {
     int n_group;      // 1..32
     int gsz;          // E / n_group
     int topk_group;   // 1..n_group
     float* lse;       // [T] or nullptr
+    float* logits;    // [T, E] (bias included) or nullptr: kept for the backward
 };
 
 // Group mask of one token (bit g set: group g kept), lane l holding the

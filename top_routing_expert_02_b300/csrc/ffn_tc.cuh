@@ -69,8 +69,21 @@ struct Args {
     const int32_t* row_token;   // gathered A: row r of the tile is x[row_token[r]]
     const uint8_t* a_base;      // gathered A: x
     uint32_t a_row_bytes;       // gathered A: bytes of one x row (x is below 4 GB)
+    float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols]
+    int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
+    int m_rows;                 // weight gradient: rows M of each expert's gradient
     unsigned long long wait_limit;
 };
+
+// Where the A operand and the K range come from:
+//   MODE_ROWS    A = x_perm rows of the expert's segment (TMA box), K = 0..K-1
+//   MODE_GATHER  A = x rows at row_token[] (cp.async), K = 0..K-1
+//   MODE_WGRAD   weight gradients: A [M, ld] and B [N, ld] are transposed,
+//                segment-packed activations; expert e contracts over its own
+//                K columns [64 kstart[e], 64 kstart[e+1]) (kept[e] rounded up
+//                to 64, zero padded); every expert has m_tiles M-tiles; the
+//                output is fp32 [E, M, N] (zeros for an expert with no rows)
+enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2 };
 
 __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tiles, int tile, int& e, int& m,
                                             int& n)
@@ -103,7 +116,7 @@ __device__ __forceinline__ void gather_offsets(const Args& g, const int* mstart,
     }
 }
 
-// GATHER: the A rows are read straight from x at row_token[] (the dispatch
+// MODE_GATHER: the A rows are read straight from x at row_token[] (the dispatch
 // permutation), so no permuted copy of x is materialised.  The 32 lanes of
 // the producer warp copy them with 16-byte cp.async (lane l: chunk l % 8 of
 // rows 4i + l / 8, written to the 128-byte-swizzled place a TMA box load would
@@ -111,11 +124,12 @@ __device__ __forceinline__ void gather_offsets(const Args& g, const int* mstart,
 // land (33 arrivals: 32 lanes + lane 0's TMA transaction arrival for the B
 // tile).  Those are generic-proxy writes: the MMA thread fences them into the
 // async proxy after its wait and before its tcgen05.mma reads them.
-template <int EPI, int BN, bool GATHER>
+template <int EPI, int BN, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const Args g)
 {
+    constexpr bool GATHER = MODE == MODE_GATHER, WGRAD = MODE == MODE_WGRAD;
     using SH = Shape<BN>;
     constexpr int STAGES = SH::STAGES, STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
     constexpr int ACC_COLS = SH::ACC_COLS, TMEM_COLS = SH::TMEM_COLS;
@@ -124,6 +138,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int mstart[257];
+    __shared__ int kstart[WGRAD ? 257 : 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem0 = (ptx::smem_u32(dsmem) + 1023u) & ~1023u;
@@ -146,7 +161,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    if (warp == 2) build_mtile_prefix<BM>(g.kept, g.E, mstart, lane);
+    if (warp == 2) {
+        if (WGRAD) {
+            for (int e = lane; e <= g.E; e += 32) mstart[e] = e * g.m_tiles;
+        } else {
+            build_mtile_prefix<BM>(g.kept, g.E, mstart, lane);
+        }
+    }
+    if (WGRAD && warp == 3) build_mtile_prefix<BK>(g.kept, g.E, kstart, lane);   // K blocks per expert
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -166,11 +188,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 int e, m, n;
                 decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
-                const int rowA = __ldg(g.offsets + e) + m * BM;
-                const int rowB0 = e * g.b_rows + n * g.n_step;
+                const int rowA = WGRAD ? m * BM : __ldg(g.offsets + e) + m * BM;
+                const int rowB0 = (WGRAD ? 0 : e * g.b_rows) + n * g.n_step;
                 const int rowB1 = rowB0 + g.half_off;
+                const int kb0 = WGRAD ? kstart[e] : 0;
+                const int nkt = WGRAD ? kstart[e + 1] - kb0 : nk;
                 if (GATHER) gather_offsets(g, mstart, tile, lane, roff);
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = 0; kb < nkt; ++kb) {
                     bool got = true;
                     if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit);
                     if (GATHER) got = __shfl_sync(0xffffffffu, got, 0);
@@ -182,9 +206,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = smem0 + stage * STAGE_BYTES;
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(fb, GATHER ? 2 * BH_BYTES : STAGE_BYTES);
-                        if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kb * BK, rowA);
-                        ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, rowB0);
-                        ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kb * BK, rowB1);
+                        const int kx = (kb0 + kb) * BK;
+                        if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kx, rowA);
+                        ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, rowB0);
+                        ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kx, rowB1);
                     }
                     if (GATHER) {
                         const uint8_t* src = g.a_base + (size_t)kb * (BK * 2);
@@ -230,7 +255,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
-                for (int kb = 0; kb < nk; ++kb) {
+                int nkt = nk;
+                if (WGRAD) {
+                    int e, m, n;
+                    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+                    nkt = kstart[e + 1] - kstart[e];   // 0: nothing accumulates, the epilogue writes zeros
+                }
+                for (int kb = 0; kb < nkt; ++kb) {
                     if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, limit)) {
                         ok = false;
                         break;
@@ -267,8 +298,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             int e, m, n;
             decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
-            const int rows_valid = __ldg(g.kept + e) - m * BM;
-            const int row = __ldg(g.offsets + e) + m * BM + r_in;
+            const int rows_valid = WGRAD ? g.m_rows - m * BM : __ldg(g.kept + e) - m * BM;
+            const int row = WGRAD ? e * g.m_rows + m * BM + r_in : __ldg(g.offsets + e) + m * BM + r_in;
             const bool rv = r_in < rows_valid;
             const bool waited = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aphase, limit);
             if (!__all_sync(0xffffffffu, waited)) {
@@ -277,7 +308,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            if (EPI == EPI_SWIGLU) {
+            if (WGRAD) {
+                const bool empty = kstart[e + 1] == kstart[e];
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t av[32];
+                    if (!empty) {
+                        ptx::tmem_ld32(tb + c, av);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) av[i] = 0u;
+                    }
+                    const int col = n * BN + c;
+                    if (rv && col < g.out_cols) {
+                        uint4* dst = reinterpret_cast<uint4*>(g.out_f32 + (size_t)row * g.out_cols + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_uint4(av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3]);
+                    }
+                }
+            } else if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
                     uint32_t gv[32], uv[32];

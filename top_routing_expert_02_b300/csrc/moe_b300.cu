@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "backward.cuh"
 #include "combine.cuh"
 #include "dispatch.cuh"
 #include "ffn_simt.cuh"
@@ -195,23 +196,26 @@ bool make_tmap_bf16_box(CUtensorMap* m, const void* base, unsigned long long row
 }
 
 // A_rows: rows of the A tensor (rows_max of x_perm, or T of x when gathering).
-template <int EPI, int BN, bool GATHER = false>
+// A_rows: rows of the A tensor (default rows_max; T of x when gathering; M in
+// the weight-gradient mode, where K is the packed column count ld).
+template <int EPI, int BN, int MODE = tcg::MODE_ROWS>
 moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W, long long w_rows_total,
                         tcg::Args args, cudaStream_t stream, long long A_rows = -1)
 {
     using SH = tcg::Shape<BN>;
     CUtensorMap ta, tb;
     if (!make_tmap_bf16_box(&ta, A, (unsigned long long)(A_rows >= 0 ? A_rows : rows_max), (unsigned long long)K,
-                            GATHER ? 1 : 128))
+                            MODE == tcg::MODE_GATHER ? 1 : 128))
         return MOE_ERR_CUDA;
     if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2))
         return MOE_ERR_CUDA;
-    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, GATHER>, SH::SMEM_DYN)) return launch_status();
-    const long long max_mtiles = (rows_max + tcg::BM - 1) / tcg::BM + args.E;
-    const long long max_tiles = max_mtiles * args.n_tiles;
+    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, SH::SMEM_DYN)) return launch_status();
+    const long long max_tiles = MODE == tcg::MODE_WGRAD
+                                    ? (long long)args.E * args.m_tiles * args.n_tiles
+                                    : ((rows_max + tcg::BM - 1) / tcg::BM + args.E) * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
-    tcg::grouped_gemm_kernel<EPI, BN, GATHER><<<grid, tcg::THREADS, SH::SMEM_DYN, stream>>>(ta, tb, args);
+    tcg::grouped_gemm_kernel<EPI, BN, MODE><<<grid, tcg::THREADS, SH::SMEM_DYN, stream>>>(ta, tb, args);
     return launch_status();
 }
 
@@ -342,6 +346,19 @@ int64_t moe_perm_rows_max(int64_t T, int k, int E, int64_t cap)
     return all < lim ? all : lim;
 }
 
+namespace {
+// Token splits of the router weight gradient: enough blocks for two waves.
+int router_wgrad_splits(int64_t T, int E, int d)
+{
+    const int base = ceil_div_i(d, 256) * ceil_div_i(E, bwd::RW_EXP);
+    int S = ceil_div_i(2 * 148, base);
+    if (S > 16) S = 16;
+    const int maxS = ceil_div_i(T, 32);
+    if (S > maxS) S = maxS;
+    return S < 1 ? 1 : S;
+}
+}  // namespace
+
 size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F, moe_act act, moe_dtype dtype)
 {
     (void)F;
@@ -352,6 +369,8 @@ size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F,
     case MOE_CALL_ROUTE: return route_ws_bytes(T, d, E);
     case MOE_CALL_DISPATCH: return dispatch_ws_bytes(T, k, E);
     case MOE_CALL_FFN: return 0;
+    case MOE_CALL_ROUTER_WGRAD:
+        return T < 1 || d < 1 ? 0 : (size_t)router_wgrad_splits(T, E, d) * E * d * sizeof(float);
     }
     return 0;
 }
@@ -464,19 +483,19 @@ moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const 
                      int E, int k, int renorm, int32_t* topk_idx, float* topk_gate, float* prob_sum, void* ws,
                      size_t ws_bytes, moe_stream_t stream)
 {
-    const RouteSel plain{1, E > 0 ? E : 1, 1, nullptr};
+    const RouteSel plain{1, E > 0 ? E : 1, 1, nullptr, nullptr};
     return route_impl(x, xdt, w_router, b_router, T, d, E, k, renorm, topk_idx, topk_gate, prob_sum, plain, ws,
                       ws_bytes, (cudaStream_t)stream);
 }
 
 moe_status moe_route_ex(const void* x, moe_dtype xdt, const float* w_router, const float* b_router, int64_t T, int d,
                         int E, int k, int renorm, int n_group, int topk_group, int32_t* topk_idx, float* topk_gate,
-                        float* prob_sum, float* lse, void* ws, size_t ws_bytes, moe_stream_t stream)
+                        float* prob_sum, float* lse, float* logits, void* ws, size_t ws_bytes, moe_stream_t stream)
 {
     if (n_group < 1 || n_group > 32 || E < 1 || E % n_group || topk_group < 1 || topk_group > n_group)
         return MOE_ERR_INVALID_ARG;
     if ((long long)k > (long long)topk_group * (E / n_group)) return MOE_ERR_INVALID_ARG;
-    const RouteSel sel{n_group, E / n_group, topk_group, T > 0 ? lse : nullptr};
+    const RouteSel sel{n_group, E / n_group, topk_group, T > 0 ? lse : nullptr, T > 0 ? logits : nullptr};
     return route_impl(x, xdt, w_router, b_router, T, d, E, k, renorm, topk_idx, topk_gate, prob_sum, sel, ws,
                       ws_bytes, (cudaStream_t)stream);
 }
@@ -623,9 +642,10 @@ moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_t
     a.half_off = sw ? F : 128;
     a.n_tiles = (F + a.n_step - 1) / a.n_step;
     const long long wr = (long long)E * N1;
-    if (sw) return launch_tc_bn<tcg::EPI_SWIGLU, 256, true>(x, rows_max, d, w1, wr, a, stream, T);
-    if (act == MOE_ACT_GELU) return launch_tc_bn<tcg::EPI_GELU, 256, true>(x, rows_max, d, w1, wr, a, stream, T);
-    return launch_tc_bn<tcg::EPI_IDENT, 256, true>(x, rows_max, d, w1, wr, a, stream, T);
+    constexpr int G = tcg::MODE_GATHER;
+    if (sw) return launch_tc_bn<tcg::EPI_SWIGLU, 256, G>(x, rows_max, d, w1, wr, a, stream, T);
+    if (act == MOE_ACT_GELU) return launch_tc_bn<tcg::EPI_GELU, 256, G>(x, rows_max, d, w1, wr, a, stream, T);
+    return launch_tc_bn<tcg::EPI_IDENT, 256, G>(x, rows_max, d, w1, wr, a, stream, T);
 }
 
 moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
@@ -787,6 +807,160 @@ moe_status noalloc_scratch(void** out)
     return MOE_OK;
 }
 }  // namespace
+
+// ============================================================== backward ===
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status moe_transpose_experts(const void* w, int E, int R, int C, moe_dtype dtype, void* wt, moe_stream_t stream)
+{
+    if (E < 1 || R <= 0 || C <= 0 || !w || !wt || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || R % 64 || C % 64 || R / 64 > 65535 || E > 65535 || !aligned16(w) || !aligned16(wt))
+        return MOE_ERR_UNSUPPORTED;
+    bwd::transpose_experts_kernel<<<dim3(C / 64, R / 64, E), 256, 0, (cudaStream_t)stream>>>(
+        (const uint16_t*)w, R, C, (uint16_t*)wt);
+    return launch_status();
+}
+
+moe_status moe_combine_bwd(const void* dy, const int32_t* slot_row, const float* row_gate, const void* y_perm,
+                           int64_t T, int k, int d, moe_dtype dtype, void* do_perm, float* dgate, moe_stream_t stream)
+{
+    if (T < 0 || k < 1 || k > MAX_K || d <= 0 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!dy || !slot_row || !row_gate || !y_perm || !do_perm || !dgate)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || d % 64) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    int grid = ceil_div_i(T, bwd::CB_THREADS / 32);
+    if (grid > sm_count() * 8) grid = sm_count() * 8;
+    bwd::combine_bwd_kernel<<<grid, bwd::CB_THREADS, 0, (cudaStream_t)stream>>>(
+        (const uint4*)dy, slot_row, row_gate, (const uint4*)y_perm, (int)T, k, d / 8, (uint4*)do_perm, dgate);
+    return launch_status();
+}
+
+moe_status moe_act_bwd(const void* z, const void* da, const int32_t* offsets, int E, int F, moe_act act,
+                       moe_dtype dtype, int64_t rows_max, void* dz, moe_stream_t stream)
+{
+    if (E < 1 || E > MAX_E || F <= 0 || rows_max < 0 || !offsets || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
+    if (rows_max > 0 && (!z || !da || !dz)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || F % 64) return MOE_ERR_UNSUPPORTED;
+    if (rows_max == 0) return MOE_OK;
+    const int grid = sm_count() * 8;
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint16_t *zp = (const uint16_t*)z, *ap = (const uint16_t*)da;
+    if (act == MOE_ACT_SWIGLU)
+        bwd::act_bwd_kernel<MOE_ACT_SWIGLU><<<grid, 256, 0, st>>>(zp, ap, offsets, E, F, (uint16_t*)dz);
+    else if (act == MOE_ACT_GELU)
+        bwd::act_bwd_kernel<MOE_ACT_GELU><<<grid, 256, 0, st>>>(zp, ap, offsets, E, F, (uint16_t*)dz);
+    else
+        bwd::act_bwd_kernel<MOE_ACT_IDENTITY><<<grid, 256, 0, st>>>(zp, ap, offsets, E, F, (uint16_t*)dz);
+    return launch_status();
+}
+
+int64_t moe_wgrad_cols(int64_t rows_max, int E)
+{
+    if (rows_max < 0 || E < 1) return -1;
+    return (rows_max + 64LL * E + 63) / 64 * 64;
+}
+
+moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const int32_t* kept, int E, int C,
+                               int64_t rows_max, int64_t ld, moe_dtype dtype, void* dst, moe_stream_t stream)
+{
+    if (E < 1 || E > MAX_E || C <= 0 || rows_max < 0 || !offsets || !kept || !dtype_ok(dtype))
+        return MOE_ERR_INVALID_ARG;
+    if (ld < moe_wgrad_cols(rows_max, E) || ld % 64) return MOE_ERR_INVALID_ARG;
+    if (rows_max > 0 && (!src || !dst)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || C % 64 || ld / 64 > 65535) return MOE_ERR_UNSUPPORTED;
+    if (rows_max == 0) return MOE_OK;
+    bwd::pack_segments_t_kernel<<<dim3(C / 64, (unsigned)(ld / 64)), 256, 0, (cudaStream_t)stream>>>(
+        (const uint16_t*)src, offsets, kept, E, C, (long long)ld, (uint16_t*)dst);
+    return launch_status();
+}
+
+moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept, int E, int M, int N, int64_t ld,
+                            moe_dtype dtype, float* dw, moe_stream_t stream)
+{
+    if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || ld <= 0 || !kept || !at || !bt || !dw || !dtype_ok(dtype))
+        return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || M % 64 || N % 64 || ld % 64 || ld >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+    tcg::Args a{};
+    a.kept = kept;
+    a.E = E;
+    a.K = (int)ld;
+    a.m_tiles = (M + 127) / 128;
+    a.m_rows = M;
+    a.n_step = 256;
+    a.half_off = 128;
+    a.n_tiles = (N + 255) / 256;
+    a.out_cols = N;
+    a.out_f32 = dw;
+    a.wait_limit = g_wait_limit.load();
+    return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD>(at, 0, (int)ld, bt, N, a, (cudaStream_t)stream, M);
+}
+
+moe_status moe_route_bwd(const float* logits, const int32_t* topk_idx, const float* dgate, const int32_t* counts,
+                         int64_t T, int E, int k, int renorm, float aux_coef, float z_coef, float* dl,
+                         moe_stream_t stream)
+{
+    if (T < 0 || E < 1 || E > MAX_E || k < 1 || k > MAX_K || k > E || !counts) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_idx || !dgate || !dl)) return MOE_ERR_INVALID_ARG;
+    if (T * k >= INT_MAX || T * E >= ((int64_t)1 << 40)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    int grid = ceil_div_i(T, 8);
+    if (grid > sm_count() * 8) grid = sm_count() * 8;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int Ti = (int)T;
+#define MOE_RB(EP) bwd::route_bwd_kernel<EP><<<grid, 256, 0, st>>>(logits, topk_idx, dgate, counts, Ti, E, k, renorm, \
+                                                                  aux_coef, z_coef, dl)
+    if (E <= 32) MOE_RB(1);
+    else if (E <= 64) MOE_RB(2);
+    else if (E <= 128) MOE_RB(4);
+    else MOE_RB(8);
+#undef MOE_RB
+    return launch_status();
+}
+
+moe_status moe_grad_x(const void* dx_perm, const int32_t* slot_row, const float* dl, const float* w_router,
+                      int64_t T, int k, int E, int d, moe_dtype dtype, void* dx, moe_stream_t stream)
+{
+    if (T < 0 || k < 1 || k > MAX_K || E < 1 || E > MAX_E || d <= 0 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!dx_perm || !slot_row || !dl || !w_router || !dx)) return MOE_ERR_INVALID_ARG;
+    if (T / bwd::GX_TOK >= 65535) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    const dim3 grid(ceil_div_i(d, 256), ceil_div_i(T, bwd::GX_TOK));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (dtype == MOE_BF16)
+        bwd::grad_x_kernel<true><<<grid, 256, 0, st>>>(dx_perm, slot_row, dl, w_router, (int)T, k, E, d, dx);
+    else
+        bwd::grad_x_kernel<false><<<grid, 256, 0, st>>>(dx_perm, slot_row, dl, w_router, (int)T, k, E, d, dx);
+    return launch_status();
+}
+
+moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64_t T, int E, int d, float* dW,
+                            float* db, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (T < 1 || E < 1 || E > MAX_E || d <= 0 || !dl || !x || !dW || !dtype_ok(xdt)) return MOE_ERR_INVALID_ARG;
+    const int S = router_wgrad_splits(T, E, d);
+    const size_t need = (size_t)S * E * d * sizeof(float);
+    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int per = ceil_div_i(ceil_div_i(T, S), 32) * 32;
+    const dim3 grid(ceil_div_i(d, 256), ceil_div_i(E, bwd::RW_EXP), S);
+    float* part = (float*)ws;
+    if (xdt == MOE_BF16)
+        bwd::router_wgrad_kernel<true><<<grid, 256, 0, st>>>(dl, x, (int)T, E, d, per, part);
+    else
+        bwd::router_wgrad_kernel<false><<<grid, 256, 0, st>>>(dl, x, (int)T, E, d, per, part);
+    moe_status s = launch_status();
+    if (s != MOE_OK) return s;
+    const long long n = (long long)E * d;
+    int g2 = ceil_div_i(n, 256);
+    if (g2 > sm_count() * 8) g2 = sm_count() * 8;
+    bwd::router_wgrad_sum_kernel<<<g2, 256, 0, st>>>(part, S, n, dW);
+    s = launch_status();
+    if (s != MOE_OK || !db) return s;
+    rtc::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
+    return launch_status();
+}
 
 extern "C" moe_status moe_dispatch_noalloc(const int32_t* topk_idx, const float* topk_gate, int64_t T, int k, int E,
                                            int64_t cap, const void* x, moe_dtype xdt, int d, int32_t* counts,

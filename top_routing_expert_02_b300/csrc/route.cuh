@@ -124,6 +124,11 @@ route_kernel(const void* __restrict__ x, const float* __restrict__ W, const floa
 #pragma unroll
         for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (sel.lse && lane == 0) sel.lse[t] = mx + logf(s);
+        if (sel.logits) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (lane + 32 * i < E) sel.logits[(size_t)t * E + lane + 32 * i] = l[i];
+        }
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             p[i] = p[i] / s;

@@ -352,6 +352,11 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
             s += p[e];
         }
         if (sel.lse) sel.lse[t] = mx + logf(s);
+        if (sel.logits) {
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e)
+                if (e < E) sel.logits[(size_t)t * E + e] = l[e];
+        }
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) acc_p[e] += p[e] / s;
         float chosen = 0.f;
@@ -414,6 +419,11 @@ route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, in
 #pragma unroll
         for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (sel.lse && lane == 0) sel.lse[t] = mx + logf(s);
+        if (sel.logits) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (lane + 32 * i < E) sel.logits[(size_t)t * E + lane + 32 * i] = l[i];
+        }
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             p[i] = p[i] / s;
