@@ -30,6 +30,12 @@ the same workload (its first S tokens, capacity recomputed for S tokens).
 ``--impl reference``: the CPU oracle alone on the host cores (the method has
 no other runnable implementation); rank 0 only.
 
+``--train``: a step is the forward and the backward (input, router and
+expert weight gradients of <dy, y> + aux loss (+ z-loss), transposed weight
+copies included) for a seeded upstream gradient dy; the JSON line reports
+the fwd+bwd rate, per-phase times and the roofline of the largest backward
+GEMM (the w1 weight gradient).
+
 Variants (same step, same JSON line; ``config.variant`` names them):
 group-limited routing (``--n-group``/``--topk-group``), the router z-loss
 (``--z-beta``), the post-drop f_i aux loss (``--aux-post-drop``) and the
@@ -69,16 +75,21 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     gather = bool(args and args.gather)
     dispatch = 2 if gather else 3          # histogram, ranks (+ row copy)
     z = 1 if (args and args.z_beta is not None) else 0
-    return route + dispatch + 1 + 1 + 1 + 1 + z   # up, down, combine, aux (+ z-loss)
+    bwd = BWD_KERNELS if (args and args.train) else 0
+    return route + dispatch + 1 + 1 + 1 + 1 + z + bwd   # up, down, combine, aux (+ z-loss) (+ backward)
 
 
 def plan_kwargs(args) -> dict:
     return dict(gather=args.gather, n_group=args.n_group, topk_group=args.topk_group, z_beta=args.z_beta,
-                aux_post_drop=args.aux_post_drop)
+                aux_post_drop=args.aux_post_drop, train=args.train)
+
+
+BWD_KERNELS = 2 + 1 + 3 + 1 + 4 + 2 + 1 + 1 + 3   # transposes, combine bwd, 3 GEMMs, act bwd, packs, wgrads,
+                                                  # router bwd, dx, router weights (partial, sum, bias)
 
 
 def variant_dict(args) -> dict:
-    return {"n_group": args.n_group, "topk_group": args.topk_group, "z_beta": args.z_beta,
+    return {"train": args.train, "n_group": args.n_group, "topk_group": args.topk_group, "z_beta": args.z_beta,
             "aux_f": "kept slots (post-drop)" if args.aux_post_drop else "every choice (pre-drop)",
             "up_projection": "gathers x rows (no x_perm)" if args.gather else "reads x_perm"}
 
@@ -223,24 +234,36 @@ def reference_arm(args, cfg):
     ri = synth.make_routing_inputs(cfg)
     w1, w2 = synth.make_expert_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
     var = oracle_variant(args)
-    cb, S, t = oracle_sample(cfg, ri, w1, w2, budget_s=max(0.2, 120.0 / max(1, args.steps + args.warmup)),
-                             variant=var)
-    # warm-up and timed steps: each step is the bounded sample
+    budget = max(0.2, 120.0 / max(1, args.steps + args.warmup))
     import oracle
+    from oracle import backward as ob
     w1h, w2h = w1.cpu(), w2.cpu()
-    sub = ri.x[:S].contiguous()
+    dy = torch.randn(cfg.T, cfg.d, generator=torch.Generator().manual_seed(777)).to(
+        torch.bfloat16 if cfg.dtype == "bf16" else torch.float32)
+    if args.train:
+        cb = oracle_sample_train(cfg, ri, w1, w2, dy, var, budget_s=budget)
+        S = int(cb["sample"].split()[1])
+    else:
+        cb, S, _ = oracle_sample(cfg, ri, w1, w2, budget_s=budget, variant=var)
+    # warm-up and timed steps: each step is the bounded sample
+    sub, dys = ri.x[:S].contiguous(), dy[:S].contiguous()
     cap = oracle.capacity(S, cfg.E, cfg.cf)
+    bvar = {k: var[k] for k in ("n_group", "topk_group", "z_beta", "aux_post_drop")}
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         oracle.forward(sub, ri.W, ri.b, w1h, w2h, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
                        alpha=cfg.alpha, **var)
+        if args.train:
+            ob.backward(sub, ri.W, ri.b, w1h, w2h, dys, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
+                        alpha=cfg.alpha, **bvar)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     ms = 1000.0 * statistics.mean(times)
     value = S / (ms / 1000.0)
     cb["value"] = value
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    metric = "MoE-layer fwd+bwd tokens/s on 1 B300" if args.train else METRIC
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(cfg, args), "cpu_baseline": cb,
@@ -480,6 +503,162 @@ def our_arm(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+def train_arm(args, cfg):
+    """--train: forward + backward per step (rank 0 prints; ranks run independent batches)."""
+    import top_routing_expert_02_b300 as moe
+    from top_routing_expert_02_b300 import dist as mdist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    moe.lib()
+    if cfg.dtype != "bf16" or args.gather:
+        raise SystemExit("--train runs bf16 layers with a materialised x_perm")
+    rcfg = cfg.replace(seed=cfg.seed + rank)
+    ri = synth.make_routing_inputs(rcfg)
+    w1, w2 = synth.make_expert_weights(cfg, device=dev)
+    x, W = ri.x.to(dev), ri.W.to(dev)
+    b = None if ri.b is None else ri.b.to(dev)
+    g = torch.Generator().manual_seed(777 + rank)
+    dy_host = torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16)
+    dy = dy_host.to(dev)
+    cap = moe.capacity(cfg.T, cfg.E, cfg.cf)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, cap, dev, cfg.alpha, cfg.renorm,
+                       **plan_kwargs(args))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    phases = ["forward", "transpose_weights", "combine_bwd", "data_grad_gemms", "pack", "wgrad_dw2", "wgrad_dw1",
+              "router_and_dx"]
+
+    def step(evs=None):
+        def mark(name):
+            if evs is not None:
+                evs[name].record(stream)
+        mark("start")
+        plan.run(x, W, b, w1, w2)
+        mark("forward")
+        plan.backward(x, W, w1, w2, dy, mark=mark)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    moe.check()
+    A = int(plan.disp.offsets[plan.E].item())
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in ["start"] + phases} for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier()
+    with sampler:
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        barrier()
+    moe.check()
+    part = {n: [] for n in phases + ["step"]}
+    for e in evs:
+        prev = "start"
+        for n in phases:
+            part[n].append(e[prev].elapsed_time(e[n]))
+            prev = n
+        part["step"].append(e["start"].elapsed_time(e[phases[-1]]))
+    ms_step = statistics.mean(part["step"])
+    if world > 1:
+        ms_step = mdist.max_over_ranks(ms_step, device=dev)
+
+    # end to end: x and dy from pinned host memory, dx and the loss back; the
+    # weight gradients stay on the device where an optimiser would use them
+    x_host, dyh = ri.x.pin_memory(), dy_host.pin_memory()
+    dx_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        x.copy_(x_host, non_blocking=True)
+        dy.copy_(dyh, non_blocking=True)
+        step()
+        dx_host.copy_(plan._bwd["dx"][:cfg.T], non_blocking=True)
+        loss_host.copy_(plan.loss, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    s1.record(stream)
+    barrier()
+    moe.check()
+    ms_e2e = s0.elapsed_time(s1) / args.steps
+    if world > 1:
+        ms_e2e = mdist.max_over_ranks(ms_e2e, device=dev)
+
+    hbm, bf16_peak, bf16_sust, peak_src = peaks()
+    dw1_flops = 2.0 * A * cfg.N1 * cfg.d
+    dw1_ms = statistics.mean(part["wgrad_dw1"])
+    achieved = dw1_flops / (dw1_ms * 1e-3) / 1e12
+    gemm_flops = 2.0 * A * cfg.d * cfg.N1 * 3 + 2.0 * A * cfg.F * cfg.d * 3   # fwd 2 + bwd 4 GEMMs + z recompute
+    line = {
+        "metric": "MoE-layer fwd+bwd tokens/s on 1 B300", "value": world * cfg.T / (ms_step / 1000.0),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded; weights random-init; seeded upstream gradient)",
+        "config": config_dict(cfg, args), "clocks": sampler.summary(),
+        "e2e": {"value": world * cfg.T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": 2 * cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2 + 4},
+        "gpu_launches": KERNELS_PER_STEP_TOTAL(cfg, args) * args.steps,
+        "roofline": {"kernel": "expert_wgrad dw1 (tcgen05 grouped GEMM, per-expert K, fp32 out)", "bound": "tensor",
+                     "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                     "peak_source": f"{peak_src} bf16 dense burst", "traffic": None,
+                     "frac_of_sustained": achieved / bf16_sust, "algorithmic_flops_per_launch": dw1_flops},
+        "gemm_tflops_step": gemm_flops / (ms_step * 1e-3) / 1e12,
+        "kernel_ms": {k: statistics.mean(v) for k, v in part.items()},
+        "routing": {"kept_slots": A},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample_train(cfg, ri, w1, w2, dy_host, oracle_variant(args))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def oracle_sample_train(cfg, ri, w1, w2, dy, variant, budget_s: float = 15.0):
+    """The CPU oracles (forward + backward) on the first S tokens."""
+    import oracle
+    from oracle import backward as ob
+    w1h, w2h = w1.cpu(), w2.cpu()
+    bvar = dict(n_group=variant["n_group"], topk_group=variant["topk_group"], z_beta=variant["z_beta"],
+                aux_post_drop=variant["aux_post_drop"])
+
+    def run(S):
+        sub, dys = ri.x[:S].contiguous(), dy[:S].contiguous()
+        cap = oracle.capacity(S, cfg.E, cfg.cf)
+        t0 = time.perf_counter()
+        oracle.forward(sub, ri.W, ri.b, w1h, w2h, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
+                       alpha=cfg.alpha, **variant)
+        ob.backward(sub, ri.W, ri.b, w1h, w2h, dys, k=cfg.k, cap=cap, act=cfg.act, renorm=cfg.renorm,
+                    alpha=cfg.alpha, **bvar)
+        return time.perf_counter() - t0
+
+    S = min(cfg.T, 8)
+    t = run(S)
+    if t < budget_s / 4 and S < cfg.T:
+        S = int(min(cfg.T, max(S + 1, S * (budget_s / max(t, 1e-3)))))
+        t = run(S)
+    return {"value": S / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {S} of {cfg.T} tokens, forward + backward in fp64 (capacity for {S} tokens), "
+                      f"{t:.1f} s"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,12 +672,15 @@ def main():
     ap.add_argument("--z-beta", type=float, default=None, help="router z-loss coefficient (off when absent)")
     ap.add_argument("--aux-post-drop", action="store_true", help="aux loss f_i from kept slots")
     ap.add_argument("--gather", action="store_true", help="up-projection gathers x rows (bf16 only)")
+    ap.add_argument("--train", action="store_true", help="time forward + backward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     args.steps = max(args.steps, 1)
     cfg = synth.workload(args.workload)
     if args.impl == "reference":
         reference_arm(args, cfg)
+    elif args.train:
+        train_arm(args, cfg)
     else:
         our_arm(args, cfg)
 

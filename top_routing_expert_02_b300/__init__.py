@@ -540,21 +540,29 @@ class MoEPlan:
         return self._bwd
 
     def backward(self, x, w_router, w1, w2, dy, *, aux_weight: float = 1.0, z_weight: float = 1.0, w1t=None,
-                 w2t=None, stream=None) -> dict:
+                 w2t=None, stream=None, mark=None) -> dict:
         """Gradients of <dy, y> + aux_weight * loss + z_weight * z_loss after
         :meth:`run` on the same inputs (``train=True``).  ``w1t`` / ``w2t``
         are the transposed expert weights ([E, d, N1] / [E, F, d]); they are
         made here when not given.  Returns dx, dW, db, dw1, dw2 (weight
-        gradients fp32) and the intermediates; all buffers belong to the plan."""
+        gradients fp32) and the intermediates; all buffers belong to the plan.
+        ``mark(name)``, when given, is called after each phase (for timing)."""
         if not self.train:
             raise ValueError("construct the plan with train=True")
+        mark = mark or (lambda name: None)
         B = self._bwd_buffers(x.device)
         D = self.disp
         R, F, E, d = self.rows_max, self.F, self.E, self.d
         N1 = 2 * F if self.act == "swiglu" else F
-        w1t = transpose_experts(w1, stream=stream) if w1t is None else w1t
-        w2t = transpose_experts(w2, stream=stream) if w2t is None else w2t
+        if w1t is None:
+            w1t = B.setdefault("w1t", torch.empty((E, d, N1), dtype=w1.dtype, device=w1.device))
+            transpose_experts(w1, out=w1t, stream=stream)
+        if w2t is None:
+            w2t = B.setdefault("w2t", torch.empty((E, F, d), dtype=w2.dtype, device=w2.device))
+            transpose_experts(w2, out=w2t, stream=stream)
+        mark("transpose_weights")
         combine_bwd(dy, D.slot_row, D.row_gate, self.y_perm, do_perm=B["do_perm"], dgate=B["dgate"], stream=stream)
+        mark("combine_bwd")
         # data gradients: recompute z, then da, dz, dx_perm (identity epilogues on transposed weights)
         _ok("moe_expert_up", lib().moe_expert_up(_ptr(D.x_perm), _ptr(D.offsets), _ptr(D.kept), E, d, N1,
                                                  ACT["identity"], _dt(D.x_perm), _ptr(w1), R, _ptr(B["z"]),
@@ -566,14 +574,18 @@ class MoEPlan:
         _ok("moe_expert_up", lib().moe_expert_up(_ptr(B["dz"]), _ptr(D.offsets), _ptr(D.kept), E, N1, d,
                                                  ACT["identity"], _dt(w1t), _ptr(w1t), R, _ptr(B["dx_perm"]),
                                                  _stream(stream)))
+        mark("data_grad_gemms")
         # weight gradients on segment-packed transposes
         ld = B["ld"]
         pack_segments_t(B["do_perm"], D.offsets, D.kept, R, ld, out=B["doT"], stream=stream)
         pack_segments_t(self.h, D.offsets, D.kept, R, ld, out=B["hT"], stream=stream)
         pack_segments_t(B["dz"], D.offsets, D.kept, R, ld, out=B["dzT"], stream=stream)
         pack_segments_t(D.x_perm, D.offsets, D.kept, R, ld, out=B["xT"], stream=stream)
+        mark("pack")
         expert_wgrad(B["doT"], B["hT"], D.kept, dw=B["dw2"], stream=stream)
+        mark("wgrad_dw2")
         expert_wgrad(B["dzT"], B["xT"], D.kept, dw=B["dw1"], stream=stream)
+        mark("wgrad_dw1")
         # router
         counts = D.kept if self.aux_post_drop else D.counts
         zc = z_weight * (self.z_beta or 0.0)
@@ -581,6 +593,7 @@ class MoEPlan:
                   dl=B["dl"], stream=stream)
         grad_x(B["dx_perm"], D.slot_row, B["dl"], w_router, dx=B["dx"], stream=stream)
         router_wgrad(B["dl"], x, dW=B["dW"], db=B["db"], ws=B["ws"], stream=stream)
+        mark("router_and_dx")
         return dict(dx=B["dx"], dW=B["dW"], db=B["db"], dw1=B["dw1"], dw2=B["dw2"], dgate=B["dgate"], dl=B["dl"],
                     do_perm=B["do_perm"], z=B["z"], da=B["da"], dz=B["dz"], dx_perm=B["dx_perm"])
 

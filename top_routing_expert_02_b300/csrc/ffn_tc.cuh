@@ -46,6 +46,11 @@ struct Shape {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 6 ? 6 : (200 * 1024) / STAGE_BYTES;
     static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;       // + slack for 1024-B alignment
+    // weight-gradient mode: one stage fewer, and a 32x32 fp32 staging tile
+    // per epilogue warp for the TMA stores of the output
+    static constexpr int WG_STAGES = STAGES - 1;
+    static constexpr int WG_STAGE_OUT = 32 * 32 * 4;
+    static constexpr int WG_SMEM_DYN = WG_STAGES * STAGE_BYTES + 4 * WG_STAGE_OUT + 1024;
     static constexpr int ACC_COLS = BN;
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
@@ -127,11 +132,12 @@ __device__ __forceinline__ void gather_offsets(const Args& g, const int* mstart,
 template <int EPI, int BN, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const Args g)
+                    const __grid_constant__ CUtensorMap tmC, const Args g)
 {
     constexpr bool GATHER = MODE == MODE_GATHER, WGRAD = MODE == MODE_WGRAD;
     using SH = Shape<BN>;
-    constexpr int STAGES = SH::STAGES, STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
+    constexpr int STAGES = WGRAD ? SH::WG_STAGES : SH::STAGES;
+    constexpr int STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
     constexpr int ACC_COLS = SH::ACC_COLS, TMEM_COLS = SH::TMEM_COLS;
     constexpr uint32_t IDESC = SH::IDESC;
     extern __shared__ uint8_t dsmem[];
@@ -156,6 +162,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ptx::fence_mbar_init();
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        if (WGRAD) ptx::tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
@@ -310,6 +317,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             if (WGRAD) {
                 const bool empty = kstart[e + 1] == kstart[e];
+                // this warp's 32 rows all inside the expert's M rows: stage each 32x32
+                // block in shared memory (128-byte swizzle) and store it with TMA;
+                // otherwise (a ragged last M-tile) masked per-thread stores
+                const bool whole = rows_valid >= q * 32 + 32;
+                const uint32_t stg = smem0 + STAGES * STAGE_BYTES + q * SH::WG_STAGE_OUT;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t av[32];
@@ -321,7 +333,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int i = 0; i < 32; ++i) av[i] = 0u;
                     }
                     const int col = n * BN + c;
-                    if (rv && col < g.out_cols) {
+                    if (col >= g.out_cols) continue;
+                    if (whole) {
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();   // the previous block has left smem
+                        __syncwarp();
+                        const uint32_t rb = stg + lane * 128;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            ptx::st_shared_v4(rb + ((v ^ (lane & 7)) << 4), av[4 * v], av[4 * v + 1], av[4 * v + 2],
+                                              av[4 * v + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&tmC, stg, col, row - lane);
+                            ptx::bulk_commit_group();
+                        }
+                    } else if (rv) {
                         uint4* dst = reinterpret_cast<uint4*>(g.out_f32 + (size_t)row * g.out_cols + col);
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
@@ -382,6 +409,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
+        if (WGRAD && lane == 0) ptx::bulk_wait_group<0>();   // every output store has completed
     }
 
     ptx::tc_fence_before();

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -196,6 +197,21 @@ bool make_tmap_bf16_box(CUtensorMap* m, const void* base, unsigned long long row
 }
 
 // A_rows: rows of the A tensor (rows_max of x_perm, or T of x when gathering).
+// fp32 [rows, cols] with a 32x32 box and the 128-byte swizzle (the output
+// tiles of the weight-gradient GEMM, stored by TMA).
+bool make_tmap_f32_out(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A_rows: rows of the A tensor (default rows_max; T of x when gathering; M in
 // the weight-gradient mode, where K is the packed column count ld).
 template <int EPI, int BN, int MODE = tcg::MODE_ROWS>
@@ -209,13 +225,19 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
         return MOE_ERR_CUDA;
     if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2))
         return MOE_ERR_CUDA;
-    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, SH::SMEM_DYN)) return launch_status();
+    CUtensorMap tc;
+    memset(&tc, 0, sizeof tc);
+    if (MODE == tcg::MODE_WGRAD &&
+        !make_tmap_f32_out(&tc, args.out_f32, (unsigned long long)args.E * args.m_rows, (unsigned long long)args.out_cols))
+        return MOE_ERR_CUDA;
+    const int smem = MODE == tcg::MODE_WGRAD ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
+    if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, smem)) return launch_status();
     const long long max_tiles = MODE == tcg::MODE_WGRAD
                                     ? (long long)args.E * args.m_tiles * args.n_tiles
                                     : ((rows_max + tcg::BM - 1) / tcg::BM + args.E) * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
-    tcg::grouped_gemm_kernel<EPI, BN, MODE><<<grid, tcg::THREADS, SH::SMEM_DYN, stream>>>(ta, tb, args);
+    tcg::grouped_gemm_kernel<EPI, BN, MODE><<<grid, tcg::THREADS, smem, stream>>>(ta, tb, tc, args);
     return launch_status();
 }
 
