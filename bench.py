@@ -30,9 +30,9 @@ the same workload (its first S tokens, capacity recomputed for S tokens).
 ``--impl reference``: the CPU oracle alone on the host cores (the method has
 no other runnable implementation); rank 0 only.
 
-``--train``: a step is the forward and the backward (input, router and
-expert weight gradients of <dy, y> + aux loss (+ z-loss), transposed weight
-copies included) for a seeded upstream gradient dy; the JSON line reports
+``--train``: a step is the forward (keeping the pre-activation) and the
+backward (input, router and expert weight gradients of <dy, y> + aux loss
+(+ z-loss)) for a seeded upstream gradient dy; the JSON line reports
 the fwd+bwd rate, per-phase times and the roofline of the largest backward
 GEMM (the w1 weight gradient).
 
@@ -84,8 +84,8 @@ def plan_kwargs(args) -> dict:
                 aux_post_drop=args.aux_post_drop, train=args.train)
 
 
-BWD_KERNELS = 2 + 1 + 3 + 1 + 4 + 2 + 1 + 1 + 3   # transposes, combine bwd, 3 GEMMs, act bwd, packs, wgrads,
-                                                  # router bwd, dx, router weights (partial, sum, bias)
+BWD_KERNELS = 1 + 2 + 1 + 4 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs, act bwd, packs, wgrads,
+                                              # router bwd, dx, router weights (partial, sum, bias)
 
 
 def variant_dict(args) -> dict:
@@ -532,8 +532,7 @@ def train_arm(args, cfg):
                        **plan_kwargs(args))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    phases = ["forward", "transpose_weights", "combine_bwd", "data_grad_gemms", "pack", "wgrad_dw2", "wgrad_dw1",
-              "router_and_dx"]
+    phases = ["forward", "combine_bwd", "data_grad_gemms", "pack", "wgrad_dw2", "wgrad_dw1", "router_and_dx"]
 
     def step(evs=None):
         def mark(name):
@@ -605,7 +604,7 @@ def train_arm(args, cfg):
     dw1_flops = 2.0 * A * cfg.N1 * cfg.d
     dw1_ms = statistics.mean(part["wgrad_dw1"])
     achieved = dw1_flops / (dw1_ms * 1e-3) / 1e12
-    gemm_flops = 2.0 * A * cfg.d * cfg.N1 * 3 + 2.0 * A * cfg.F * cfg.d * 3   # fwd 2 + bwd 4 GEMMs + z recompute
+    gemm_flops = 2.0 * A * cfg.d * cfg.N1 * 3 + 2.0 * A * cfg.F * cfg.d * 3   # forward 2 + backward 4 GEMMs
     line = {
         "metric": "MoE-layer fwd+bwd tokens/s on 1 B300", "value": world * cfg.T / (ms_step / 1000.0),
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

@@ -24,9 +24,9 @@
  * item 3 returns the gradients by the reverse exchange; the pages give no
  * formula, so each call computes a derivative of the forward):
  *   moe_combine_bwd, moe_act_bwd, moe_route_bwd, moe_grad_x,
- *   moe_router_wgrad, moe_expert_wgrad (+ moe_pack_segments_t), with
- *   moe_expert_up reused for the data-gradient GEMMs on transposed weights
- *   (moe_transpose_experts) and for recomputing the pre-activation.
+ *   moe_router_wgrad, moe_expert_wgrad (+ moe_pack_segments_t),
+ *   moe_expert_dgrad (the data-gradient GEMMs, B operand MN-major) and
+ *   moe_expert_up_z (the forward keeping the pre-activation).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -199,6 +199,14 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
                          int E, int d, int F, moe_act act, moe_dtype dtype, const void* w1,
                          int64_t rows_max, void* h, moe_stream_t stream);
 
+/* moe_expert_up that also keeps the pre-activation for the backward:
+ *   z [rows_max, N1] bf16 = w1[e] . x_perm[r] before the activation (SwiGLU:
+ *   gate columns 0..F-1, up columns F..2F-1), rows < offsets[E] written.
+ * BF16 only (MOE_ERR_UNSUPPORTED otherwise); the 1-SM kernel always runs. */
+moe_status moe_expert_up_z(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                           moe_act act, moe_dtype dtype, const void* w1, int64_t rows_max, void* h, void* z,
+                           moe_stream_t stream);
+
 /* moe_expert_up reading its A rows straight from x: row r of the permuted
  * order is x[row_token[r]] (row_token from moe_dispatch), so the dispatch can
  * skip materialising x_perm (the tutorial's §5.3 packs tokens for contiguous
@@ -261,15 +269,25 @@ moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_
  * results where noted.  A training step runs, after the forward (with
  * moe_route_ex keeping logits):
  *   do_perm, dgate   = moe_combine_bwd(dy, ...)
- *   z                = moe_expert_up(x_perm, ..., IDENTITY, F := N1, w1)  (recompute)
- *   da               = moe_expert_up(do_perm, ..., IDENTITY, F, w2t)      (w2t = w2 transposed)
+ *   z                = kept by moe_expert_up_z in the forward, or recomputed:
+ *                      moe_expert_up(x_perm, ..., IDENTITY, F := N1, w1)
+ *   da               = moe_expert_dgrad(do_perm, ..., K = d, N = F, w2)
  *   dz               = moe_act_bwd(z, da, ...)
- *   dx_perm          = moe_expert_up(dz, ..., d := N1, F := d, IDENTITY, w1t)
+ *   dx_perm          = moe_expert_dgrad(dz, ..., K = N1, N = d, w1)
  *   dw2[e]           = moe_expert_wgrad(pack(do_perm), pack(h), M = d, N = F)
  *   dw1[e]           = moe_expert_wgrad(pack(dz), pack(x_perm), M = N1, N = d)
  *   dl               = moe_route_bwd(logits, topk_idx, dgate, counts, ...)
  *   dx               = moe_grad_x(dx_perm, slot_row, dl, w_router)
  *   dW, db           = moe_router_wgrad(dl, x)                                */
+
+/* Data-gradient GEMM on the weights as stored (no transposed copy):
+ *   out[r, n] = sum_k a[r, k] * w[e][k][n]   for kept rows r of expert e
+ * a [rows_max, K] (segments as from moe_dispatch), w [E, K, N] (N contiguous:
+ * w2 as [E, d, F] gives da from do_perm; w1 as [E, N1, d] gives dx_perm from
+ * dz), out [rows_max, N]; bf16, fp32 accumulation, one rounding.
+ * K % 64 == 0, N % 64 == 0. */
+moe_status moe_expert_dgrad(const void* a, const int32_t* offsets, const int32_t* kept, int E, int K, int N,
+                            moe_dtype dtype, const void* w, int64_t rows_max, void* out, moe_stream_t stream);
 
 /* w [E, R, C] -> wt [E, C, R] (2-byte elements; R, C multiples of 64;
  * 16-byte aligned). */

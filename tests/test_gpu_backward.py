@@ -141,3 +141,42 @@ def test_expert_wgrad_against_torch_per_expert():
         ref = at[:, col:col + n].float() @ bt[:, col:col + n].float().T
         assert torch.allclose(dw[e], ref, rtol=1e-4, atol=1e-3), e
         col += (n + 63) // 64 * 64
+
+
+@pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot"])
+def test_kept_pre_activation_equals_recompute(name):
+    """The z that the training forward keeps (moe_expert_up_z) is bit for bit
+    the identity-epilogue GEMM of w1 on x_perm, and h is unchanged by keeping it."""
+    cfg = CASES[name][0]
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], case["x"].device,
+                       cfg.alpha, cfg.renorm, train=True)
+    plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+    D = plan.disp
+    R = plan.rows_max
+    A = int(D.offsets[-1])
+    N1 = case["w1"].shape[1]
+    z2 = moe.expert_up(D.x_perm, D.offsets, D.kept, case["w1"], N1, "identity", R)
+    h2 = moe.expert_up(D.x_perm, D.offsets, D.kept, case["w1"], cfg.F, cfg.act, R)
+    moe.check()
+    assert torch.equal(plan.z[:A], z2[:A])
+    assert torch.equal(plan.h[:A], h2[:A])
+
+
+def test_expert_dgrad_mn_major_against_torch():
+    """out[r] = a[r] . w[e] with w [E, K, N] read MN-major, against torch fp32
+    per expert: ragged segments, an empty expert, N not a multiple of 256."""
+    g = torch.Generator(device="cuda").manual_seed(7)
+    E, K, N = 4, 192, 320
+    kept = torch.tensor([150, 0, 7, 300], dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    offsets[1:] = torch.cumsum(kept, 0)
+    R = int(offsets[-1])
+    a = torch.randn(R, K, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(E, K, N, device="cuda", generator=g) / 8).to(torch.bfloat16)
+    out = moe.expert_dgrad(a, offsets, kept, w, R)
+    moe.check()
+    for e in range(E):
+        o, n = int(offsets[e]), int(kept[e])
+        ref = a[o:o + n].float() @ w[e].float()
+        assert torch.allclose(out[o:o + n].float(), ref, rtol=1e-2, atol=2e-2), e

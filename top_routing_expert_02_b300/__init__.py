@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
-    "expert_up_gathered", "expert_down", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
+    "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
     "pack_segments_t", "expert_wgrad", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
@@ -59,6 +59,8 @@ _SIGS = {
     "moe_dispatch": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                             _P, _SZ, _P]),
     "moe_expert_up": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_expert_dgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_expert_up_z": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P, _P]),
     "moe_expert_up_gathered": (_I32, [_P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
     "moe_expert_down": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P]),
     "moe_expert_ffn": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P, _P, _SZ,
@@ -271,6 +273,17 @@ def expert_up(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=N
     return h
 
 
+def expert_up_z(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None, z=None, stream=None):
+    """moe_expert_up_z: h and the pre-activation z [rows, N1] (kept for the backward)."""
+    E, N1, d = w1.shape
+    h = torch.empty((max(rows_max, 1), F), dtype=x_perm.dtype, device=x_perm.device) if h is None else h
+    z = torch.empty((max(rows_max, 1), N1), dtype=x_perm.dtype, device=x_perm.device) if z is None else z
+    _ok("moe_expert_up_z", lib().moe_expert_up_z(_ptr(x_perm), _ptr(offsets), _ptr(kept), E, d, F, ACT[act],
+                                                 _dt(x_perm), _ptr(w1), rows_max, _ptr(h), _ptr(z),
+                                                 _stream(stream)))
+    return h, z
+
+
 def expert_up_gathered(x, row_token, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None,
                        stream=None):
     """moe_expert_up with the A rows read from x at row_token (no x_perm)."""
@@ -328,6 +341,15 @@ def z_loss(lse, beta: float, *, loss=None, stream=None):
 
 
 # --------------------------------------------------------------- backward ---
+
+def expert_dgrad(a, offsets, kept, w, rows_max: int, *, out=None, stream=None):
+    """out [rows, N] = a[r] . w[e] per kept row r of expert e, w [E, K, N] as stored (moe_expert_dgrad)."""
+    E, K, N = w.shape
+    out = torch.empty((max(rows_max, 1), N), dtype=a.dtype, device=a.device) if out is None else out
+    _ok("moe_expert_dgrad", lib().moe_expert_dgrad(_ptr(a), _ptr(offsets), _ptr(kept), E, K, N, _dt(a), _ptr(w),
+                                                   rows_max, _ptr(out), _stream(stream)))
+    return out
+
 
 def transpose_experts(w, *, out=None, stream=None):
     """w [E, R, C] -> [E, C, R] (moe_transpose_experts)."""
@@ -472,6 +494,8 @@ class MoEPlan:
         if self.train and (dtype != torch.bfloat16 or self.gather):
             raise ValueError("the backward runs on bf16 layers with a materialised x_perm")
         self.logits = torch.empty((max(T, 1), E), **f32) if self.train else None
+        N1 = 2 * F if act == "swiglu" else F
+        self.z = torch.empty((max(self.rows_max, 1), N1), dtype=dtype, device=dev) if self.train else None
         self._bwd = None
         self.lse = torch.empty(max(T, 1), **f32) if self.z_beta is not None else None
         self.z_loss = torch.empty(1, **f32) if self.z_beta is not None else None
@@ -508,6 +532,11 @@ class MoEPlan:
                                stream=stream)
             expert_down(self.h, D.offsets, D.kept, w2, D.row_gate, self.rows_max, y_perm=self.y_perm,
                         stream=stream)
+        elif self.train:
+            expert_up_z(D.x_perm, D.offsets, D.kept, w1, self.F, self.act, self.rows_max, h=self.h, z=self.z,
+                        stream=stream)
+            expert_down(self.h, D.offsets, D.kept, w2, D.row_gate, self.rows_max, y_perm=self.y_perm,
+                        stream=stream)
         else:
             expert_ffn(D.x_perm, D.offsets, D.kept, w1, w2, D.row_gate, self.act, self.rows_max, h=self.h,
                        y_perm=self.y_perm, stream=stream)
@@ -530,7 +559,7 @@ class MoEPlan:
             f32 = dict(dtype=torch.float32, device=dev)
             self._bwd = dict(
                 do_perm=torch.empty((R, d), **bf), dgate=torch.empty((max(T, 1), k), **f32),
-                z=torch.empty((R, N1), **bf), da=torch.empty((R, F), **bf), dz=torch.empty((R, N1), **bf),
+                da=torch.empty((R, F), **bf), dz=torch.empty((R, N1), **bf),
                 dx_perm=torch.empty((R, d), **bf), ld=ld,
                 doT=torch.empty((d, ld), **bf), hT=torch.empty((F, ld), **bf), dzT=torch.empty((N1, ld), **bf),
                 xT=torch.empty((d, ld), **bf), dw1=torch.empty((E, N1, d), **f32), dw2=torch.empty((E, d, F), **f32),
@@ -539,41 +568,26 @@ class MoEPlan:
                 ws=_empty_ws(workspace_bytes("router_wgrad", max(T, 1), d, E, k, F), dev))
         return self._bwd
 
-    def backward(self, x, w_router, w1, w2, dy, *, aux_weight: float = 1.0, z_weight: float = 1.0, w1t=None,
-                 w2t=None, stream=None, mark=None) -> dict:
+    def backward(self, x, w_router, w1, w2, dy, *, aux_weight: float = 1.0, z_weight: float = 1.0, stream=None,
+                 mark=None) -> dict:
         """Gradients of <dy, y> + aux_weight * loss + z_weight * z_loss after
-        :meth:`run` on the same inputs (``train=True``).  ``w1t`` / ``w2t``
-        are the transposed expert weights ([E, d, N1] / [E, F, d]); they are
-        made here when not given.  Returns dx, dW, db, dw1, dw2 (weight
-        gradients fp32) and the intermediates; all buffers belong to the plan.
-        ``mark(name)``, when given, is called after each phase (for timing)."""
+        :meth:`run` on the same inputs (``train=True``).  Returns dx, dW, db,
+        dw1, dw2 (weight gradients fp32) and the intermediates; all buffers
+        belong to the plan.  ``mark(name)``, when given, is called after each
+        phase (for timing)."""
         if not self.train:
             raise ValueError("construct the plan with train=True")
         mark = mark or (lambda name: None)
         B = self._bwd_buffers(x.device)
         D = self.disp
         R, F, E, d = self.rows_max, self.F, self.E, self.d
-        N1 = 2 * F if self.act == "swiglu" else F
-        if w1t is None:
-            w1t = B.setdefault("w1t", torch.empty((E, d, N1), dtype=w1.dtype, device=w1.device))
-            transpose_experts(w1, out=w1t, stream=stream)
-        if w2t is None:
-            w2t = B.setdefault("w2t", torch.empty((E, F, d), dtype=w2.dtype, device=w2.device))
-            transpose_experts(w2, out=w2t, stream=stream)
-        mark("transpose_weights")
         combine_bwd(dy, D.slot_row, D.row_gate, self.y_perm, do_perm=B["do_perm"], dgate=B["dgate"], stream=stream)
         mark("combine_bwd")
-        # data gradients: recompute z, then da, dz, dx_perm (identity epilogues on transposed weights)
-        _ok("moe_expert_up", lib().moe_expert_up(_ptr(D.x_perm), _ptr(D.offsets), _ptr(D.kept), E, d, N1,
-                                                 ACT["identity"], _dt(D.x_perm), _ptr(w1), R, _ptr(B["z"]),
-                                                 _stream(stream)))
-        _ok("moe_expert_up", lib().moe_expert_up(_ptr(B["do_perm"]), _ptr(D.offsets), _ptr(D.kept), E, d, F,
-                                                 ACT["identity"], _dt(w2t), _ptr(w2t), R, _ptr(B["da"]),
-                                                 _stream(stream)))
-        act_bwd(B["z"], B["da"], D.offsets, F, self.act, R, dz=B["dz"], stream=stream)
-        _ok("moe_expert_up", lib().moe_expert_up(_ptr(B["dz"]), _ptr(D.offsets), _ptr(D.kept), E, N1, d,
-                                                 ACT["identity"], _dt(w1t), _ptr(w1t), R, _ptr(B["dx_perm"]),
-                                                 _stream(stream)))
+        # data gradients on the weights as stored: da = do . w2[e], dz from the
+        # forward's pre-activation z, dx_perm = dz . w1[e]
+        expert_dgrad(B["do_perm"], D.offsets, D.kept, w2, R, out=B["da"], stream=stream)
+        act_bwd(self.z, B["da"], D.offsets, F, self.act, R, dz=B["dz"], stream=stream)
+        expert_dgrad(B["dz"], D.offsets, D.kept, w1, R, out=B["dx_perm"], stream=stream)
         mark("data_grad_gemms")
         # weight gradients on segment-packed transposes
         ld = B["ld"]
@@ -595,7 +609,7 @@ class MoEPlan:
         router_wgrad(B["dl"], x, dW=B["dW"], db=B["db"], ws=B["ws"], stream=stream)
         mark("router_and_dx")
         return dict(dx=B["dx"], dW=B["dW"], db=B["db"], dw1=B["dw1"], dw2=B["dw2"], dgate=B["dgate"], dl=B["dl"],
-                    do_perm=B["do_perm"], z=B["z"], da=B["da"], dz=B["dz"], dx_perm=B["dx_perm"])
+                    do_perm=B["do_perm"], z=self.z, da=B["da"], dz=B["dz"], dx_perm=B["dx_perm"])
 
 
 def moe_forward(x, w_router, b_router, w1, w2, *, k: int, cf: float, act: str, renorm: bool = True,

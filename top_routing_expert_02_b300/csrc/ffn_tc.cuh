@@ -74,6 +74,8 @@ struct Args {
     const int32_t* row_token;   // gathered A: row r of the tile is x[row_token[r]]
     const uint8_t* a_base;      // gathered A: x
     uint32_t a_row_bytes;       // gathered A: bytes of one x row (x is below 4 GB)
+    uint16_t* out_z;            // up projection, optional: the pre-activation, bf16 [rows_max, N1]
+    int z_cols;                 // columns of out_z (N1)
     float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols]
     int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
     int m_rows;                 // weight gradient: rows M of each expert's gradient
@@ -83,12 +85,16 @@ struct Args {
 // Where the A operand and the K range come from:
 //   MODE_ROWS    A = x_perm rows of the expert's segment (TMA box), K = 0..K-1
 //   MODE_GATHER  A = x rows at row_token[] (cp.async), K = 0..K-1
+//   MODE_BMN     A as MODE_ROWS; B stored MN-major, [E * K rows, N cols] (N
+//                contiguous: w2[e] as [d, F] or w1[e] as [N1, d]), loaded as
+//                four 64x64 boxes per stage -- the data-gradient GEMMs of the
+//                backward run on the weights as they are, without transposes
 //   MODE_WGRAD   weight gradients: A [M, ld] and B [N, ld] are transposed,
 //                segment-packed activations; expert e contracts over its own
 //                K columns [64 kstart[e], 64 kstart[e+1]) (kept[e] rounded up
 //                to 64, zero padded); every expert has m_tiles M-tiles; the
 //                output is fp32 [E, M, N] (zeros for an expert with no rows)
-enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2 };
+enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2, MODE_BMN = 3 };
 
 __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tiles, int tile, int& e, int& m,
                                             int& n)
@@ -134,12 +140,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const Args g)
 {
-    constexpr bool GATHER = MODE == MODE_GATHER, WGRAD = MODE == MODE_WGRAD;
+    constexpr bool GATHER = MODE == MODE_GATHER, WGRAD = MODE == MODE_WGRAD, BMN = MODE == MODE_BMN;
+    static_assert(!BMN || BN == 256, "MN-major B is staged as four 64-column boxes");
     using SH = Shape<BN>;
     constexpr int STAGES = WGRAD ? SH::WG_STAGES : SH::STAGES;
     constexpr int STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
     constexpr int ACC_COLS = SH::ACC_COLS, TMEM_COLS = SH::TMEM_COLS;
-    constexpr uint32_t IDESC = SH::IDESC;
+    constexpr uint32_t IDESC = BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
@@ -215,8 +222,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ptx::mbar_arrive_expect_tx(fb, GATHER ? 2 * BH_BYTES : STAGE_BYTES);
                         const int kx = (kb0 + kb) * BK;
                         if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kx, rowA);
-                        ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, rowB0);
-                        ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kx, rowB1);
+                        if (BMN) {
+                            // B rows e*K + kx.. (K), columns n*BN + 64j.. (N): four 64x64 boxes
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                ptx::tma_load_2d(sa + A_BYTES + j * (BK * 128), &tmB, fb, n * BN + 64 * j,
+                                                 e * g.K + kx);
+                        } else {
+                            ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, rowB0);
+                            ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kx, rowB1);
+                        }
                     }
                     if (GATHER) {
                         const uint8_t* src = g.a_base + (size_t)kb * (BK * 2);
@@ -277,9 +292,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (GATHER) ptx::fence_proxy_async_smem();   // the A tile came through the generic proxy
                     const uint32_t sa = smem0 + stage * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32),
-                                      ptx::sdesc_kmajor_sw128(sb + kk * 32), IDESC, (kb | kk) != 0);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // K-major B: 16 K columns = 32 bytes on; MN-major B: 16 K rows = 2048 bytes on
+                        const uint64_t bdesc = BMN ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, BK * 128)
+                                                   : ptx::sdesc_kmajor_sw128(sb + kk * 32);
+                        ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), bdesc, IDESC, (kb | kk) != 0);
+                    }
                     ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -363,6 +381,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     ptx::tmem_ld32(tb + BN / 2 + c, uv);
                     ptx::tmem_ld_wait();
                     const int col = n * (BN / 2) + c;
+                    if (rv && col < g.out_cols && g.out_z) {
+                        // keep the pre-activation (gate | up) for the backward
+                        uint32_t zg[16], zu[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            zg[i] = pack_bf16x2(f32(gv[2 * i]), f32(gv[2 * i + 1]));
+                            zu[i] = pack_bf16x2(f32(uv[2 * i]), f32(uv[2 * i + 1]));
+                        }
+                        uint4* dg = reinterpret_cast<uint4*>(g.out_z + (size_t)row * g.z_cols + col);
+                        uint4* du = reinterpret_cast<uint4*>(g.out_z + (size_t)row * g.z_cols + g.out_cols + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            dg[v] = make_uint4(zg[4 * v], zg[4 * v + 1], zg[4 * v + 2], zg[4 * v + 3]);
+                            du[v] = make_uint4(zu[4 * v], zu[4 * v + 1], zu[4 * v + 2], zu[4 * v + 3]);
+                        }
+                    }
                     if (rv && col < g.out_cols) {
                         uint32_t pk[16];
 #pragma unroll
@@ -383,6 +417,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     ptx::tmem_ld32(tb + c, av);
                     ptx::tmem_ld_wait();
                     const int col = n * BN + c;
+                    if (EPI != EPI_GATE && rv && col < g.out_cols && g.out_z) {
+                        uint32_t zk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) zk[i] = pack_bf16x2(f32(av[2 * i]), f32(av[2 * i + 1]));
+                        uint4* dz = reinterpret_cast<uint4*>(g.out_z + (size_t)row * g.z_cols + col);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dz[v] = make_uint4(zk[4 * v], zk[4 * v + 1], zk[4 * v + 2], zk[4 * v + 3]);
+                    }
                     if (rv && col < g.out_cols) {
                         uint32_t pk[16];
 #pragma unroll

@@ -223,8 +223,12 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
     if (!make_tmap_bf16_box(&ta, A, (unsigned long long)(A_rows >= 0 ? A_rows : rows_max), (unsigned long long)K,
                             MODE == tcg::MODE_GATHER ? 1 : 128))
         return MOE_ERR_CUDA;
-    if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2))
+    if (MODE == tcg::MODE_BMN) {   // B [E*K rows, N cols], N contiguous: 64x64 boxes
+        if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)args.out_cols, 64))
+            return MOE_ERR_CUDA;
+    } else if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2)) {
         return MOE_ERR_CUDA;
+    }
     CUtensorMap tc;
     memset(&tc, 0, sizeof tc);
     if (MODE == tcg::MODE_WGRAD &&
@@ -576,11 +580,10 @@ static moe_status ffn_common_checks(const int32_t* offsets, const int32_t* kept,
     return MOE_OK;
 }
 
-moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
-                         moe_act act, moe_dtype dtype, const void* w1, int64_t rows_max, void* h,
-                         moe_stream_t stream_)
+static moe_status expert_up_impl(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d,
+                                 int F, moe_act act, moe_dtype dtype, const void* w1, int64_t rows_max, void* h,
+                                 void* z, cudaStream_t stream)
 {
-    cudaStream_t stream = (cudaStream_t)stream_;
     moe_status st = ffn_common_checks(offsets, kept, E, d, F, dtype, rows_max);
     if (st != MOE_OK) return st;
     if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
@@ -597,7 +600,7 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
         default: return launch_simt<simt::ACT_IDENT>(A, offsets, kept, E, d, F, F, W, nullptr, out, rows_max, stream);
         }
     }
-    if (use_pair_kernel()) {
+    if (use_pair_kernel() && !z) {
         tc2::Args b{};
         b.offsets = offsets;
         b.kept = kept;
@@ -624,11 +627,29 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
     a.out_cols = F;
     a.out = (uint16_t*)h;
     a.row_gate = nullptr;
+    a.out_z = (uint16_t*)z;
+    a.z_cols = N1;
     a.wait_limit = g_wait_limit.load();
     if (act == MOE_ACT_SWIGLU)
         return launch_tc<tcg::EPI_SWIGLU>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
     if (act == MOE_ACT_GELU) return launch_tc<tcg::EPI_GELU>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
     return launch_tc<tcg::EPI_IDENT>(x_perm, rows_max, d, w1, (long long)E * N1, a, F, stream);
+}
+
+moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                         moe_act act, moe_dtype dtype, const void* w1, int64_t rows_max, void* h, moe_stream_t stream)
+{
+    return expert_up_impl(x_perm, offsets, kept, E, d, F, act, dtype, w1, rows_max, h, nullptr,
+                          (cudaStream_t)stream);
+}
+
+moe_status moe_expert_up_z(const void* x_perm, const int32_t* offsets, const int32_t* kept, int E, int d, int F,
+                           moe_act act, moe_dtype dtype, const void* w1, int64_t rows_max, void* h, void* z,
+                           moe_stream_t stream)
+{
+    if (dtype != MOE_BF16) return dtype_ok(dtype) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    if (rows_max > 0 && !z) return MOE_ERR_INVALID_ARG;
+    return expert_up_impl(x_perm, offsets, kept, E, d, F, act, dtype, w1, rows_max, h, z, (cudaStream_t)stream);
 }
 
 moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_token, const int32_t* offsets,
@@ -882,6 +903,29 @@ int64_t moe_wgrad_cols(int64_t rows_max, int E)
 {
     if (rows_max < 0 || E < 1) return -1;
     return (rows_max + 64LL * E + 63) / 64 * 64;
+}
+
+moe_status moe_expert_dgrad(const void* a, const int32_t* offsets, const int32_t* kept, int E, int K, int N,
+                            moe_dtype dtype, const void* w, int64_t rows_max, void* out, moe_stream_t stream)
+{
+    moe_status st = ffn_common_checks(offsets, kept, E, K, N, dtype, rows_max);
+    if (st != MOE_OK) return st;
+    if (!w || (rows_max > 0 && (!a || !out))) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (rows_max == 0) return MOE_OK;
+    tcg::Args g{};
+    g.offsets = offsets;
+    g.kept = kept;
+    g.E = E;
+    g.K = K;
+    g.n_step = 256;
+    g.half_off = 128;
+    g.n_tiles = (N + 255) / 256;
+    g.out_cols = N;
+    g.out = (uint16_t*)out;
+    g.wait_limit = g_wait_limit.load();
+    return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_BMN>(a, rows_max, K, w, (long long)E * K, g,
+                                                             (cudaStream_t)stream);
 }
 
 moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const int32_t* kept, int E, int C,

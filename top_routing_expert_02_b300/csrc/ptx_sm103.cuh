@@ -257,12 +257,29 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+// Shared-memory descriptor of an MN-major operand, 128-byte swizzle: each K
+// row holds 64 consecutive MN elements (128 B), 8 K rows form one 1024-byte
+// swizzle atom; `mn_block_bytes` is the distance between the 64-wide MN
+// blocks (leading byte offset), 1024 B between 8-row K groups (stride).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);               // bits  0-13 start address >> 4
+    d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;  // bits 16-29 leading byte offset
+    d |= (uint64_t)(1024u >> 4) << 32;                      // bits 32-45 stride byte offset
+    d |= (uint64_t)1 << 46;                                 // bits 46-48 fixed 0b001
+    d |= (uint64_t)2 << 61;                                 // bits 61-63 swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (both K-major unless
+// b_mn_major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false)
 {
     return (1u << 4)                        // D format f32
            | (1u << 7)                      // A format bf16
            | (1u << 10)                     // B format bf16
+           | ((b_mn_major ? 1u : 0u) << 16) // B major-ness: 1 = MN-major
            | ((uint32_t)(N >> 3) << 17)     // N / 8
            | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
