@@ -80,8 +80,11 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
 
 
 def plan_kwargs(args) -> dict:
-    return dict(gather=args.gather, n_group=args.n_group, topk_group=args.topk_group, z_beta=args.z_beta,
-                aux_post_drop=args.aux_post_drop, train=args.train)
+    kw = dict(gather=args.gather, n_group=args.n_group, topk_group=args.topk_group, z_beta=args.z_beta,
+              aux_post_drop=args.aux_post_drop, train=args.train)
+    if args.train:
+        kw["grad_dtype"] = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
+    return kw
 
 
 BWD_KERNELS = 1 + 2 + 1 + 4 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs, act bwd, packs, wgrads,
@@ -89,7 +92,8 @@ BWD_KERNELS = 1 + 2 + 1 + 4 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEM
 
 
 def variant_dict(args) -> dict:
-    return {"train": args.train, "n_group": args.n_group, "topk_group": args.topk_group, "z_beta": args.z_beta,
+    return {"train": args.train, "weight_grad_dtype": args.grad_dtype if args.train else None,
+            "n_group": args.n_group, "topk_group": args.topk_group, "z_beta": args.z_beta,
             "aux_f": "kept slots (post-drop)" if args.aux_post_drop else "every choice (pre-drop)",
             "up_projection": "gathers x rows (no x_perm)" if args.gather else "reads x_perm"}
 
@@ -672,6 +676,7 @@ def main():
     ap.add_argument("--aux-post-drop", action="store_true", help="aux loss f_i from kept slots")
     ap.add_argument("--gather", action="store_true", help="up-projection gathers x rows (bf16 only)")
     ap.add_argument("--train", action="store_true", help="time forward + backward")
+    ap.add_argument("--grad-dtype", default="f32", choices=["f32", "bf16"], help="expert weight gradients (--train)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     args.steps = max(args.steps, 1)

@@ -325,12 +325,13 @@ moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const in
                                int64_t rows_max, int64_t ld, moe_dtype dtype, void* dst, moe_stream_t stream);
 
 /* Per-expert weight gradient on the tensor cores:
- *   dw[e] = at[:, seg_e] . bt[:, seg_e]^T      fp32 [E, M, N]
- * at [M, ld] and bt [N, ld] come from moe_pack_segments_t (seg_e = expert e's
- * packed, zero-padded columns); an expert with no rows gets zeros.
- * M % 64 == 0, N % 64 == 0, ld % 64 == 0. */
+ *   dw[e] = at[:, seg_e] . bt[:, seg_e]^T      [E, M, N], fp32 accumulation
+ * at [M, ld] and bt [N, ld] (dtype bf16) come from moe_pack_segments_t
+ * (seg_e = expert e's packed, zero-padded columns); an expert with no rows
+ * gets zeros.  dw_dtype: MOE_F32, or MOE_BF16 (the weights' own type, one
+ * rounding).  M % 64 == 0, N % 64 == 0, ld % 64 == 0. */
 moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept, int E, int M, int N, int64_t ld,
-                            moe_dtype dtype, float* dw, moe_stream_t stream);
+                            moe_dtype dtype, void* dw, moe_dtype dw_dtype, moe_stream_t stream);
 
 /* Router backward to the logits, per token (logits [T, E] from moe_route_ex,
  * topk_idx and dgate [T, k], counts [E] = f_e * T: counts for the pre-drop

@@ -154,7 +154,8 @@ def test_backward_argument_errors():
     assert L.moe_act_bwd(FAKE, FAKE, FAKE, 8, 96, 1, 1, 10, FAKE, None) == 2       # F % 64
     assert L.moe_act_bwd(FAKE, FAKE, FAKE, 8, 128, 7, 1, 10, FAKE, None) == 1      # bad activation
     assert L.moe_pack_segments_t(FAKE, FAKE, FAKE, 8, 128, 5120, 5000, 1, FAKE, None) == 1   # ld too small
-    assert L.moe_expert_wgrad(FAKE, FAKE, FAKE, 8, 100, 128, 5632, 1, FAKE, None) == 2      # M % 64
+    assert L.moe_expert_wgrad(FAKE, FAKE, FAKE, 8, 100, 128, 5632, 1, FAKE, 0, None) == 2   # M % 64
+    assert L.moe_expert_wgrad(FAKE, FAKE, FAKE, 8, 128, 128, 5632, 1, FAKE, 5, None) == 1   # bad output type
     assert L.moe_route_bwd(FAKE, FAKE, FAKE, None, 16, 8, 2, 1, f(0.1), f(0.0), FAKE, None) == 1
     assert L.moe_route_bwd(FAKE, FAKE, FAKE, FAKE, 16, 8, 9, 1, f(0.1), f(0.0), FAKE, None) == 1
     assert L.moe_grad_x(FAKE, FAKE, FAKE, None, 16, 2, 8, 128, 1, FAKE, None) == 1

@@ -49,10 +49,11 @@ def _dy(cfg):
     return torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16)
 
 
-def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0):
+def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0, grad_dtype=torch.float32):
     case = make_case(cfg)
     plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], case["x"].device,
-                       cfg.alpha, cfg.renorm, z_beta=z_beta if z_beta else None, aux_post_drop=post, train=True)
+                       cfg.alpha, cfg.renorm, z_beta=z_beta if z_beta else None, aux_post_drop=post, train=True,
+                       grad_dtype=grad_dtype)
     moe.set_wait_limit(400_000_000)
     try:
         plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
@@ -68,10 +69,12 @@ def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0):
     return plan, g, ref, case
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_backward_against_oracle(name):
+@pytest.mark.parametrize("name,grad_dtype", [(n, torch.float32) for n in CASES] +
+                         [("swiglu_e8", torch.bfloat16), ("swiglu_e64_zipf", torch.bfloat16)])
+def test_backward_against_oracle(name, grad_dtype):
     cfg, z_beta, post = CASES[name]
-    plan, g, ref, _ = _run(cfg, z_beta, post)
+    plan, g, ref, _ = _run(cfg, z_beta, post, grad_dtype=grad_dtype)
+    assert g["dw1"].dtype == grad_dtype
     errs = {}
     for key in ("dx", "dW", "db", "dw1", "dw2", "dgate", "dl"):
         got = g[key].float().cpu().numpy().astype(np.float64)
@@ -134,12 +137,14 @@ def test_expert_wgrad_against_torch_per_expert():
         bt[:, col:col + n] = torch.randn(N, n, device="cuda", generator=g).to(torch.bfloat16)
         col += (n + 63) // 64 * 64
     dw = moe.expert_wgrad(at, bt, kept)
+    dwb = moe.expert_wgrad(at, bt, kept, dtype=torch.bfloat16)
     moe.check()
     col = 0
     for e in range(E):
         n = int(kept[e])
         ref = at[:, col:col + n].float() @ bt[:, col:col + n].float().T
         assert torch.allclose(dw[e], ref, rtol=1e-4, atol=1e-3), e
+        assert torch.equal(dwb[e], dw[e].to(torch.bfloat16)), e          # one rounding of the same sums
         col += (n + 63) // 64 * 64
 
 

@@ -76,7 +76,7 @@ _SIGS = {
     "moe_act_bwd": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I64, _P, _P]),
     "moe_wgrad_cols": (_I64, [_I64, _I32]),
     "moe_pack_segments_t": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I64, _I32, _P, _P]),
-    "moe_expert_wgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I64, _I32, _P, _P]),
+    "moe_expert_wgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I64, _I32, _P, _I32, _P]),
     "moe_route_bwd": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _F, _F, _P, _P]),
     "moe_grad_x": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_router_wgrad": (_I32, [_P, _P, _I32, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
@@ -393,14 +393,14 @@ def pack_segments_t(src, offsets, kept, rows_max: int, ld: int, *, out=None, str
     return out
 
 
-def expert_wgrad(at, bt, kept, *, dw=None, stream=None):
-    """dw [E, M, N] f32 = per-expert at[:, seg] bt[:, seg]^T (moe_expert_wgrad)."""
+def expert_wgrad(at, bt, kept, *, dw=None, dtype=torch.float32, stream=None):
+    """dw [E, M, N] (fp32 or bf16) = per-expert at[:, seg] bt[:, seg]^T (moe_expert_wgrad)."""
     M, ld = at.shape
     N = bt.shape[0]
     E = kept.shape[0]
-    dw = torch.empty((E, M, N), dtype=torch.float32, device=at.device) if dw is None else dw
+    dw = torch.empty((E, M, N), dtype=dtype, device=at.device) if dw is None else dw
     _ok("moe_expert_wgrad", lib().moe_expert_wgrad(_ptr(at), _ptr(bt), _ptr(kept), E, M, N, ld, _dt(at), _ptr(dw),
-                                                   _stream(stream)))
+                                                   _dt(dw), _stream(stream)))
     return dw
 
 
@@ -458,14 +458,15 @@ class MoEPlan:
     log-sum-exp in ``lse``; None skips it) and ``aux_post_drop`` (f_i from
     the kept slots instead of every choice).
 
-    ``train=True`` keeps the router logits so that :meth:`backward` can run
-    after :meth:`run` (bf16 layers, x_perm path).
+    ``train=True`` keeps the router logits and the pre-activation so that
+    :meth:`backward` can run after :meth:`run` (bf16 layers, x_perm path);
+    the expert weight gradients come out in ``grad_dtype`` (fp32 or bf16).
     """
 
     def __init__(self, T: int, d: int, E: int, k: int, F: int, act: str, dtype: torch.dtype, cap: int,
                  device="cuda", alpha: float = 0.01, renorm: bool = True, gather: bool = False, *,
                  n_group: int = 1, topk_group: int = 1, z_beta: Optional[float] = None,
-                 aux_post_drop: bool = False, train: bool = False):
+                 aux_post_drop: bool = False, train: bool = False, grad_dtype: torch.dtype = torch.float32):
         self.T, self.d, self.E, self.k, self.F, self.act = T, d, E, k, F, act
         self.dtype, self.cap, self.alpha, self.renorm = dtype, int(cap), float(alpha), bool(renorm)
         self.n_group, self.topk_group = int(n_group), int(topk_group)
@@ -491,6 +492,7 @@ class MoEPlan:
         self.y = torch.empty((T, d), dtype=dtype, device=dev)
         self.loss = torch.empty(1, **f32)
         self.train = bool(train)
+        self.grad_dtype = grad_dtype
         if self.train and (dtype != torch.bfloat16 or self.gather):
             raise ValueError("the backward runs on bf16 layers with a materialised x_perm")
         self.logits = torch.empty((max(T, 1), E), **f32) if self.train else None
@@ -562,7 +564,9 @@ class MoEPlan:
                 da=torch.empty((R, F), **bf), dz=torch.empty((R, N1), **bf),
                 dx_perm=torch.empty((R, d), **bf), ld=ld,
                 doT=torch.empty((d, ld), **bf), hT=torch.empty((F, ld), **bf), dzT=torch.empty((N1, ld), **bf),
-                xT=torch.empty((d, ld), **bf), dw1=torch.empty((E, N1, d), **f32), dw2=torch.empty((E, d, F), **f32),
+                xT=torch.empty((d, ld), **bf),
+                dw1=torch.empty((E, N1, d), dtype=self.grad_dtype, device=dev),
+                dw2=torch.empty((E, d, F), dtype=self.grad_dtype, device=dev),
                 dl=torch.empty((max(T, 1), E), **f32), dx=torch.empty((max(T, 1), d), **bf),
                 dW=torch.empty((E, d), **f32), db=torch.empty(E, **f32),
                 ws=_empty_ws(workspace_bytes("router_wgrad", max(T, 1), d, E, k, F), dev))

@@ -76,7 +76,7 @@ struct Args {
     uint32_t a_row_bytes;       // gathered A: bytes of one x row (x is below 4 GB)
     uint16_t* out_z;            // up projection, optional: the pre-activation, bf16 [rows_max, N1]
     int z_cols;                 // columns of out_z (N1)
-    float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols]
+    float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols], or nullptr: bf16 into out
     int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
     int m_rows;                 // weight gradient: rows M of each expert's gradient
     unsigned long long wait_limit;
@@ -93,7 +93,8 @@ struct Args {
 //                segment-packed activations; expert e contracts over its own
 //                K columns [64 kstart[e], 64 kstart[e+1]) (kept[e] rounded up
 //                to 64, zero padded); every expert has m_tiles M-tiles; the
-//                output is fp32 [E, M, N] (zeros for an expert with no rows)
+//                output is fp32 or bf16 [E, M, N] (zeros for an expert with
+//                no rows)
 enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2, MODE_BMN = 3 };
 
 __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tiles, int tile, int& e, int& m,
@@ -335,31 +336,45 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             if (WGRAD) {
                 const bool empty = kstart[e + 1] == kstart[e];
-                // this warp's 32 rows all inside the expert's M rows: stage each 32x32
-                // block in shared memory (128-byte swizzle) and store it with TMA;
-                // otherwise (a ragged last M-tile) masked per-thread stores
+                // this warp's 32 rows all inside the expert's M rows: stage each block of
+                // 32 rows x 128 bytes in shared memory (128-byte swizzle) and store it with
+                // TMA; otherwise (a ragged last M-tile) masked per-thread stores
                 const bool whole = rows_valid >= q * 32 + 32;
+                const bool f32_out = g.out_f32 != nullptr;
                 const uint32_t stg = smem0 + STAGES * STAGE_BYTES + q * SH::WG_STAGE_OUT;
+                const int step = f32_out ? 32 : 64;   // output columns per 128-byte row block
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t av[32];
+                for (int c = 0; c < BN; c += step) {
+                    uint32_t av[32], bv[32];
                     if (!empty) {
                         ptx::tmem_ld32(tb + c, av);
+                        if (!f32_out) ptx::tmem_ld32(tb + c + 32, bv);
                         ptx::tmem_ld_wait();
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) av[i] = 0u;
+                        for (int i = 0; i < 32; ++i) av[i] = bv[i] = 0u;
                     }
                     const int col = n * BN + c;
                     if (col >= g.out_cols) continue;
+                    uint32_t w[32];   // this thread's 128 output bytes
+                    if (f32_out) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = av[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            w[i] = pack_bf16x2(f32(av[2 * i]), f32(av[2 * i + 1]));
+                            w[16 + i] = pack_bf16x2(f32(bv[2 * i]), f32(bv[2 * i + 1]));
+                        }
+                    }
                     if (whole) {
                         if (lane == 0) ptx::bulk_wait_group_read<0>();   // the previous block has left smem
                         __syncwarp();
                         const uint32_t rb = stg + lane * 128;
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            ptx::st_shared_v4(rb + ((v ^ (lane & 7)) << 4), av[4 * v], av[4 * v + 1], av[4 * v + 2],
-                                              av[4 * v + 3]);
+                            ptx::st_shared_v4(rb + ((v ^ (lane & 7)) << 4), w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                                              w[4 * v + 3]);
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
@@ -367,10 +382,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             ptx::bulk_commit_group();
                         }
                     } else if (rv) {
-                        uint4* dst = reinterpret_cast<uint4*>(g.out_f32 + (size_t)row * g.out_cols + col);
+                        uint4* dst = f32_out ? reinterpret_cast<uint4*>(g.out_f32 + (size_t)row * g.out_cols + col)
+                                             : reinterpret_cast<uint4*>(g.out + (size_t)row * g.out_cols + col);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[v] = make_uint4(av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3]);
+                        for (int v = 0; v < 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                     }
                 }
             } else if (EPI == EPI_SWIGLU) {

@@ -231,9 +231,12 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
     }
     CUtensorMap tc;
     memset(&tc, 0, sizeof tc);
-    if (MODE == tcg::MODE_WGRAD &&
-        !make_tmap_f32_out(&tc, args.out_f32, (unsigned long long)args.E * args.m_rows, (unsigned long long)args.out_cols))
-        return MOE_ERR_CUDA;
+    if (MODE == tcg::MODE_WGRAD) {
+        const unsigned long long rows = (unsigned long long)args.E * args.m_rows, cols = args.out_cols;
+        if (args.out_f32 ? !make_tmap_f32_out(&tc, args.out_f32, rows, cols)
+                         : !make_tmap_bf16_box(&tc, args.out, rows, cols, 32))
+            return MOE_ERR_CUDA;
+    }
     const int smem = MODE == tcg::MODE_WGRAD ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
     if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, smem)) return launch_status();
     const long long max_tiles = MODE == tcg::MODE_WGRAD
@@ -943,9 +946,10 @@ moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const in
 }
 
 moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept, int E, int M, int N, int64_t ld,
-                            moe_dtype dtype, float* dw, moe_stream_t stream)
+                            moe_dtype dtype, void* dw, moe_dtype dw_dtype, moe_stream_t stream)
 {
-    if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || ld <= 0 || !kept || !at || !bt || !dw || !dtype_ok(dtype))
+    if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || ld <= 0 || !kept || !at || !bt || !dw || !dtype_ok(dtype) ||
+        !dtype_ok(dw_dtype))
         return MOE_ERR_INVALID_ARG;
     if (dtype != MOE_BF16 || M % 64 || N % 64 || ld % 64 || ld >= INT_MAX) return MOE_ERR_UNSUPPORTED;
     tcg::Args a{};
@@ -958,7 +962,8 @@ moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept,
     a.half_off = 128;
     a.n_tiles = (N + 255) / 256;
     a.out_cols = N;
-    a.out_f32 = dw;
+    a.out_f32 = dw_dtype == MOE_F32 ? (float*)dw : nullptr;
+    a.out = dw_dtype == MOE_BF16 ? (uint16_t*)dw : nullptr;
     a.wait_limit = g_wait_limit.load();
     return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD>(at, 0, (int)ld, bt, N, a, (cudaStream_t)stream, M);
 }
