@@ -347,14 +347,16 @@ moe_status moe_route_bwd(const float* logits, const int32_t* topk_idx, const flo
 
 /* Input gradient: dx[t] = sum over kept j of dx_perm[slot_row[t, j]] +
  * sum_e dl[t, e] w_router[e] (fp32 sums, one rounding to dtype).
- * dx_perm [rows_max, d] and dx [T, d] in dtype; dl [T, E]; w_router [E, d]. */
+ * dx_perm [rows_max, d] and dx [T, d] in dtype; dl [T, E]; w_router [E, d];
+ * d % 64 == 0 and 16-byte aligned dx_perm, w_router, dx (else UNSUPPORTED). */
 moe_status moe_grad_x(const void* dx_perm, const int32_t* slot_row, const float* dl, const float* w_router,
                       int64_t T, int k, int E, int d, moe_dtype dtype, void* dx, moe_stream_t stream);
 
 /* Router weight gradient: dW[e, c] = sum_t dl[t, e] x[t, c] (fp32 [E, d]) and,
  * when db != NULL, db[e] = sum_t dl[t, e] (fp32 [E]); token splits summed in a
  * fixed order (bitwise reproducible).  ws >=
- * moe_workspace_bytes(MOE_CALL_ROUTER_WGRAD, T, d, E, ...) bytes; T >= 1. */
+ * moe_workspace_bytes(MOE_CALL_ROUTER_WGRAD, T, d, E, ...) bytes; T >= 1;
+ * d % 64 == 0 and x 16-byte aligned (else UNSUPPORTED). */
 moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64_t T, int E, int d, float* dW,
                             float* db, void* ws, size_t ws_bytes, moe_stream_t stream);
 

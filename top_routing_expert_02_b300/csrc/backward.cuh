@@ -286,21 +286,24 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ i
 // ------------------------------------------------------- input gradient ---
 
 // dx[t][c] = sum_e dl[t,e] W[e,c] + sum over kept j of dx_perm[slot_row[t,j]][c].
-// Block: 32 tokens x 256 columns; dl rows and slot rows staged in shared memory,
-// each W element read once per block; fp32 sums, one rounding.
-constexpr int GX_TOK = 32;
+// Block: GX_TOK tokens x 1024 columns, 4 adjacent columns per thread; dl is
+// staged transposed in shared memory (dlT[e][token], read as 16-byte
+// vectors), each W element is read once per block; fp32 sums in a fixed
+// order (router part over e, then the kept slots in j order), one rounding.
+constexpr int GX_TOK = 16;
+constexpr int GX_COLS = 1024;
 template <bool BF16>
 __global__ void __launch_bounds__(256)
 grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot_row, const float* __restrict__ dl,
               const float* __restrict__ W, int T, int k, int E, int d, void* __restrict__ dx)
 {
-    __shared__ float dls[GX_TOK][257];
+    __shared__ __align__(16) float dlT[256][GX_TOK];
     __shared__ int rows[GX_TOK][16];
     const int t0 = blockIdx.y * GX_TOK;
-    const int c = blockIdx.x * 256 + threadIdx.x;
+    const int c = blockIdx.x * GX_COLS + threadIdx.x * 4;
     for (int v = threadIdx.x; v < GX_TOK * E; v += 256) {
         const int tk = v / E, e = v - tk * E;
-        dls[tk][e] = (t0 + tk < T) ? __ldg(dl + (size_t)(t0 + tk) * E + e) : 0.f;
+        dlT[e][tk] = (t0 + tk < T) ? __ldg(dl + (size_t)(t0 + tk) * E + e) : 0.f;
     }
     for (int v = threadIdx.x; v < GX_TOK * k; v += 256) {
         const int tk = v / k, j = v - tk * k;
@@ -308,29 +311,52 @@ grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot
     }
     __syncthreads();
     if (c >= d) return;
-    float acc[GX_TOK];
+    float acc[GX_TOK][4];
 #pragma unroll
-    for (int tk = 0; tk < GX_TOK; ++tk) acc[tk] = 0.f;
+    for (int tk = 0; tk < GX_TOK; ++tk)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[tk][q] = 0.f;
     for (int e = 0; e < E; ++e) {
-        const float w = __ldg(W + (size_t)e * d + c);
+        const float4 w = __ldg(reinterpret_cast<const float4*>(W + (size_t)e * d + c));
 #pragma unroll
-        for (int tk = 0; tk < GX_TOK; ++tk) acc[tk] = fmaf(dls[tk][e], w, acc[tk]);
+        for (int t4 = 0; t4 < GX_TOK; t4 += 4) {
+            const float4 l = *reinterpret_cast<const float4*>(&dlT[e][t4]);
+            const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc[t4 + u][0] = fmaf(lv[u], w.x, acc[t4 + u][0]);
+                acc[t4 + u][1] = fmaf(lv[u], w.y, acc[t4 + u][1]);
+                acc[t4 + u][2] = fmaf(lv[u], w.z, acc[t4 + u][2]);
+                acc[t4 + u][3] = fmaf(lv[u], w.w, acc[t4 + u][3]);
+            }
+        }
     }
 #pragma unroll
     for (int tk = 0; tk < GX_TOK; ++tk) {
         if (t0 + tk >= T) continue;
-        float a = acc[tk];
+        float a[4] = {acc[tk][0], acc[tk][1], acc[tk][2], acc[tk][3]};
         for (int j = 0; j < k; ++j) {
             const int r = rows[tk][j];
             if (r < 0) continue;
-            a += BF16 ? bf16_bits_to_f32(__ldg((const uint16_t*)dx_perm + (size_t)r * d + c))
-                      : __ldg((const float*)dx_perm + (size_t)r * d + c);
+            if (BF16) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>((const uint16_t*)dx_perm + (size_t)r * d + c));
+                a[0] += __uint_as_float(u.x << 16);
+                a[1] += __uint_as_float(u.x & 0xffff0000u);
+                a[2] += __uint_as_float(u.y << 16);
+                a[3] += __uint_as_float(u.y & 0xffff0000u);
+            } else {
+                const float4 u = __ldg(reinterpret_cast<const float4*>((const float*)dx_perm + (size_t)r * d + c));
+                a[0] += u.x;
+                a[1] += u.y;
+                a[2] += u.z;
+                a[3] += u.w;
+            }
         }
         if (BF16) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(a);
-            ((__nv_bfloat16*)dx)[(size_t)(t0 + tk) * d + c] = h;
+            *reinterpret_cast<uint2*>((uint16_t*)dx + (size_t)(t0 + tk) * d + c) =
+                make_uint2(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]));
         } else {
-            ((float*)dx)[(size_t)(t0 + tk) * d + c] = a;
+            *reinterpret_cast<float4*>((float*)dx + (size_t)(t0 + tk) * d + c) = make_float4(a[0], a[1], a[2], a[3]);
         }
     }
 }
@@ -338,23 +364,27 @@ grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot
 // ------------------------------------------------------ router weights ---
 
 // partial[s][e][c] = sum over tokens t of split s of dl[t,e] x[t,c].
-// Block (x, y, s): 256 columns, 16 experts, token split s; dl staged 32
-// tokens at a time.  The splits are summed in order by router_wgrad_sum_kernel.
+// Block (x, y, s): 1024 columns (4 adjacent per thread), 16 experts, token
+// split s; dl staged 32 tokens at a time (read back as 16-byte vectors).
+// The splits are summed in order by router_wgrad_sum_kernel.
 constexpr int RW_EXP = 16;
+constexpr int RW_COLS = 1024;
 template <bool BF16>
 __global__ void __launch_bounds__(256)
 router_wgrad_kernel(const float* __restrict__ dl, const void* __restrict__ x, int T, int E, int d, int tok_per_split,
                     float* __restrict__ partial)
 {
-    __shared__ float dls[32][RW_EXP];
-    const int c = blockIdx.x * 256 + threadIdx.x;
+    __shared__ __align__(16) float dls[32][RW_EXP];
+    const int c = blockIdx.x * RW_COLS + threadIdx.x * 4;
     const int e0 = blockIdx.y * RW_EXP;
     const int s = blockIdx.z;
     const int ta = s * tok_per_split;
     const int tb = min(T, ta + tok_per_split);
-    float acc[RW_EXP];
+    float acc[RW_EXP][4];
 #pragma unroll
-    for (int i = 0; i < RW_EXP; ++i) acc[i] = 0.f;
+    for (int i = 0; i < RW_EXP; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
     for (int t0 = ta; t0 < tb; t0 += 32) {
         __syncthreads();
         for (int v = threadIdx.x; v < 32 * RW_EXP; v += 256) {
@@ -363,19 +393,51 @@ router_wgrad_kernel(const float* __restrict__ dl, const void* __restrict__ x, in
         }
         __syncthreads();
         if (c < d) {
-            const int n = min(32, tb - t0);
-            for (int tk = 0; tk < n; ++tk) {
-                const float xv = BF16 ? bf16_bits_to_f32(__ldg((const uint16_t*)x + (size_t)(t0 + tk) * d + c))
-                                      : __ldg((const float*)x + (size_t)(t0 + tk) * d + c);
+            // eight token rows of x in flight at a time (rows past the split read as 0)
+            for (int tk0 = 0; tk0 < 32; tk0 += 8) {
+                float xv[8][4];
 #pragma unroll
-                for (int i = 0; i < RW_EXP; ++i) acc[i] = fmaf(dls[tk][i], xv, acc[i]);
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + tk0 + u;
+                    if (t < tb) {
+                        if (BF16) {
+                            const uint2 w = __ldg(reinterpret_cast<const uint2*>((const uint16_t*)x + (size_t)t * d + c));
+                            xv[u][0] = __uint_as_float(w.x << 16);
+                            xv[u][1] = __uint_as_float(w.x & 0xffff0000u);
+                            xv[u][2] = __uint_as_float(w.y << 16);
+                            xv[u][3] = __uint_as_float(w.y & 0xffff0000u);
+                        } else {
+                            const float4 w = __ldg(reinterpret_cast<const float4*>((const float*)x + (size_t)t * d + c));
+                            xv[u][0] = w.x;
+                            xv[u][1] = w.y;
+                            xv[u][2] = w.z;
+                            xv[u][3] = w.w;
+                        }
+                    } else {
+                        xv[u][0] = xv[u][1] = xv[u][2] = xv[u][3] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+#pragma unroll
+                    for (int i4 = 0; i4 < RW_EXP; i4 += 4) {
+                        const float4 l = *reinterpret_cast<const float4*>(&dls[tk0 + u][i4]);
+                        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[i4 + v][q] = fmaf(lv[v], xv[u][q], acc[i4 + v][q]);
+                    }
+                }
             }
         }
     }
     if (c < d) {
 #pragma unroll
         for (int i = 0; i < RW_EXP; ++i)
-            if (e0 + i < E) partial[((size_t)s * E + e0 + i) * d + c] = acc[i];
+            if (e0 + i < E)
+                *reinterpret_cast<float4*>(partial + ((size_t)s * E + e0 + i) * d + c) =
+                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
 }
 

@@ -379,7 +379,7 @@ namespace {
 // Token splits of the router weight gradient: enough blocks for two waves.
 int router_wgrad_splits(int64_t T, int E, int d)
 {
-    const int base = ceil_div_i(d, 256) * ceil_div_i(E, bwd::RW_EXP);
+    const int base = ceil_div_i(d, bwd::RW_COLS) * ceil_div_i(E, bwd::RW_EXP);
     int S = ceil_div_i(2 * 148, base);
     if (S > 16) S = 16;
     const int maxS = ceil_div_i(T, 32);
@@ -995,9 +995,10 @@ moe_status moe_grad_x(const void* dx_perm, const int32_t* slot_row, const float*
 {
     if (T < 0 || k < 1 || k > MAX_K || E < 1 || E > MAX_E || d <= 0 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!dx_perm || !slot_row || !dl || !w_router || !dx)) return MOE_ERR_INVALID_ARG;
-    if (T / bwd::GX_TOK >= 65535) return MOE_ERR_UNSUPPORTED;
+    if (T / bwd::GX_TOK >= 65535 || d % 64) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!aligned16(dx_perm) || !aligned16(w_router) || !aligned16(dx))) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
-    const dim3 grid(ceil_div_i(d, 256), ceil_div_i(T, bwd::GX_TOK));
+    const dim3 grid(ceil_div_i(d, bwd::GX_COLS), ceil_div_i(T, bwd::GX_TOK));
     cudaStream_t st = (cudaStream_t)stream;
     if (dtype == MOE_BF16)
         bwd::grad_x_kernel<true><<<grid, 256, 0, st>>>(dx_perm, slot_row, dl, w_router, (int)T, k, E, d, dx);
@@ -1010,12 +1011,13 @@ moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64
                             float* db, void* ws, size_t ws_bytes, moe_stream_t stream)
 {
     if (T < 1 || E < 1 || E > MAX_E || d <= 0 || !dl || !x || !dW || !dtype_ok(xdt)) return MOE_ERR_INVALID_ARG;
+    if (d % 64 || !aligned16(x)) return MOE_ERR_UNSUPPORTED;
     const int S = router_wgrad_splits(T, E, d);
     const size_t need = (size_t)S * E * d * sizeof(float);
     if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     const int per = ceil_div_i(ceil_div_i(T, S), 32) * 32;
-    const dim3 grid(ceil_div_i(d, 256), ceil_div_i(E, bwd::RW_EXP), S);
+    const dim3 grid(ceil_div_i(d, bwd::RW_COLS), ceil_div_i(E, bwd::RW_EXP), S);
     float* part = (float*)ws;
     if (xdt == MOE_BF16)
         bwd::router_wgrad_kernel<true><<<grid, 256, 0, st>>>(dl, x, (int)T, E, d, per, part);
