@@ -42,6 +42,7 @@ from __future__ import annotations
 import math
 
 import numpy as np
+import scipy.special
 
 from . import _host, dispatch, logsumexp, route, route_grouped, router_logits
 
@@ -81,16 +82,18 @@ def act_backward(z: np.ndarray, da: np.ndarray, act: str) -> np.ndarray:
     return da.copy()
 
 
-_erf = np.vectorize(math.erf, otypes=[np.float64])
+_erf = scipy.special.erf   # float64 erf (library routine)
 
 
 def backward(x, W, b, w1, w2, dy, *, k: int, cap: int, act: str, renorm: bool = True, alpha: float = 0.01,
              aux_weight: float = 1.0, z_beta: float = 0.0, z_weight: float = 1.0, aux_post_drop: bool = False,
-             n_group: int = 1, topk_group: int = 1) -> dict:
+             n_group: int = 1, topk_group: int = 1, wgrad_dtype=np.float64) -> dict:
     """Gradients of L (module docstring) with respect to x, the router W and b,
-    w1 and w2, plus the intermediates dgate [T,k] and dl [T,E]."""
+    w1 and w2, plus the intermediates dgate [T,k] and dl [T,E].  Everything is
+    computed in float64; ``wgrad_dtype`` only sets how dw1 and dw2 are stored
+    (float32 keeps full-size layers within host memory).  The expert weights
+    are widened one expert at a time."""
     X, Wr, DY = _f64(x), _f64(W), _f64(dy)
-    W1, W2 = _f64(w1), _f64(w2)
     L = router_logits(x, W, b)
     T, E = L.shape
     if n_group > 1:
@@ -103,24 +106,25 @@ def backward(x, W, b, w1, w2, dy, *, k: int, cap: int, act: str, renorm: bool = 
     # expert part, one expert at a time over its kept slots
     dgate = np.zeros((T, k))
     dX = np.zeros((T, d))
-    dW1 = np.zeros_like(W1)
-    dW2 = np.zeros_like(W2)
+    dW1 = np.zeros(tuple(w1.shape), dtype=wgrad_dtype)
+    dW2 = np.zeros(tuple(w2.shape), dtype=wgrad_dtype)
     for e in range(E):
         ts, js = np.nonzero((idx == e) & (pos >= 0))
         if ts.size == 0:
             continue
+        W1e, W2e = _f64(w1[e]), _f64(w2[e])
         Xe = X[ts]
-        Z = Xe @ W1[e].T
+        Z = Xe @ W1e.T
         A = act_forward(Z, act)
-        O = A @ W2[e].T
+        O = A @ W2e.T
         g = gate[ts, js]
         dgate[ts, js] = np.sum(DY[ts] * O, axis=1)
         dO = g[:, None] * DY[ts]
         dW2[e] = dO.T @ A
-        dA = dO @ W2[e]
+        dA = dO @ W2e
         dZ = act_backward(Z, dA, act)
         dW1[e] = dZ.T @ Xe
-        np.add.at(dX, ts, dZ @ W1[e])
+        np.add.at(dX, ts, dZ @ W1e)
 
     # gates -> full softmax probabilities
     dP = np.zeros((T, E))

@@ -9,6 +9,8 @@ Bar (bf16 layers): relative Frobenius error <= 2e-2 for dx, dW, db, dw1,
 dw2, dgate and dl, the bar of the bf16 forward output.  The path rounds
 to bf16 at do, z, da, dz and dx_perm (each ~2^-9 relative), so the
 expected error is a few 1e-3."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -185,3 +187,67 @@ def test_expert_dgrad_mn_major_against_torch():
         o, n = int(offsets[e]), int(kept[e])
         ref = a[o:o + n].float() @ w[e].float()
         assert torch.allclose(out[o:o + n].float(), ref, rtol=1e-2, atol=2e-2), e
+
+
+def test_backward_capacity_zero_and_empty_batch():
+    """cap = 0: every slot dropped, so the expert weights get zero gradients
+    and dx is the router's part alone (against the oracle); T = 0: the call
+    runs and every weight gradient is zero."""
+    cfg = C("cap0", 300, 128, 8, 2, 128, "swiglu", 1.0, "bf16")
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, 0, case["x"].device, cfg.alpha,
+                       cfg.renorm, train=True)
+    plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+    dy = _dy(cfg)
+    g = plan.backward(case["x"], case["W"], case["w1"], case["w2"], dy.cuda())
+    moe.check()
+    assert not g["dw1"].any() and not g["dw2"].any()
+    ref = OB.backward(case["x_h"], case["W_h"], case["b_h"], case["w1"].cpu(), case["w2"].cpu(), dy, k=cfg.k, cap=0,
+                      act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha)
+    for key in ("dx", "dW", "db", "dl"):
+        got = g[key].float().cpu().numpy().astype(np.float64)
+        if key in ("dx", "dl"):
+            got = got[:cfg.T]
+        assert rel_fro(got, ref[key]) <= TOL, key
+
+    x0 = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    plan0 = moe.MoEPlan(0, 128, 8, 2, 128, "swiglu", torch.bfloat16, 0, "cuda", train=True)
+    plan0.run(x0, case["W"], case["b"], case["w1"], case["w2"])
+    g0 = plan0.backward(x0, case["W"], case["w1"], case["w2"], x0)
+    moe.check()
+    assert not g0["dw1"].any() and not g0["dw2"].any() and not g0["dW"].any() and not g0["db"].any()
+
+
+@pytest.mark.slow
+def test_backward_full_size_e8_swiglu():
+    """The 8-expert bench layer at full size (T=4096, d=4096, F=14336, 2.8 GB of
+    weights): every gradient against the fp64 oracle (weight gradients
+    stored in fp32 on the host side)."""
+    cfg = synth.workload("e8_swiglu")
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], case["x"].device,
+                       cfg.alpha, cfg.renorm, train=True)
+    plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+    dy = _dy(cfg)
+    g = plan.backward(case["x"], case["W"], case["w1"], case["w2"], dy.cuda())
+    moe.check()
+    ref = OB.backward(case["x_h"], case["W_h"], case["b_h"], case["w1"].cpu(), case["w2"].cpu(), dy, k=cfg.k,
+                      cap=case["cap"], act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha, wgrad_dtype=np.float32)
+    def rel_fro_chunked(a, b):
+        num = den = 0.0
+        for i in range(a.shape[0]):          # one expert (or row) at a time keeps host memory bounded
+            ai, bi = a[i].astype(np.float64), b[i].astype(np.float64)
+            num += float(np.sum((ai - bi) ** 2))
+            den += float(np.sum(bi * bi))
+        return math.sqrt(num / den) if den > 0 else math.sqrt(num)
+
+    errs = {}
+    for key in ("dx", "dW", "db", "dw1", "dw2", "dgate", "dl"):
+        got = g[key].float().cpu().numpy()
+        if key in ("dx", "dgate", "dl"):
+            got = got[:cfg.T]
+        errs[key] = rel_fro_chunked(got[None] if got.ndim == 1 else got, ref[key][None] if ref[key].ndim == 1
+                                    else ref[key])
+    print("[backward parity] e8_swiglu full size: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()))
+    for key, err in errs.items():
+        assert err <= TOL, (key, err)

@@ -124,7 +124,7 @@ BWD_MUTANTS = {
     "z-loss gradient without the factor 2": ("(2.0 * z_beta / T)", "(z_beta / T)"),
     "aux gradient without the 1/T of P_i": ("dP += aux_weight * alpha * E * f[None, :] / T",
                                             "dP += aux_weight * alpha * E * f[None, :]"),
-    "expert input gradient dropped": ("np.add.at(dX, ts, dZ @ W1[e])", "pass"),
+    "expert input gradient dropped": ("np.add.at(dX, ts, dZ @ W1e)", "pass"),
     "w2 gradient from the ungated dy": ("dW2[e] = dO.T @ A", "dW2[e] = DY[ts].T @ A"),
     "router input gradient dropped": ("dX += dL @ Wr", "pass"),
 }

@@ -610,7 +610,11 @@ class MoEPlan:
         route_bwd(self.logits, self.topk_idx, B["dgate"], counts, self.renorm, aux_weight * self.alpha * E, zc,
                   dl=B["dl"], stream=stream)
         grad_x(B["dx_perm"], D.slot_row, B["dl"], w_router, dx=B["dx"], stream=stream)
-        router_wgrad(B["dl"], x, dW=B["dW"], db=B["db"], ws=B["ws"], stream=stream)
+        if self.T > 0:
+            router_wgrad(B["dl"], x, dW=B["dW"], db=B["db"], ws=B["ws"], stream=stream)
+        else:   # no tokens: the router gets no gradient
+            B["dW"].zero_()
+            B["db"].zero_()
         mark("router_and_dx")
         return dict(dx=B["dx"], dW=B["dW"], db=B["db"], dw1=B["dw1"], dw2=B["dw2"], dgate=B["dgate"], dl=B["dl"],
                     do_perm=B["do_perm"], z=self.z, da=B["da"], dz=B["dz"], dx_perm=B["dx_perm"])
