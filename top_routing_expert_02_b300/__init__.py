@@ -407,8 +407,8 @@ def expert_wgrad(at, bt, kept, *, dw=None, dtype=torch.float32, stream=None):
 def route_bwd(logits, topk_idx, dgate, counts, renorm: bool, aux_coef: float, z_coef: float, *, dl=None,
               stream=None):
     """dl [T, E] f32, the gradient at the router logits (moe_route_bwd)."""
-    T, E = logits.shape
-    k = topk_idx.shape[1]
+    T, k = topk_idx.shape
+    E = logits.shape[1]
     dl = torch.empty((T, E), dtype=torch.float32, device=logits.device) if dl is None else dl
     _ok("moe_route_bwd", lib().moe_route_bwd(_ptr(logits), _ptr(topk_idx), _ptr(dgate), _ptr(counts), T, E, k,
                                              int(renorm), float(aux_coef), float(z_coef), _ptr(dl),
