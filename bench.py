@@ -283,9 +283,10 @@ def config_dict(cfg, args=None):
                   "host-to-device copy every step, weights (GBs) exceed L2"}
 
 
-def traffic_from_profile(kernel_src: str):
+def traffic_from_profile(kernel_src: str, workload: str):
     """DRAM bytes per launch of the up-projection GEMM from the committed ncu
-    summary, only while the kernel source is unchanged since the capture."""
+    summary, only for the workload it was captured for and only while the
+    kernel source is unchanged since the capture."""
     p = os.path.join(ROOT, "profiles", "expert_up_gemm_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -296,7 +297,7 @@ def traffic_from_profile(kernel_src: str):
         if "=" in line and not line.startswith("#"):
             k, v = line.split("=", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != sha:
+    if vals.get("kernel_source_sha256_16") != sha or vals.get("workload") != workload:
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -476,7 +477,9 @@ def our_arm(args, cfg):
     down_ms = statistics.mean(part["expert_down"])
     achieved = up_flops / (up_ms * 1e-3) / 1e12
     gemm_tflops = (up_flops + down_flops) / ((up_ms + down_ms) * 1e-3) / 1e12
-    traffic = traffic_from_profile(os.path.join(ROOT, "top_routing_expert_02_b300", "csrc", "ffn_tc.cuh"))
+    traffic = traffic_from_profile(os.path.join(ROOT, "top_routing_expert_02_b300", "csrc", "ffn_tc.cuh"), cfg.name)
+    if args.gather:
+        traffic = None   # captured on the x_perm kernel
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
