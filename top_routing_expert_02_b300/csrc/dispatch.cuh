@@ -139,28 +139,47 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
     }
 }
 
-// One warp per row, rows strided over the grid; vec16 = 16-byte vectors per row.
+// Row permutation, token-major: one warp per token reads x[t] once and writes
+// it to every kept slot row of the token (slot_row[t, j] >= 0), so a token
+// routed to k experts costs one read and k writes instead of k of each.
+// Tokens strided over the grid; vec16 = 16-byte vectors per row; four loads in
+// flight per lane.
 __global__ void __launch_bounds__(THREADS)
-gather_rows_kernel(const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets, int E,
-                   const uint4* __restrict__ x, uint4* __restrict__ x_perm, int vec16)
+scatter_tokens_kernel(const int32_t* __restrict__ slot_row, int T, int k, const uint4* __restrict__ x,
+                      uint4* __restrict__ x_perm, int vec16)
 {
     const int lane = threadIdx.x & 31;
-    const int A = __ldg(offsets + E);
     const int warps_total = gridDim.x * WARPS;
-    for (int row = blockIdx.x * WARPS + (threadIdx.x >> 5); row < A; row += warps_total) {
-        const int t = __ldg(row_token + row);
+    for (int t = blockIdx.x * WARPS + (threadIdx.x >> 5); t < T; t += warps_total) {
+        int rows[16];
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            rows[j] = j < k ? __ldg(slot_row + (size_t)t * k + j) : -1;
+            any |= rows[j] >= 0;
+        }
+        if (!any) continue;   // every slot dropped: the row is never read
         const uint4* src = x + (size_t)t * vec16;
-        uint4* dst = x_perm + (size_t)row * vec16;
         int v = lane;
         for (; v + 96 < vec16; v += 128) {
             const uint4 a0 = ldg_nc_v4(src + v), a1 = ldg_nc_v4(src + v + 32);
             const uint4 a2 = ldg_nc_v4(src + v + 64), a3 = ldg_nc_v4(src + v + 96);
-            dst[v] = a0;
-            dst[v + 32] = a1;
-            dst[v + 64] = a2;
-            dst[v + 96] = a3;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (rows[j] < 0) continue;
+                uint4* dst = x_perm + (size_t)rows[j] * vec16;
+                dst[v] = a0;
+                dst[v + 32] = a1;
+                dst[v + 64] = a2;
+                dst[v + 96] = a3;
+            }
         }
-        for (; v < vec16; v += 32) dst[v] = ldg_nc_v4(src + v);
+        for (; v < vec16; v += 32) {
+            const uint4 a0 = ldg_nc_v4(src + v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (rows[j] >= 0) x_perm[(size_t)rows[j] * vec16 + v] = a0;
+        }
     }
 }
 

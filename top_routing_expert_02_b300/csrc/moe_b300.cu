@@ -566,10 +566,10 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     moe_status st = launch_status();
     if (st != MOE_OK || rows_max == 0 || !x_perm) return st;   // x_perm NULL: the up GEMM gathers from x
     const int vec16 = d * esize(xdt) / 16;
-    long long grid = (rows_max + dispatch::WARPS - 1) / dispatch::WARPS;
+    long long grid = (T + dispatch::WARPS - 1) / dispatch::WARPS;
     if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
-    dispatch::gather_rows_kernel<<<(int)grid, dispatch::THREADS, 0, stream>>>(row_token, offsets, E, (const uint4*)x,
-                                                                              (uint4*)x_perm, vec16);
+    dispatch::scatter_tokens_kernel<<<(int)grid, dispatch::THREADS, 0, stream>>>(slot_row, (int)T, k, (const uint4*)x,
+                                                                                 (uint4*)x_perm, vec16);
     return launch_status();
 }
 
