@@ -199,6 +199,14 @@ moe_status moe_expert_up(const void* x_perm, const int32_t* offsets, const int32
                          int E, int d, int F, moe_act act, moe_dtype dtype, const void* w1,
                          int64_t rows_max, void* h, moe_stream_t stream);
 
+/* Row permutation: dst[i] = src[index[i]] for i < n (rows of d elements of
+ * dtype; rows 16-byte multiples, 16-byte aligned buffers).  The pages' §2.1
+ * token exchange regroups received rows by expert; the expert-parallel
+ * layer uses this to turn rows grouped by source rank into rows grouped by
+ * local expert and back. */
+moe_status moe_permute_rows(const void* src, const int32_t* index, int64_t n, int d, moe_dtype dtype, void* dst,
+                            moe_stream_t stream);
+
 /* moe_expert_up that also keeps the pre-activation for the backward:
  *   z [rows_max, N1] bf16 = w1[e] . x_perm[r] before the activation (SwiGLU:
  *   gate columns 0..F-1, up columns F..2F-1), rows < offsets[E] written.

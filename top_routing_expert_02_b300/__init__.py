@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
-    "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
+    "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
     "pack_segments_t", "expert_wgrad", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
@@ -59,6 +59,7 @@ _SIGS = {
     "moe_dispatch": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                             _P, _SZ, _P]),
     "moe_expert_up": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_permute_rows": (_I32, [_P, _P, _I64, _I32, _I32, _P, _P]),
     "moe_expert_dgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
     "moe_expert_up_z": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P, _P]),
     "moe_expert_up_gathered": (_I32, [_P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
@@ -341,6 +342,16 @@ def z_loss(lse, beta: float, *, loss=None, stream=None):
 
 
 # --------------------------------------------------------------- backward ---
+
+def permute_rows(src, index, *, out=None, stream=None):
+    """out[i] = src[index[i]] (moe_permute_rows); index int32 on the device."""
+    n = index.shape[0]
+    d = src.shape[1]
+    out = torch.empty((n, d), dtype=src.dtype, device=src.device) if out is None else out
+    _ok("moe_permute_rows", lib().moe_permute_rows(_ptr(src), _ptr(index), n, d, _dt(src), _ptr(out),
+                                                   _stream(stream)))
+    return out
+
 
 def expert_dgrad(a, offsets, kept, w, rows_max: int, *, out=None, stream=None):
     """out [rows, N] = a[r] . w[e] per kept row r of expert e, w [E, K, N] as stored (moe_expert_dgrad)."""

@@ -183,4 +183,19 @@ scatter_tokens_kernel(const int32_t* __restrict__ slot_row, int T, int k, const 
     }
 }
 
+// dst[i] = src[index[i]] for i < n: one warp per row, 16-byte vectors (the
+// regrouping of received rows in the expert-parallel exchange).
+__global__ void __launch_bounds__(THREADS)
+permute_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ index, long long n, int vec16,
+                    uint4* __restrict__ dst)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps_total = (long long)gridDim.x * WARPS;
+    for (long long i = blockIdx.x * WARPS + (threadIdx.x >> 5); i < n; i += warps_total) {
+        const uint4* s = src + (size_t)__ldg(index + i) * vec16;
+        uint4* o = dst + (size_t)i * vec16;
+        for (int v = lane; v < vec16; v += 32) o[v] = ldg_nc_v4(s + v);
+    }
+}
+
 }  // namespace dispatch

@@ -573,6 +573,20 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     return launch_status();
 }
 
+moe_status moe_permute_rows(const void* src, const int32_t* index, int64_t n, int d, moe_dtype dtype, void* dst,
+                            moe_stream_t stream)
+{
+    if (n < 0 || d <= 0 || !dtype_ok(dtype) || (n > 0 && (!src || !index || !dst))) return MOE_ERR_INVALID_ARG;
+    const int row_bytes = d * esize(dtype);
+    if (row_bytes % 16 || ((uintptr_t)src & 15u) || ((uintptr_t)dst & 15u)) return MOE_ERR_UNSUPPORTED;
+    if (n == 0) return MOE_OK;
+    long long grid = (n + dispatch::WARPS - 1) / dispatch::WARPS;
+    if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
+    dispatch::permute_rows_kernel<<<(int)grid, dispatch::THREADS, 0, (cudaStream_t)stream>>>(
+        (const uint4*)src, index, (long long)n, row_bytes / 16, (uint4*)dst);
+    return launch_status();
+}
+
 static moe_status ffn_common_checks(const int32_t* offsets, const int32_t* kept, int E, int d, int F,
                                     moe_dtype dtype, int64_t rows_max)
 {
