@@ -98,7 +98,8 @@ pack_segments_t_kernel(const uint16_t* __restrict__ src, const int32_t* __restri
 
 // One warp per token.  For each kept slot r = slot_row[t, j]:
 //   do_perm[r] = g_r * dy[t]   (bf16),   dgate[t, j] = <dy[t], y_perm[r]> / g_r
-// (y_perm holds g_r o_r); a dropped slot gets dgate 0 and no row.
+// (y_perm holds g_r o_r); a dropped slot gets dgate 0 and no row.  Each lane
+// works on four 16-byte vectors at a time (4 (k + 1) loads in flight).
 constexpr int CB_THREADS = 256;
 __global__ void __launch_bounds__(CB_THREADS)
 combine_bwd_kernel(const uint4* __restrict__ dy, const int32_t* __restrict__ slot_row,
@@ -116,22 +117,37 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const int32_t* __restrict__ slo
             g[j] = rows[j] >= 0 ? __ldg(row_gate + rows[j]) : 0.f;
             dot[j] = 0.f;
         }
-        for (int v = lane; v < vec16; v += 32) {
-            float f[8];
-            unpack_bf16x8(ldg_nc_v4(dy + (size_t)t * vec16 + v), f);
+        for (int v0 = lane; v0 < vec16; v0 += 128) {
+            float f[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u;
+                unpack_bf16x8(v < vec16 ? ldg_nc_v4(dy + (size_t)t * vec16 + v) : make_uint4(0, 0, 0, 0), f[u]);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 if (rows[j] < 0) continue;
-                float o[8];
-                unpack_bf16x8(ldg_nc_v4(y_perm + (size_t)rows[j] * vec16 + v), o);
+                uint4 q[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dot[j] = fmaf(f[i], o[i], dot[j]);
-                uint4 w;
-                w.x = pack_bf16x2(g[j] * f[0], g[j] * f[1]);
-                w.y = pack_bf16x2(g[j] * f[2], g[j] * f[3]);
-                w.z = pack_bf16x2(g[j] * f[4], g[j] * f[5]);
-                w.w = pack_bf16x2(g[j] * f[6], g[j] * f[7]);
-                do_perm[(size_t)rows[j] * vec16 + v] = w;
+                for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + 32 * u;
+                    q[u] = v < vec16 ? ldg_nc_v4(y_perm + (size_t)rows[j] * vec16 + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + 32 * u;
+                    if (v >= vec16) break;
+                    float o[8];
+                    unpack_bf16x8(q[u], o);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dot[j] = fmaf(f[u][i], o[i], dot[j]);
+                    uint4 w;
+                    w.x = pack_bf16x2(g[j] * f[u][0], g[j] * f[u][1]);
+                    w.y = pack_bf16x2(g[j] * f[u][2], g[j] * f[u][3]);
+                    w.z = pack_bf16x2(g[j] * f[u][4], g[j] * f[u][5]);
+                    w.w = pack_bf16x2(g[j] * f[u][6], g[j] * f[u][7]);
+                    do_perm[(size_t)rows[j] * vec16 + v] = w;
+                }
             }
         }
 #pragma unroll

@@ -17,7 +17,8 @@ constexpr int WARPS = THREADS / 32;
 
 // One warp per token; each lane sums 16-byte vectors of the token's k rows
 // in j order (fp32) and rounds once.  Dropped slots (-1) are skipped; a token
-// with none kept gets zeros.
+// with none kept gets zeros.  Each lane works on four vectors at a time, so
+// 4·k loads are in flight before the first sum.
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ slot_row, int T, int k,
@@ -27,39 +28,52 @@ combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ slo
     const int warps_total = gridDim.x * WARPS;
     for (int t = blockIdx.x * WARPS + (threadIdx.x >> 5); t < T; t += warps_total) {
         int rows[16];
-        int nk = 0;
-        for (int j = 0; j < k; ++j) {
-            const int r = __ldg(slot_row + (size_t)t * k + j);
-            if (r >= 0) rows[nk++] = r;
-        }
-        for (int v = lane; v < vec16; v += 32) {
-            if (BF16) {
-                float acc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-                for (int q = 0; q < nk; ++q) {
-                    float f[8];
-                    unpack_bf16x8(ldg_nc_v4(y_perm + (size_t)rows[q] * vec16 + v), f);
+        for (int j = 0; j < 16; ++j) rows[j] = j < k ? __ldg(slot_row + (size_t)t * k + j) : -1;
+        for (int v0 = lane; v0 < vec16; v0 += 128) {
+            float acc[4][8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (rows[j] < 0) continue;
+                const uint4* src = y_perm + (size_t)rows[j] * vec16;
+                uint4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    q[u] = (v0 + 32 * u < vec16) ? ldg_nc_v4(src + v0 + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (BF16) {
+                        float f[8];
+                        unpack_bf16x8(q[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[u][i] += f[i];
+                    } else {
+                        acc[u][0] += __uint_as_float(q[u].x);
+                        acc[u][1] += __uint_as_float(q[u].y);
+                        acc[u][2] += __uint_as_float(q[u].z);
+                        acc[u][3] += __uint_as_float(q[u].w);
+                    }
                 }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= vec16) break;
                 uint4 o;
-                o.x = pack_bf16x2(acc[0], acc[1]);
-                o.y = pack_bf16x2(acc[2], acc[3]);
-                o.z = pack_bf16x2(acc[4], acc[5]);
-                o.w = pack_bf16x2(acc[6], acc[7]);
-                y[(size_t)t * vec16 + v] = o;
-            } else {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int q = 0; q < nk; ++q) {
-                    const uint4 u = ldg_nc_v4(y_perm + (size_t)rows[q] * vec16 + v);
-                    acc[0] += __uint_as_float(u.x);
-                    acc[1] += __uint_as_float(u.y);
-                    acc[2] += __uint_as_float(u.z);
-                    acc[3] += __uint_as_float(u.w);
+                if (BF16) {
+                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                } else {
+                    o = make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]), __float_as_uint(acc[u][2]),
+                                   __float_as_uint(acc[u][3]));
                 }
-                y[(size_t)t * vec16 + v] = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                                                      __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+                y[(size_t)t * vec16 + v] = o;
             }
         }
     }
