@@ -51,11 +51,11 @@ def _dy(cfg):
     return torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16)
 
 
-def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0, grad_dtype=torch.float32):
-    case = make_case(cfg)
+def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0, grad_dtype=torch.float32, n_group=1, topk_group=1):
+    case = make_case(cfg, n_group=n_group, topk_group=topk_group)
     plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], case["x"].device,
                        cfg.alpha, cfg.renorm, z_beta=z_beta if z_beta else None, aux_post_drop=post, train=True,
-                       grad_dtype=grad_dtype)
+                       grad_dtype=grad_dtype, n_group=n_group, topk_group=topk_group)
     moe.set_wait_limit(400_000_000)
     try:
         plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
@@ -67,7 +67,7 @@ def _run(cfg, z_beta, post, aux_weight=1.0, z_weight=1.0, grad_dtype=torch.float
         moe.set_wait_limit(0)
     ref = OB.backward(case["x_h"], case["W_h"], case["b_h"], case["w1"].cpu(), case["w2"].cpu(), dy, k=cfg.k,
                       cap=case["cap"], act=cfg.act, renorm=cfg.renorm, alpha=cfg.alpha, aux_weight=aux_weight,
-                      z_beta=z_beta, z_weight=z_weight, aux_post_drop=post)
+                      z_beta=z_beta, z_weight=z_weight, aux_post_drop=post, n_group=n_group, topk_group=topk_group)
     return plan, g, ref, case
 
 
@@ -86,6 +86,19 @@ def test_backward_against_oracle(name, grad_dtype):
     print(f"[backward parity] {name}: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()))
     for key, err in errs.items():
         assert err <= TOL, (key, err)
+
+
+@pytest.mark.parametrize("name,G,M,aw,zw", [("swiglu_e64_zipf", 16, 3, 0.5, 2.0), ("swiglu_e128_top8", 8, 4, 1.0, 1.0),
+                                           ("gelu_e32_norenorm", 8, 2, 2.0, 0.0)])
+def test_backward_with_group_routing_and_loss_weights(name, G, M, aw, zw):
+    """Group-limited routing in the forward, other aux / z-loss weights."""
+    cfg, z_beta, post = CASES[name]
+    plan, g, ref, _ = _run(cfg, z_beta or 1e-3, post, aux_weight=aw, z_weight=zw, n_group=G, topk_group=M)
+    for key in ("dx", "dW", "db", "dw1", "dw2", "dgate", "dl"):
+        got = g[key].float().cpu().numpy().astype(np.float64)
+        if key in ("dx", "dgate", "dl"):
+            got = got[:cfg.T]
+        assert rel_fro(got, ref[key]) <= TOL, key
 
 
 def test_backward_is_bitwise_reproducible():
