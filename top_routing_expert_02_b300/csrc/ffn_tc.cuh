@@ -46,11 +46,12 @@ struct Shape {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 6 ? 6 : (200 * 1024) / STAGE_BYTES;
     static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;       // + slack for 1024-B alignment
-    // weight-gradient mode: one stage fewer, and a 32x32 fp32 staging tile
-    // per epilogue warp for the TMA stores of the output
-    static constexpr int WG_STAGES = STAGES - 1;
+    // weight-gradient mode: the same ring plus a 32x32 fp32 staging tile per
+    // epilogue warp for the TMA stores of the output (fits next to 4 stages of 48 KB)
+    static constexpr int WG_STAGES = STAGES;
     static constexpr int WG_STAGE_OUT = 32 * 32 * 4;
     static constexpr int WG_SMEM_DYN = WG_STAGES * STAGE_BYTES + 4 * WG_STAGE_OUT + 1024;
+    static_assert(WG_SMEM_DYN <= 227 * 1024, "weight-gradient mode exceeds shared memory");
     static constexpr int ACC_COLS = BN;
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
     static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
