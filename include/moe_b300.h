@@ -279,8 +279,8 @@ moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_
  *   do_perm, dgate   = moe_combine_bwd(dy, ...)
  *   z                = kept by moe_expert_up_z in the forward, or recomputed:
  *                      moe_expert_up(x_perm, ..., IDENTITY, F := N1, w1)
- *   da               = moe_expert_dgrad(do_perm, ..., K = d, N = F, w2)
- *   dz               = moe_act_bwd(z, da, ...)
+ *   dz               = moe_expert_dgrad_act(do_perm, ..., w2, z)  (the da GEMM
+ *                      with moe_act_bwd in its epilogue; identity: moe_expert_dgrad)
  *   dx_perm          = moe_expert_dgrad(dz, ..., K = N1, N = d, w1)
  *   dw2[e]           = moe_expert_wgrad(pack(do_perm), pack(h), M = d, N = F)
  *   dw1[e]           = moe_expert_wgrad(pack(dz), pack(x_perm), M = N1, N = d)
@@ -296,6 +296,14 @@ moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_
  * K % 64 == 0, N % 64 == 0. */
 moe_status moe_expert_dgrad(const void* a, const int32_t* offsets, const int32_t* kept, int E, int K, int N,
                             moe_dtype dtype, const void* w, int64_t rows_max, void* out, moe_stream_t stream);
+
+/* The da GEMM with the activation backward in its epilogue:
+ *   da = do_perm[r] . w2[e] (fp32, never stored), dz = act'(z) * da  as
+ *   moe_act_bwd, from the kept pre-activation z [rows_max, N1]
+ * dz [rows_max, N1] bf16.  act GELU or SWIGLU; d % 64 == 0, F % 64 == 0. */
+moe_status moe_expert_dgrad_act(const void* do_perm, const int32_t* offsets, const int32_t* kept, int E, int d,
+                                int F, moe_act act, moe_dtype dtype, const void* w2, const void* z, int64_t rows_max,
+                                void* dz, moe_stream_t stream);
 
 /* w [E, R, C] -> wt [E, C, R] (2-byte elements; R, C multiples of 64;
  * 16-byte aligned). */

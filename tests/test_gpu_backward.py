@@ -264,3 +264,36 @@ def test_backward_full_size_e8_swiglu():
     print("[backward parity] e8_swiglu full size: " + ", ".join(f"{k} {v:.2e}" for k, v in errs.items()))
     for key, err in errs.items():
         assert err <= TOL, (key, err)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+def test_act_bwd_and_fused_dgrad_act(act):
+    """moe_act_bwd against the torch fp32 formula; moe_expert_dgrad_act (the da
+    GEMM with the activation backward in its epilogue) against
+    moe_act_bwd(z, moe_expert_dgrad(...)) -- the same values up to the bf16
+    rounding of da that the fused path skips."""
+    g = torch.Generator(device="cuda").manual_seed(9)
+    E, d, F = 3, 256, 320
+    N1 = 2 * F if act == "swiglu" else F
+    kept = torch.tensor([130, 0, 70], dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    offsets[1:] = torch.cumsum(kept, 0)
+    R = int(offsets[-1])
+    do = torch.randn(R, d, device="cuda", generator=g).to(torch.bfloat16)
+    w2 = (torch.randn(E, d, F, device="cuda", generator=g) / 16).to(torch.bfloat16)
+    z = torch.randn(R, N1, device="cuda", generator=g).to(torch.bfloat16)
+    da = moe.expert_dgrad(do, offsets, kept, w2, R)
+    dz = moe.act_bwd(z, da, offsets, F, act, R)
+    dz_fused = moe.expert_dgrad_act(do, offsets, kept, w2, z, act, R)
+    moe.check()
+    zf, daf = z.float(), da.float()
+    if act == "swiglu":
+        zg, zu = zf[:, :F], zf[:, F:]
+        s = torch.sigmoid(zg)
+        ref = torch.cat([daf * zu * s * (1 + zg * (1 - s)), daf * zg * s], dim=1)
+    else:
+        cdf = 0.5 * (1 + torch.erf(zf / 2 ** 0.5))
+        ref = daf * (cdf + zf * torch.exp(-0.5 * zf * zf) / (2 * torch.pi) ** 0.5)
+    assert torch.allclose(dz.float(), ref, rtol=1e-2, atol=1e-2)
+    err = (dz_fused.float() - dz.float()).norm() / dz.float().norm()
+    assert err < 1e-2, err

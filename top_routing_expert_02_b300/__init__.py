@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
-    "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
+    "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "expert_dgrad_act", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
     "pack_segments_t", "expert_wgrad", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
@@ -59,6 +59,7 @@ _SIGS = {
     "moe_dispatch": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                             _P, _SZ, _P]),
     "moe_expert_up": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_expert_dgrad_act": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P]),
     "moe_permute_rows": (_I32, [_P, _P, _I64, _I32, _I32, _P, _P]),
     "moe_expert_dgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P, _P]),
     "moe_expert_up_z": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _P, _P]),
@@ -343,6 +344,16 @@ def z_loss(lse, beta: float, *, loss=None, stream=None):
 
 # --------------------------------------------------------------- backward ---
 
+def expert_dgrad_act(do_perm, offsets, kept, w2, z, act: str, rows_max: int, *, dz=None, stream=None):
+    """dz = act'(z) * (do_perm . w2[e]) per kept row (moe_expert_dgrad_act)."""
+    E, d, F = w2.shape
+    dz = torch.empty_like(z) if dz is None else dz
+    _ok("moe_expert_dgrad_act", lib().moe_expert_dgrad_act(_ptr(do_perm), _ptr(offsets), _ptr(kept), E, d, F,
+                                                           ACT[act], _dt(do_perm), _ptr(w2), _ptr(z), rows_max,
+                                                           _ptr(dz), _stream(stream)))
+    return dz
+
+
 def permute_rows(src, index, *, out=None, stream=None):
     """out[i] = src[index[i]] (moe_permute_rows); index int32 on the device."""
     n = index.shape[0]
@@ -572,7 +583,7 @@ class MoEPlan:
             f32 = dict(dtype=torch.float32, device=dev)
             self._bwd = dict(
                 do_perm=torch.empty((R, d), **bf), dgate=torch.empty((max(T, 1), k), **f32),
-                da=torch.empty((R, F), **bf), dz=torch.empty((R, N1), **bf),
+                dz=torch.empty((R, N1), **bf),
                 dx_perm=torch.empty((R, d), **bf), ld=ld,
                 doT=torch.empty((d, ld), **bf), hT=torch.empty((F, ld), **bf), dzT=torch.empty((N1, ld), **bf),
                 xT=torch.empty((d, ld), **bf),
@@ -598,10 +609,12 @@ class MoEPlan:
         R, F, E, d = self.rows_max, self.F, self.E, self.d
         combine_bwd(dy, D.slot_row, D.row_gate, self.y_perm, do_perm=B["do_perm"], dgate=B["dgate"], stream=stream)
         mark("combine_bwd")
-        # data gradients on the weights as stored: da = do . w2[e], dz from the
-        # forward's pre-activation z, dx_perm = dz . w1[e]
-        expert_dgrad(B["do_perm"], D.offsets, D.kept, w2, R, out=B["da"], stream=stream)
-        act_bwd(self.z, B["da"], D.offsets, F, self.act, R, dz=B["dz"], stream=stream)
+        # data gradients on the weights as stored: dz = act'(z) * (do . w2[e]) in
+        # one GEMM (z kept by the forward), dx_perm = dz . w1[e]
+        if self.act == "identity":
+            expert_dgrad(B["do_perm"], D.offsets, D.kept, w2, R, out=B["dz"], stream=stream)
+        else:
+            expert_dgrad_act(B["do_perm"], D.offsets, D.kept, w2, self.z, self.act, R, dz=B["dz"], stream=stream)
         expert_dgrad(B["dz"], D.offsets, D.kept, w1, R, out=B["dx_perm"], stream=stream)
         mark("data_grad_gemms")
         # weight gradients on segment-packed transposes
@@ -628,7 +641,7 @@ class MoEPlan:
             B["db"].zero_()
         mark("router_and_dx")
         return dict(dx=B["dx"], dW=B["dW"], db=B["db"], dw1=B["dw1"], dw2=B["dw2"], dgate=B["dgate"], dl=B["dl"],
-                    do_perm=B["do_perm"], z=self.z, da=B["da"], dz=B["dz"], dx_perm=B["dx_perm"])
+                    do_perm=B["do_perm"], z=self.z, dz=B["dz"], dx_perm=B["dx_perm"])
 
 
 def moe_forward(x, w_router, b_router, w1, w2, *, k: int, cf: float, act: str, renorm: bool = True,

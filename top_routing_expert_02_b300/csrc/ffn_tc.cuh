@@ -58,7 +58,12 @@ struct Shape {
 };
 constexpr int MAX_STAGES = 6;
 
-enum { EPI_GELU = 0, EPI_SWIGLU = 1, EPI_IDENT = 2, EPI_GATE = 3 };
+// EPI_DGELU / EPI_DSWIGLU: activation backward fused into the da = do . w2[e]
+// epilogue: the accumulator column c is da[:, c]; the epilogue reads the kept
+// pre-activation z (in_z, row stride z_cols = N1) and writes dz (out, row
+// stride z_cols): GELU dz = da (Phi(z) + z phi(z)); SwiGLU dz[:, c] = da
+// z_up silu'(z_gate), dz[:, F + c] = da silu(z_gate).
+enum { EPI_GELU = 0, EPI_SWIGLU = 1, EPI_IDENT = 2, EPI_GATE = 3, EPI_DGELU = 4, EPI_DSWIGLU = 5 };
 
 struct Args {
     const int32_t* offsets;
@@ -76,7 +81,8 @@ struct Args {
     const uint8_t* a_base;      // gathered A: x
     uint32_t a_row_bytes;       // gathered A: bytes of one x row (x is below 4 GB)
     uint16_t* out_z;            // up projection, optional: the pre-activation, bf16 [rows_max, N1]
-    int z_cols;                 // columns of out_z (N1)
+    const uint16_t* in_z;       // activation backward: the pre-activation, bf16 [rows_max, N1]
+    int z_cols;                 // columns of out_z / in_z (N1)
     float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols], or nullptr: bf16 into out
     int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
     int m_rows;                 // weight gradient: rows M of each expert's gradient
@@ -431,8 +437,59 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t av[32];
                     ptx::tmem_ld32(tb + c, av);
-                    ptx::tmem_ld_wait();
                     const int col = n * BN + c;
+                    if (EPI == EPI_DGELU || EPI == EPI_DSWIGLU) {
+                        // z loads issued before the TMEM wait; 32 columns of this row
+                        uint4 zg[4], zu[4];
+                        const bool live = rv && col < g.out_cols;
+                        const uint16_t* zr = g.in_z + (size_t)row * g.z_cols + col;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            zg[v] = live ? ldg_nc_v4(zr + 8 * v) : make_uint4(0, 0, 0, 0);
+                            if (EPI == EPI_DSWIGLU)
+                                zu[v] = live ? ldg_nc_v4(zr + g.out_cols + 8 * v) : make_uint4(0, 0, 0, 0);
+                        }
+                        ptx::tmem_ld_wait();
+                        if (live) {
+                            uint32_t pg[16], pu[16];
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                float a[8], u[8];
+                                unpack_bf16x8(zg[v], a);
+                                if (EPI == EPI_DSWIGLU) unpack_bf16x8(zu[v], u);
+#pragma unroll
+                                for (int i = 0; i < 8; i += 2) {
+                                    float o[2], ou[2];
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        const float da = f32(av[8 * v + i + h]), z = a[i + h];
+                                        if (EPI == EPI_DGELU) {
+                                            const float cdf = 0.5f * (1.0f + erff(z * 0.70710678118654752f));
+                                            const float pdf = 0.39894228040143268f * expf(-0.5f * z * z);
+                                            o[h] = da * (cdf + z * pdf);
+                                        } else {
+                                            const float sg = 1.0f / (1.0f + expf(-z));
+                                            o[h] = da * u[i + h] * (sg * (1.0f + z * (1.0f - sg)));
+                                            ou[h] = da * (z * sg);
+                                        }
+                                    }
+                                    pg[4 * v + i / 2] = pack_bf16x2(o[0], o[1]);
+                                    if (EPI == EPI_DSWIGLU) pu[4 * v + i / 2] = pack_bf16x2(ou[0], ou[1]);
+                                }
+                            }
+                            uint4* dg = reinterpret_cast<uint4*>(g.out + (size_t)row * g.z_cols + col);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) dg[v] = make_uint4(pg[4 * v], pg[4 * v + 1], pg[4 * v + 2], pg[4 * v + 3]);
+                            if (EPI == EPI_DSWIGLU) {
+                                uint4* du = reinterpret_cast<uint4*>(g.out + (size_t)row * g.z_cols + g.out_cols + col);
+#pragma unroll
+                                for (int v = 0; v < 4; ++v)
+                                    du[v] = make_uint4(pu[4 * v], pu[4 * v + 1], pu[4 * v + 2], pu[4 * v + 3]);
+                            }
+                        }
+                        continue;
+                    }
+                    ptx::tmem_ld_wait();
                     if (EPI != EPI_GATE && rv && col < g.out_cols && g.out_z) {
                         uint32_t zk[16];
 #pragma unroll

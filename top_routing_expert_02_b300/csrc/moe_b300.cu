@@ -945,6 +945,35 @@ moe_status moe_expert_dgrad(const void* a, const int32_t* offsets, const int32_t
                                                              (cudaStream_t)stream);
 }
 
+moe_status moe_expert_dgrad_act(const void* do_perm, const int32_t* offsets, const int32_t* kept, int E, int d,
+                                int F, moe_act act, moe_dtype dtype, const void* w2, const void* z, int64_t rows_max,
+                                void* dz, moe_stream_t stream)
+{
+    moe_status st = ffn_common_checks(offsets, kept, E, d, F, dtype, rows_max);
+    if (st != MOE_OK) return st;
+    if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+    if (!w2 || (rows_max > 0 && (!do_perm || !z || !dz))) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (rows_max == 0) return MOE_OK;
+    tcg::Args g{};
+    g.offsets = offsets;
+    g.kept = kept;
+    g.E = E;
+    g.K = d;
+    g.n_step = 256;
+    g.half_off = 128;
+    g.n_tiles = (F + 255) / 256;
+    g.out_cols = F;
+    g.out = (uint16_t*)dz;
+    g.in_z = (const uint16_t*)z;
+    g.z_cols = act == MOE_ACT_SWIGLU ? 2 * F : F;
+    g.wait_limit = g_wait_limit.load();
+    cudaStream_t s = (cudaStream_t)stream;
+    if (act == MOE_ACT_SWIGLU)
+        return launch_tc_bn<tcg::EPI_DSWIGLU, 256, tcg::MODE_BMN>(do_perm, rows_max, d, w2, (long long)E * d, g, s);
+    return launch_tc_bn<tcg::EPI_DGELU, 256, tcg::MODE_BMN>(do_perm, rows_max, d, w2, (long long)E * d, g, s);
+}
+
 moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const int32_t* kept, int E, int C,
                                int64_t rows_max, int64_t ld, moe_dtype dtype, void* dst, moe_stream_t stream)
 {
