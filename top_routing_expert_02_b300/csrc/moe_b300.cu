@@ -85,12 +85,13 @@ inline bool route_tc_shape(int E, RouteTcShape* s)
     return true;
 }
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
-// Blocks per 128-token tile: split d so that small batches still fill the GPU
-// (148 SMs), at most 16 ways and never below one K block of 64 per split.
+// Split-K factor of the tensor-core router: as many splits as keep ntiles * S
+// within one wave of the 148 SMs (rounding up would start a second, mostly
+// empty wave), at most MAX_SPLITS and at most one split per K block.
 inline int route_tc_splits(long long ntiles, int d)
 {
     const int nk = d / rtc::BK;
-    long long S = (148 + ntiles - 1) / (ntiles > 0 ? ntiles : 1);
+    long long S = 148 / (ntiles > 0 ? ntiles : 1);
     if (S > rtc::MAX_SPLITS) S = rtc::MAX_SPLITS;
     if (S > nk) S = nk;
     return S < 1 ? 1 : (int)S;
