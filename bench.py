@@ -580,6 +580,25 @@ def train_arm(args, cfg):
     if world > 1:
         ms_step = mdist.max_over_ranks(ms_step, device=dev)
 
+    # the same step as one CUDA-graph replay
+    graph = plan.capture(x, W, b, w1, w2, dy=dy)
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        gev[i][0].record(stream)
+        graph.replay()
+        gev[i][1].record(stream)
+    barrier()
+    moe.check()
+    ms_graph = sum(a.elapsed_time(c) for a, c in gev) / args.steps
+    if world > 1:
+        ms_graph = mdist.max_over_ranks(ms_graph, device=dev)
+    del graph
+
     # end to end: x and dy from pinned host memory, dx and the loss back; the
     # weight gradients stay on the device where an optimiser would use them
     x_host, dyh = ri.x.pin_memory(), dy_host.pin_memory()
@@ -626,6 +645,7 @@ def train_arm(args, cfg):
                      "peak_source": f"{peak_src} bf16 dense burst", "traffic": None,
                      "frac_of_sustained": achieved / bf16_sust, "algorithmic_flops_per_launch": dw1_flops},
         "gemm_tflops_step": gemm_flops / (ms_step * 1e-3) / 1e12,
+        "graph_ms_per_step": ms_graph, "graph_tokens_per_s": world * cfg.T / (ms_graph / 1000.0),
         "kernel_ms": {k: statistics.mean(v) for k, v in part.items()},
         "routing": {"kept_slots": A},
     }

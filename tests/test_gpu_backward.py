@@ -297,3 +297,21 @@ def test_act_bwd_and_fused_dgrad_act(act):
     assert torch.allclose(dz.float(), ref, rtol=1e-2, atol=1e-2)
     err = (dz_fused.float() - dz.float()).norm() / dz.float().norm()
     assert err < 1e-2, err
+
+
+def test_training_step_as_one_cuda_graph():
+    """Forward + backward captured once and replayed: bit-identical to eager."""
+    cfg, z_beta, post = CASES["swiglu_e64_zipf"]
+    p1, g1, _, case = _run(cfg, z_beta, post)
+    snap = {k: g1[k].clone() for k in ("dx", "dW", "db", "dw1", "dw2")}
+    y = p1.y.clone()
+    dy = _dy(cfg).cuda()
+    graph = p1.capture(case["x"], case["W"], case["b"], case["w1"], case["w2"], dy=dy)
+    for k in snap:
+        p1._bwd[k].zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    moe.check()
+    assert torch.equal(p1.y, y)
+    for k, v in snap.items():
+        assert torch.equal(p1._bwd[k], v), k

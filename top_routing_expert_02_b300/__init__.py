@@ -526,20 +526,26 @@ class MoEPlan:
         self.ws_route = _empty_ws(workspace_bytes("route", T, d, E, k, F), dev)
         self.ws_dispatch = _empty_ws(workspace_bytes("dispatch", T, d, E, k, F), dev)
 
-    def capture(self, x, w_router, b_router, w1, w2) -> "torch.cuda.CUDAGraph":
-        """Record run() on these exact tensors into a CUDA graph (one launch per
-        replay).  The inputs' addresses are baked in: refill the same tensors
-        and call ``graph.replay()``.  One eager run happens first so every
-        one-time setup (kernel attributes, driver entry points) is done before
-        capture."""
-        self.run(x, w_router, b_router, w1, w2)
+    def capture(self, x, w_router, b_router, w1, w2, dy=None, **backward_kw) -> "torch.cuda.CUDAGraph":
+        """Record run() -- and, given ``dy`` (``train=True``), backward() after
+        it -- on these exact tensors into a CUDA graph (one launch per replay).
+        The inputs' addresses are baked in: refill the same tensors and call
+        ``graph.replay()``.  One eager pass happens first so every one-time
+        setup (kernel attributes, driver entry points, backward buffers) is
+        done before capture."""
+        def step():
+            self.run(x, w_router, b_router, w1, w2)
+            if dy is not None:
+                self.backward(x, w_router, w1, w2, dy, **backward_kw)
+
+        step()
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             with torch.cuda.graph(graph, stream=side):
-                self.run(x, w_router, b_router, w1, w2)
+                step()
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         return graph
