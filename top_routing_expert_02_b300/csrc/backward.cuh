@@ -332,8 +332,10 @@ grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot
     for (int tk = 0; tk < GX_TOK; ++tk)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[tk][q] = 0.f;
+    float4 wn = __ldg(reinterpret_cast<const float4*>(W + c));
     for (int e = 0; e < E; ++e) {
-        const float4 w = __ldg(reinterpret_cast<const float4*>(W + (size_t)e * d + c));
+        const float4 w = wn;   // this expert's W row; the next one is fetched before the FMAs
+        if (e + 1 < E) wn = __ldg(reinterpret_cast<const float4*>(W + (size_t)(e + 1) * d + c));
 #pragma unroll
         for (int t4 = 0; t4 < GX_TOK; t4 += 4) {
             const float4 l = *reinterpret_cast<const float4*>(&dlT[e][t4]);
@@ -385,6 +387,32 @@ grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot
 // The splits are summed in order by router_wgrad_sum_kernel.
 constexpr int RW_EXP = 16;
 constexpr int RW_COLS = 1024;
+
+// Columns c..c+3 of x rows t..t+7 (as fp32; rows at or past tb read as 0).
+template <bool BF16>
+__device__ __forceinline__ void load_x_rows(const void* __restrict__ x, int t, int tb, int d, int c, float (&xv)[8][4])
+{
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        if (t + u < tb) {
+            if (BF16) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2*>((const uint16_t*)x + (size_t)(t + u) * d + c));
+                xv[u][0] = __uint_as_float(w.x << 16);
+                xv[u][1] = __uint_as_float(w.x & 0xffff0000u);
+                xv[u][2] = __uint_as_float(w.y << 16);
+                xv[u][3] = __uint_as_float(w.y & 0xffff0000u);
+            } else {
+                const float4 w = __ldg(reinterpret_cast<const float4*>((const float*)x + (size_t)(t + u) * d + c));
+                xv[u][0] = w.x;
+                xv[u][1] = w.y;
+                xv[u][2] = w.z;
+                xv[u][3] = w.w;
+            }
+        } else {
+            xv[u][0] = xv[u][1] = xv[u][2] = xv[u][3] = 0.f;
+        }
+    }
+}
 template <bool BF16>
 __global__ void __launch_bounds__(256)
 router_wgrad_kernel(const float* __restrict__ dl, const void* __restrict__ x, int T, int E, int d, int tok_per_split,
@@ -412,27 +440,7 @@ router_wgrad_kernel(const float* __restrict__ dl, const void* __restrict__ x, in
             // eight token rows of x in flight at a time (rows past the split read as 0)
             for (int tk0 = 0; tk0 < 32; tk0 += 8) {
                 float xv[8][4];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = t0 + tk0 + u;
-                    if (t < tb) {
-                        if (BF16) {
-                            const uint2 w = __ldg(reinterpret_cast<const uint2*>((const uint16_t*)x + (size_t)t * d + c));
-                            xv[u][0] = __uint_as_float(w.x << 16);
-                            xv[u][1] = __uint_as_float(w.x & 0xffff0000u);
-                            xv[u][2] = __uint_as_float(w.y << 16);
-                            xv[u][3] = __uint_as_float(w.y & 0xffff0000u);
-                        } else {
-                            const float4 w = __ldg(reinterpret_cast<const float4*>((const float*)x + (size_t)t * d + c));
-                            xv[u][0] = w.x;
-                            xv[u][1] = w.y;
-                            xv[u][2] = w.z;
-                            xv[u][3] = w.w;
-                        }
-                    } else {
-                        xv[u][0] = xv[u][1] = xv[u][2] = xv[u][3] = 0.f;
-                    }
-                }
+                load_x_rows<BF16>(x, t0 + tk0, tb, d, c, xv);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
 #pragma unroll
