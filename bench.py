@@ -87,7 +87,7 @@ def plan_kwargs(args) -> dict:
     return kw
 
 
-BWD_KERNELS = 1 + 2 + 1 + 4 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs, act bwd, packs, wgrads,
+BWD_KERNELS = 1 + 2 + 4 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs (act bwd fused), packs, wgrads,
                                               # router bwd, dx, router weights (partial, sum, bias)
 
 
