@@ -161,3 +161,22 @@ def test_backward_argument_errors():
     assert L.moe_grad_x(FAKE, FAKE, FAKE, None, 16, 2, 8, 128, 1, FAKE, None) == 1
     assert L.moe_router_wgrad(FAKE, FAKE, 1, 0, 8, 128, FAKE, None, FAKE, 1 << 20, None) == 1
     assert L.moe_router_wgrad(FAKE, FAKE, 1, 64, 8, 128, FAKE, None, FAKE, 8, None) == 3    # workspace
+
+
+def test_misaligned_buffers_are_refused_before_any_work():
+    """Buffers moved with 16-byte vectors or TMA must be 16-byte aligned; a
+    misaligned one is MOE_ERR_UNSUPPORTED, returned before anything runs."""
+    L = moe.lib()
+    MIS = ctypes.c_void_p(0x1008)
+    f = ctypes.c_float
+    assert L.moe_route(MIS, 1, FAKE, None, 16, 128, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 2
+    assert L.moe_dispatch(FAKE, FAKE, 16, 2, 8, 4, MIS, 1, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                          1 << 20, None) == 2
+    assert L.moe_expert_up(MIS, FAKE, FAKE, 8, 128, 128, 0, 1, FAKE, 10, FAKE, None) == 2
+    assert L.moe_expert_down(FAKE, FAKE, FAKE, 8, 128, 128, 1, FAKE, FAKE, 10, MIS, None) == 2
+    assert L.moe_combine(MIS, FAKE, 16, 2, 128, 1, FAKE, None) == 2
+    assert L.moe_combine_bwd(FAKE, FAKE, FAKE, FAKE, 16, 2, 128, 1, MIS, FAKE, None) == 2
+    assert L.moe_expert_dgrad(FAKE, FAKE, FAKE, 8, 128, 128, 1, MIS, 10, FAKE, None) == 2
+    assert L.moe_expert_wgrad(FAKE, MIS, FAKE, 8, 128, 128, 5632, 1, FAKE, 0, None) == 2
+    assert L.moe_pack_segments_t(MIS, FAKE, FAKE, 8, 128, 10, 576, 1, FAKE, None) == 2
+    assert L.moe_grad_x(MIS, FAKE, FAKE, FAKE, 16, 2, 8, 128, 1, FAKE, None) == 2

@@ -5,6 +5,7 @@
 // arguments, encodes TMA tensor maps, picks launch shapes and enqueues the
 // kernels; it allocates nothing.
 #include <atomic>
+#include <initializer_list>
 #include <climits>
 #include <cstdio>
 #include <cstring>
@@ -48,6 +49,15 @@ int sm_count()
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
     return n;
+}
+
+// Every buffer moved with 16-byte vectors or TMA must start on a 16-byte
+// boundary; a misaligned pointer is refused before anything is enqueued.
+static bool all_aligned16(std::initializer_list<const void*> ps)
+{
+    for (const void* p : ps)
+        if (p && ((uintptr_t)p & 15u)) return false;
+    return true;
 }
 
 // Router block shape: experts per lane and tokens per warp.
@@ -413,6 +423,7 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         return MOE_ERR_INVALID_ARG;
     if (T * k >= INT_MAX || (long long)T * d >= (1LL << 40)) return MOE_ERR_INVALID_ARG;
     if (!prob_sum || (T > 0 && (!x || !w_router || !topk_idx || !topk_gate))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({x, w_router, ws})) return MOE_ERR_UNSUPPORTED;
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     const size_t need = route_ws_bytes(T, d, E);
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
@@ -550,6 +561,7 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     const int64_t rows_max = moe_perm_rows_max(T, k, E, cap);
     if (T > 0 && (!topk_idx || !topk_gate || !x || !slot_row)) return MOE_ERR_INVALID_ARG;
     if (rows_max > 0 && (!row_token || !row_gate)) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({x, x_perm})) return MOE_ERR_UNSUPPORTED;
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     const size_t need = dispatch_ws_bytes(T, k, E);
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
@@ -606,6 +618,7 @@ static moe_status expert_up_impl(const void* x_perm, const int32_t* offsets, con
     if (st != MOE_OK) return st;
     if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
     if (!w1 || (rows_max > 0 && (!x_perm || !h))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({x_perm, w1, h, z})) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0) return MOE_OK;
     const int N1 = act == MOE_ACT_SWIGLU ? 2 * F : F;
     if (dtype == MOE_F32) {
@@ -679,6 +692,7 @@ moe_status moe_expert_up_gathered(const void* x, int64_t T, const int32_t* row_t
     if (st != MOE_OK) return st;
     if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
     if (T < 0 || T >= INT_MAX || !w1 || (rows_max > 0 && (!x || !row_token || !h))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({x, w1, h})) return MOE_ERR_UNSUPPORTED;
     if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0 || T == 0) return MOE_OK;
     // the copies address x with 32-bit row offsets and 16-byte vectors
@@ -717,6 +731,7 @@ moe_status moe_expert_down(const void* h, const int32_t* offsets, const int32_t*
     moe_status st = ffn_common_checks(offsets, kept, E, d, F, dtype, rows_max);
     if (st != MOE_OK) return st;
     if (!w2 || (rows_max > 0 && (!h || !row_gate || !y_perm))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({h, w2, y_perm})) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0) return MOE_OK;
     if (dtype == MOE_F32)
         return launch_simt<simt::ACT_GATE>((const float*)h, offsets, kept, E, F, d, F, (const float*)w2, row_gate,
@@ -766,6 +781,7 @@ moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, i
     cudaStream_t stream = (cudaStream_t)stream_;
     if (T < 0 || k < 1 || k > MAX_K || d <= 0 || !dtype_ok(dtype) || T * k >= INT_MAX) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!slot_row || !y || !y_perm)) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({y_perm, y})) return MOE_ERR_UNSUPPORTED;
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     const int vec16 = d * esize(dtype) / 16;
@@ -888,6 +904,7 @@ moe_status moe_combine_bwd(const void* dy, const int32_t* slot_row, const float*
 {
     if (T < 0 || k < 1 || k > MAX_K || d <= 0 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!dy || !slot_row || !row_gate || !y_perm || !do_perm || !dgate)) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({dy, y_perm, do_perm})) return MOE_ERR_UNSUPPORTED;
     if (dtype != MOE_BF16 || d % 64) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     int grid = ceil_div_i(T, bwd::CB_THREADS / 32);
@@ -903,6 +920,7 @@ moe_status moe_act_bwd(const void* z, const void* da, const int32_t* offsets, in
     if (E < 1 || E > MAX_E || F <= 0 || rows_max < 0 || !offsets || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
     if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU && act != MOE_ACT_IDENTITY) return MOE_ERR_INVALID_ARG;
     if (rows_max > 0 && (!z || !da || !dz)) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({z, da, dz})) return MOE_ERR_UNSUPPORTED;
     if (dtype != MOE_BF16 || F % 64) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0) return MOE_OK;
     const int grid = sm_count() * 8;
@@ -929,6 +947,7 @@ moe_status moe_expert_dgrad(const void* a, const int32_t* offsets, const int32_t
     moe_status st = ffn_common_checks(offsets, kept, E, K, N, dtype, rows_max);
     if (st != MOE_OK) return st;
     if (!w || (rows_max > 0 && (!a || !out))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({a, w, out})) return MOE_ERR_UNSUPPORTED;
     if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0) return MOE_OK;
     tcg::Args g{};
@@ -954,6 +973,7 @@ moe_status moe_expert_dgrad_act(const void* do_perm, const int32_t* offsets, con
     if (st != MOE_OK) return st;
     if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
     if (!w2 || (rows_max > 0 && (!do_perm || !z || !dz))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({do_perm, w2, z, dz})) return MOE_ERR_UNSUPPORTED;
     if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0) return MOE_OK;
     tcg::Args g{};
@@ -982,6 +1002,7 @@ moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const in
         return MOE_ERR_INVALID_ARG;
     if (ld < moe_wgrad_cols(rows_max, E) || ld % 64) return MOE_ERR_INVALID_ARG;
     if (rows_max > 0 && (!src || !dst)) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({src, dst})) return MOE_ERR_UNSUPPORTED;
     if (dtype != MOE_BF16 || C % 64 || ld / 64 > 65535) return MOE_ERR_UNSUPPORTED;
     if (rows_max == 0) return MOE_OK;
     bwd::pack_segments_t_kernel<<<dim3(C / 64, (unsigned)(ld / 64)), 256, 0, (cudaStream_t)stream>>>(
@@ -996,6 +1017,7 @@ moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept,
         !dtype_ok(dw_dtype))
         return MOE_ERR_INVALID_ARG;
     if (dtype != MOE_BF16 || M % 64 || N % 64 || ld % 64 || ld >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+    if (!all_aligned16({at, bt, dw})) return MOE_ERR_UNSUPPORTED;
     tcg::Args a{};
     a.kept = kept;
     a.E = E;
@@ -1055,7 +1077,7 @@ moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64
                             float* db, void* ws, size_t ws_bytes, moe_stream_t stream)
 {
     if (T < 1 || E < 1 || E > MAX_E || d <= 0 || !dl || !x || !dW || !dtype_ok(xdt)) return MOE_ERR_INVALID_ARG;
-    if (d % 64 || !aligned16(x)) return MOE_ERR_UNSUPPORTED;
+    if (d % 64 || !all_aligned16({x, ws})) return MOE_ERR_UNSUPPORTED;
     const int S = router_wgrad_splits(T, E, d);
     const size_t need = (size_t)S * E * d * sizeof(float);
     if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
