@@ -130,6 +130,26 @@ def _dt(t: torch.Tensor) -> int:
         raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16") from None
 
 
+# MOE_NVTX=1 wraps every call below in an NVTX range named after it (for
+# nsight timelines); otherwise the functions are left as they are.
+_NVTX = os.environ.get("MOE_NVTX", "") == "1"
+
+
+def _traced(fn):
+    if not _NVTX:
+        return fn
+    import functools
+
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        torch.cuda.nvtx.range_push("moe_" + fn.__name__)
+        try:
+            return fn(*args, **kwargs)
+        finally:
+            torch.cuda.nvtx.range_pop()
+    return wrapper
+
+
 def _ok(fn: str, code: int):
     if code != 0:
         raise MoEError(fn, code)
@@ -179,6 +199,7 @@ def selftest_wait_timeout(stream=None):
 
 # --------------------------------------------------------------- compute ---
 
+@_traced
 def route(x, w_router, b_router, k: int, renorm: bool = True, *, topk_idx=None, topk_gate=None, prob_sum=None,
           ws=None, stream=None, n_group: int = 1, topk_group: int = 1, lse=None, logits=None):
     """Router (moe_route): returns (topk_idx [T,k] int32, topk_gate [T,k] f32, prob_sum [E] f32).
@@ -220,6 +241,7 @@ class Dispatched:
     rows_max: int
 
 
+@_traced
 def dispatch(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatched] = None, ws=None,
              stream=None, copy_rows: bool = True) -> Dispatched:
     """Capacity dispatch + row permutation (moe_dispatch).  With
@@ -244,6 +266,7 @@ def dispatch(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatch
     return out
 
 
+@_traced
 def dispatch_noalloc(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[Dispatched] = None,
                      stream=None) -> Dispatched:
     """moe_dispatch_noalloc: dispatch with the library's built-in scratch
@@ -267,6 +290,7 @@ def dispatch_noalloc(topk_idx, topk_gate, x, E: int, cap: int, *, out: Optional[
     return out
 
 
+@_traced
 def expert_up(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None, stream=None):
     E, _, d = w1.shape
     h = torch.empty((max(rows_max, 1), F), dtype=x_perm.dtype, device=x_perm.device) if h is None else h
@@ -275,6 +299,7 @@ def expert_up(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=N
     return h
 
 
+@_traced
 def expert_up_z(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None, z=None, stream=None):
     """moe_expert_up_z: h and the pre-activation z [rows, N1] (kept for the backward)."""
     E, N1, d = w1.shape
@@ -286,6 +311,7 @@ def expert_up_z(x_perm, offsets, kept, w1, F: int, act: str, rows_max: int, *, h
     return h, z
 
 
+@_traced
 def expert_up_gathered(x, row_token, offsets, kept, w1, F: int, act: str, rows_max: int, *, h=None,
                        stream=None):
     """moe_expert_up with the A rows read from x at row_token (no x_perm)."""
@@ -298,6 +324,7 @@ def expert_up_gathered(x, row_token, offsets, kept, w1, F: int, act: str, rows_m
     return h
 
 
+@_traced
 def expert_down(h, offsets, kept, w2, row_gate, rows_max: int, *, y_perm=None, stream=None):
     E, d, F = w2.shape
     y_perm = torch.empty((max(rows_max, 1), d), dtype=h.dtype, device=h.device) if y_perm is None else y_perm
@@ -306,6 +333,7 @@ def expert_down(h, offsets, kept, w2, row_gate, rows_max: int, *, y_perm=None, s
     return y_perm
 
 
+@_traced
 def expert_ffn(x_perm, offsets, kept, w1, w2, row_gate, act: str, rows_max: int, *, h=None, y_perm=None,
                stream=None):
     E, d, F = w2.shape
@@ -318,6 +346,7 @@ def expert_ffn(x_perm, offsets, kept, w1, w2, row_gate, act: str, rows_max: int,
     return h, y_perm
 
 
+@_traced
 def combine(y_perm, slot_row, *, y=None, stream=None):
     T, k = slot_row.shape
     d = y_perm.shape[1]
@@ -327,6 +356,7 @@ def combine(y_perm, slot_row, *, y=None, stream=None):
     return y
 
 
+@_traced
 def aux_loss(counts, prob_sum, T: int, alpha: float, *, loss=None, stream=None):
     E = counts.shape[0]
     loss = torch.empty(1, dtype=torch.float32, device=counts.device) if loss is None else loss
@@ -335,6 +365,7 @@ def aux_loss(counts, prob_sum, T: int, alpha: float, *, loss=None, stream=None):
     return loss
 
 
+@_traced
 def z_loss(lse, beta: float, *, loss=None, stream=None):
     """Router z-loss beta * mean_t lse[t]^2 (moe_z_loss); lse from route(..., lse=)."""
     loss = torch.empty(1, dtype=torch.float32, device=lse.device) if loss is None else loss
@@ -344,6 +375,7 @@ def z_loss(lse, beta: float, *, loss=None, stream=None):
 
 # --------------------------------------------------------------- backward ---
 
+@_traced
 def expert_dgrad_act(do_perm, offsets, kept, w2, z, act: str, rows_max: int, *, dz=None, stream=None):
     """dz = act'(z) * (do_perm . w2[e]) per kept row (moe_expert_dgrad_act)."""
     E, d, F = w2.shape
@@ -354,6 +386,7 @@ def expert_dgrad_act(do_perm, offsets, kept, w2, z, act: str, rows_max: int, *, 
     return dz
 
 
+@_traced
 def permute_rows(src, index, *, out=None, stream=None):
     """out[i] = src[index[i]] (moe_permute_rows); index int32 on the device."""
     n = index.shape[0]
@@ -364,6 +397,7 @@ def permute_rows(src, index, *, out=None, stream=None):
     return out
 
 
+@_traced
 def expert_dgrad(a, offsets, kept, w, rows_max: int, *, out=None, stream=None):
     """out [rows, N] = a[r] . w[e] per kept row r of expert e, w [E, K, N] as stored (moe_expert_dgrad)."""
     E, K, N = w.shape
@@ -373,6 +407,7 @@ def expert_dgrad(a, offsets, kept, w, rows_max: int, *, out=None, stream=None):
     return out
 
 
+@_traced
 def transpose_experts(w, *, out=None, stream=None):
     """w [E, R, C] -> [E, C, R] (moe_transpose_experts)."""
     E, R, C = w.shape
@@ -381,6 +416,7 @@ def transpose_experts(w, *, out=None, stream=None):
     return out
 
 
+@_traced
 def combine_bwd(dy, slot_row, row_gate, y_perm, *, do_perm=None, dgate=None, stream=None):
     """(do_perm [rows, d], dgate [T, k] f32) (moe_combine_bwd)."""
     T, k = slot_row.shape
@@ -392,6 +428,7 @@ def combine_bwd(dy, slot_row, row_gate, y_perm, *, do_perm=None, dgate=None, str
     return do_perm, dgate
 
 
+@_traced
 def act_bwd(z, da, offsets, F: int, act: str, rows_max: int, *, dz=None, stream=None):
     """dz [rows, N1] from the pre-activation z and da (moe_act_bwd)."""
     E = offsets.shape[0] - 1
@@ -405,6 +442,7 @@ def wgrad_cols(rows_max: int, E: int) -> int:
     return int(lib().moe_wgrad_cols(rows_max, E))
 
 
+@_traced
 def pack_segments_t(src, offsets, kept, rows_max: int, ld: int, *, out=None, stream=None):
     """src [rows, C] -> [C, ld], expert segments as zero-padded column blocks (moe_pack_segments_t)."""
     C = src.shape[1]
@@ -415,6 +453,7 @@ def pack_segments_t(src, offsets, kept, rows_max: int, ld: int, *, out=None, str
     return out
 
 
+@_traced
 def expert_wgrad(at, bt, kept, *, dw=None, dtype=torch.float32, stream=None):
     """dw [E, M, N] (fp32 or bf16) = per-expert at[:, seg] bt[:, seg]^T (moe_expert_wgrad)."""
     M, ld = at.shape
@@ -426,6 +465,7 @@ def expert_wgrad(at, bt, kept, *, dw=None, dtype=torch.float32, stream=None):
     return dw
 
 
+@_traced
 def route_bwd(logits, topk_idx, dgate, counts, renorm: bool, aux_coef: float, z_coef: float, *, dl=None,
               stream=None):
     """dl [T, E] f32, the gradient at the router logits (moe_route_bwd)."""
@@ -438,6 +478,7 @@ def route_bwd(logits, topk_idx, dgate, counts, renorm: bool, aux_coef: float, z_
     return dl
 
 
+@_traced
 def grad_x(dx_perm, slot_row, dl, w_router, *, dx=None, stream=None):
     """dx [T, d] (moe_grad_x)."""
     T, k = slot_row.shape
@@ -448,6 +489,7 @@ def grad_x(dx_perm, slot_row, dl, w_router, *, dx=None, stream=None):
     return dx
 
 
+@_traced
 def router_wgrad(dl, x, *, dW=None, db=None, ws=None, stream=None):
     """(dW [E, d] f32, db [E] f32) (moe_router_wgrad)."""
     T, E = dl.shape
