@@ -36,6 +36,8 @@ CASES = {
     "gelu_e32_norenorm": (C("gelu_e32_norenorm", 900, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False), 0.0,
                           True),
     "small_T": (C("small_T", 50, 128, 8, 2, 128, "swiglu", 1.25, "bf16"), 0.0, False),
+    "e256_top16": (C("e256_top16", 600, 128, 256, 16, 64, "swiglu", 0.0, "bf16"), 1e-3, False),
+    "min_d64_f64": (C("min_d64_f64", 3, 64, 2, 1, 64, "gelu", 0.0, "bf16"), 0.0, False),
 }
 
 

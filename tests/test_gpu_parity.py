@@ -34,6 +34,12 @@ SMALL = {
     "bf16_e160_top16": C("bf16_e160_top16", 300, 192, 160, 16, 128, "swiglu", 0.0, "bf16", renorm=False),
     # fewer tokens than one 128-row tile, and fewer kept rows than one GEMM tile
     "small_T": C("small_T", 50, 128, 8, 2, 128, "swiglu", 1.25, "bf16"),
+    # the largest expert count and top-k: 256 experts (CUDA-core router), top-16
+    "bf16_e256_top16": C("bf16_e256_top16", 600, 128, 256, 16, 64, "swiglu", 0.0, "bf16"),
+    # the smallest shapes: d = F = 64 (one K block, one half N tile), two experts, top-1, one token
+    "min_d64_f64": C("min_d64_f64", 1, 64, 2, 1, 64, "gelu", 0.0, "bf16"),
+    # fp32 layer with GELU and drops, two K blocks
+    "f32_gelu_e4": C("f32_gelu_e4", 333, 128, 4, 2, 192, "gelu", 1.0, "f32"),
 }
 
 
