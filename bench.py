@@ -155,27 +155,40 @@ class ClockSampler:
             time.sleep(self._period)
 
     def _run_smi(self):
+        """Fallback: one nvidia-smi process streaming a sample every 20 ms (its own child, ended by PID)."""
         import subprocess
         q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         sel = ["-i", "GPU-" + self._uuid if self._uuid and not self._uuid.startswith("GPU-") else self._uuid] \
             if self._uuid else []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        while not self._stop.is_set():
+        try:
+            proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                     "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:
+            self.err = f"{self.err}; nvidia-smi: {type(e).__name__}: {e}"
+            return
+        try:
+            while not self._stop.is_set():
+                line = proc.stdout.readline()
+                if not line:
+                    break
+                try:
+                    f = [v.strip() for v in line.split(",")]
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                    for name, v in zip(names, f[2:]):
+                        if v.lower().startswith("active"):
+                            self.reasons.add(name)
+                    self.ok = True
+                except (ValueError, IndexError):
+                    continue
+        finally:
+            proc.terminate()
             try:
-                out = subprocess.run(["nvidia-smi", *sel, f"--query-gpu={q}", "--format=csv,noheader,nounits"],
-                                     capture_output=True, text=True, timeout=5).stdout.strip().splitlines()
-                f = [v.strip() for v in out[0].split(",")]
-                self.samples.append(float(f[0]))
-                self.max_mhz = float(f[1])
-                for name, v in zip(names, f[2:]):
-                    if v.lower().startswith("active"):
-                        self.reasons.add(name)
-                self.ok = True
-            except Exception as e:
-                self.err = f"{self.err}; nvidia-smi: {type(e).__name__}: {e}"
-                return
-            time.sleep(0.05)
+                proc.wait(timeout=5)
+            except Exception:
+                proc.kill()
 
     def __enter__(self):
         target = self._run if self.ok else self._run_smi
@@ -222,7 +235,9 @@ def oracle_sample(cfg: synth.MoEConfig, ri, w1, w2, budget_s: float = 15.0, vari
 
     S = min(cfg.T, 8)
     t = run(S)
-    if t < budget_s / 4 and S < cfg.T:
+    for _ in range(3):   # grow the sample towards the budget (the cost is not linear in S)
+        if t >= budget_s / 2 or S >= cfg.T:
+            break
         S = int(min(cfg.T, max(S + 1, S * (budget_s / max(t, 1e-3)))))
         t = run(S)
     return {"value": S / t, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
