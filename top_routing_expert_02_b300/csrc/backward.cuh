@@ -332,10 +332,13 @@ grad_x_kernel(const void* __restrict__ dx_perm, const int32_t* __restrict__ slot
     for (int tk = 0; tk < GX_TOK; ++tk)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[tk][q] = 0.f;
+    // W rows two experts ahead of the FMAs that use them
     float4 wn = __ldg(reinterpret_cast<const float4*>(W + c));
+    float4 wnn = E > 1 ? __ldg(reinterpret_cast<const float4*>(W + (size_t)d + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int e = 0; e < E; ++e) {
-        const float4 w = wn;   // this expert's W row; the next one is fetched before the FMAs
-        if (e + 1 < E) wn = __ldg(reinterpret_cast<const float4*>(W + (size_t)(e + 1) * d + c));
+        const float4 w = wn;
+        wn = wnn;
+        if (e + 2 < E) wnn = __ldg(reinterpret_cast<const float4*>(W + (size_t)(e + 2) * d + c));
 #pragma unroll
         for (int t4 = 0; t4 < GX_TOK; t4 += 4) {
             const float4 l = *reinterpret_cast<const float4*>(&dlT[e][t4]);

@@ -387,12 +387,13 @@ int64_t moe_perm_rows_max(int64_t T, int k, int E, int64_t cap)
 }
 
 namespace {
-// Token splits of the router weight gradient: enough blocks for two waves.
+// Token splits of the router weight gradient: enough blocks for two waves
+// (at most 64 splits, at least 32 tokens each).
 int router_wgrad_splits(int64_t T, int E, int d)
 {
     const int base = ceil_div_i(d, bwd::RW_COLS) * ceil_div_i(E, bwd::RW_EXP);
     int S = ceil_div_i(2 * 148, base);
-    if (S > 16) S = 16;
+    if (S > 64) S = 64;
     const int maxS = ceil_div_i(T, 32);
     if (S > maxS) S = maxS;
     return S < 1 ? 1 : S;
