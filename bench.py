@@ -87,8 +87,8 @@ def plan_kwargs(args) -> dict:
     return kw
 
 
-BWD_KERNELS = 1 + 2 + 4 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs (act bwd fused), packs, wgrads,
-                                              # router bwd, dx, router weights (partial, sum, bias)
+BWD_KERNELS = 1 + 2 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs (act bwd fused), 2 weight-gradient
+                                      # GEMMs, router bwd, dx, router weights (partial, sum, bias)
 
 
 def variant_dict(args) -> dict:
@@ -554,7 +554,7 @@ def train_arm(args, cfg):
                        **plan_kwargs(args))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    phases = ["forward", "combine_bwd", "data_grad_gemms", "pack", "wgrad_dw2", "wgrad_dw1", "router_and_dx"]
+    phases = ["forward", "combine_bwd", "data_grad_gemms", "wgrad_dw2", "wgrad_dw1", "router_and_dx"]
 
     def step(evs=None):
         def mark(name):

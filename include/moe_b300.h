@@ -24,7 +24,8 @@
  * item 3 returns the gradients by the reverse exchange; the pages give no
  * formula, so each call computes a derivative of the forward):
  *   moe_combine_bwd, moe_act_bwd, moe_route_bwd, moe_grad_x,
- *   moe_router_wgrad, moe_expert_wgrad (+ moe_pack_segments_t),
+ *   moe_router_wgrad, moe_expert_wgrad_rows (or moe_expert_wgrad on the
+ *   packed transposes of moe_pack_segments_t),
  *   moe_expert_dgrad (the data-gradient GEMMs, B operand MN-major) and
  *   moe_expert_up_z (the forward keeping the pre-activation).
  *
@@ -282,8 +283,9 @@ moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_
  *   dz               = moe_expert_dgrad_act(do_perm, ..., w2, z)  (the da GEMM
  *                      with moe_act_bwd in its epilogue; identity: moe_expert_dgrad)
  *   dx_perm          = moe_expert_dgrad(dz, ..., K = N1, N = d, w1)
- *   dw2[e]           = moe_expert_wgrad(pack(do_perm), pack(h), M = d, N = F)
- *   dw1[e]           = moe_expert_wgrad(pack(dz), pack(x_perm), M = N1, N = d)
+ *   dw2[e]           = moe_expert_wgrad_rows(do_perm, h, M = d, N = F)
+ *   dw1[e]           = moe_expert_wgrad_rows(dz, x_perm, M = N1, N = d)
+ *                      (or moe_expert_wgrad on moe_pack_segments_t copies)
  *   dl               = moe_route_bwd(logits, topk_idx, dgate, counts, ...)
  *   dx               = moe_grad_x(dx_perm, slot_row, dl, w_router)
  *   dW, db           = moe_router_wgrad(dl, x)                                */
@@ -348,6 +350,20 @@ moe_status moe_pack_segments_t(const void* src, const int32_t* offsets, const in
  * rounding).  M % 64 == 0, N % 64 == 0, ld % 64 == 0. */
 moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept, int E, int M, int N, int64_t ld,
                             moe_dtype dtype, void* dw, moe_dtype dw_dtype, moe_stream_t stream);
+
+/* The same weight gradient read straight from the row-major activations (no
+ * packed copies):
+ *   dw[e] = sum over rows r in [offsets[e], offsets[e] + kept[e]) of
+ *           a[r, :]^T b[r, :]                   [E, M, N], fp32 accumulation
+ * a [rows_max, M] and b [rows_max, N] (dtype bf16): do_perm and h give dw2
+ * (M = d, N = F), dz and x_perm give dw1 (M = N1, N = d).  Only the rows of
+ * the segments are read into the sums; rows between or past them may hold
+ * anything.  An expert with no rows (and every expert when rows_max == 0)
+ * gets zeros.  dw_dtype MOE_F32 or MOE_BF16 (one rounding).  M % 64 == 0,
+ * N % 64 == 0; offsets[e] + kept[e] <= rows_max. */
+moe_status moe_expert_wgrad_rows(const void* a, const void* b, const int32_t* offsets, const int32_t* kept, int E,
+                                 int M, int N, int64_t rows_max, moe_dtype dtype, void* dw, moe_dtype dw_dtype,
+                                 moe_stream_t stream);
 
 /* Router backward to the logits, per token (logits [T, E] from moe_route_ex,
  * topk_idx and dgate [T, k], counts [E] = f_e * T: counts for the pre-drop

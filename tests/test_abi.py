@@ -156,6 +156,12 @@ def test_backward_argument_errors():
     assert L.moe_pack_segments_t(FAKE, FAKE, FAKE, 8, 128, 5120, 5000, 1, FAKE, None) == 1   # ld too small
     assert L.moe_expert_wgrad(FAKE, FAKE, FAKE, 8, 100, 128, 5632, 1, FAKE, 0, None) == 2   # M % 64
     assert L.moe_expert_wgrad(FAKE, FAKE, FAKE, 8, 128, 128, 5632, 1, FAKE, 5, None) == 1   # bad output type
+    assert L.moe_expert_wgrad_rows(FAKE, FAKE, FAKE, FAKE, 8, 100, 128, 640, 1, FAKE, 0, None) == 2   # M % 64
+    assert L.moe_expert_wgrad_rows(FAKE, FAKE, FAKE, FAKE, 8, 128, 96, 640, 1, FAKE, 0, None) == 2    # N % 64
+    assert L.moe_expert_wgrad_rows(FAKE, FAKE, None, FAKE, 8, 128, 128, 640, 1, FAKE, 0, None) == 1   # no offsets
+    assert L.moe_expert_wgrad_rows(None, FAKE, FAKE, FAKE, 8, 128, 128, 640, 1, FAKE, 0, None) == 1   # rows, no a
+    assert L.moe_expert_wgrad_rows(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, -1, 1, FAKE, 0, None) == 1    # rows < 0
+    assert L.moe_expert_wgrad_rows(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, 640, 0, FAKE, 0, None) == 2   # fp32 inputs
     assert L.moe_route_bwd(FAKE, FAKE, FAKE, None, 16, 8, 2, 1, f(0.1), f(0.0), FAKE, None) == 1
     assert L.moe_route_bwd(FAKE, FAKE, FAKE, FAKE, 16, 8, 9, 1, f(0.1), f(0.0), FAKE, None) == 1
     assert L.moe_grad_x(FAKE, FAKE, FAKE, None, 16, 2, 8, 128, 1, FAKE, None) == 1
@@ -178,5 +184,6 @@ def test_misaligned_buffers_are_refused_before_any_work():
     assert L.moe_combine_bwd(FAKE, FAKE, FAKE, FAKE, 16, 2, 128, 1, MIS, FAKE, None) == 2
     assert L.moe_expert_dgrad(FAKE, FAKE, FAKE, 8, 128, 128, 1, MIS, 10, FAKE, None) == 2
     assert L.moe_expert_wgrad(FAKE, MIS, FAKE, 8, 128, 128, 5632, 1, FAKE, 0, None) == 2
+    assert L.moe_expert_wgrad_rows(FAKE, MIS, FAKE, FAKE, 8, 128, 128, 640, 1, FAKE, 0, None) == 2
     assert L.moe_pack_segments_t(MIS, FAKE, FAKE, 8, 128, 10, 576, 1, FAKE, None) == 2
     assert L.moe_grad_x(MIS, FAKE, FAKE, FAKE, 16, 2, 8, 128, 1, FAKE, None) == 2

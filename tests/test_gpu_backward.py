@@ -165,6 +165,61 @@ def test_expert_wgrad_against_torch_per_expert():
         col += (n + 63) // 64 * 64
 
 
+def test_expert_wgrad_rows_against_torch_and_packed():
+    """dw[e] = a[seg]^T b[seg] read straight from row-major a [rows, M], b [rows, N]:
+    against torch fp32 and bit for bit against the packed-transpose path (the
+    same products in the same order).  The segments leave gaps and a tail that
+    hold NaN, so a partial 64-row block that read past its segment would show;
+    M % 128 == 64, N % 256 == 64, an empty expert, segments of 1, 64 and 65 rows."""
+    g = torch.Generator(device="cuda").manual_seed(16)
+    kept_l = [100, 0, 300, 64, 1, 65]
+    gaps = [3, 7, 0, 5, 2, 1]
+    E, M, N = len(kept_l), 192, 320
+    offs, pos = [], 0
+    for n, gp in zip(kept_l, gaps):
+        pos += gp
+        offs.append(pos)
+        pos += n
+    R = pos + 37   # NaN rows past the last segment
+    a = torch.full((R, M), float("nan"), dtype=torch.bfloat16, device="cuda")
+    b = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for o, n in zip(offs, kept_l):
+        a[o:o + n] = torch.randn(n, M, device="cuda", generator=g).to(torch.bfloat16)
+        b[o:o + n] = torch.randn(n, N, device="cuda", generator=g).to(torch.bfloat16)
+    offsets = torch.tensor(offs + [pos], dtype=torch.int32, device="cuda")
+    kept = torch.tensor(kept_l, dtype=torch.int32, device="cuda")
+    dw = moe.expert_wgrad_rows(a, b, offsets, kept, R)
+    dwb = moe.expert_wgrad_rows(a, b, offsets, kept, R, dtype=torch.bfloat16)
+    # the packed path on the same segments (gap-free copies)
+    cont = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    cont[1:] = torch.cumsum(kept, 0)
+    A = int(cont[-1])
+    ac = torch.cat([a[o:o + n] for o, n in zip(offs, kept_l)])
+    bc = torch.cat([b[o:o + n] for o, n in zip(offs, kept_l)])
+    ld = moe.wgrad_cols(A, E)
+    dwp = moe.expert_wgrad(moe.pack_segments_t(ac, cont, kept, A, ld), moe.pack_segments_t(bc, cont, kept, A, ld),
+                           kept)
+    moe.check()
+    assert bool(torch.isfinite(dw).all())
+    for e, (o, n) in enumerate(zip(offs, kept_l)):
+        ref = a[o:o + n].float().T @ b[o:o + n].float()
+        assert torch.allclose(dw[e], ref, rtol=1e-4, atol=1e-3), e
+        assert torch.equal(dwb[e], dw[e].to(torch.bfloat16)), e
+    assert torch.equal(dw, dwp)
+
+
+def test_expert_wgrad_rows_no_rows_gives_zeros():
+    kept = torch.zeros(3, dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(4, dtype=torch.int32, device="cuda")
+    a = torch.full((1, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    b = torch.full((1, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for rows_max in (0, 1):   # no buffer rows at all / rows but empty segments
+        dw = torch.full((3, 64, 128), 5.0, device="cuda")
+        moe.expert_wgrad_rows(a, b, offsets, kept, rows_max, dw=dw)
+        moe.check()
+        assert bool((dw == 0).all()), rows_max
+
+
 @pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot"])
 def test_kept_pre_activation_equals_recompute(name):
     """The z that the training forward keeps (moe_expert_up_z) is bit for bit

@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
     "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "expert_dgrad_act", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
-    "pack_segments_t", "expert_wgrad", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
+    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
@@ -79,6 +79,7 @@ _SIGS = {
     "moe_wgrad_cols": (_I64, [_I64, _I32]),
     "moe_pack_segments_t": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I64, _I32, _P, _P]),
     "moe_expert_wgrad": (_I32, [_P, _P, _P, _I32, _I32, _I32, _I64, _I32, _P, _I32, _P]),
+    "moe_expert_wgrad_rows": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _I32, _P, _I32, _P]),
     "moe_route_bwd": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _F, _F, _P, _P]),
     "moe_grad_x": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_router_wgrad": (_I32, [_P, _P, _I32, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
@@ -466,6 +467,19 @@ def expert_wgrad(at, bt, kept, *, dw=None, dtype=torch.float32, stream=None):
 
 
 @_traced
+def expert_wgrad_rows(a, b, offsets, kept, rows_max: int, *, dw=None, dtype=torch.float32, stream=None):
+    """dw [E, M, N] (fp32 or bf16) = per-expert a[seg]^T b[seg] over the row
+    segments [offsets[e], offsets[e] + kept[e]) of a [rows, M], b [rows, N]
+    (moe_expert_wgrad_rows)."""
+    M, N = a.shape[1], b.shape[1]
+    E = kept.shape[0]
+    dw = torch.empty((E, M, N), dtype=dtype, device=a.device) if dw is None else dw
+    _ok("moe_expert_wgrad_rows", lib().moe_expert_wgrad_rows(_ptr(a), _ptr(b), _ptr(offsets), _ptr(kept), E, M, N,
+                                                             rows_max, _dt(a), _ptr(dw), _dt(dw), _stream(stream)))
+    return dw
+
+
+@_traced
 def route_bwd(logits, topk_idx, dgate, counts, renorm: bool, aux_coef: float, z_coef: float, *, dl=None,
               stream=None):
     """dl [T, E] f32, the gradient at the router logits (moe_route_bwd)."""
@@ -626,15 +640,12 @@ class MoEPlan:
             T, d, E, k, F = self.T, self.d, self.E, self.k, self.F
             R = max(self.rows_max, 1)
             N1 = 2 * F if self.act == "swiglu" else F
-            ld = wgrad_cols(self.rows_max, E)
             bf = dict(dtype=torch.bfloat16, device=dev)
             f32 = dict(dtype=torch.float32, device=dev)
             self._bwd = dict(
                 do_perm=torch.empty((R, d), **bf), dgate=torch.empty((max(T, 1), k), **f32),
                 dz=torch.empty((R, N1), **bf),
-                dx_perm=torch.empty((R, d), **bf), ld=ld,
-                doT=torch.empty((d, ld), **bf), hT=torch.empty((F, ld), **bf), dzT=torch.empty((N1, ld), **bf),
-                xT=torch.empty((d, ld), **bf),
+                dx_perm=torch.empty((R, d), **bf),
                 dw1=torch.empty((E, N1, d), dtype=self.grad_dtype, device=dev),
                 dw2=torch.empty((E, d, F), dtype=self.grad_dtype, device=dev),
                 dl=torch.empty((max(T, 1), E), **f32), dx=torch.empty((max(T, 1), d), **bf),
@@ -665,16 +676,10 @@ class MoEPlan:
             expert_dgrad_act(B["do_perm"], D.offsets, D.kept, w2, self.z, self.act, R, dz=B["dz"], stream=stream)
         expert_dgrad(B["dz"], D.offsets, D.kept, w1, R, out=B["dx_perm"], stream=stream)
         mark("data_grad_gemms")
-        # weight gradients on segment-packed transposes
-        ld = B["ld"]
-        pack_segments_t(B["do_perm"], D.offsets, D.kept, R, ld, out=B["doT"], stream=stream)
-        pack_segments_t(self.h, D.offsets, D.kept, R, ld, out=B["hT"], stream=stream)
-        pack_segments_t(B["dz"], D.offsets, D.kept, R, ld, out=B["dzT"], stream=stream)
-        pack_segments_t(D.x_perm, D.offsets, D.kept, R, ld, out=B["xT"], stream=stream)
-        mark("pack")
-        expert_wgrad(B["doT"], B["hT"], D.kept, dw=B["dw2"], stream=stream)
+        # weight gradients straight from the row-major activations
+        expert_wgrad_rows(B["do_perm"], self.h, D.offsets, D.kept, R, dw=B["dw2"], stream=stream)
         mark("wgrad_dw2")
-        expert_wgrad(B["dzT"], B["xT"], D.kept, dw=B["dw1"], stream=stream)
+        expert_wgrad_rows(B["dz"], D.x_perm, D.offsets, D.kept, R, dw=B["dw1"], stream=stream)
         mark("wgrad_dw1")
         # router
         counts = D.kept if self.aux_post_drop else D.counts

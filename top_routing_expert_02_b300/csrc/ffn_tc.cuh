@@ -102,7 +102,15 @@ struct Args {
 //                to 64, zero padded); every expert has m_tiles M-tiles; the
 //                output is fp32 or bf16 [E, M, N] (zeros for an expert with
 //                no rows)
-enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2, MODE_BMN = 3 };
+//   MODE_WGRAD_ROWS  weight gradients straight from the row-major activations:
+//                A [rows, M] and B [rows, N] are both read MN-major (two and
+//                four 64x64 boxes per stage, rows = K); expert e contracts over
+//                rows [offsets[e], offsets[e] + kept[e]) in blocks of 64 rows.
+//                The rows of a last, partial block that lie past the segment
+//                are zeroed in shared memory by the MMA warp before its MMAs
+//                read the stage, so neighbouring segments or unwritten rows
+//                never leak in; output as MODE_WGRAD
+enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2, MODE_BMN = 3, MODE_WGRAD_ROWS = 4 };
 
 __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tiles, int tile, int& e, int& m,
                                             int& n)
@@ -148,13 +156,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const Args g)
 {
-    constexpr bool GATHER = MODE == MODE_GATHER, WGRAD = MODE == MODE_WGRAD, BMN = MODE == MODE_BMN;
-    static_assert(!BMN || BN == 256, "MN-major B is staged as four 64-column boxes");
+    constexpr bool GATHER = MODE == MODE_GATHER, BMN = MODE == MODE_BMN, WGR = MODE == MODE_WGRAD_ROWS;
+    constexpr bool WGRAD = MODE == MODE_WGRAD || WGR;   // weight-gradient tiles and epilogue
+    static_assert(!(BMN || WGR) || BN == 256, "MN-major B is staged as four 64-column boxes");
     using SH = Shape<BN>;
     constexpr int STAGES = WGRAD ? SH::WG_STAGES : SH::STAGES;
     constexpr int STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
     constexpr int ACC_COLS = SH::ACC_COLS, TMEM_COLS = SH::TMEM_COLS;
-    constexpr uint32_t IDESC = BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
+    constexpr int BOX_BYTES = BK * 128;   // one 64x64 bf16 box
+    constexpr uint32_t IDESC = WGR ? ptx::idesc_bf16_f32(128, BN, true, true)
+                               : BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
@@ -215,6 +226,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int rowB1 = rowB0 + g.half_off;
                 const int kb0 = WGRAD ? kstart[e] : 0;
                 const int nkt = WGRAD ? kstart[e + 1] - kb0 : nk;
+                const int rowK0 = WGR ? __ldg(g.offsets + e) : 0;   // first row of the expert's segment
                 if (GATHER) gather_offsets(g, mstart, tile, lane, roff);
                 for (int kb = 0; kb < nkt; ++kb) {
                     bool got = true;
@@ -229,16 +241,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(fb, GATHER ? 2 * BH_BYTES : STAGE_BYTES);
                         const int kx = (kb0 + kb) * BK;
-                        if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kx, rowA);
-                        if (BMN) {
-                            // B rows e*K + kx.. (K), columns n*BN + 64j.. (N): four 64x64 boxes
+                        if (WGR) {
+                            // rows rowK0 + 64 kb.. (K); A columns m*128.. (M), B columns n*256.. (N)
+                            const int ky = rowK0 + kb * BK;
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) ptx::tma_load_2d(sa + j * BOX_BYTES, &tmA, fb, m * BM + 64 * j, ky);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                ptx::tma_load_2d(sa + A_BYTES + j * (BK * 128), &tmB, fb, n * BN + 64 * j,
-                                                 e * g.K + kx);
+                                ptx::tma_load_2d(sa + A_BYTES + j * BOX_BYTES, &tmB, fb, n * BN + 64 * j, ky);
                         } else {
-                            ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, rowB0);
-                            ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kx, rowB1);
+                            if (!GATHER) ptx::tma_load_2d(sa, &tmA, fb, kx, rowA);
+                            if (BMN) {
+                                // B rows e*K + kx.. (K), columns n*BN + 64j.. (N): four 64x64 boxes
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    ptx::tma_load_2d(sa + A_BYTES + j * BOX_BYTES, &tmB, fb, n * BN + 64 * j,
+                                                     e * g.K + kx);
+                            } else {
+                                ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, rowB0);
+                                ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kx, rowB1);
+                            }
                         }
                     }
                     if (GATHER) {
@@ -274,53 +296,77 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         __syncwarp();   // reconverge before the block-wide barrier below
     } else if (warp == 1) {
-        if (lane == 0) {
+        // lane 0 issues the MMAs; in MODE_WGRAD_ROWS the whole warp runs the
+        // loop (every lane waits and votes) to zero the tails of partial blocks
+        if (lane == 0 || WGR) {
+            auto wait = [&](uint64_t* bar, uint32_t par) {
+                const bool w = ptx::mbar_wait(ptx::smem_u32(bar), par, limit);
+                return WGR ? __all_sync(0xffffffffu, w) : w;
+            };
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), aphase ^ 1u, limit)) {
+                if (!wait(&tempty_bar[acc], aphase ^ 1u)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
-                int nkt = nk;
+                int nkt = nk, kept_e = 0;
                 if (WGRAD) {
                     int e, m, n;
                     decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
                     nkt = kstart[e + 1] - kstart[e];   // 0: nothing accumulates, the epilogue writes zeros
+                    if (WGR) kept_e = __ldg(g.kept + e);
                 }
                 for (int kb = 0; kb < nkt; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, limit)) {
+                    if (!wait(&full_bar[stage], phase)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    if (GATHER) ptx::fence_proxy_async_smem();   // the A tile came through the generic proxy
                     const uint32_t sa = smem0 + stage * STAGE_BYTES, sb = sa + A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // K-major B: 16 K columns = 32 bytes on; MN-major B: 16 K rows = 2048 bytes on
-                        const uint64_t bdesc = BMN ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, BK * 128)
-                                                   : ptx::sdesc_kmajor_sw128(sb + kk * 32);
-                        ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), bdesc, IDESC, (kb | kk) != 0);
+                    if (WGR) {
+                        const int valid = kept_e - kb * BK;   // rows of this block inside the segment (>= 1)
+                        if (valid < BK) {
+                            // rows [valid, 64) of the six boxes are whole 128-byte lines: zero them
+                            for (int b6 = 0; b6 < 6; ++b6)
+                                for (int c = valid * 8 + lane; c < BK * 8; c += 32)
+                                    ptx::st_shared_v4(sa + b6 * BOX_BYTES + c * 16, 0u, 0u, 0u, 0u);
+                            ptx::fence_proxy_async_smem();   // generic writes before the MMAs read them
+                        }
+                        __syncwarp();
                     }
-                    ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+                    if (lane == 0) {
+                        if (GATHER) ptx::fence_proxy_async_smem();   // the A tile came through the generic proxy
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            // K-major: 16 K columns = 32 bytes on; MN-major: 16 K rows = 2048 bytes on
+                            const uint64_t adesc = WGR ? ptx::sdesc_mnmajor_sw128(sa + kk * 2048, BOX_BYTES)
+                                                       : ptx::sdesc_kmajor_sw128(sa + kk * 32);
+                            const uint64_t bdesc = (BMN || WGR) ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, BOX_BYTES)
+                                                                : ptx::sdesc_kmajor_sw128(sb + kk * 32);
+                            ptx::mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
+                        }
+                        ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(ptx::smem_u32(&tfull_bar[acc]));
+                if (lane == 0) ptx::mma_commit(ptx::smem_u32(&tfull_bar[acc]));
                 acc ^= 1;
                 if (acc == 0) aphase ^= 1u;
             }
-            if (!ok) moe_flag(MOE_DEV_TIMEOUT);
-            // no MMA may still write TMEM when the block frees it
-            ptx::mma_commit(ptx::smem_u32(&drain_bar));
-            if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, limit)) moe_flag(MOE_DEV_TIMEOUT);
+            if (lane == 0) {
+                if (!ok) moe_flag(MOE_DEV_TIMEOUT);
+                // no MMA may still write TMEM when the block frees it
+                ptx::mma_commit(ptx::smem_u32(&drain_bar));
+                if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, limit)) moe_flag(MOE_DEV_TIMEOUT);
+            }
         }
         __syncwarp();   // reconverge before the block-wide barrier below
     } else {

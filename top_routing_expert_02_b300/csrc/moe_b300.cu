@@ -230,27 +230,35 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
                         tcg::Args args, cudaStream_t stream, long long A_rows = -1)
 {
     using SH = tcg::Shape<BN>;
+    constexpr bool wg = MODE == tcg::MODE_WGRAD || MODE == tcg::MODE_WGRAD_ROWS;
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16_box(&ta, A, (unsigned long long)(A_rows >= 0 ? A_rows : rows_max), (unsigned long long)K,
-                            MODE == tcg::MODE_GATHER ? 1 : 128))
+    if (MODE == tcg::MODE_WGRAD_ROWS) {
+        // A [rows_max, M] and B [rows_max, N], both read as 64x64 boxes (rows = K)
+        if (!make_tmap_bf16_box(&ta, A, (unsigned long long)rows_max, (unsigned long long)args.m_rows, 64) ||
+            !make_tmap_bf16_box(&tb, W, (unsigned long long)rows_max, (unsigned long long)args.out_cols, 64))
+            return MOE_ERR_CUDA;
+    } else if (!make_tmap_bf16_box(&ta, A, (unsigned long long)(A_rows >= 0 ? A_rows : rows_max),
+                                   (unsigned long long)K, MODE == tcg::MODE_GATHER ? 1 : 128)) {
         return MOE_ERR_CUDA;
+    }
     if (MODE == tcg::MODE_BMN) {   // B [E*K rows, N cols], N contiguous: 64x64 boxes
         if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)args.out_cols, 64))
             return MOE_ERR_CUDA;
-    } else if (!make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2)) {
+    } else if (MODE != tcg::MODE_WGRAD_ROWS &&
+               !make_tmap_bf16_box(&tb, W, (unsigned long long)w_rows_total, (unsigned long long)K, BN / 2)) {
         return MOE_ERR_CUDA;
     }
     CUtensorMap tc;
     memset(&tc, 0, sizeof tc);
-    if (MODE == tcg::MODE_WGRAD) {
+    if (wg) {
         const unsigned long long rows = (unsigned long long)args.E * args.m_rows, cols = args.out_cols;
         if (args.out_f32 ? !make_tmap_f32_out(&tc, args.out_f32, rows, cols)
                          : !make_tmap_bf16_box(&tc, args.out, rows, cols, 32))
             return MOE_ERR_CUDA;
     }
-    const int smem = MODE == tcg::MODE_WGRAD ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
+    const int smem = wg ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
     if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, smem)) return launch_status();
-    const long long max_tiles = MODE == tcg::MODE_WGRAD
+    const long long max_tiles = wg
                                     ? (long long)args.E * args.m_tiles * args.n_tiles
                                     : ((rows_max + tcg::BM - 1) / tcg::BM + args.E) * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
@@ -1033,6 +1041,39 @@ moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept,
     a.out = dw_dtype == MOE_BF16 ? (uint16_t*)dw : nullptr;
     a.wait_limit = g_wait_limit.load();
     return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD>(at, 0, (int)ld, bt, N, a, (cudaStream_t)stream, M);
+}
+
+moe_status moe_expert_wgrad_rows(const void* a, const void* b, const int32_t* offsets, const int32_t* kept, int E,
+                                 int M, int N, int64_t rows_max, moe_dtype dtype, void* dw, moe_dtype dw_dtype,
+                                 moe_stream_t stream)
+{
+    if (E < 1 || E > MAX_E || M <= 0 || N <= 0 || rows_max < 0 || !offsets || !kept || !dw || !dtype_ok(dtype) ||
+        !dtype_ok(dw_dtype))
+        return MOE_ERR_INVALID_ARG;
+    if (rows_max > 0 && (!a || !b)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || M % 64 || N % 64 || rows_max >= INT_MAX)
+        return MOE_ERR_UNSUPPORTED;
+    if (!all_aligned16({a, b, dw})) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (rows_max == 0) {   // no rows: every expert's gradient is zero
+        const size_t bytes = (size_t)E * M * N * (dw_dtype == MOE_F32 ? 4 : 2);
+        return cudaMemsetAsync(dw, 0, bytes, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    tcg::Args g{};
+    g.offsets = offsets;
+    g.kept = kept;
+    g.E = E;
+    g.K = 0;
+    g.m_tiles = (M + 127) / 128;
+    g.m_rows = M;
+    g.n_step = 256;
+    g.half_off = 128;
+    g.n_tiles = (N + 255) / 256;
+    g.out_cols = N;
+    g.out_f32 = dw_dtype == MOE_F32 ? (float*)dw : nullptr;
+    g.out = dw_dtype == MOE_BF16 ? (uint16_t*)dw : nullptr;
+    g.wait_limit = g_wait_limit.load();
+    return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD_ROWS>(a, rows_max, 0, b, 0, g, st);
 }
 
 moe_status moe_route_bwd(const float* logits, const int32_t* topk_idx, const float* dgate, const int32_t* counts,

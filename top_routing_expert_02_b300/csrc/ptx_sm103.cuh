@@ -272,13 +272,14 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major unless
-// b_mn_major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false)
+// Instruction descriptor, kind::f16: bf16 A and B (each K-major unless its
+// *_mn_major flag is set), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false, bool a_mn_major = false)
 {
     return (1u << 4)                        // D format f32
            | (1u << 7)                      // A format bf16
            | (1u << 10)                     // B format bf16
+           | ((a_mn_major ? 1u : 0u) << 15) // A major-ness: 1 = MN-major
            | ((b_mn_major ? 1u : 0u) << 16) // B major-ness: 1 = MN-major
            | ((uint32_t)(N >> 3) << 17)     // N / 8
            | ((uint32_t)(M >> 4) << 24);    // M / 16
