@@ -87,8 +87,8 @@ def plan_kwargs(args) -> dict:
     return kw
 
 
-BWD_KERNELS = 1 + 2 + 2 + 1 + 1 + 3   # combine bwd, 2 data-gradient GEMMs (act bwd fused), 2 weight-gradient
-                                      # GEMMs, router bwd, dx, router weights (partial, sum, bias)
+BWD_KERNELS = 1 + 2 + 2 + 1 + 6   # combine bwd, 2 data-gradient GEMMs (act bwd fused), 2 weight-gradient GEMMs,
+                                  # router bwd, router grads (prep, dl.W GEMM, dx gather, dW GEMM, dW sum, db)
 
 
 def variant_dict(args) -> dict:

@@ -23,8 +23,8 @@
  * tutorial's §5.1 aux loss acts through its gradient, and the guide's 步骤三
  * item 3 returns the gradients by the reverse exchange; the pages give no
  * formula, so each call computes a derivative of the forward):
- *   moe_combine_bwd, moe_act_bwd, moe_route_bwd, moe_grad_x,
- *   moe_router_wgrad, moe_expert_wgrad_rows (or moe_expert_wgrad on the
+ *   moe_combine_bwd, moe_act_bwd, moe_route_bwd, moe_router_grads (or
+ *   moe_grad_x + moe_router_wgrad), moe_expert_wgrad_rows (or moe_expert_wgrad on the
  *   packed transposes of moe_pack_segments_t),
  *   moe_expert_dgrad (the data-gradient GEMMs, B operand MN-major) and
  *   moe_expert_up_z (the forward keeping the pre-activation).
@@ -85,7 +85,13 @@ typedef enum {
     MOE_ACT_IDENTITY = 2   /* h = z; for checks (identity experts)                 */
 } moe_act;
 
-typedef enum { MOE_CALL_ROUTE = 0, MOE_CALL_DISPATCH = 1, MOE_CALL_FFN = 2, MOE_CALL_ROUTER_WGRAD = 3 } moe_call;
+typedef enum {
+    MOE_CALL_ROUTE = 0,
+    MOE_CALL_DISPATCH = 1,
+    MOE_CALL_FFN = 2,
+    MOE_CALL_ROUTER_WGRAD = 3,
+    MOE_CALL_ROUTER_GRADS = 4
+} moe_call;
 
 /* ---------------------------------------------------------------- host --- */
 
@@ -287,8 +293,8 @@ moe_status moe_z_loss(const float* lse, int64_t T, float beta, float* loss, moe_
  *   dw1[e]           = moe_expert_wgrad_rows(dz, x_perm, M = N1, N = d)
  *                      (or moe_expert_wgrad on moe_pack_segments_t copies)
  *   dl               = moe_route_bwd(logits, topk_idx, dgate, counts, ...)
- *   dx               = moe_grad_x(dx_perm, slot_row, dl, w_router)
- *   dW, db           = moe_router_wgrad(dl, x)                                */
+ *   dx, dW, db       = moe_router_grads(dx_perm, slot_row, dl, w_router, x)
+ *                      (tensor cores; or moe_grad_x + moe_router_wgrad)       */
 
 /* Data-gradient GEMM on the weights as stored (no transposed copy):
  *   out[r, n] = sum_k a[r, k] * w[e][k][n]   for kept rows r of expert e
@@ -390,6 +396,23 @@ moe_status moe_grad_x(const void* dx_perm, const int32_t* slot_row, const float*
  * moe_workspace_bytes(MOE_CALL_ROUTER_WGRAD, T, d, E, ...) bytes; T >= 1;
  * d % 64 == 0 and x 16-byte aligned (else UNSUPPORTED). */
 moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64_t T, int E, int d, float* dW,
+                            float* db, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The input gradient and the router weight gradient of moe_grad_x and
+ * moe_router_wgrad in one call, their two contractions on the tensor cores:
+ *   dx[t] = rn(sum_e dl[t, e] w_router[e] + sum over kept j of dx_perm[slot_row[t, j]])
+ *   dW    = dl^T x   (fp32 [E, d]),   db[e] = sum_t dl[t, e]   (fp32 [E])
+ * The fp32 dl and w_router enter the bf16 MMAs as hi + lo parts (hi = rn(v),
+ * lo = rn(v - hi)): dl . W takes hi.hi + lo.hi + hi.lo, dl^T x takes
+ * hi + lo (x is bf16), fp32 accumulation; the relative error of the parts
+ * is ~2^-17, far below dx's bf16 rounding.  Sums run in a fixed order
+ * (bitwise reproducible).  dtype (x, dx_perm, dx) MOE_BF16; d % 64 == 0;
+ * 16-byte aligned x, dx_perm, w_router, dx, dW, ws.  ws >=
+ * moe_workspace_bytes(MOE_CALL_ROUTER_GRADS, T, d, E, ...) bytes (it holds
+ * the bf16 parts, the fp32 dl . W and the split weight-gradient partials).
+ * T == 0 zeroes dW and db. */
+moe_status moe_router_grads(const void* dx_perm, const int32_t* slot_row, const float* dl, const float* w_router,
+                            const void* x, int64_t T, int k, int E, int d, moe_dtype dtype, void* dx, float* dW,
                             float* db, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------- no-allocation variant --- */

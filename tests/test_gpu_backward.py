@@ -208,6 +208,65 @@ def test_expert_wgrad_rows_against_torch_and_packed():
     assert torch.equal(dw, dwp)
 
 
+def _router_grad_inputs(T, E, k, d, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    R = T * k + 7
+    dx_perm = torch.randn(R, d, device="cuda", generator=g).to(torch.bfloat16)
+    slot_row = torch.randperm(R, device="cuda", generator=g)[:T * k].view(T, k).to(torch.int32)
+    drop = torch.rand(T, k, device="cuda", generator=g) < 0.2
+    slot_row[drop] = -1
+    dl = torch.randn(T, E, device="cuda", generator=g) * 1e-2
+    W = torch.randn(E, d, device="cuda", generator=g) * 0.05
+    x = torch.randn(T, d, device="cuda", generator=g).to(torch.bfloat16)
+    return dx_perm, slot_row.contiguous(), dl, W, x
+
+
+def _router_grad_refs(dx_perm, slot_row, dl, W, x):
+    """fp64 torch: dx = sum of the kept dx_perm rows + dl W, dW = dl^T x, db = sum_t dl."""
+    T, k = slot_row.shape
+    rows = dx_perm.double()
+    gath = torch.where((slot_row >= 0)[..., None], rows[slot_row.clamp(min=0).long()], torch.zeros((), dtype=torch.float64,
+                                                                                             device="cuda"))
+    dx = gath.sum(1) + dl.double() @ W.double()
+    return dx, dl.double().T @ x.double(), dl.double().sum(0)
+
+
+@pytest.mark.parametrize("T,E,k,d", [(1000, 8, 2, 256), (777, 128, 8, 128), (300, 256, 16, 64), (4097, 64, 2, 512)])
+def test_router_grads_on_tensor_cores(T, E, k, d):
+    """moe_router_grads (bf16 hi/lo parts on the tensor cores) against fp64:
+    dx within one bf16 rounding, dW and db to fp32 accuracy; the CUDA-core
+    pair moe_grad_x + moe_router_wgrad against the same references; both
+    bitwise reproducible.  The shapes cover E = 8 (padded to 64), E = 256
+    with top-16, d = 64 (one partial N tile) and ragged token splits."""
+    dx_perm, slot_row, dl, W, x = _router_grad_inputs(T, E, k, d, T + E)
+    dx, dW, db = moe.router_grads(dx_perm, slot_row, dl, W, x)
+    dx2, dW2, db2 = moe.router_grads(dx_perm, slot_row, dl, W, x)
+    dx_c = moe.grad_x(dx_perm, slot_row, dl, W)
+    dW_c, db_c = moe.router_wgrad(dl, x)
+    moe.check()
+    rdx, rdW, rdb = _router_grad_refs(dx_perm, slot_row, dl, W, x)
+    for got in (dx, dx_c):
+        err = (got.double() - rdx).abs()
+        assert bool((err <= rdx.abs() * 2.0 ** -8 + 1e-5).all()), float(err.max())
+    for got in (dW, dW_c):
+        assert float((got.double() - rdW).norm() / rdW.norm()) < 1e-5
+    for got in (db, db_c):
+        assert float((got.double() - rdb).norm() / rdb.norm()) < 1e-6
+    assert torch.equal(dx, dx2) and torch.equal(dW, dW2) and torch.equal(db, db2)
+
+
+def test_router_grads_no_tokens():
+    E, d = 8, 128
+    dW = torch.full((E, d), 3.0, device="cuda")
+    db = torch.full((E,), 3.0, device="cuda")
+    x = torch.empty((0, d), dtype=torch.bfloat16, device="cuda")
+    moe.router_grads(torch.empty((1, d), dtype=torch.bfloat16, device="cuda"),
+                     torch.empty((0, 2), dtype=torch.int32, device="cuda"), torch.empty((0, E), device="cuda"),
+                     torch.zeros(E, d, device="cuda"), x, dW=dW, db=db)
+    moe.check()
+    assert bool((dW == 0).all()) and bool((db == 0).all())
+
+
 def test_expert_wgrad_rows_no_rows_gives_zeros():
     kept = torch.zeros(3, dtype=torch.int32, device="cuda")
     offsets = torch.zeros(4, dtype=torch.int32, device="cuda")

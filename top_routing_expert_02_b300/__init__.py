@@ -26,14 +26,14 @@ import torch
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
     "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "expert_dgrad_act", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
-    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
+    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "router_grads", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
 
 ACT = {"gelu": 0, "swiglu": 1, "identity": 2}
-CALL = {"route": 0, "dispatch": 1, "ffn": 2, "router_wgrad": 3}
+CALL = {"route": 0, "dispatch": 1, "ffn": 2, "router_wgrad": 3, "router_grads": 4}
 _DT = {torch.float32: 0, torch.bfloat16: 1}
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
@@ -83,6 +83,7 @@ _SIGS = {
     "moe_route_bwd": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _F, _F, _P, _P]),
     "moe_grad_x": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_router_wgrad": (_I32, [_P, _P, _I32, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "moe_router_grads": (_I32, [_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_z_loss": (_I32, [_P, _I64, _F, _P, _P]),
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
@@ -517,6 +518,22 @@ def router_wgrad(dl, x, *, dW=None, db=None, ws=None, stream=None):
     return dW, db
 
 
+@_traced
+def router_grads(dx_perm, slot_row, dl, w_router, x, *, dx=None, dW=None, db=None, ws=None, stream=None):
+    """(dx [T, d] bf16, dW [E, d] f32, db [E] f32) on the tensor cores (moe_router_grads)."""
+    T, d = x.shape
+    k = slot_row.shape[1]
+    E = w_router.shape[0]
+    dx = torch.empty((T, d), dtype=x.dtype, device=x.device) if dx is None else dx
+    dW = torch.empty((E, d), dtype=torch.float32, device=x.device) if dW is None else dW
+    db = torch.empty(E, dtype=torch.float32, device=x.device) if db is None else db
+    ws = _empty_ws(workspace_bytes("router_grads", T, d, E, k, 64), x.device) if ws is None else ws
+    _ok("moe_router_grads", lib().moe_router_grads(_ptr(dx_perm), _ptr(slot_row), _ptr(dl), _ptr(w_router), _ptr(x),
+                                                   T, k, E, d, _dt(x), _ptr(dx), _ptr(dW), _ptr(db), _ptr(ws),
+                                                   ws.numel(), _stream(stream)))
+    return dx, dW, db
+
+
 # ------------------------------------------------------------ whole layer ---
 
 class MoEPlan:
@@ -650,7 +667,7 @@ class MoEPlan:
                 dw2=torch.empty((E, d, F), dtype=self.grad_dtype, device=dev),
                 dl=torch.empty((max(T, 1), E), **f32), dx=torch.empty((max(T, 1), d), **bf),
                 dW=torch.empty((E, d), **f32), db=torch.empty(E, **f32),
-                ws=_empty_ws(workspace_bytes("router_wgrad", max(T, 1), d, E, k, F), dev))
+                ws=_empty_ws(workspace_bytes("router_grads", max(T, 1), d, E, k, F), dev))
         return self._bwd
 
     def backward(self, x, w_router, w1, w2, dy, *, aux_weight: float = 1.0, z_weight: float = 1.0, stream=None,
@@ -686,12 +703,8 @@ class MoEPlan:
         zc = z_weight * (self.z_beta or 0.0)
         route_bwd(self.logits, self.topk_idx, B["dgate"], counts, self.renorm, aux_weight * self.alpha * E, zc,
                   dl=B["dl"], stream=stream)
-        grad_x(B["dx_perm"], D.slot_row, B["dl"], w_router, dx=B["dx"], stream=stream)
-        if self.T > 0:
-            router_wgrad(B["dl"], x, dW=B["dW"], db=B["db"], ws=B["ws"], stream=stream)
-        else:   # no tokens: the router gets no gradient
-            B["dW"].zero_()
-            B["db"].zero_()
+        router_grads(B["dx_perm"], D.slot_row, B["dl"], w_router, x, dx=B["dx"], dW=B["dW"], db=B["db"],
+                     ws=B["ws"], stream=stream)
         mark("router_and_dx")
         return dict(dx=B["dx"], dW=B["dW"], db=B["db"], dw1=B["dw1"], dw2=B["dw2"], dgate=B["dgate"], dl=B["dl"],
                     do_perm=B["do_perm"], z=self.z, dz=B["dz"], dx_perm=B["dx_perm"])

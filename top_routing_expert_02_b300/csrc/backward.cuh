@@ -478,4 +478,136 @@ router_wgrad_sum_kernel(const float* __restrict__ partial, int S, long long n, f
     }
 }
 
+// ---------------------------------------------------------------------------
+// Router gradients on the tensor cores.  dx_router = dl . W and dW = dl^T x
+// are dense contractions over E and over T; their fp32 operands (dl, W) are
+// split into bf16 parts, v = hi + lo with hi = rn(v), lo = rn(v - hi), so that
+// bf16 MMAs with fp32 accumulation keep ~16 significant bits:
+//   dl . W  ~ hi(dl).hi(W) + lo(dl).hi(W) + hi(dl).lo(W)     (one GEMM, K = 3 Ep)
+//   dl^T x  = hi(dl)^T x + lo(dl)^T x                        (x is bf16: exact)
+// Ep = E rounded up to 64; the padding experts are zero.
+//
+// router_grads_prep_kernel writes
+//   dl3 [T, 3 Ep] bf16, row t = [hi(dl[t]) | lo(dl[t]) | hi(dl[t])]
+//   W3  [3 Ep, d] bf16, rows   = [hi(W); hi(W); lo(W)]
+// and the row segments of the two GEMMs: one segment [0, T) (seg1) and S
+// equal token splits (segS) for the weight gradient.
+__global__ void __launch_bounds__(256)
+router_grads_prep_kernel(const float* __restrict__ dl, const float* __restrict__ W, int T, int E, int Ep, int d,
+                         int S, uint16_t* __restrict__ dl3, uint16_t* __restrict__ W3, int32_t* __restrict__ seg1,
+                         int32_t* __restrict__ segS)
+{
+    const long long n_dl = (long long)T * Ep, n_w = (long long)Ep * d;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_dl + n_w; i += stride) {
+        if (i < n_dl) {
+            const long long t = i / Ep;
+            const int c = (int)(i - t * Ep);
+            const float v = c < E ? __ldg(dl + t * E + c) : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+            uint16_t* row = dl3 + t * (3LL * Ep);
+            row[c] = *reinterpret_cast<const uint16_t*>(&hi);
+            row[Ep + c] = *reinterpret_cast<const uint16_t*>(&lo);
+            row[2 * Ep + c] = *reinterpret_cast<const uint16_t*>(&hi);
+        } else {
+            const long long j = i - n_dl;
+            const int e = (int)(j / d);
+            const float v = e < E ? __ldg(W + j) : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+            W3[j] = *reinterpret_cast<const uint16_t*>(&hi);
+            W3[n_w + j] = *reinterpret_cast<const uint16_t*>(&hi);
+            W3[2 * n_w + j] = *reinterpret_cast<const uint16_t*>(&lo);
+        }
+    }
+    if (blockIdx.x == 0) {
+        // seg1: offsets {0, T}, kept {T};  segS: offsets [S + 1], kept [S]
+        if (threadIdx.x == 0) {
+            seg1[0] = 0;
+            seg1[1] = T;
+            seg1[2] = T;
+        }
+        for (int s = threadIdx.x; s <= S; s += blockDim.x) {
+            const int o = (int)((long long)s * T / S);
+            segS[s] = o;
+            if (s < S) segS[S + 1 + s] = (int)((long long)(s + 1) * T / S) - o;
+        }
+    }
+}
+
+// dx[t] = rn_bf16(zr[t] + sum_j dx_perm[slot_row[t, j]]): zr [T, d] fp32 is the
+// router part dl . W, the slots are added in j order (dropped ones skipped).
+// One warp per token, four 16-byte vectors (8 columns each) per lane in flight.
+__global__ void __launch_bounds__(256)
+grad_x_gather_kernel(const uint4* __restrict__ dx_perm, const int32_t* __restrict__ slot_row,
+                     const float4* __restrict__ zr, int T, int k, int vec16, uint4* __restrict__ dx)
+{
+    const int lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * 8;
+    for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += warps_total) {
+        int rows[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) rows[j] = j < k ? __ldg(slot_row + (size_t)t * k + j) : -1;
+        for (int v0 = lane; v0 < vec16; v0 += 128) {
+            float acc[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                if (v < vec16) {
+                    a = __ldcs(zr + ((size_t)t * vec16 + v) * 2);
+                    b = __ldcs(zr + ((size_t)t * vec16 + v) * 2 + 1);
+                }
+                acc[u][0] = a.x; acc[u][1] = a.y; acc[u][2] = a.z; acc[u][3] = a.w;
+                acc[u][4] = b.x; acc[u][5] = b.y; acc[u][6] = b.z; acc[u][7] = b.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (rows[j] < 0) continue;
+                const uint4* src = dx_perm + (size_t)rows[j] * vec16;
+                uint4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    q[u] = (v0 + 32 * u < vec16) ? ldg_nc_v4(src + v0 + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float f[8];
+                    unpack_bf16x8(q[u], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[u][i] += f[i];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= vec16) break;
+                uint4 o;
+                o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                dx[(size_t)t * vec16 + v] = o;
+            }
+        }
+    }
+}
+
+// dW[e, c] = sum_s P[s, e, c] + sum_s P[s, Ep + e, c]  (hi part, then lo part,
+// splits in order); P [S, 2 Ep, d] fp32 from the split weight-gradient GEMM.
+__global__ void __launch_bounds__(256)
+router_grads_reduce_kernel(const float4* __restrict__ P, int S, int E, int Ep, int d4, float4* __restrict__ dW)
+{
+    const long long n = (long long)E * d4, plane = 2LL * Ep * d4, lo_off = (long long)Ep * d4;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        float4 h = __ldcs(P + i), l = __ldcs(P + lo_off + i);
+        for (int s = 1; s < S; ++s) {
+            const float4 a = __ldcs(P + s * plane + i), b = __ldcs(P + s * plane + lo_off + i);
+            h.x += a.x; h.y += a.y; h.z += a.z; h.w += a.w;
+            l.x += b.x; l.y += b.y; l.z += b.z; l.w += b.w;
+        }
+        dW[i] = make_float4(h.x + l.x, h.y + l.y, h.z + l.z, h.w + l.w);
+    }
+}
+
 }  // namespace bwd

@@ -83,9 +83,11 @@ struct Args {
     uint16_t* out_z;            // up projection, optional: the pre-activation, bf16 [rows_max, N1]
     const uint16_t* in_z;       // activation backward: the pre-activation, bf16 [rows_max, N1]
     int z_cols;                 // columns of out_z / in_z (N1)
-    float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols], or nullptr: bf16 into out
+    float* out_f32;             // weight gradient: fp32 [E, m_rows, out_cols]; identity epilogue: fp32
+                                // [rows_max, out_cols]; nullptr: bf16 into out
     int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
     int m_rows;                 // weight gradient: rows M of each expert's gradient
+    int lda;                    // MODE_WGRAD_ROWS: row stride of A in elements (>= m_rows)
     unsigned long long wait_limit;
 };
 
@@ -164,6 +166,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int STAGE_BYTES = SH::STAGE_BYTES, BH_BYTES = SH::BH_BYTES;
     constexpr int ACC_COLS = SH::ACC_COLS, TMEM_COLS = SH::TMEM_COLS;
     constexpr int BOX_BYTES = BK * 128;   // one 64x64 bf16 box
+    // fp32 output tiles of the MN-major identity GEMM go out through the same
+    // shared-memory staging and TMA stores as the weight gradients
+    constexpr bool TMA_OUT_OK = WGRAD || (BMN && EPI == EPI_IDENT);
     constexpr uint32_t IDESC = WGR ? ptx::idesc_bf16_f32(128, BN, true, true)
                                : BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
     extern __shared__ uint8_t dsmem[];
@@ -387,8 +392,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            if (WGRAD) {
-                const bool empty = kstart[e + 1] == kstart[e];
+            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr)) {
+                const bool empty = WGRAD && kstart[e + 1] == kstart[e];
                 // this warp's 32 rows all inside the expert's M rows: stage each block of
                 // 32 rows x 128 bytes in shared memory (128-byte swizzle) and store it with
                 // TMA; otherwise (a ragged last M-tile) masked per-thread stores
@@ -545,6 +550,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int v = 0; v < 4; ++v)
                             dz[v] = make_uint4(zk[4 * v], zk[4 * v + 1], zk[4 * v + 2], zk[4 * v + 3]);
                     }
+                    if (EPI == EPI_IDENT && g.out_f32) {   // fp32 output, no rounding
+                        if (rv && col < g.out_cols) {
+                            float4* dst = reinterpret_cast<float4*>(g.out_f32 + (size_t)row * g.out_cols + col);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                dst[v] = make_float4(f32(av[4 * v]), f32(av[4 * v + 1]), f32(av[4 * v + 2]),
+                                                     f32(av[4 * v + 3]));
+                        }
+                        continue;
+                    }
                     if (rv && col < g.out_cols) {
                         uint32_t pk[16];
 #pragma unroll
@@ -571,7 +586,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
-        if (WGRAD && lane == 0) ptx::bulk_wait_group<0>();   // every output store has completed
+        if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr) && lane == 0)
+            ptx::bulk_wait_group<0>();   // every output store has completed
     }
 
     ptx::tc_fence_before();

@@ -207,7 +207,21 @@ bool make_tmap_bf16_box(CUtensorMap* m, const void* base, unsigned long long row
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A_rows: rows of the A tensor (rows_max of x_perm, or T of x when gathering).
+// bf16 [rows, cols] with a row stride of ld elements (ld >= cols), 64x64 boxes.
+bool make_tmap_bf16_box_ld(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols,
+                           unsigned long long ld)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 [rows, cols] with a 32x32 box and the 128-byte swizzle (the output
 // tiles of the weight-gradient GEMM, stored by TMA).
 bool make_tmap_f32_out(CUtensorMap* m, const void* base, unsigned long long rows, unsigned long long cols)
@@ -234,7 +248,8 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
     CUtensorMap ta, tb;
     if (MODE == tcg::MODE_WGRAD_ROWS) {
         // A [rows_max, M] and B [rows_max, N], both read as 64x64 boxes (rows = K)
-        if (!make_tmap_bf16_box(&ta, A, (unsigned long long)rows_max, (unsigned long long)args.m_rows, 64) ||
+        const unsigned long long lda = (unsigned long long)(args.lda > 0 ? args.lda : args.m_rows);
+        if (!make_tmap_bf16_box_ld(&ta, A, (unsigned long long)rows_max, (unsigned long long)args.m_rows, lda) ||
             !make_tmap_bf16_box(&tb, W, (unsigned long long)rows_max, (unsigned long long)args.out_cols, 64))
             return MOE_ERR_CUDA;
     } else if (!make_tmap_bf16_box(&ta, A, (unsigned long long)(A_rows >= 0 ? A_rows : rows_max),
@@ -255,8 +270,11 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
         if (args.out_f32 ? !make_tmap_f32_out(&tc, args.out_f32, rows, cols)
                          : !make_tmap_bf16_box(&tc, args.out, rows, cols, 32))
             return MOE_ERR_CUDA;
+    } else if (MODE == tcg::MODE_BMN && EPI == tcg::EPI_IDENT && args.out_f32) {   // fp32 [rows_max, N] by TMA
+        if (!make_tmap_f32_out(&tc, args.out_f32, (unsigned long long)rows_max, (unsigned long long)args.out_cols))
+            return MOE_ERR_CUDA;
     }
-    const int smem = wg ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
+    const int smem = (wg || MODE == tcg::MODE_BMN) ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
     if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, smem)) return launch_status();
     const long long max_tiles = wg
                                     ? (long long)args.E * args.m_tiles * args.n_tiles
@@ -408,6 +426,37 @@ int router_wgrad_splits(int64_t T, int E, int d)
 }
 }  // namespace
 
+namespace {
+// Router gradients on the tensor cores: Ep = E rounded up to 64, S token
+// splits of the weight-gradient GEMM (enough tiles for two waves, >= 256 rows each).
+struct RouterGradsLayout {
+    int Ep, S;
+    size_t dl3, W3, zr, P, seg1, segS, total;   // byte offsets in the workspace
+};
+
+RouterGradsLayout router_grads_layout(int64_t T, int E, int d)
+{
+    RouterGradsLayout L{};
+    L.Ep = (E + 63) / 64 * 64;
+    const int tiles = ceil_div_i(2 * L.Ep, 128) * ceil_div_i(d, 256);
+    int S = ceil_div_i(2 * 148, tiles);
+    const int maxS = (int)(T / 256 > 0 ? T / 256 : 1);
+    if (S > maxS) S = maxS;
+    if (S > 64) S = 64;
+    L.S = S < 1 ? 1 : S;
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    size_t o = 0;
+    L.dl3 = o;  o += up((size_t)T * 3 * L.Ep * 2);
+    L.W3 = o;   o += up((size_t)3 * L.Ep * d * 2);
+    L.zr = o;   o += up((size_t)T * d * 4);
+    L.P = o;    o += up((size_t)L.S * 2 * L.Ep * d * 4);
+    L.seg1 = o; o += 256;
+    L.segS = o; o += up((size_t)(2 * L.S + 1) * 4);
+    L.total = o;
+    return L;
+}
+}  // namespace
+
 size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F, moe_act act, moe_dtype dtype)
 {
     (void)F;
@@ -420,6 +469,8 @@ size_t moe_workspace_bytes(moe_call call, int64_t T, int d, int E, int k, int F,
     case MOE_CALL_FFN: return 0;
     case MOE_CALL_ROUTER_WGRAD:
         return T < 1 || d < 1 ? 0 : (size_t)router_wgrad_splits(T, E, d) * E * d * sizeof(float);
+    case MOE_CALL_ROUTER_GRADS:
+        return T < 1 || d < 1 ? 0 : router_grads_layout(T, E, d).total;
     }
     return 0;
 }
@@ -1141,6 +1192,101 @@ moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64
     if (s != MOE_OK || !db) return s;
     rtc::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
     return launch_status();
+}
+
+moe_status moe_router_grads(const void* dx_perm, const int32_t* slot_row, const float* dl, const float* w_router,
+                            const void* x, int64_t T, int k, int E, int d, moe_dtype dtype, void* dx, float* dW,
+                            float* db, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (T < 0 || k < 1 || k > MAX_K || E < 1 || E > MAX_E || d <= 0 || !dtype_ok(dtype) || !dW || !db)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!dx_perm || !slot_row || !dl || !w_router || !x || !dx)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_BF16 || d % 64 || T >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+    if (!all_aligned16({dx_perm, w_router, x, dx, dW, ws})) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {   // no tokens: the router gets no gradient
+        if (cudaMemsetAsync(dW, 0, (size_t)E * d * sizeof(float), st) != cudaSuccess ||
+            cudaMemsetAsync(db, 0, (size_t)E * sizeof(float), st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    const RouterGradsLayout L = router_grads_layout(T, E, d);
+    if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t* w = (uint8_t*)ws;
+    uint16_t* dl3 = (uint16_t*)(w + L.dl3);
+    uint16_t* W3 = (uint16_t*)(w + L.W3);
+    float* zr = (float*)(w + L.zr);
+    float* P = (float*)(w + L.P);
+    int32_t* seg1 = (int32_t*)(w + L.seg1);
+    int32_t* segS = (int32_t*)(w + L.segS);
+    const int Ep = L.Ep, K3 = 3 * Ep;
+
+    // 1. bf16 parts of dl and W, row segments
+    {
+        const long long n = (long long)T * Ep + (long long)Ep * d;
+        long long g1 = (n + 255) / 256;
+        if (g1 > sm_count() * 8LL) g1 = sm_count() * 8LL;
+        bwd::router_grads_prep_kernel<<<(int)g1, 256, 0, st>>>(dl, w_router, (int)T, E, Ep, d, L.S, dl3, W3, seg1,
+                                                              segS);
+        moe_status s = launch_status();
+        if (s != MOE_OK) return s;
+    }
+    // 2. zr = dl3 . W3  [T, d] fp32 (one segment of T rows, B MN-major)
+    {
+        tcg::Args g{};
+        g.offsets = seg1;
+        g.kept = seg1 + 2;
+        g.E = 1;
+        g.K = K3;
+        g.n_step = 256;
+        g.half_off = 128;
+        g.n_tiles = (d + 255) / 256;
+        g.out_cols = d;
+        g.out_f32 = zr;
+        g.wait_limit = g_wait_limit.load();
+        moe_status s = launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_BMN>(dl3, T, K3, W3, K3, g, st);
+        if (s != MOE_OK) return s;
+    }
+    // 3. dx = zr + sum over the kept slots of dx_perm, one rounding
+    {
+        const int vec16 = d / 8;
+        long long g3 = (T + 7) / 8;
+        if (g3 > sm_count() * 16LL) g3 = sm_count() * 16LL;
+        bwd::grad_x_gather_kernel<<<(int)g3, 256, 0, st>>>((const uint4*)dx_perm, slot_row, (const float4*)zr, (int)T,
+                                                          k, vec16, (uint4*)dx);
+        moe_status s = launch_status();
+        if (s != MOE_OK) return s;
+    }
+    // 4. P[s] = [hi | lo](rows of split s)^T x[rows of split s]  [S, 2 Ep, d] fp32
+    //    (the first 2 Ep columns of dl3, row stride 3 Ep)
+    {
+        tcg::Args g{};
+        g.offsets = segS;
+        g.kept = segS + L.S + 1;
+        g.E = L.S;
+        g.m_tiles = (2 * Ep + 127) / 128;
+        g.m_rows = 2 * Ep;
+        g.lda = K3;
+        g.n_step = 256;
+        g.half_off = 128;
+        g.n_tiles = (d + 255) / 256;
+        g.out_cols = d;
+        g.out_f32 = P;
+        g.wait_limit = g_wait_limit.load();
+        moe_status s = launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD_ROWS>(dl3, T, 0, x, 0, g, st);
+        if (s != MOE_OK) return s;
+    }
+    // 5. dW = hi part + lo part over the splits; db = sum_t dl (fixed-order fp64 tree)
+    {
+        const long long n4 = (long long)E * d / 4;
+        long long g5 = (n4 + 255) / 256;
+        if (g5 > sm_count() * 8LL) g5 = sm_count() * 8LL;
+        bwd::router_grads_reduce_kernel<<<(int)g5, 256, 0, st>>>((const float4*)P, L.S, E, Ep, d / 4, (float4*)dW);
+        moe_status s = launch_status();
+        if (s != MOE_OK) return s;
+        rtc::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
+        return launch_status();
+    }
 }
 
 extern "C" moe_status moe_dispatch_noalloc(const int32_t* topk_idx, const float* topk_gate, int64_t T, int k, int E,
