@@ -517,7 +517,8 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         a.nb_rows = sh.nb_rows;
         a.stage_bytes = rtc::A_BYTES + 3 * sh.E_pad * 128;
         const int grid = ntiles * S;
-        const int budget = (grid <= sm_count() ? 200 : 100) * 1024;
+        // two blocks per SM only when two rings of >= 2 stages fit; else one deep ring
+        const int budget = (grid <= sm_count() || 2 * a.stage_bytes > 100 * 1024 ? 200 : 100) * 1024;
         int stages = budget / a.stage_bytes;
         if (stages > rtc::MAX_STAGES) stages = rtc::MAX_STAGES;
         if (stages < 2) stages = 2;

@@ -23,7 +23,8 @@
 // sums the probabilities per block; prob_sum_kernel then adds the block rows
 // with one fixed-shape tree per expert.  E <= 32: one lane per token (all E logits in
 // registers, sorted top-k insertion); larger E: one warp per token (lane l
-// owns experts l, l+32, ...; k rounds of warp argmax).
+// owns experts l, l+32, ... sorted in registers; k rounds of two redux.sync
+// over order-preserving keys).
 // Every sum runs in a fixed order, so the result is the same bits on every run.
 #pragma once
 #include "common.cuh"
@@ -73,7 +74,10 @@ __global__ void split_weight_kernel(const float* __restrict__ W, int E, int E_pa
 }
 
 // Block (tile, s): tile = blockIdx.x / S covers tokens [128*tile, 128*tile + 128),
-// split s covers K blocks [s*nk/S, (s+1)*nk/S).
+// split s covers K blocks [s*nk/S, (s+1)*nk/S).  Each block walks its K range
+// starting at a block-dependent offset (wrapping around), so that the blocks
+// running at the same time read different columns of the stacked weight
+// instead of all hitting the same lines of L2.
 __global__ void __launch_bounds__(THREADS, 1)
 route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Args g)
 {
@@ -86,6 +90,8 @@ route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const int tile = blockIdx.x / g.S, split = blockIdx.x - tile * g.S;
     const int t0 = tile * BM;
     const int kb0 = (int)((long long)split * g.nk / g.S), kb1 = (int)((long long)(split + 1) * g.nk / g.S);
+    const int nkb = kb1 - kb0;
+    const int rot = nkb > 0 ? (int)(((long long)tile * 5) % nkb) : 0;   // first K block of this block's walk
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < g.stages; ++s) {
@@ -114,7 +120,8 @@ route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             uint32_t phase = 0;
             int fills = 0;
             bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int i = 0; i < nkb; ++i) {
+                const int kb = kb0 + (i + rot) % nkb;
                 if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit)) {
                     ok = false;
                     break;
@@ -145,7 +152,7 @@ route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int i = 0; i < nkb; ++i) {
                 if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, limit)) {
                     ok = false;
                     break;
@@ -157,7 +164,7 @@ route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     for (int c = 0; c < g.nb_chunks; ++c)
                         ptx::mma_bf16(tmem_base + (uint32_t)(c * g.nb_rows), ptx::sdesc_kmajor_sw128(sa + kk * 32),
                                       ptx::sdesc_kmajor_sw128(sb + c * b_box_bytes + kk * 32), idesc,
-                                      (kb > kb0 || kk > 0) ? 1u : 0u);
+                                      (i > 0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
                 if (++stage == g.stages) {
                     stage = 0;
@@ -210,17 +217,21 @@ route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 constexpr int FIN_THREADS = 256;
 constexpr int FIN_WARPS = FIN_THREADS / 32;
 
-// Sum of the S partial logits of token t, expert e, in split order (loads first).
+// Sum of the S partial logits of token t, expert e, in split order (four
+// loads in flight at a time).
 __device__ __forceinline__ float sum_splits(const float* __restrict__ part, int S, int T, int E_pad, int t, int e)
 {
-    float v[MAX_SPLITS];
+    const size_t plane = (size_t)T * E_pad;
+    const float* p = part + (size_t)t * E_pad + e;
+    float acc = __ldcg(p);
+    for (int s0 = 1; s0 < S; s0 += 4) {
+        float v[4];
 #pragma unroll
-    for (int s = 0; s < MAX_SPLITS; ++s)
-        if (s < S) v[s] = __ldcg(part + ((size_t)s * T + t) * E_pad + e);
-    float acc = v[0];
+        for (int u = 0; u < 4; ++u) v[u] = s0 + u < S ? __ldcg(p + (size_t)(s0 + u) * plane) : 0.f;
 #pragma unroll
-    for (int s = 1; s < MAX_SPLITS; ++s)
-        if (s < S) acc += v[s];
+        for (int u = 0; u < 4; ++u)
+            if (s0 + u < S) acc += v[u];
+    }
     return acc;
 }
 
@@ -273,26 +284,28 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
     }
     for (int t = (blockIdx.x * FIN_WARPS + warp) * 32 + lane; t < T; t += gridDim.x * FIN_THREADS) {
         float l[EMAX];
+        // this token's E_pad partial logits of split 0, then the other splits in order
 #pragma unroll
         for (int e4 = 0; e4 < EMAX; e4 += 4) {
-            float4 v[MAX_SPLITS];
-#pragma unroll
-            for (int s = 0; s < MAX_SPLITS; ++s)
-                if (s < S && e4 < E_pad)
-                    v[s] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)s * T + t) * E_pad + e4));
-            float4 a = v[0];
-#pragma unroll
-            for (int s = 1; s < MAX_SPLITS; ++s)
-                if (s < S) {
-                    a.x += v[s].x;
-                    a.y += v[s].y;
-                    a.z += v[s].z;
-                    a.w += v[s].w;
-                }
+            const float4 a = e4 < E_pad ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)t * E_pad + e4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
             l[e4] = a.x;
             l[e4 + 1] = a.y;
             l[e4 + 2] = a.z;
             l[e4 + 3] = a.w;
+        }
+        for (int sp = 1; sp < S; ++sp) {
+            const float* row = part + ((size_t)sp * T + t) * E_pad;
+#pragma unroll
+            for (int e4 = 0; e4 < EMAX; e4 += 4) {
+                if (e4 < E_pad) {
+                    const float4 a = __ldcg(reinterpret_cast<const float4*>(row + e4));
+                    l[e4] += a.x;
+                    l[e4 + 1] += a.y;
+                    l[e4 + 2] += a.z;
+                    l[e4 + 3] += a.w;
+                }
+            }
         }
         float tv[KMAX];
         int ti[KMAX];
@@ -381,9 +394,55 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
     block_prob_sums(red, E, psum);
 }
 
-// E > 32: one warp per token, lane l owns experts l, l+32, ...
+// Order-preserving map of a float onto uint32 (a < b  <=>  key(a) < key(b) for
+// non-NaN values), so that one redux.sync finds a warp's maximum; key 0 lies
+// below every float and marks "not selectable".
+__device__ __forceinline__ unsigned fkey(float v)
+{
+    const unsigned u = __float_as_uint(v);
+    return u ^ ((u & 0x80000000u) ? 0xffffffffu : 0x80000000u);
+}
+__device__ __forceinline__ float fkey_value(unsigned k)
+{
+    return __uint_as_float(k ^ ((k & 0x80000000u) ? 0x80000000u : 0xffffffffu));
+}
+
+// Sorts a lane's EPL (key, expert) pairs by key descending, expert ascending.
 template <int EPL>
-__global__ void __launch_bounds__(FIN_THREADS)
+__device__ __forceinline__ void sort_lane(unsigned (&ck)[EPL], int (&ce)[EPL])
+{
+    auto cx = [&](int a, int b) {
+        if (ck[b] > ck[a] || (ck[b] == ck[a] && ce[b] < ce[a])) {
+            const unsigned tk = ck[a];
+            ck[a] = ck[b];
+            ck[b] = tk;
+            const int te = ce[a];
+            ce[a] = ce[b];
+            ce[b] = te;
+        }
+    };
+    if (EPL == 2) {
+        cx(0, 1);
+    } else if (EPL == 4) {
+        cx(0, 1); cx(2, 3); cx(0, 2); cx(1, 3); cx(1, 2);
+    } else if (EPL == 8) {   // Batcher's odd-even merge sort, 19 comparators
+        cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+        cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+        cx(1, 2); cx(5, 6);
+        cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+        cx(2, 4); cx(3, 5);
+        cx(1, 2); cx(3, 4); cx(5, 6);
+    }
+}
+
+// E > 32: one warp per token, lane l owns experts l, l+32, ...  The softmax
+// maximum is one redux.sync over order-preserving keys.  For the top-k every
+// lane sorts its EPL candidates (key descending, expert ascending); each of
+// the k rounds takes the largest head key over the warp (redux max), then the
+// lowest expert id among the lanes holding it (redux min: ties go to the
+// lower index), and the winning lane drops its head.
+template <int EPL>
+__global__ void __launch_bounds__(FIN_THREADS, 4)
 route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, int E_pad, int k, int renorm,
                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                          float* __restrict__ gate_out, float* __restrict__ psum, RouteSel sel)
@@ -401,15 +460,14 @@ route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, in
     }
     for (int t = blockIdx.x * FIN_WARPS + warp; t < T; t += gridDim.x * FIN_WARPS) {
         float l[EPL];
-        float mx = -INFINITY;
+        unsigned km = 0u;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             l[i] = (e < E) ? sum_splits(part, S, T, E_pad, t, e) + bia[i] : -INFINITY;
-            mx = fmaxf(mx, l[i]);
+            km = max(km, fkey(l[i]));
         }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float mx = fkey_value(__reduce_max_sync(0xffffffffu, km));
         float p[EPL], s = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
@@ -425,47 +483,35 @@ route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, in
                 if (lane + 32 * i < E) sel.logits[(size_t)t * E + lane + 32 * i] = l[i];
         }
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            p[i] = p[i] / s;
-            acc_p[i] += p[i];
-        }
+        for (int i = 0; i < EPL; ++i) acc_p[i] += p[i] / s;
         const unsigned gkeep = keep_groups<EPL>(l, grp, E, sel, lane);
-        unsigned taken = 0;
+        unsigned ck[EPL];
+        int ce[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            ce[i] = e;
+            ck[i] = (e < E && ((gkeep >> grp[i]) & 1u)) ? fkey(l[i]) : 0u;
+        }
+        sort_lane<EPL>(ck, ce);
         int my_e = 0;
         float my_p = 0.f, chosen = 0.f;
         for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && ((gkeep >> grp[i]) & 1u) &&
-                    (l[i] > bv || (l[i] == bv && e < bi))) {
-                    bv = l[i];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            float pv = 0.f;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i)
-                if (lane + 32 * i == bi) {
-                    pv = p[i];
-                    taken |= 1u << i;
-                }
-            const float pw = __shfl_sync(0xffffffffu, pv, bi & 31);
+            const unsigned m = __reduce_max_sync(0xffffffffu, ck[0]);
+            const unsigned w = __reduce_min_sync(0xffffffffu, ck[0] == m ? (unsigned)ce[0] : 0xffffffffu);
+            const float pw = expf(fkey_value(m) - mx) / s;   // the winner's probability, as p[] above
             chosen += pw;
             if (lane == j) {
-                my_e = bi;
+                my_e = (int)w;
                 my_p = pw;
+            }
+            if ((unsigned)ce[0] == w) {   // the winning lane drops its head
+#pragma unroll
+                for (int i = 0; i + 1 < EPL; ++i) {
+                    ck[i] = ck[i + 1];
+                    ce[i] = ce[i + 1];
+                }
+                ck[EPL - 1] = 0u;
             }
         }
         if (lane < k) {
