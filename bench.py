@@ -73,10 +73,11 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     tc_router = cfg.dtype == "bf16" and cfg.E <= 160
     route = 4 if tc_router else 2          # split + logits + finish + prob sums | router + sums
     gather = bool(args and args.gather)
-    dispatch = 2 if gather else 3          # histogram, ranks (+ row copy)
+    ranks = 1 if cfg.T * cfg.k <= 16384 else 2   # one-block histogram + ranks, or the two-kernel form
+    dispatch = ranks + (0 if gather else 1)      # (+ row copy)
     z = 1 if (args and args.z_beta is not None) else 0
     bwd = BWD_KERNELS if (args and args.train) else 0
-    return route + dispatch + 1 + 1 + 1 + 1 + z + bwd   # up, down, combine, aux (+ z-loss) (+ backward)
+    return route + dispatch + 1 + 1 + 1 + z + bwd   # up, down, combine with the aux loss (+ z-loss) (+ backward)
 
 
 def plan_kwargs(args) -> dict:
@@ -368,8 +369,8 @@ def our_arm(args, cfg):
         mark(3)
         moe.expert_down(plan.h, D.offsets, D.kept, w2, D.row_gate, plan.rows_max, y_perm=plan.y_perm)
         mark(4)
-        moe.combine(plan.y_perm, D.slot_row, y=plan.y)
-        moe.aux_loss(D.kept if plan.aux_post_drop else D.counts, plan.prob_sum, plan.T, plan.alpha, loss=plan.loss)
+        moe.combine_aux(plan.y_perm, D.slot_row, D.kept if plan.aux_post_drop else D.counts, plan.prob_sum,
+                        plan.alpha, y=plan.y, loss=plan.loss)
         if plan.z_beta is not None:
             moe.z_loss(plan.lse, plan.z_beta, loss=plan.z_loss)
         mark(5)

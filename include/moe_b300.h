@@ -268,6 +268,13 @@ moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, i
 moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T, int E,
                         float alpha, float* loss, moe_stream_t stream);
 
+/* moe_combine and moe_aux_loss in one launch (the first warp of the combine
+ * computes the loss, with the same arithmetic as moe_aux_loss): the two
+ * closing steps of the forward.  Arguments as in the two calls; T >= 1. */
+moe_status moe_combine_aux(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d, moe_dtype dtype,
+                           void* y, const int32_t* counts, const float* prob_sum, int E, float alpha, float* loss,
+                           moe_stream_t stream);
+
 /* Router z-loss.  "ETP专家并行加速MoE模型：ms-swift中稀疏架构的极致优化", section
  * on dynamic routing, names a routing z-loss that spreads the router's
  * choices but gives no formula; this is the router z-loss of ST-MoE (Zoph et

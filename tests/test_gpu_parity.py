@@ -174,6 +174,52 @@ def test_identity_experts_return_x_bf16():
     assert int(plan.disp.n_dropped.item()) == 0
 
 
+@pytest.mark.parametrize("T,k,E,cap", [(8192, 2, 64, 160), (8193, 2, 64, 160), (2048, 8, 128, 100),
+                                       (4097, 8, 128, 300), (1, 1, 8, 1), (33, 16, 256, 2)])
+def test_dispatch_both_rank_paths_against_oracle(T, k, E, cap):
+    """The one-block rank kernel (T*k <= 16384) and the histogram + rank pair
+    (larger T*k) against the oracle's queue simulation: counts, kept,
+    n_dropped, offsets (exclusive scan of kept) and every slot's row, bit for
+    bit, on skewed expert choices (distinct experts per token)."""
+    g = torch.Generator().manual_seed(T * 31 + k)
+    w = torch.arange(E, 0, -1, dtype=torch.float64) ** 1.5          # skewed: low experts are hot
+    idx = torch.multinomial(w.expand(T, E), k, replacement=False, generator=g).to(torch.int32)
+    gate = torch.rand(T, k, generator=g)
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    D = moe.dispatch(idx.cuda(), gate.cuda(), x.cuda(), E, cap)
+    moe.check()
+    counts, kept, pos, nd = oracle.dispatch(idx.numpy(), E, cap)
+    assert np.array_equal(D.counts.cpu().numpy(), counts)
+    assert np.array_equal(D.kept.cpu().numpy(), kept)
+    assert int(D.n_dropped.cpu()) == nd
+    off = np.concatenate([[0], np.cumsum(kept)]).astype(np.int32)
+    assert np.array_equal(D.offsets.cpu().numpy(), off)
+    want = np.where(pos >= 0, off[idx.numpy()] + pos, -1)
+    sr = D.slot_row.cpu().numpy()
+    assert np.array_equal(sr, want)
+    rows = sr[sr >= 0]
+    tok = np.nonzero(sr >= 0)[0]
+    assert np.array_equal(D.row_token.cpu().numpy()[rows], tok)
+    assert np.array_equal(D.row_gate.cpu().numpy()[rows], gate.numpy()[sr >= 0])
+    assert torch.equal(D.x_perm[torch.as_tensor(rows, dtype=torch.long).cuda()].cpu(), x[torch.as_tensor(tok)])
+
+
+def test_combine_aux_equals_the_two_calls():
+    """moe_combine_aux: the same y and the same loss bits as moe_combine then moe_aux_loss."""
+    cfg = SMALL["swiglu_e8"]
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], "cuda", cfg.alpha,
+                       cfg.renorm)
+    plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+    D = plan.disp
+    y1 = moe.combine(plan.y_perm, D.slot_row)
+    l1 = moe.aux_loss(D.counts, plan.prob_sum, cfg.T, cfg.alpha)
+    y2, l2 = moe.combine_aux(plan.y_perm, D.slot_row, D.counts, plan.prob_sum, cfg.alpha)
+    moe.check()
+    assert torch.equal(y1, y2) and torch.equal(l1, l2)
+    assert torch.equal(plan.y, y2) and torch.equal(plan.loss, l2)
+
+
 def test_capacity_zero_drops_everything():
     cfg = C("cap0", 256, 128, 8, 2, 128, "swiglu", 0.001, "bf16")
     case = make_case(cfg)

@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
     "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "expert_dgrad_act", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
-    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "router_grads", "expert_ffn", "combine", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
+    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "router_grads", "expert_ffn", "combine", "combine_aux", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
@@ -69,6 +69,7 @@ _SIGS = {
                               _P]),
     "moe_combine": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P]),
     "moe_aux_loss": (_I32, [_P, _P, _I64, _I32, _F, _P, _P]),
+    "moe_combine_aux": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P, _I32, _F, _P, _P]),
     "moe_dispatch_noalloc": (_I32, [_P, _P, _I64, _I32, _I32, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P]),
     "moe_route_ex": (_I32, [_P, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
@@ -359,6 +360,20 @@ def combine(y_perm, slot_row, *, y=None, stream=None):
 
 
 @_traced
+def combine_aux(y_perm, slot_row, counts, prob_sum, alpha: float, *, y=None, loss=None, stream=None):
+    """combine + aux loss in one launch (moe_combine_aux): returns (y, loss)."""
+    T, k = slot_row.shape
+    d = y_perm.shape[1]
+    E = counts.shape[0]
+    y = torch.empty((T, d), dtype=y_perm.dtype, device=y_perm.device) if y is None else y
+    loss = torch.empty(1, dtype=torch.float32, device=y_perm.device) if loss is None else loss
+    _ok("moe_combine_aux", lib().moe_combine_aux(_ptr(y_perm), _ptr(slot_row), T, k, d, _dt(y_perm), _ptr(y),
+                                                 _ptr(counts), _ptr(prob_sum), E, float(alpha), _ptr(loss),
+                                                 _stream(stream)))
+    return y, loss
+
+
+@_traced
 def aux_loss(counts, prob_sum, T: int, alpha: float, *, loss=None, stream=None):
     E = counts.shape[0]
     loss = torch.empty(1, dtype=torch.float32, device=counts.device) if loss is None else loss
@@ -643,10 +658,9 @@ class MoEPlan:
         else:
             expert_ffn(D.x_perm, D.offsets, D.kept, w1, w2, D.row_gate, self.act, self.rows_max, h=self.h,
                        y_perm=self.y_perm, stream=stream)
-        combine(self.y_perm, D.slot_row, y=self.y, stream=stream)
         if self.T > 0:
-            aux_loss(D.kept if self.aux_post_drop else D.counts, self.prob_sum, self.T, self.alpha, loss=self.loss,
-                     stream=stream)
+            combine_aux(self.y_perm, D.slot_row, D.kept if self.aux_post_drop else D.counts, self.prob_sum,
+                        self.alpha, y=self.y, loss=self.loss, stream=stream)
             if self.z_beta is not None:
                 z_loss(self.lse, self.z_beta, loss=self.z_loss, stream=stream)
         return self.y

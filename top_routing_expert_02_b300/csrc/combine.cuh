@@ -15,6 +15,30 @@ namespace combine {
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
 
+// One warp: f_e = counts[e] / T, P_e = prob_sum[e] / T, fixed-order fp64 sum
+// (lane-strided partial sums, then a butterfly).
+__device__ __forceinline__ void aux_loss_warp(const int32_t* __restrict__ counts, const float* __restrict__ prob_sum,
+                                              long long T, int E, float alpha, float* __restrict__ loss, int lane)
+{
+    double s = 0.0;
+    for (int e = lane; e < E; e += 32)
+        s += ((double)counts[e] / (double)T) * ((double)prob_sum[e] / (double)T);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) *loss = (float)((double)alpha * (double)E * s);
+}
+
+// Optional auxiliary loss computed by the first warp of a combine launch
+// (saves the aux-loss launch; loss == nullptr: none).
+struct AuxArgs {
+    const int32_t* counts;
+    const float* prob_sum;
+    long long T;
+    int E;
+    float alpha;
+    float* loss;
+};
+
 // One warp per token; each lane sums 16-byte vectors of the token's k rows
 // in j order (fp32) and rounds once.  Dropped slots (-1) are skipped; a token
 // with none kept gets zeros.  Each lane works on four vectors at a time, so
@@ -22,9 +46,11 @@ constexpr int WARPS = THREADS / 32;
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ slot_row, int T, int k,
-               int vec16, uint4* __restrict__ y)
+               int vec16, uint4* __restrict__ y, AuxArgs aux)
 {
     const int lane = threadIdx.x & 31;
+    if (aux.loss && blockIdx.x == 0 && threadIdx.x < 32)
+        aux_loss_warp(aux.counts, aux.prob_sum, aux.T, aux.E, aux.alpha, aux.loss, lane);
     const int warps_total = gridDim.x * WARPS;
     for (int t = blockIdx.x * WARPS + (threadIdx.x >> 5); t < T; t += warps_total) {
         int rows[16];
@@ -79,17 +105,11 @@ combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ slo
     }
 }
 
-// One warp: f_e = counts[e] / T, P_e = prob_sum[e] / T, fixed-order fp64 sum.
+// The aux loss alone (one warp).
 __global__ void aux_loss_kernel(const int32_t* __restrict__ counts, const float* __restrict__ prob_sum,
                                 long long T, int E, float alpha, float* __restrict__ loss)
 {
-    const int lane = threadIdx.x;
-    double s = 0.0;
-    for (int e = lane; e < E; e += 32)
-        s += ((double)counts[e] / (double)T) * ((double)prob_sum[e] / (double)T);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) *loss = (float)((double)alpha * (double)E * s);
+    aux_loss_warp(counts, prob_sum, T, E, alpha, loss, threadIdx.x);
 }
 
 // Router z-loss (the ms-swift ETP page names a routing z-loss that spreads

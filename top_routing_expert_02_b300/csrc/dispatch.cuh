@@ -139,6 +139,145 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
     }
 }
 
+// hist + rank in one block for small T*k (<= SMALL_MAX assignments): 32 warps,
+// warp w owns the contiguous assignments [w*per, (w+1)*per), at most
+// SMALL_PER_LANE per lane, whose expert ids and gates are loaded once, all at
+// the start (one memory latency instead of one per round).
+//   1. per-warp expert histograms in shared memory
+//   2. per expert: exclusive scan over the warps (the base of each warp's
+//      run in the expert's queue), counts, kept, n_dropped; exclusive scan of
+//      kept over experts gives offsets
+//   3. each warp walks its range in order, 32 assignments at a time: the rank
+//      inside the 32 (match_any) plus the warp's running count gives the
+//      place in the expert's queue
+// Same results as hist_kernel + rank_kernel, in one launch without the
+// global histogram round trip.
+constexpr int SMALL_THREADS = 1024;
+constexpr int SMALL_WARPS = SMALL_THREADS / 32;
+constexpr int SMALL_PER_LANE = 16;
+constexpr int SMALL_MAX = SMALL_THREADS * SMALL_PER_LANE;
+
+__global__ void __launch_bounds__(SMALL_THREADS)
+dispatch_small_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int k, int E, int cap,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ slot_row, int32_t* __restrict__ row_token, float* __restrict__ row_gate,
+                      int32_t* __restrict__ n_dropped)
+{
+    __shared__ int wh[SMALL_WARPS][MAX_E];
+    __shared__ int off[MAX_E + 1];
+    __shared__ int drop_w[SMALL_WARPS];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = T * k;
+    const int per = (n + SMALL_WARPS - 1) / SMALL_WARPS;
+    const int a0 = warp * per, a1 = min(n, a0 + per);
+    const unsigned lt_mask = (1u << lane) - 1u;
+
+    // this lane's assignments a0 + 32 i + lane: expert (-1 none, -2 invalid) and gate
+    int ev[SMALL_PER_LANE];
+    float gv[SMALL_PER_LANE];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < SMALL_PER_LANE; ++i) {
+        const int a = a0 + 32 * i + lane;
+        ev[i] = -1;
+        gv[i] = 0.f;
+        if (a < a1) {
+            const int j = a / T, t = a - j * T;
+            ev[i] = __ldg(idx + (size_t)t * k + j);
+            gv[i] = __ldg(gate + (size_t)t * k + j);
+        }
+    }
+    for (int e = lane; e < E; e += 32) wh[warp][e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < SMALL_PER_LANE; ++i) {
+        if (a0 + 32 * i + lane >= a1) continue;
+        if (ev[i] >= 0 && ev[i] < E) {
+            atomicAdd(&wh[warp][ev[i]], 1);
+        } else {
+            ev[i] = -2;
+            bad = true;
+        }
+    }
+    if (bad) moe_flag(MOE_DEV_BAD_EXPERT);
+    __syncthreads();
+
+    // 2. warp bases, totals, kept; offsets by a scan over experts (warp 0)
+    int kp = 0, dr = 0;
+    if (tid < E) {
+        int tot = 0;
+        for (int w = 0; w < SMALL_WARPS; ++w) {
+            const int c = wh[w][tid];
+            wh[w][tid] = tot;
+            tot += c;
+        }
+        kp = tot < cap ? tot : cap;
+        dr = tot - kp;
+        counts[tid] = tot;
+        kept[tid] = kp;
+        off[tid] = kp;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) dr += __shfl_xor_sync(0xffffffffu, dr, o);
+    if (lane == 0) drop_w[warp] = dr;
+    __syncthreads();
+    if (warp == 0) {
+        int d = drop_w[lane];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if (lane == 0) *n_dropped = d;
+        // exclusive scan of kept over E <= 256 experts: lane l owns experts 8l .. 8l+7
+        int v[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            v[i] = e < E ? off[e] : 0;
+            sum += v[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int run = incl - sum;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < E) off[e] = run;
+            run += v[i];
+        }
+        if (lane == 31) off[E] = incl;
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += SMALL_THREADS) offsets[e] = off[e];
+
+    // 3. ranks, in assignment order inside each warp's range
+#pragma unroll
+    for (int i = 0; i < SMALL_PER_LANE; ++i) {
+        if (a0 + 32 * i >= a1) break;   // warp-uniform
+        const int a = a0 + 32 * i + lane;
+        const int e = ev[i];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int intra = __popc(peers & lt_mask);
+        const int pos = e >= 0 ? wh[warp][e] + intra : 0;
+        __syncwarp();
+        if (e >= 0 && intra == 0) wh[warp][e] += __popc(peers);
+        __syncwarp();
+        if (a < a1) {
+            const int j = a / T, t = a - j * T;
+            int32_t row = -1;
+            if (e >= 0 && pos < cap) {
+                row = off[e] + pos;
+                row_token[row] = t;
+                row_gate[row] = gv[i];
+            }
+            slot_row[(size_t)t * k + j] = row;
+        }
+    }
+}
+
 // Row permutation, token-major: one warp per token reads x[t] once and writes
 // it to every kept slot row of the token (slot_row[t, j] >= 0), so a token
 // routed to k experts costs one read and k writes instead of k of each.

@@ -106,13 +106,15 @@ inline int route_tc_splits(long long ntiles, int d)
     if (S > nk) S = nk;
     return S < 1 ? 1 : (int)S;
 }
-// Blocks of the finishing kernel: one lane per token for E <= 32, else one warp
-// per token; up to four blocks per SM (many warps hide the shuffle latency).
+// Blocks of the finishing kernel: one lane per token for E <= 32 (64-thread
+// blocks, up to 16 per SM), else one warp per token (256-thread blocks, up to
+// four per SM: many warps hide the reduction latency).
 inline int route_fin_blocks(long long T, int E)
 {
-    const long long per_block = E <= 32 ? rtc::FIN_THREADS : rtc::FIN_WARPS;
+    const long long per_block = E <= 32 ? rtc::LANE_THREADS : rtc::FIN_WARPS;
+    const long long cap = E <= 32 ? 148 * 16 : 148 * 4;
     const long long b = (T + per_block - 1) / per_block;
-    return (int)(b < 592 ? (b > 0 ? b : 1) : 592);
+    return (int)(b < cap ? (b > 0 ? b : 1) : cap);
 }
 struct RouteTcWs {
     size_t ws_off, part_off, psum_off, cnt_off, total;
@@ -534,7 +536,7 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         const int fgrid = route_fin_blocks(T, E);
         const int Ti = (int)T;
         const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16;
-#define MOE_FIN_LANE(EM, KM) rtc::route_finish_lane_kernel<EM, KM><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
+#define MOE_FIN_LANE(EM, KM) rtc::route_finish_lane_kernel<EM, KM><<<fgrid, rtc::LANE_THREADS, 0, stream>>>( \
     part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum, sel)
 #define MOE_FIN_WARP(EP) rtc::route_finish_warp_kernel<EP><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
     part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum, sel)
@@ -629,14 +631,17 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     const int nchunk = (int)dispatch_chunks(T, k);
     const int cap32 = cap > INT_MAX ? INT_MAX : (int)cap;
     int* hist = (int*)ws;
-    if (nchunk > 0) {
+    if (T * k <= dispatch::SMALL_MAX) {   // one block: no histogram round trip through global memory
+        dispatch::dispatch_small_kernel<<<1, dispatch::SMALL_THREADS, 0, stream>>>(
+            topk_idx, topk_gate, (int)T, k, E, cap32, counts, kept, offsets, slot_row, row_token, row_gate, n_dropped);
+    } else {
         dispatch::hist_kernel<<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T, k, E, hist);
         const moe_status st = launch_status();
         if (st != MOE_OK) return st;
+        dispatch::rank_kernel<<<nchunk, dispatch::THREADS, 0, stream>>>(
+            topk_idx, topk_gate, (int)T, k, E, cap32, hist, nchunk, counts, kept, offsets, slot_row, row_token,
+            row_gate, n_dropped);
     }
-    dispatch::rank_kernel<<<nchunk > 0 ? nchunk : 1, dispatch::THREADS, 0, stream>>>(
-        topk_idx, topk_gate, (int)T, k, E, cap32, hist, nchunk, counts, kept, offsets, slot_row, row_token, row_gate,
-        n_dropped);
     moe_status st = launch_status();
     if (st != MOE_OK || rows_max == 0 || !x_perm) return st;   // x_perm NULL: the up GEMM gathers from x
     const int vec16 = d * esize(xdt) / 16;
@@ -836,10 +841,10 @@ moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const int3
     return moe_expert_down(h, offsets, kept, E, d, F, dtype, w2, row_gate, rows_max, y_perm, stream);
 }
 
-moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d, moe_dtype dtype, void* y,
-                       moe_stream_t stream_)
+namespace {
+moe_status combine_impl(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d, moe_dtype dtype, void* y,
+                        combine::AuxArgs aux, cudaStream_t stream)
 {
-    cudaStream_t stream = (cudaStream_t)stream_;
     if (T < 0 || k < 1 || k > MAX_K || d <= 0 || !dtype_ok(dtype) || T * k >= INT_MAX) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!slot_row || !y || !y_perm)) return MOE_ERR_INVALID_ARG;
     if (!all_aligned16({y_perm, y})) return MOE_ERR_UNSUPPORTED;
@@ -850,11 +855,27 @@ moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, i
     if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
     if (dtype == MOE_BF16)
         combine::combine_kernel<true><<<(int)grid, combine::THREADS, 0, stream>>>((const uint4*)y_perm, slot_row,
-                                                                                  (int)T, k, vec16, (uint4*)y);
+                                                                                  (int)T, k, vec16, (uint4*)y, aux);
     else
         combine::combine_kernel<false><<<(int)grid, combine::THREADS, 0, stream>>>((const uint4*)y_perm, slot_row,
-                                                                                   (int)T, k, vec16, (uint4*)y);
+                                                                                   (int)T, k, vec16, (uint4*)y, aux);
     return launch_status();
+}
+}  // namespace
+
+moe_status moe_combine(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d, moe_dtype dtype, void* y,
+                       moe_stream_t stream)
+{
+    return combine_impl(y_perm, slot_row, T, k, d, dtype, y, combine::AuxArgs{}, (cudaStream_t)stream);
+}
+
+moe_status moe_combine_aux(const void* y_perm, const int32_t* slot_row, int64_t T, int k, int d, moe_dtype dtype,
+                           void* y, const int32_t* counts, const float* prob_sum, int E, float alpha, float* loss,
+                           moe_stream_t stream)
+{
+    if (T < 1 || E < 1 || E > MAX_E || !counts || !prob_sum || !loss) return MOE_ERR_INVALID_ARG;
+    return combine_impl(y_perm, slot_row, T, k, d, dtype, y, combine::AuxArgs{counts, prob_sum, (long long)T, E, alpha, loss},
+                        (cudaStream_t)stream);
 }
 
 moe_status moe_aux_loss(const int32_t* counts, const float* prob_sum, int64_t T, int E, float alpha, float* loss,

@@ -214,8 +214,10 @@ route_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     }
 }
 
-constexpr int FIN_THREADS = 256;
+constexpr int FIN_THREADS = 256;   // warp-per-token finisher
 constexpr int FIN_WARPS = FIN_THREADS / 32;
+constexpr int LANE_THREADS = 64;   // lane-per-token finisher: small blocks spread few tokens over many SMs
+constexpr int LANE_WARPS = LANE_THREADS / 32;
 
 // Sum of the S partial logits of token t, expert e, in split order (four
 // loads in flight at a time).
@@ -236,13 +238,14 @@ __device__ __forceinline__ float sum_splits(const float* __restrict__ part, int 
 }
 
 // Per-block probability sums (rows in warp order) -> psum[block].
+template <int NW>
 __device__ __forceinline__ void block_prob_sums(float (*red)[256], int E, float* __restrict__ psum)
 {
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += FIN_THREADS) {
+    for (int e = threadIdx.x; e < E; e += NW * 32) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < FIN_WARPS; ++w) v += red[w][e];
+        for (int w = 0; w < NW; ++w) v += red[w][e];
         psum[(size_t)blockIdx.x * E + e] = v;
     }
 }
@@ -267,12 +270,12 @@ __global__ void __launch_bounds__(256) prob_sum_kernel(const float* __restrict__
 
 // E <= 32: one lane per token, its E logits in registers.
 template <int EMAX, int KMAX>
-__global__ void __launch_bounds__(FIN_THREADS)
+__global__ void __launch_bounds__(LANE_THREADS)
 route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, int E_pad, int k, int renorm,
                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                          float* __restrict__ gate_out, float* __restrict__ psum, RouteSel sel)
 {
-    __shared__ float red[FIN_WARPS][256];
+    __shared__ float red[LANE_WARPS][256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float bia[EMAX], acc_p[EMAX];
     int grp[EMAX];
@@ -282,7 +285,7 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
         acc_p[e] = 0.f;
         grp[e] = e / sel.gsz;
     }
-    for (int t = (blockIdx.x * FIN_WARPS + warp) * 32 + lane; t < T; t += gridDim.x * FIN_THREADS) {
+    for (int t = (blockIdx.x * LANE_WARPS + warp) * 32 + lane; t < T; t += gridDim.x * LANE_THREADS) {
         float l[EMAX];
         // this token's E_pad partial logits of split 0, then the other splits in order
 #pragma unroll
@@ -294,16 +297,28 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
             l[e4 + 2] = a.z;
             l[e4 + 3] = a.w;
         }
-        for (int sp = 1; sp < S; ++sp) {
+        for (int sp = 1; sp < S; sp += 2) {   // two splits' loads in flight, added in split order
             const float* row = part + ((size_t)sp * T + t) * E_pad;
+            const bool two = sp + 1 < S;
+            float4 q[EMAX / 4], r[EMAX / 4];
 #pragma unroll
             for (int e4 = 0; e4 < EMAX; e4 += 4) {
-                if (e4 < E_pad) {
-                    const float4 a = __ldcg(reinterpret_cast<const float4*>(row + e4));
-                    l[e4] += a.x;
-                    l[e4 + 1] += a.y;
-                    l[e4 + 2] += a.z;
-                    l[e4 + 3] += a.w;
+                const bool in = e4 < E_pad;
+                q[e4 / 4] = in ? __ldcg(reinterpret_cast<const float4*>(row + e4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                r[e4 / 4] = (in && two) ? __ldcg(reinterpret_cast<const float4*>(row + (size_t)T * E_pad + e4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int e4 = 0; e4 < EMAX; e4 += 4) {
+                l[e4] += q[e4 / 4].x;
+                l[e4 + 1] += q[e4 / 4].y;
+                l[e4 + 2] += q[e4 / 4].z;
+                l[e4 + 3] += q[e4 / 4].w;
+                if (two) {
+                    l[e4] += r[e4 / 4].x;
+                    l[e4 + 1] += r[e4 / 4].y;
+                    l[e4 + 2] += r[e4 / 4].z;
+                    l[e4 + 3] += r[e4 / 4].w;
                 }
             }
         }
@@ -391,7 +406,7 @@ route_finish_lane_kernel(const float* __restrict__ part, int S, int T, int E, in
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) red[warp][e] = v;
     }
-    block_prob_sums(red, E, psum);
+    block_prob_sums<LANE_WARPS>(red, E, psum);
 }
 
 // Order-preserving map of a float onto uint32 (a < b  <=>  key(a) < key(b) for
@@ -521,7 +536,7 @@ route_finish_warp_kernel(const float* __restrict__ part, int S, int T, int E, in
     }
 #pragma unroll
     for (int i = 0; i < EPL; ++i) red[warp][lane + 32 * i] = acc_p[i];
-    block_prob_sums(red, E, psum);
+    block_prob_sums<FIN_WARPS>(red, E, psum);
 }
 
 }  // namespace rtc
