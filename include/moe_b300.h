@@ -478,6 +478,12 @@ moe_status moe_set_gemm_kernel(int kind);
  * any other value. */
 moe_status moe_set_gemm_tile_n(int bn);
 
+/* Tile order of the weight-gradient GEMMs (moe_expert_wgrad,
+ * moe_expert_wgrad_rows) inside each expert: 0 (default) automatic
+ * (N-fastest), 1 M-fastest, 2 N-fastest.  The results do not depend on it.
+ * Process-wide; for tests and tuning.  MOE_ERR_INVALID_ARG otherwise. */
+moe_status moe_set_wgrad_order(int order);
+
 /* Launches one block that waits, under the current limit, on a barrier that
  * nothing ever completes, so that a test can watch the time-limit path end
  * in MOE_ERR_TIMEOUT from moe_check() with the context still usable. */

@@ -114,6 +114,10 @@ def test_gemm_tile_width_setter_validates():
     assert L.moe_set_gemm_tile_n(100) == 1
     assert L.moe_set_gemm_tile_n(192) == 0
     assert L.moe_set_gemm_tile_n(0) == 0
+    assert L.moe_set_wgrad_order(3) == 1
+    assert L.moe_set_wgrad_order(-1) == 1
+    assert L.moe_set_wgrad_order(1) == 0
+    assert L.moe_set_wgrad_order(0) == 0
 
 
 def test_binding_rejects_unsupported_dtype():

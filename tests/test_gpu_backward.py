@@ -267,6 +267,27 @@ def test_router_grads_no_tokens():
     assert bool((dW == 0).all()) and bool((db == 0).all())
 
 
+def test_weight_gradient_tile_orders_agree():
+    """M-fastest and N-fastest tile orders give the same bits (the order only
+    changes which blocks run together)."""
+    cfg = CASES["swiglu_e8"][0]
+    case = make_case(cfg)
+    plan = moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, case["cap"], "cuda", cfg.alpha,
+                       cfg.renorm, train=True)
+    plan.run(case["x"], case["W"], case["b"], case["w1"], case["w2"])
+    dy = _dy(cfg).cuda()
+    out = {}
+    try:
+        for order in (1, 2):
+            moe.set_wgrad_order(order)
+            g = plan.backward(case["x"], case["W"], case["w1"], case["w2"], dy)
+            out[order] = (g["dw1"].clone(), g["dw2"].clone())
+    finally:
+        moe.set_wgrad_order(0)
+    moe.check()
+    assert torch.equal(out[1][0], out[2][0]) and torch.equal(out[1][1], out[2][1])
+
+
 def test_expert_wgrad_rows_no_rows_gives_zeros():
     kept = torch.zeros(3, dtype=torch.int32, device="cuda")
     offsets = torch.zeros(4, dtype=torch.int32, device="cuda")

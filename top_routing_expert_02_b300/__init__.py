@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "MoEError", "lib", "capacity", "perm_rows_max", "workspace_bytes", "route", "z_loss", "dispatch", "expert_up",
     "expert_up_gathered", "expert_up_z", "expert_down", "expert_dgrad", "expert_dgrad_act", "permute_rows", "transpose_experts", "combine_bwd", "act_bwd", "wgrad_cols",
-    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "router_grads", "expert_ffn", "combine", "combine_aux", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_gemm_kernel", "selftest_wait_timeout",
+    "pack_segments_t", "expert_wgrad", "expert_wgrad_rows", "route_bwd", "grad_x", "router_wgrad", "router_grads", "expert_ffn", "combine", "combine_aux", "aux_loss", "check", "dispatch_noalloc", "set_wait_limit", "set_gemm_tile_n", "set_wgrad_order", "set_gemm_kernel", "selftest_wait_timeout",
     "MoEPlan", "moe_forward", "ACT", "CALL",
 ]
 
@@ -89,6 +89,7 @@ _SIGS = {
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
     "moe_set_gemm_tile_n": (_I32, [_I32]),
+    "moe_set_wgrad_order": (_I32, [_I32]),
     "moe_set_gemm_kernel": (_I32, [_I32]),
     "moe_selftest_wait_timeout": (_I32, [_P]),
 }
@@ -189,6 +190,11 @@ def set_wait_limit(cycles: int):
 def set_gemm_tile_n(bn: int):
     """Force the bf16 expert GEMM tile width (128, 192, 256) or 0 for automatic."""
     _ok("moe_set_gemm_tile_n", lib().moe_set_gemm_tile_n(int(bn)))
+
+
+def set_wgrad_order(order: int):
+    """Weight-gradient tile order: 0 automatic, 1 M-fastest, 2 N-fastest (results unchanged)."""
+    _ok("moe_set_wgrad_order", lib().moe_set_wgrad_order(int(order)))
 
 
 def set_gemm_kernel(kind: int):

@@ -88,6 +88,7 @@ struct Args {
     int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
     int m_rows;                 // weight gradient: rows M of each expert's gradient
     int lda;                    // MODE_WGRAD_ROWS: row stride of A in elements (>= m_rows)
+    int n_fastest;              // weight-gradient modes: tile order N-fastest inside an expert
     unsigned long long wait_limit;
 };
 
@@ -114,11 +115,19 @@ struct Args {
 //                never leak in; output as MODE_WGRAD
 enum { MODE_ROWS = 0, MODE_GATHER = 1, MODE_WGRAD = 2, MODE_BMN = 3, MODE_WGRAD_ROWS = 4 };
 
+// Tile -> (expert, M-tile, N-tile): M-fastest inside an expert, so the blocks
+// running together share the B tile (the weights); n_fastest: N-fastest, so
+// they share the A tile instead.
 __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tiles, int tile, int& e, int& m,
-                                            int& n)
+                                            int& n, bool n_fastest = false)
 {
     e = find_expert(mstart, E, tile / n_tiles);
     const int local = tile - mstart[e] * n_tiles;
+    if (n_fastest) {
+        m = local / n_tiles;
+        n = local - m * n_tiles;
+        return;
+    }
     const int mt = mstart[e + 1] - mstart[e];
     n = local / mt;
     m = local - n * mt;
@@ -225,7 +234,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t roff[GATHER ? 32 : 1];   // gathered rows: this lane's 32 offsets in x
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 int e, m, n;
-                decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+                decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, WGRAD && g.n_fastest);
                 const int rowA = WGRAD ? m * BM : __ldg(g.offsets + e) + m * BM;
                 const int rowB0 = (WGRAD ? 0 : e * g.b_rows) + n * g.n_step;
                 const int rowB1 = rowB0 + g.half_off;
@@ -321,7 +330,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 int nkt = nk, kept_e = 0;
                 if (WGRAD) {
                     int e, m, n;
-                    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+                    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, WGRAD && g.n_fastest);
                     nkt = kstart[e + 1] - kstart[e];   // 0: nothing accumulates, the epilogue writes zeros
                     if (WGR) kept_e = __ldg(g.kept + e);
                 }
@@ -381,7 +390,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t aphase = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             int e, m, n;
-            decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+            decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, WGRAD && g.n_fastest);
             const int rows_valid = WGRAD ? g.m_rows - m * BM : __ldg(g.kept + e) - m * BM;
             const int row = WGRAD ? e * g.m_rows + m * BM + r_in : __ldg(g.offsets + e) + m * BM + r_in;
             const bool rv = r_in < rows_valid;

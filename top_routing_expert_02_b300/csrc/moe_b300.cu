@@ -28,6 +28,16 @@ constexpr int MAX_K = 16;
 constexpr unsigned long long DEFAULT_WAIT_LIMIT = 4000000000ull;   // ~2 s of SM cycles
 std::atomic<unsigned long long> g_wait_limit{DEFAULT_WAIT_LIMIT};
 std::atomic<int> g_forced_bn{0};   // 0: pick the GEMM tile width per call
+std::atomic<int> g_wgrad_order{0};  // weight-gradient tile order: 0 automatic, 1 M-fastest, 2 N-fastest
+
+// Weight-gradient tile order.  N-fastest (the blocks running together share
+// the A tile and write neighbouring column blocks of the same output rows)
+// measured 3-7% faster for dw1 on the e8 and e128 layers and for dw2 on e8,
+// 2-4% slower for dw2 on e128; it is the automatic choice.
+inline int wgrad_n_fastest(int, int)
+{
+    return g_wgrad_order.load() == 1 ? 0 : 1;
+}
 std::atomic<int> g_gemm_kind{0};   // 0 auto, 1 one-SM tiles, 2 CTA-pair tiles
 
 inline bool dtype_ok(int dt) { return dt == MOE_F32 || dt == MOE_BF16; }
@@ -911,6 +921,13 @@ moe_status moe_set_gemm_kernel(int kind)
     return MOE_OK;
 }
 
+moe_status moe_set_wgrad_order(int order)
+{
+    if (order < 0 || order > 2) return MOE_ERR_INVALID_ARG;
+    g_wgrad_order.store(order);
+    return MOE_OK;
+}
+
 moe_status moe_set_gemm_tile_n(int bn)
 {
     if (bn != 0 && bn != 128 && bn != 192 && bn != 256) return MOE_ERR_INVALID_ARG;
@@ -1112,6 +1129,7 @@ moe_status moe_expert_wgrad(const void* at, const void* bt, const int32_t* kept,
     a.out_cols = N;
     a.out_f32 = dw_dtype == MOE_F32 ? (float*)dw : nullptr;
     a.out = dw_dtype == MOE_BF16 ? (uint16_t*)dw : nullptr;
+    a.n_fastest = wgrad_n_fastest(M, N);
     a.wait_limit = g_wait_limit.load();
     return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD>(at, 0, (int)ld, bt, N, a, (cudaStream_t)stream, M);
 }
@@ -1145,6 +1163,7 @@ moe_status moe_expert_wgrad_rows(const void* a, const void* b, const int32_t* of
     g.out_cols = N;
     g.out_f32 = dw_dtype == MOE_F32 ? (float*)dw : nullptr;
     g.out = dw_dtype == MOE_BF16 ? (uint16_t*)dw : nullptr;
+    g.n_fastest = wgrad_n_fastest(M, N);
     g.wait_limit = g_wait_limit.load();
     return launch_tc_bn<tcg::EPI_IDENT, 256, tcg::MODE_WGRAD_ROWS>(a, rows_max, 0, b, 0, g, st);
 }
