@@ -167,6 +167,20 @@ def test_backward_argument_errors():
     assert L.moe_expert_wgrad_rows(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, -1, 1, FAKE, 0, None) == 1    # rows < 0
     assert L.moe_expert_wgrad_rows(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, 640, 0, FAKE, 0, None) == 2   # fp32 inputs
     assert L.moe_route_bwd(FAKE, FAKE, FAKE, None, 16, 8, 2, 1, f(0.1), f(0.0), FAKE, None) == 1
+    # moe_router_grads(dx_perm, slot_row, dl, W, x, T, k, E, d, dtype, dx, dW, db, ws, ws_bytes, stream)
+    rg = lambda **o: L.moe_router_grads(o.get("dxp", FAKE), FAKE, FAKE, FAKE, o.get("x", FAKE), o.get("T", 64),
+                                        o.get("k", 2), o.get("E", 8), o.get("d", 128), o.get("dt", 1), FAKE,
+                                        o.get("dW", FAKE), FAKE, o.get("ws", FAKE), o.get("wsb", 1 << 30), None)
+    assert rg(k=0) == 1 and rg(E=0) == 1 and rg(T=-1) == 1 and rg(dW=None) == 1 and rg(x=None) == 1
+    assert rg(d=96) == 2                 # d % 64
+    assert rg(dt=0) == 2                 # bf16 only
+    assert rg(dxp=ctypes.c_void_p(0x1008)) == 2   # 16-byte alignment
+    assert rg(wsb=16) == 3               # workspace too small
+    assert L.moe_workspace_bytes(4, 4096, 4096, 8, 2, 64, 0, 1) > 4096 * 4096 * 4   # holds the fp32 dl . W
+    # moe_combine_aux(y_perm, slot_row, T, k, d, dtype, y, counts, prob_sum, E, alpha, loss, stream)
+    assert L.moe_combine_aux(FAKE, FAKE, 0, 2, 128, 1, FAKE, FAKE, FAKE, 8, f(0.01), FAKE, None) == 1   # T >= 1
+    assert L.moe_combine_aux(FAKE, FAKE, 16, 2, 128, 1, FAKE, FAKE, FAKE, 8, f(0.01), None, None) == 1
+    assert L.moe_combine_aux(FAKE, FAKE, 16, 2, 120, 1, FAKE, FAKE, FAKE, 8, f(0.01), FAKE, None) == 2  # d % 64
     assert L.moe_route_bwd(FAKE, FAKE, FAKE, FAKE, 16, 8, 9, 1, f(0.1), f(0.0), FAKE, None) == 1
     assert L.moe_grad_x(FAKE, FAKE, FAKE, None, 16, 2, 8, 128, 1, FAKE, None) == 1
     assert L.moe_router_wgrad(FAKE, FAKE, 1, 0, 8, 128, FAKE, None, FAKE, 1 << 20, None) == 1
