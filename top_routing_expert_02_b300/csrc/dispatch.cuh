@@ -63,6 +63,7 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
     int my_drop = 0;
     for (int e = tid; e < E; e += THREADS) {
         int before = 0, total = 0;
+#pragma unroll 8
         for (int c = 0; c < nchunk; ++c) {
             const int v = __ldg(hist + (size_t)c * E + e);
             if (c < chunk) before += v;
@@ -98,10 +99,26 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
     if (chunk == 0)
         for (int e = tid; e <= E; e += THREADS) offsets[e] = off[e];
 
-    // 3. stable rank inside the chunk, THREADS assignments per round
+    // 3. stable rank inside the chunk, THREADS assignments per round; every
+    //    round's expert id and gate are loaded up front (one memory latency)
     const long long n = (long long)T * k;
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int r = 0; r < CHUNK / THREADS; ++r) {
+    constexpr int ROUNDS = CHUNK / THREADS;
+    int ev[ROUNDS];
+    float gv[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const long long a = (long long)chunk * CHUNK + (long long)r * THREADS + tid;
+        ev[r] = -1;
+        gv[r] = 0.f;
+        if (a < n) {
+            const int j = (int)(a / T), t = (int)(a - (long long)j * T);
+            ev[r] = __ldg(idx + (size_t)t * k + j);
+            gv[r] = __ldg(gate + (size_t)t * k + j);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
         for (int v = tid; v < WARPS * E; v += THREADS) wcnt[v / E][v % E] = 0;
         __syncthreads();
         const long long a = (long long)chunk * CHUNK + (long long)r * THREADS + tid;
@@ -109,7 +126,7 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
         if (a < n) {
             j = (int)(a / T);
             t = (int)(a - (long long)j * T);
-            e = __ldg(idx + (size_t)t * k + j);
+            e = ev[r];
             if (e < 0 || e >= E) e = -2;   // flagged by hist_kernel; the slot is dropped
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -124,7 +141,7 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
                 if (pos < cap) {
                     row = off[e] + pos;
                     row_token[row] = t;
-                    row_gate[row] = __ldg(gate + (size_t)t * k + j);
+                    row_gate[row] = gv[r];
                 }
             }
             slot_row[(size_t)t * k + j] = row;
