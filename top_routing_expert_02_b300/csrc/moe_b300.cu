@@ -106,12 +106,17 @@ inline bool route_tc_shape(int E, RouteTcShape* s)
 }
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 // Split-K factor of the tensor-core router: as many splits as keep ntiles * S
-// within one wave of the 148 SMs (rounding up would start a second, mostly
-// empty wave), at most MAX_SPLITS and at most one split per K block.
-inline int route_tc_splits(long long ntiles, int d)
+// within the blocks that can be resident at once (rounding up would start a
+// second, mostly empty wave), at most MAX_SPLITS and at most one split per K
+// block.  Two blocks fit on an SM when two rings of 4 stages and two
+// accumulators do (small E), else one.
+inline int route_tc_splits(long long ntiles, int d, const RouteTcShape& sh)
 {
     const int nk = d / rtc::BK;
-    long long S = 148 / (ntiles > 0 ? ntiles : 1);
+    const int stage = rtc::A_BYTES + 3 * sh.E_pad * 128;
+    const bool two = 2 * (4 * stage + 1024) <= 227 * 1024 && 2 * sh.tmem_cols <= 512;
+    const long long resident = two ? 2 * 148 : 148;
+    long long S = resident / (ntiles > 0 ? ntiles : 1);
     if (S > rtc::MAX_SPLITS) S = rtc::MAX_SPLITS;
     if (S > nk) S = nk;
     return S < 1 ? 1 : (int)S;
@@ -132,7 +137,7 @@ struct RouteTcWs {
 inline RouteTcWs route_tc_ws(long long T, int d, int E, const RouteTcShape& sh)
 {
     const long long ntiles = (T + rtc::BM - 1) / rtc::BM;
-    const int S = route_tc_splits(ntiles, d);
+    const int S = route_tc_splits(ntiles, d, sh);
     RouteTcWs w;
     w.ws_off = 0;
     w.part_off = align256((size_t)3 * sh.E_pad * d * 2);
@@ -508,7 +513,7 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         float* part = (float*)((char*)ws + wl.part_off);
         float* psum = (float*)((char*)ws + wl.psum_off);
         const int ntiles = (int)((T + rtc::BM - 1) / rtc::BM);
-        const int S = route_tc_splits(ntiles, d);
+        const int S = route_tc_splits(ntiles, d, sh);
         const long long nsplit = (long long)sh.E_pad * d;
         int sgrid = (int)((nsplit + 255) / 256);
         if (sgrid > sm_count() * 4) sgrid = sm_count() * 4;
