@@ -77,7 +77,9 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     dispatch = ranks + (0 if gather else 1)      # (+ row copy)
     z = 1 if (args and args.z_beta is not None) else 0
     bwd = BWD_KERNELS if (args and args.train) else 0
-    return route + dispatch + 1 + 1 + 1 + z + bwd   # up, down, combine with the aux loss (+ z-loss) (+ backward)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    aux = 1 if (world > 1 and not (args and args.train)) else 0   # replicas: the global aux loss is its own launch
+    return route + dispatch + 1 + 1 + 1 + aux + z + bwd   # up, down, combine (+ aux) (+ z-loss) (+ backward)
 
 
 def plan_kwargs(args) -> dict:
@@ -369,8 +371,14 @@ def our_arm(args, cfg):
         mark(3)
         moe.expert_down(plan.h, D.offsets, D.kept, w2, D.row_gate, plan.rows_max, y_perm=plan.y_perm)
         mark(4)
-        moe.combine_aux(plan.y_perm, D.slot_row, D.kept if plan.aux_post_drop else D.counts, plan.prob_sum,
-                        plan.alpha, y=plan.y, loss=plan.loss)
+        f_counts = D.kept if plan.aux_post_drop else D.counts
+        if world > 1:
+            # token-sharded replicas: the aux loss spans all shards (one all-reduce of 2E sums)
+            moe.combine(plan.y_perm, D.slot_row, y=plan.y)
+            c, p, t = mdist.global_aux_inputs(f_counts, plan.prob_sum, plan.T, T_total=world * plan.T)
+            moe.aux_loss(c, p, t, plan.alpha, loss=plan.loss)
+        else:
+            moe.combine_aux(plan.y_perm, D.slot_row, f_counts, plan.prob_sum, plan.alpha, y=plan.y, loss=plan.loss)
         if plan.z_beta is not None:
             moe.z_loss(plan.lse, plan.z_beta, loss=plan.z_loss)
         mark(5)

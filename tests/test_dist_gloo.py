@@ -39,8 +39,11 @@ def _worker(rank, world, port, out_dir):
     counts, _, _, _ = oracle.dispatch(idx, E, cap)
     c, p, t = mdist.global_aux_inputs(torch.from_numpy(counts), torch.from_numpy(ps), T)
     loss = oracle.aux_loss(c.numpy(), p.numpy().astype(np.float64), t, alpha)
+    # the host-sync-free form (total token count known): the same sums
+    c2, p2, t2 = mdist.global_aux_inputs(torch.from_numpy(counts), torch.from_numpy(ps), T, T_total=50 + 57)
+    same = float(torch.equal(c, c2) and torch.equal(p, p2) and t2 == t)
     worst = mdist.max_over_ranks(1.0 + rank)
-    np.save(os.path.join(out_dir, f"r{rank}.npy"), np.array([loss, t, worst]))
+    np.save(os.path.join(out_dir, f"r{rank}.npy"), np.array([loss, t, worst, same]))
     dist.destroy_process_group()
 
 
@@ -60,3 +63,4 @@ def test_two_gloo_ranks_reproduce_whole_batch_aux_loss(tmp_path):
         assert int(r[1]) == x.shape[0]
         assert abs(r[0] - whole) <= 1e-6 * whole     # prob sums cross ranks in fp32
         assert r[2] == 2.0
+        assert r[3] == 1.0

@@ -17,17 +17,22 @@ import torch.distributed as dist
 __all__ = ["global_aux_inputs", "global_aux_loss", "max_over_ranks"]
 
 
-def global_aux_inputs(counts: torch.Tensor, prob_sum: torch.Tensor, T: int, group=None):
+def global_aux_inputs(counts: torch.Tensor, prob_sum: torch.Tensor, T: int, group=None, T_total=None):
     """Sum this rank's counts [E], prob_sum [E] and T over all ranks.
 
     Returns (counts int32 [E], prob_sum fp32 [E], T_total) on the inputs' device.
     The probability sums travel as fp64 so the reduction adds no rounding of
-    its own beyond the final conversion."""
-    packed = torch.cat([counts.to(torch.float64), prob_sum.to(torch.float64),
-                        torch.tensor([float(T)], dtype=torch.float64, device=counts.device)])
+    its own beyond the final conversion.  A caller that knows the total token
+    count passes ``T_total``: then only the 2E sums are reduced and nothing
+    waits on the host (no device-to-host read), so the step stays asynchronous."""
+    parts = [counts.to(torch.float64), prob_sum.to(torch.float64)]
+    if T_total is None:
+        parts.append(torch.tensor([float(T)], dtype=torch.float64, device=counts.device))
+    packed = torch.cat(parts)
     dist.all_reduce(packed, op=dist.ReduceOp.SUM, group=group)
     E = counts.numel()
-    return (packed[:E].round().to(torch.int32), packed[E:2 * E].to(torch.float32), int(packed[2 * E].item()))
+    total = int(packed[2 * E].item()) if T_total is None else int(T_total)
+    return packed[:E].round().to(torch.int32), packed[E:2 * E].to(torch.float32), total
 
 
 def global_aux_loss(counts: torch.Tensor, prob_sum: torch.Tensor, T: int, alpha: float, group=None):
