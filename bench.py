@@ -624,31 +624,60 @@ def train_arm(args, cfg):
     del graph
 
     # end to end: x and dy from pinned host memory, dx and the loss back; the
-    # weight gradients stay on the device where an optimiser would use them
+    # weight gradients stay on the device where an optimiser would use them.  A
+    # three-stream pipeline (copy in / layer / copy out) over two plans, so step
+    # i+1's input copies and step i-1's output copies overlap step i's layer.
+    plans = [plan, moe.MoEPlan(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.act, torch.bfloat16, cap, dev, cfg.alpha,
+                               cfg.renorm, **plan_kwargs(args))]
+    x_dev, dy_dev = [x, x.clone()], [dy, dy.clone()]
+    graphs = [plans[i].capture(x_dev[i], W, b, w1, w2, dy=dy_dev[i]) for i in range(2)]
     x_host, dyh = ri.x.pin_memory(), dy_host.pin_memory()
-    dx_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
-    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    dx_host = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    loss_host = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp_done = [None, None]
+    out_done = [None, None]
 
-    def e2e_step():
-        x.copy_(x_host, non_blocking=True)
-        dy.copy_(dyh, non_blocking=True)
-        step()
-        dx_host.copy_(plan._bwd["dx"][:cfg.T], non_blocking=True)
-        loss_host.copy_(plan.loss, non_blocking=True)
+    def e2e_step(i):
+        sb = i % 2
+        with torch.cuda.stream(s_in):
+            if comp_done[sb] is not None:
+                s_in.wait_event(comp_done[sb])          # step i-2 no longer reads x_dev[sb], dy_dev[sb]
+            x_dev[sb].copy_(x_host, non_blocking=True)
+            dy_dev[sb].copy_(dyh, non_blocking=True)
+            in_done = torch.cuda.Event()
+            in_done.record(s_in)
+        stream.wait_event(in_done)
+        if out_done[sb] is not None:
+            stream.wait_event(out_done[sb])             # dx of step i-2 has reached the host
+        graphs[sb].replay()                             # forward + backward: one graph launch
+        comp_done[sb] = torch.cuda.Event()
+        comp_done[sb].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[sb])
+            dx_host[sb].copy_(plans[sb]._bwd["dx"][:cfg.T], non_blocking=True)
+            loss_host[sb].copy_(plans[sb].loss, non_blocking=True)
+            out_done[sb] = torch.cuda.Event()
+            out_done[sb].record(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
     barrier()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    s1.record(stream)
+    s0.record(s_in)
+    for i in range(args.warmup, args.warmup + args.steps):
+        e2e_step(i)
+    for ev in out_done:
+        s_out.wait_event(ev)
+    s1.record(s_out)
+    torch.cuda.synchronize(dev)
     barrier()
     moe.check()
     ms_e2e = s0.elapsed_time(s1) / args.steps
     if world > 1:
         ms_e2e = mdist.max_over_ranks(ms_e2e, device=dev)
+    del graphs
 
     hbm, bf16_peak, bf16_sust, peak_src = peaks()
     dw1_flops = 2.0 * A * cfg.N1 * cfg.d
