@@ -1,0 +1,38 @@
+"""bench.py's launch-count claim (`gpu_launches`) against the launch lists
+captured with ncu on the same workloads: nine library kernels per e8_swiglu
+forward step (router 4, one-block dispatch ranks + row scatter 2, up and down
+GEMMs, combine with the aux loss) and 21 per training step; the two-kernel
+dispatch above 16384 assignments; one more for the global aux loss of
+token-sharded replicas."""
+import argparse
+import importlib.util
+import os
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _args(**over):
+    a = dict(gather=False, z_beta=None, train=False)
+    a.update(over)
+    return argparse.Namespace(**a)
+
+
+def test_forward_and_training_launch_counts(monkeypatch):
+    b = _bench()
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    e8 = b.synth.workload("e8_swiglu")
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 9
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(train=True)) == 21
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(gather=True)) == 8          # no row scatter
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(z_beta=1e-3)) == 10         # + z-loss
+    e64 = b.synth.workload("e64_zipf")                                     # T*k = 32768: hist + rank
+    assert b.KERNELS_PER_STEP_TOTAL(e64, _args()) == 10
+    monkeypatch.setenv("WORLD_SIZE", "2")                                  # replicas: + global aux loss
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 10
