@@ -412,7 +412,7 @@ moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64
  * The fp32 dl and w_router enter the bf16 MMAs as hi + lo parts (hi = rn(v),
  * lo = rn(v - hi)): dl . W takes hi.hi + lo.hi + hi.lo, dl^T x takes
  * hi + lo (x is bf16), fp32 accumulation; the relative error of the parts
- * is ~2^-17, far below dx's bf16 rounding.  Sums run in a fixed order
+ * is at most 2^-16 (~2^-17 seen), far below dx's bf16 rounding.  Sums run in a fixed order
  * (bitwise reproducible).  dtype (x, dx_perm, dx) MOE_BF16; d % 64 == 0;
  * 16-byte aligned x, dx_perm, w_router, dx, dW, ws.  ws >=
  * moe_workspace_bytes(MOE_CALL_ROUTER_GRADS, T, d, E, ...) bytes (it holds
