@@ -231,13 +231,15 @@ def _router_grad_refs(dx_perm, slot_row, dl, W, x):
     return dx, dl.double().T @ x.double(), dl.double().sum(0)
 
 
-@pytest.mark.parametrize("T,E,k,d", [(1000, 8, 2, 256), (777, 128, 8, 128), (300, 256, 16, 64), (4097, 64, 2, 512)])
+@pytest.mark.parametrize("T,E,k,d", [(1000, 8, 2, 256), (777, 128, 8, 128), (300, 256, 16, 64), (4097, 64, 2, 512),
+                                     (5, 1, 1, 64), (129, 3, 2, 128)])
 def test_router_grads_on_tensor_cores(T, E, k, d):
     """moe_router_grads (bf16 hi/lo parts on the tensor cores) against fp64:
     dx within one bf16 rounding, dW and db to fp32 accuracy; the CUDA-core
     pair moe_grad_x + moe_router_wgrad against the same references; both
     bitwise reproducible.  The shapes cover E = 8 (padded to 64), E = 256
-    with top-16, d = 64 (one partial N tile) and ragged token splits."""
+    with top-16, d = 64 (one partial N tile), ragged token splits, a single
+    expert with five tokens and three experts over 129 tokens."""
     dx_perm, slot_row, dl, W, x = _router_grad_inputs(T, E, k, d, T + E)
     dx, dW, db = moe.router_grads(dx_perm, slot_row, dl, W, x)
     dx2, dW2, db2 = moe.router_grads(dx_perm, slot_row, dl, W, x)
