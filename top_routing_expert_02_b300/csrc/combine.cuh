@@ -116,14 +116,28 @@ __global__ void aux_loss_kernel(const int32_t* __restrict__ counts, const float*
 // the router's choices; its formula is the one of ST-MoE, Zoph et al. 2022,
 // eq. 5): loss = beta * (1/T) * sum_t lse[t]^2.  One block: each thread sums
 // the squares of its elements (16-byte loads, eight in flight, when lse is
-// 16-byte aligned), then a fixed shared-memory tree in fp64; the result does
-// not depend on timing.
+// 16-byte aligned) in fp32 with Kahan compensation -- a single block has few
+// fp64 units, and compensated fp32 keeps the sum within a few fp32 ulps for
+// any T -- then the per-thread sums go through a fixed shared-memory tree in
+// fp64; the result does not depend on timing.
 constexpr int ZL_THREADS = 1024;
+
+struct Kahan {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float v)
+    {
+        const float y = v - c;
+        const float t = s + y;
+        c = (t - s) - y;
+        s = t;
+    }
+};
+
 __global__ void __launch_bounds__(ZL_THREADS)
 z_loss_kernel(const float* __restrict__ lse, long long T, float beta, float* __restrict__ loss)
 {
     __shared__ double sh[ZL_THREADS];
-    double s = 0.0;
+    Kahan k;
     long long done = 0;
     if ((reinterpret_cast<uintptr_t>(lse) & 15u) == 0) {
         const float4* v = reinterpret_cast<const float4*>(lse);
@@ -136,17 +150,20 @@ z_loss_kernel(const float* __restrict__ lse, long long T, float beta, float* __r
                 q[u] = i < n4 ? __ldg(v + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                s += (double)q[u].x * q[u].x + (double)q[u].y * q[u].y + (double)q[u].z * q[u].z +
-                     (double)q[u].w * q[u].w;
+            for (int u = 0; u < 8; ++u) {
+                k.add(q[u].x * q[u].x);
+                k.add(q[u].y * q[u].y);
+                k.add(q[u].z * q[u].z);
+                k.add(q[u].w * q[u].w);
+            }
         }
         done = n4 * 4;
     }
     for (long long t = done + threadIdx.x; t < T; t += ZL_THREADS) {
-        const double x = (double)__ldg(lse + t);
-        s += x * x;
+        const float x = __ldg(lse + t);
+        k.add(x * x);
     }
-    sh[threadIdx.x] = s;
+    sh[threadIdx.x] = (double)k.s - (double)k.c;
     __syncthreads();
     for (int w = ZL_THREADS / 2; w > 0; w >>= 1) {
         if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
