@@ -131,19 +131,12 @@ def ep_forward(x, W, b, w1_local, w2_local, *, k: int, cap: int, act: str, renor
     _a2a(x_recv, x_send, out_splits, in_splits, group)
     _a2a(g_recv, g_send, out_splits, in_splits, group)
 
-    # regroup: received [src][local expert] blocks -> [local expert][src] segments
-    starts = torch.zeros((G, El), dtype=torch.int64)
-    pos = 0
-    for s in range(G):
-        for e in range(El):
-            starts[s, e] = pos
-            pos += int(recv_counts[s, e])
-    order = []
-    for e in range(El):
-        for s in range(G):
-            n = int(recv_counts[s, e])
-            order.extend(range(int(starts[s, e]), int(starts[s, e]) + n))
-    perm = torch.tensor(order, dtype=torch.int64)
+    # regroup: received [src][local expert] blocks -> [local expert][src] segments;
+    # every received row gets the key (local expert, src) of its block, and a
+    # stable sort of the keys is the permutation (rows keep their order inside a block)
+    block_key = (torch.arange(El, dtype=torch.int64)[None, :] * G + torch.arange(G, dtype=torch.int64)[:, None])
+    row_key = torch.repeat_interleave(block_key.reshape(-1), recv_counts.reshape(-1).to(torch.int64))
+    perm = torch.argsort(row_key, stable=True)
     kept_loc = recv_counts.sum(0).to(torch.int32)
     off_loc = torch.zeros(El + 1, dtype=torch.int32)
     off_loc[1:] = torch.cumsum(kept_loc, 0)
