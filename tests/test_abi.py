@@ -35,6 +35,12 @@ def test_library_exports_every_declared_function():
     assert L.moe_abi_version() == 1
 
 
+def test_binding_declares_a_signature_for_every_function():
+    src = open(os.path.join(ROOT, "top_routing_expert_02_b300", "__init__.py")).read()
+    missing = [n for n in declared_functions() if f'"{n}"' not in src]
+    assert not missing, missing
+
+
 def _golden_caps():
     rows = []
     for line in open(GOLDEN):
