@@ -6,8 +6,10 @@
 
 A step is one whole layer forward (route, dispatch, expert up/down GEMMs,
 combine, aux loss) over one batch of seeded synthetic tokens already resident
-in HBM.  Default workload: bf16, T=4096 tokens, d=4096, 8 experts, top-2,
-SwiGLU d_ff=14336, capacity factor 1.25.
+in HBM.  Default workload: the largest single-GPU configuration, bf16,
+T=32768 tokens, d=4096, 128 experts, top-8, SwiGLU d_ff=1536, dropless
+(``--workload`` selects the others, e.g. e8_swiglu: T=4096, 8 experts, top-2,
+SwiGLU d_ff=14336, capacity factor 1.25).
 
 Timing: W untimed warm-up steps; then K steps, each preceded (outside the
 timed events) by a 512 MB write that flushes the 126 MB L2; CUDA events on
@@ -23,6 +25,16 @@ buffer sets (copy-in of step i+1 and copy-out of step i-1 overlap step i).
 ``roofline``: the dominant kernel (the expert up-projection GEMM) -- its
 algorithmic FLOPs (2 * kept slots * d * N1) over its CUDA-event duration,
 against the measured dense bf16 peak.
+
+``roofline_hbm``: the three bandwidth-bound calls (route, dispatch, combine
+with the aux loss) -- each one's algorithmic bytes (below) over its CUDA-event
+duration, against the measured HBM copy bandwidth and against 8 TB/s:
+  route     T*d*b (x) + E*d*4 (router weight) + T*k*8 (indices, gates)
+  dispatch  T*k*8 (indices, gates read) + T*k*4 (slot rows) + A*8 (row maps)
+            + T_u*d*b (x rows of tokens with a kept slot) + A*d*b (x_perm)
+  combine   A*d*b (y_perm) + T*d*b (y) + T*k*4 (slot rows)
+with A the kept slots, T_u the tokens with at least one kept slot and b the
+bytes of one element.
 
 ``cpu_baseline`` (rank 0, N=1): the CPU oracle timed on a bounded sample of
 the same workload (its first S tokens, capacity recomputed for S tokens).
@@ -301,6 +313,28 @@ def config_dict(cfg, args=None):
                   "host-to-device copy every step, weights (GBs) exceed L2"}
 
 
+def hbm_bytes(cfg, A: int, T_used: int, esz: int, gather: bool = False) -> dict:
+    """Algorithmic HBM bytes of one call of each bandwidth-bound step (the
+    minimum any implementation must move: every input read once, every output
+    written once)."""
+    T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+    route = T * d * esz + E * d * 4 + T * k * 8
+    dispatch = T * k * 8 + T * k * 4 + A * 8 + (0 if gather else T_used * d * esz + A * d * esz)
+    combine = A * d * esz + T * d * esz + T * k * 4
+    return {"route": route, "dispatch": dispatch, "combine_aux": combine}
+
+
+def hbm_rooflines(cfg, A, T_used, esz, part, hbm_gbs, peak_src, gather=False) -> dict:
+    out = {}
+    for name, nbytes in hbm_bytes(cfg, A, T_used, esz, gather).items():
+        ms = statistics.mean(part[name])
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"bound": "hbm", "bytes": nbytes, "us": 1000.0 * ms, "achieved": gbs, "peak": hbm_gbs,
+                     "unit": "GB/s", "frac": gbs / hbm_gbs, "frac_of_8TBs": gbs / 8000.0,
+                     "peak_source": f"{peak_src} HBM copy"}
+    return out
+
+
 def traffic_from_profile(kernel_src: str, workload: str):
     """DRAM bytes per launch of the up-projection GEMM from the committed ncu
     summary, only for the workload it was captured for and only while the
@@ -395,6 +429,7 @@ def our_arm(args, cfg):
     A = int(D.offsets[plan.E].item())
     n_drop = int(D.n_dropped.item())
     counts = D.counts.cpu()
+    T_used = int((D.slot_row >= 0).any(dim=1).sum().item()) if cfg.T > 0 else 0
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
@@ -522,8 +557,9 @@ def our_arm(args, cfg):
         "gemm_tflops": gemm_tflops, "gemm_frac_of_peak": gemm_tflops / bf16_peak,
         "graph_ms_per_step": ms_graph, "graph_tokens_per_s": world * cfg.T / (ms_graph / 1000.0),
         "kernel_ms": {k: statistics.mean(v) for k, v in part.items()},
-        "routing": {"kept_slots": A, "dropped_slots": n_drop, "max_over_mean_load":
-                    float(counts.max()) / (cfg.T * cfg.k / cfg.E)},
+        "routing": {"kept_slots": A, "dropped_slots": n_drop, "tokens_with_a_kept_slot": T_used,
+                    "max_over_mean_load": float(counts.max()) / (cfg.T * cfg.k / cfg.E)},
+        "roofline_hbm": hbm_rooflines(cfg, A, T_used, esz, part, hbm, peak_src, gather=args.gather),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb, _, _ = oracle_sample(cfg, ri, w1, w2, variant=oracle_variant(args))
@@ -743,7 +779,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="e8_swiglu", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="e128_top8_T32768", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-group", type=int, default=1, help="group-limited routing: contiguous expert groups")

@@ -22,7 +22,7 @@ import oracle
 import top_routing_expert_02_b300 as moe
 from top_routing_expert_02_b300 import synth
 
-GATE_RTOL = {"f32": 1e-5, "bf16": 2e-4}
+GATE_RTOL = {"f32": 1e-5, "bf16": 1e-5}
 Y_TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 

@@ -28,9 +28,9 @@ SMALL = {
     "gelu_e32_norenorm": C("gelu_e32_norenorm", 900, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False),
     # fp32 x with E=200 (8 experts per lane), through the fp32 FFN
     "f32_e200": C("f32_e200", 400, 128, 200, 3, 128, "swiglu", 2.0, "f32"),
-    # bf16 x with E=200: above the tensor-core router's 160 experts -> CUDA-core router
+    # bf16 x with E=200: above the tensor-core router's 128 experts -> CUDA-core router
     "bf16_e200": C("bf16_e200", 257, 128, 200, 2, 128, "gelu", 0.0, "bf16"),
-    # bf16, E=160 (largest tensor-core router: two 240-column MMAs), top-16
+    # bf16, E=160, top-16: above the tensor-core router's 128 experts -> CUDA-core router
     "bf16_e160_top16": C("bf16_e160_top16", 300, 192, 160, 16, 128, "swiglu", 0.0, "bf16", renorm=False),
     # fewer tokens than one 128-row tile, and fewer kept rows than one GEMM tile
     "small_T": C("small_T", 50, 128, 8, 2, 128, "swiglu", 1.25, "bf16"),

@@ -19,7 +19,7 @@
 #include "ffn_tc.cuh"
 #include "ffn_tc2.cuh"
 #include "route.cuh"
-#include "route_tc.cuh"
+#include "route_fused.cuh"
 
 namespace {
 
@@ -53,6 +53,18 @@ inline moe_status launch_status()
     return MOE_OK;
 }
 
+// Status of a cudaLaunchKernelEx call (its error is also cleared from the
+// runtime's last-error slot).
+inline moe_status launch_ex_status(cudaError_t e)
+{
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "moe_b300: CUDA launch error: %s\n", cudaGetErrorString(e));
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;
@@ -80,77 +92,47 @@ inline size_t route_ws_bytes_simt(long long T, int E)
     return (size_t)nblk * E * sizeof(float);
 }
 
-// Tensor-core router shape: E_pad experts per weight part, one or two MMAs of nb_rows.
-struct RouteTcShape {
-    int E_pad, nb_chunks, nb_rows;
+// Fused tensor-core router (bf16 x, E <= 128): launch shape.
+struct RouteFuShape {
+    int E_pad, cps, S, stages, stage_bytes, smem, ntiles, grid;
     uint32_t tmem_cols;
 };
-inline bool route_tc_shape(int E, RouteTcShape* s)
+inline bool route_fu_shape(long long T, int d, int E, RouteFuShape* s)
 {
-    if (E > rtc::MAX_EPAD) return false;
-    int ep = (E + 15) / 16 * 16;
-    if (3 * ep <= 256) {
-        s->E_pad = ep;
-        s->nb_chunks = 1;
-        s->nb_rows = 3 * ep;
-    } else {
-        ep = (E + 31) / 32 * 32;
-        s->E_pad = ep;
-        s->nb_chunks = 2;
-        s->nb_rows = 3 * ep / 2;
-    }
+    if (E > rfu::MAX_EPAD || T <= 0 || d % rfu::BK) return false;
+    s->E_pad = (E + 15) / 16 * 16;
     uint32_t c = 32;
-    while (c < (uint32_t)(3 * s->E_pad)) c <<= 1;
+    while (c < (uint32_t)(4 * s->E_pad)) c <<= 1;
     s->tmem_cols = c;
+    s->stage_bytes = rfu::X_BYTES + 3 * s->E_pad * 128;
+    // two CTAs per SM when each still gets a ring of >= 3 stages and both fit in TMEM
+    const int st2 = 110 * 1024 / s->stage_bytes;
+    s->cps = (st2 >= 3 && 2 * c <= 512) ? 2 : 1;
+    int st = (s->cps == 2 ? 110 : 220) * 1024 / s->stage_bytes;
+    if (st > rfu::MAX_STAGES) st = rfu::MAX_STAGES;
+    if (st < 2) st = 2;
+    s->stages = st;
+    const int fin = rfu::red_bytes(s->E_pad) + rfu::fin_bytes(s->E_pad);
+    s->smem = (st * s->stage_bytes > fin ? st * s->stage_bytes : fin) + 1024;
+    s->ntiles = (int)((T + rfu::BM - 1) / rfu::BM);
+    // split d over a cluster of S CTAs while the CTAs still fit on the GPU at once
+    const int nk = d / rfu::BK;
+    const long long resident = (long long)sm_count() * s->cps;
+    int S = 1;
+    while (S < rfu::MAX_SPLITS && 2 * S <= nk && (long long)s->ntiles * S * 2 <= resident) S *= 2;
+    s->S = S;
+    s->grid = s->ntiles * S;
     return true;
 }
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
-// Split-K factor of the tensor-core router: as many splits as keep ntiles * S
-// within the blocks that can be resident at once (rounding up would start a
-// second, mostly empty wave), at most MAX_SPLITS and at most one split per K
-// block.  Two blocks fit on an SM when two rings of 4 stages and two
-// accumulators do (small E), else one.
-inline int route_tc_splits(long long ntiles, int d, const RouteTcShape& sh)
-{
-    const int nk = d / rtc::BK;
-    const int stage = rtc::A_BYTES + 3 * sh.E_pad * 128;
-    const bool two = 2 * (4 * stage + 1024) <= 227 * 1024 && 2 * sh.tmem_cols <= 512;
-    const long long resident = two ? 2 * 148 : 148;
-    long long S = resident / (ntiles > 0 ? ntiles : 1);
-    if (S > rtc::MAX_SPLITS) S = rtc::MAX_SPLITS;
-    if (S > nk) S = nk;
-    return S < 1 ? 1 : (int)S;
-}
-// Blocks of the finishing kernel: one lane per token for E <= 32 (64-thread
-// blocks, up to 16 per SM), else one warp per token (256-thread blocks, up to
-// four per SM: many warps hide the reduction latency).
-inline int route_fin_blocks(long long T, int E)
-{
-    const long long per_block = E <= 32 ? rtc::LANE_THREADS : rtc::FIN_WARPS;
-    const long long cap = E <= 32 ? 148 * 16 : 148 * 4;
-    const long long b = (T + per_block - 1) / per_block;
-    return (int)(b < cap ? (b > 0 ? b : 1) : cap);
-}
-struct RouteTcWs {
-    size_t ws_off, part_off, psum_off, cnt_off, total;
-};
-inline RouteTcWs route_tc_ws(long long T, int d, int E, const RouteTcShape& sh)
-{
-    const long long ntiles = (T + rtc::BM - 1) / rtc::BM;
-    const int S = route_tc_splits(ntiles, d, sh);
-    RouteTcWs w;
-    w.ws_off = 0;
-    w.part_off = align256((size_t)3 * sh.E_pad * d * 2);
-    w.psum_off = w.part_off + align256((size_t)S * T * sh.E_pad * sizeof(float));
-    w.cnt_off = w.psum_off + align256((size_t)route_fin_blocks(T, E) * E * sizeof(float));
-    w.total = w.cnt_off;
-    return w;
-}
+// Workspace of the fused router: the three bf16 parts of the weight
+// [3 E_pad, d], then one row of E probability sums per CTA.
+inline size_t route_parts_bytes(int d, const RouteFuShape& sh) { return align256((size_t)3 * sh.E_pad * d * 2); }
 inline size_t route_ws_bytes_tc(long long T, int d, int E)
 {
-    RouteTcShape sh;
-    if (T <= 0 || !route_tc_shape(E, &sh)) return 0;
-    return route_tc_ws(T, d, E, sh).total;
+    RouteFuShape sh;
+    if (!route_fu_shape(T, d, E, &sh)) return 0;
+    return route_parts_bytes(d, sh) + align256((size_t)sh.grid * E * sizeof(float));
 }
 inline size_t route_ws_bytes(long long T, int d, int E)
 {
@@ -504,80 +486,73 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     const size_t need = route_ws_bytes(T, d, E);
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
-    RouteTcShape sh;
-    if (xdt == MOE_BF16 && T > 0 && route_tc_shape(E, &sh)) {
-        // tensor-core router: split weights, partial logits, softmax / top-k per token
-        // with per-block probability sums, then the sums over blocks
-        const RouteTcWs wl = route_tc_ws(T, d, E, sh);
-        uint16_t* Ws = (uint16_t*)((char*)ws + wl.ws_off);
-        float* part = (float*)((char*)ws + wl.part_off);
-        float* psum = (float*)((char*)ws + wl.psum_off);
-        const int ntiles = (int)((T + rtc::BM - 1) / rtc::BM);
-        const int S = route_tc_splits(ntiles, d, sh);
-        const long long nsplit = (long long)sh.E_pad * d;
-        int sgrid = (int)((nsplit + 255) / 256);
-        if (sgrid > sm_count() * 4) sgrid = sm_count() * 4;
-        rtc::split_weight_kernel<<<sgrid, 256, 0, stream>>>(w_router, E, sh.E_pad, d, Ws);
+    RouteFuShape sh;
+    if (xdt == MOE_BF16 && route_fu_shape(T, d, E, &sh)) {
+        // the weight split into three bf16 parts; the fused tensor-core router
+        // (logits, softmax, top-k, per-CTA probability sums); the fixed-order
+        // sums over CTAs.  The second and third launches are programmatic
+        // dependents of the one before, so their set-up overlaps its tail.
+        uint4* parts = (uint4*)ws;
+        float* psum = (float*)((char*)ws + route_parts_bytes(d, sh));
+        const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16;
+        void (*kern)(const CUtensorMap, const CUtensorMap, const rfu::Args) =
+            kmax == 2 ? rfu::route_fused_kernel<2> : kmax == 4 ? rfu::route_fused_kernel<4> :
+            kmax == 8 ? rfu::route_fused_kernel<8> : rfu::route_fused_kernel<16>;
+        if (!ensure_dyn_smem((const void*)kern, sh.smem)) return launch_status();
+        CUtensorMap tx, tw;
+        if (!make_tmap_bf16_box(&tx, x, (unsigned long long)T, (unsigned long long)d, rfu::BM)) return MOE_ERR_CUDA;
+        if (!make_tmap_bf16_box(&tw, parts, (unsigned long long)(3 * sh.E_pad), (unsigned long long)d,
+                                (unsigned)sh.E_pad))
+            return MOE_ERR_CUDA;
+        rfu::Args a{};
+        a.T = (int)T;
+        a.d = d;
+        a.E = E;
+        a.E_pad = sh.E_pad;
+        a.k = k;
+        a.renorm = renorm;
+        a.nk = d / rfu::BK;
+        a.S = sh.S;
+        a.stages = sh.stages;
+        a.stage_bytes = sh.stage_bytes;
+        a.tmem_cols = sh.tmem_cols;
+        a.bias = b_router;
+        a.idx = topk_idx;
+        a.gate = topk_gate;
+        a.psum = psum;
+        a.sel = sel;
+        a.wait_limit = g_wait_limit.load();
+
+        const long long n8 = (long long)sh.E_pad * (d / 8);
+        long long sg = (n8 + 255) / 256;
+        if (sg > 4LL * sm_count()) sg = 4LL * sm_count();
+        rfu::split_weight_kernel<<<(int)sg, 256, 0, stream>>>(w_router, E, sh.E_pad, d, parts);
         moe_status st = launch_status();
         if (st != MOE_OK) return st;
-        CUtensorMap tx, tw;
-        if (!make_tmap_bf16_box(&tx, x, (unsigned long long)T, (unsigned long long)d, 128)) return MOE_ERR_CUDA;
-        if (!make_tmap_bf16_box(&tw, Ws, (unsigned long long)(3 * sh.E_pad), (unsigned long long)d,
-                                (unsigned)sh.nb_rows))
-            return MOE_ERR_CUDA;
-        rtc::Args a{};
-        a.T = (int)T;
-        a.E_pad = sh.E_pad;
-        a.nk = d / rtc::BK;
-        a.S = S;
-        a.nb_chunks = sh.nb_chunks;
-        a.nb_rows = sh.nb_rows;
-        a.stage_bytes = rtc::A_BYTES + 3 * sh.E_pad * 128;
-        const int grid = ntiles * S;
-        // two blocks per SM only when two rings of >= 2 stages fit; else one deep ring
-        const int budget = (grid <= sm_count() || 2 * a.stage_bytes > 100 * 1024 ? 200 : 100) * 1024;
-        int stages = budget / a.stage_bytes;
-        if (stages > rtc::MAX_STAGES) stages = rtc::MAX_STAGES;
-        if (stages < 2) stages = 2;
-        a.stages = stages;
-        a.tmem_cols = sh.tmem_cols;
-        a.part = part;
-        a.wait_limit = g_wait_limit.load();
-        const int smem = stages * a.stage_bytes + 1024;
-        if (!ensure_dyn_smem((const void*)rtc::route_logits_kernel, smem)) return launch_status();
-        rtc::route_logits_kernel<<<grid, rtc::THREADS, smem, stream>>>(tx, tw, a);
-        st = launch_status();
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)sh.S;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)sh.grid);
+        cfg.blockDim = dim3(rfu::THREADS);
+        cfg.dynamicSmemBytes = (size_t)sh.smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = sh.S > 1 ? 2 : 1;
+        st = launch_ex_status(cudaLaunchKernelEx(&cfg, kern, tx, tw, a));
         if (st != MOE_OK) return st;
-        const int fgrid = route_fin_blocks(T, E);
-        const int Ti = (int)T;
-        const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16;
-#define MOE_FIN_LANE(EM, KM) rtc::route_finish_lane_kernel<EM, KM><<<fgrid, rtc::LANE_THREADS, 0, stream>>>( \
-    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum, sel)
-#define MOE_FIN_WARP(EP) rtc::route_finish_warp_kernel<EP><<<fgrid, rtc::FIN_THREADS, 0, stream>>>( \
-    part, S, Ti, E, sh.E_pad, k, renorm, b_router, topk_idx, topk_gate, psum, sel)
-        if (E <= 16) {
-            if (kmax == 2) MOE_FIN_LANE(16, 2);
-            else if (kmax == 4) MOE_FIN_LANE(16, 4);
-            else if (kmax == 8) MOE_FIN_LANE(16, 8);
-            else MOE_FIN_LANE(16, 16);
-        } else if (E <= 32) {
-            if (kmax == 2) MOE_FIN_LANE(32, 2);
-            else if (kmax == 4) MOE_FIN_LANE(32, 4);
-            else if (kmax == 8) MOE_FIN_LANE(32, 8);
-            else MOE_FIN_LANE(32, 16);
-        } else if (E <= 64) {
-            MOE_FIN_WARP(2);
-        } else if (E <= 128) {
-            MOE_FIN_WARP(4);
-        } else {
-            MOE_FIN_WARP(8);
-        }
-#undef MOE_FIN_LANE
-#undef MOE_FIN_WARP
-        st = launch_status();
-        if (st != MOE_OK) return st;
-        rtc::prob_sum_kernel<<<E, 256, 0, stream>>>(psum, fgrid, E, prob_sum);
-        return launch_status();
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3((unsigned)E);
+        pcfg.blockDim = dim3(256);
+        pcfg.stream = stream;
+        pcfg.attrs = attr;
+        pcfg.numAttrs = 1;
+        return launch_ex_status(cudaLaunchKernelEx(&pcfg, rfu::prob_sum_kernel, (const float*)psum, sh.grid, E,
+                                                   prob_sum));
     }
     const int tpb = route_tokens_per_block(E);
     const int nblk = (int)((T + tpb - 1) / tpb);
@@ -1236,7 +1211,7 @@ moe_status moe_router_wgrad(const float* dl, const void* x, moe_dtype xdt, int64
     bwd::router_wgrad_sum_kernel<<<g2, 256, 0, st>>>(part, S, n, dW);
     s = launch_status();
     if (s != MOE_OK || !db) return s;
-    rtc::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
+    rfu::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
     return launch_status();
 }
 
@@ -1330,7 +1305,7 @@ moe_status moe_router_grads(const void* dx_perm, const int32_t* slot_row, const 
         bwd::router_grads_reduce_kernel<<<(int)g5, 256, 0, st>>>((const float4*)P, L.S, E, Ep, d / 4, (float4*)dW);
         moe_status s = launch_status();
         if (s != MOE_OK) return s;
-        rtc::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
+        rfu::prob_sum_kernel<<<E, 256, 0, st>>>(dl, (int)T, E, db);
         return launch_status();
     }
 }
