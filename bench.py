@@ -82,8 +82,9 @@ L2_FLUSH_BYTES = 512 << 20
 def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     """Library kernels launched by one layer forward of this workload (the
     device-timed region launches exactly these, K times)."""
-    tc_router = cfg.dtype == "bf16" and cfg.E <= 160
-    route = 4 if tc_router else 2          # split + logits + finish + prob sums | router + sums
+    tc_router = cfg.dtype == "bf16" and cfg.E <= 128
+    # weight split + logits (+ softmax/top-k for E > 64) + prob sums | CUDA-core router + sums
+    route = (3 if cfg.E <= 64 else 4) if tc_router else 2
     gather = bool(args and args.gather)
     ranks = 1 if cfg.T * cfg.k <= 16384 else 2   # one-block histogram + ranks, or the two-kernel form
     dispatch = ranks + (0 if gather else 1)      # (+ row copy)

@@ -1,9 +1,11 @@
 """GPU parity of the bf16 router (moe_route) on its own, on shapes chosen for
 the fused tensor-core kernel's code paths: one CTA per tile with many K
-blocks (the W0 accumulator drained in chunks of four K blocks, including a
-ragged last chunk), clusters of 2 to 8 CTAs splitting d, expert counts that
-are not multiples of 16 (zero-padded weight rows), ragged token tails, a
-bias, and the largest expert count (128) at top-8.  Indices bit-exact,
+blocks (the accumulators drained in chunks of four K blocks, including a
+ragged last chunk), clusters of 2 to 4 CTAs splitting d, one or two 128-token
+tiles per CTA in both accumulator layouts (three parts in one MMA, E <= 32;
+one MMA per part above), expert counts that are not multiples of 16
+(zero-padded weight rows), ragged token tails, a bias, and the largest
+expert count (128) at top-8.  Indices bit-exact,
 gates and probability sums within the gate bar of moe_cases, against the
 oracle's fp64 router on the same stored inputs."""
 import numpy as np
@@ -25,9 +27,9 @@ CASES = {
     "e64_chunks": C("r_e64_chunks", 20000, 1024, 64, 2, 64, "gelu", 0.0, "bf16"),
     # E = 128, top-8, 20 K blocks: 5 chunks, 150 tiles
     "e128_top8_chunks": C("r_e128_chunks", 19100, 1280, 128, 8, 64, "gelu", 0.0, "bf16"),
-    # 8 tiles: clusters of 8 CTAs, 8 K blocks each (2 chunks), ragged tail of 104 tokens
+    # 8 tiles: clusters of 4 CTAs, 16 K blocks each (4 chunks), ragged tail of 104 tokens
     "e8_cluster8": C("r_e8_cl8", 1000, 4096, 8, 2, 64, "gelu", 0.0, "bf16"),
-    # 10 K blocks over a cluster of 8: K ranges of 1 and 2 blocks
+    # 10 K blocks over a cluster of 4: K ranges of 2 and 3 blocks
     "e16_cluster4_ragged_k": C("r_e16_cl4", 777, 640, 16, 2, 64, "gelu", 0.0, "bf16", bias="hot2"),
     # E = 40 (padded to 48 weight rows), 10 K blocks over one CTA: chunks 4, 4, 2
     "e40_pad": C("r_e40", 19000, 640, 40, 3, 64, "gelu", 0.0, "bf16"),
@@ -35,6 +37,10 @@ CASES = {
     "e100_zipf": C("r_e100", 5000, 2048, 100, 6, 64, "gelu", 0.0, "bf16", bias="zipf"),
     # one token
     "one_token": C("r_one", 1, 512, 32, 4, 64, "gelu", 0.0, "bf16"),
+    # two 128-token tiles per CTA, all three parts in one MMA (E <= 32)
+    "e16_two_tiles": C("r_e16_2t", 8100, 512, 16, 2, 64, "gelu", 0.0, "bf16"),
+    # two tiles per CTA, one MMA per part (32 < E <= 64), ragged last tile pair
+    "e48_two_tiles": C("r_e48_2t", 16000, 1024, 48, 4, 64, "gelu", 0.0, "bf16", bias="zipf"),
 }
 
 

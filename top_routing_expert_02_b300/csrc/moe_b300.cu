@@ -94,45 +94,70 @@ inline size_t route_ws_bytes_simt(long long T, int E)
 
 // Fused tensor-core router (bf16 x, E <= 128): launch shape.
 struct RouteFuShape {
-    int E_pad, cps, S, stages, stage_bytes, smem, ntiles, grid;
+    int E_pad, emax, TPB, S, xstages, wstages, smem, ngroups, grid;
     uint32_t tmem_cols;
 };
 inline bool route_fu_shape(long long T, int d, int E, RouteFuShape* s)
 {
     if (E > rfu::MAX_EPAD || T <= 0 || d % rfu::BK) return false;
     s->E_pad = (E + 15) / 16 * 16;
-    uint32_t c = 32;
-    while (c < (uint32_t)(4 * s->E_pad)) c <<= 1;
-    s->tmem_cols = c;
-    s->stage_bytes = rfu::X_BYTES + 3 * s->E_pad * 128;
-    // two CTAs per SM when each still gets a ring of >= 3 stages and both fit in TMEM
-    const int st2 = 110 * 1024 / s->stage_bytes;
-    s->cps = (st2 >= 3 && 2 * c <= 512) ? 2 : 1;
-    int st = (s->cps == 2 ? 110 : 220) * 1024 / s->stage_bytes;
-    if (st > rfu::MAX_STAGES) st = rfu::MAX_STAGES;
-    if (st < 2) st = 2;
-    s->stages = st;
-    const int fin = rfu::red_bytes(s->E_pad) + rfu::fin_bytes(s->E_pad);
-    s->smem = (st * s->stage_bytes > fin ? st * s->stage_bytes : fin) + 1024;
-    s->ntiles = (int)((T + rfu::BM - 1) / rfu::BM);
-    // split d over a cluster of S CTAs while the CTAs still fit on the GPU at once
+    s->emax = s->E_pad <= 16 ? 16 : s->E_pad <= 32 ? 32 : s->E_pad <= 64 ? 64 : 128;
+    // E_pad <= 32: one MMA per tile and K step for the three stacked parts
+    const bool fused_parts = s->emax <= 32;
+    const long long ntiles = (T + rfu::BM - 1) / rfu::BM;
+    const int tcols = rfu::tile_tmem_cols(fused_parts, s->E_pad);
     const int nk = d / rfu::BK;
-    const long long resident = (long long)sm_count() * s->cps;
-    int S = 1;
-    while (S < rfu::MAX_SPLITS && 2 * S <= nk && (long long)s->ntiles * S * 2 <= resident) S *= 2;
-    s->S = S;
-    s->grid = s->ntiles * S;
+    const long long sms = (long long)sm_count();
+    // CTAs of one launch for TPB tiles per CTA: clusters of S CTAs split d
+    // while the CTAs still fit on the GPU at once (one CTA per SM)
+    auto splits = [&](long long groups) {
+        int S = 1;
+        while (S < rfu::MAX_SPLITS && 2 * S <= nk && groups * S * 2 <= sms) S *= 2;
+        return S;
+    };
+    // two 128-token tiles per CTA (one weight block serves both) when their
+    // TMEM columns fit and the launch still fills the GPU as well
+    const long long g1 = ntiles, g2 = (ntiles + 1) / 2;
+    const long long c1 = g1 * splits(g1), c2 = g2 * splits(g2);
+    s->TPB = (2 * tcols <= 512 && ntiles >= 2 && (c2 >= c1 || c2 >= sms * 3 / 4)) ? 2 : 1;
+    uint32_t c = 32;
+    while (c < (uint32_t)(s->TPB * tcols)) c <<= 1;
+    s->tmem_cols = c;
+    // one CTA per SM: x and weight rings of the same depth in K blocks, as
+    // deep as the 227 KB (less alignment and static use) allow
+    const int xbytes = s->TPB * rfu::X_BYTES, wbytes = 3 * s->E_pad * 128;
+    int st = (232448 - 1024 - 1536) / (xbytes + wbytes);
+    if (st > rfu::MAX_XSTAGES) st = rfu::MAX_XSTAGES;
+    if (st < 2) st = 2;
+    s->xstages = s->wstages = st;
+    const int ring = st * (xbytes + wbytes);
+    const int fin = rfu::finish_smem_bytes(s->TPB, s->E_pad);
+    s->smem = (ring > fin ? ring : fin) + 1024;
+    s->ngroups = (int)((ntiles + s->TPB - 1) / s->TPB);
+    s->S = splits(s->ngroups);
+    s->grid = s->ngroups * s->S;
     return true;
 }
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
-// Workspace of the fused router: the three bf16 parts of the weight
-// [3 E_pad, d], then one row of E probability sums per CTA.
+// Workspace of the tensor-core router: the three bf16 parts of the weight
+// [3 E_pad, d], the fp32 logits [T, E], one row of E probability sums per
+// finishing block.
 inline size_t route_parts_bytes(int d, const RouteFuShape& sh) { return align256((size_t)3 * sh.E_pad * d * 2); }
+inline long long route_fin_blocks(long long T) { return (T + rfu::FIN_TOKENS - 1) / rfu::FIN_TOKENS; }
+// E <= 64: the logits kernel finishes its own tokens (one probability-sum row
+// per CTA); larger E: fp32 logits [T, E] for route_finish_kernel (one row per
+// finishing block)
+inline bool route_finish_here(const RouteFuShape& sh) { return sh.emax <= 64; }
+inline size_t route_logits_bytes(long long T, int E, const RouteFuShape& sh)
+{
+    return route_finish_here(sh) ? 0 : align256((size_t)T * E * sizeof(float));
+}
 inline size_t route_ws_bytes_tc(long long T, int d, int E)
 {
     RouteFuShape sh;
     if (!route_fu_shape(T, d, E, &sh)) return 0;
-    return route_parts_bytes(d, sh) + align256((size_t)sh.grid * E * sizeof(float));
+    const long long rows = route_finish_here(sh) ? sh.grid : route_fin_blocks(T);
+    return route_parts_bytes(d, sh) + route_logits_bytes(T, E, sh) + align256((size_t)rows * E * sizeof(float));
 }
 inline size_t route_ws_bytes(long long T, int d, int E)
 {
@@ -488,21 +513,36 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
     RouteFuShape sh;
     if (xdt == MOE_BF16 && route_fu_shape(T, d, E, &sh)) {
-        // the weight split into three bf16 parts; the fused tensor-core router
-        // (logits, softmax, top-k, per-CTA probability sums); the fixed-order
-        // sums over CTAs.  The second and third launches are programmatic
-        // dependents of the one before, so their set-up overlaps its tail.
+        // the weight split into three bf16 parts; the tensor-core logits
+        // kernel; the softmax / top-k / per-block probability sums; the
+        // fixed-order sums over blocks.  Each launch after the first is a
+        // programmatic dependent of the one before, so its set-up overlaps
+        // that kernel's tail.
+        const bool here = route_finish_here(sh);
         uint4* parts = (uint4*)ws;
-        float* psum = (float*)((char*)ws + route_parts_bytes(d, sh));
+        float* logits = here ? nullptr
+                             : (sel.logits ? sel.logits : (float*)((char*)ws + route_parts_bytes(d, sh)));
+        float* psum = (float*)((char*)ws + route_parts_bytes(d, sh) + route_logits_bytes(T, E, sh));
         const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : k <= 8 ? 8 : 16;
-        void (*kern)(const CUtensorMap, const CUtensorMap, const rfu::Args) =
-            kmax == 2 ? rfu::route_fused_kernel<2> : kmax == 4 ? rfu::route_fused_kernel<4> :
-            kmax == 8 ? rfu::route_fused_kernel<8> : rfu::route_fused_kernel<16>;
+        void (*kern)(const CUtensorMap, const CUtensorMap, const rfu::Args) = nullptr;
+        void (*fin)(const rfu::FinArgs) = nullptr;
+#define MOE_RFU(EM)                                                                                       \
+        kern = kmax == 2 ? rfu::route_fused_kernel<EM, 2> : kmax == 4 ? rfu::route_fused_kernel<EM, 4> :       \
+               kmax == 8 ? rfu::route_fused_kernel<EM, 8> : rfu::route_fused_kernel<EM, 16>
+        if (sh.emax == 16) MOE_RFU(16);
+        else if (sh.emax == 32) MOE_RFU(32);
+        else if (sh.emax == 64) MOE_RFU(64);
+        else {
+            kern = rfu::route_fused_kernel<128, 2>;   // finishing is left to route_finish_kernel
+            fin = kmax == 2 ? rfu::route_finish_kernel<128, 2> : kmax == 4 ? rfu::route_finish_kernel<128, 4> :
+                  kmax == 8 ? rfu::route_finish_kernel<128, 8> : rfu::route_finish_kernel<128, 16>;
+        }
+#undef MOE_RFU
         if (!ensure_dyn_smem((const void*)kern, sh.smem)) return launch_status();
         CUtensorMap tx, tw;
         if (!make_tmap_bf16_box(&tx, x, (unsigned long long)T, (unsigned long long)d, rfu::BM)) return MOE_ERR_CUDA;
         if (!make_tmap_bf16_box(&tw, parts, (unsigned long long)(3 * sh.E_pad), (unsigned long long)d,
-                                (unsigned)sh.E_pad))
+                                (unsigned)(3 * sh.E_pad <= 256 ? 3 * sh.E_pad : sh.E_pad)))
             return MOE_ERR_CUDA;
         rfu::Args a{};
         a.T = (int)T;
@@ -513,15 +553,28 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         a.renorm = renorm;
         a.nk = d / rfu::BK;
         a.S = sh.S;
-        a.stages = sh.stages;
-        a.stage_bytes = sh.stage_bytes;
+        a.TPB = sh.TPB;
+        a.xstages = sh.xstages;
+        a.wstages = sh.wstages;
         a.tmem_cols = sh.tmem_cols;
         a.bias = b_router;
         a.idx = topk_idx;
         a.gate = topk_gate;
         a.psum = psum;
         a.sel = sel;
+        a.logits = logits;
         a.wait_limit = g_wait_limit.load();
+        rfu::FinArgs f{};
+        f.T = (int)T;
+        f.E = E;
+        f.k = k;
+        f.renorm = renorm;
+        f.logits = logits;
+        f.idx = topk_idx;
+        f.gate = topk_gate;
+        f.psum = psum;
+        f.sel = sel;
+        const int rows = here ? sh.grid : (int)route_fin_blocks(T);
 
         const long long n8 = (long long)sh.E_pad * (d / 8);
         long long sg = (n8 + 255) / 256;
@@ -545,13 +598,23 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         cfg.numAttrs = sh.S > 1 ? 2 : 1;
         st = launch_ex_status(cudaLaunchKernelEx(&cfg, kern, tx, tw, a));
         if (st != MOE_OK) return st;
+        if (!here) {
+            cudaLaunchConfig_t fcfg = {};
+            fcfg.gridDim = dim3((unsigned)rows);
+            fcfg.blockDim = dim3(rfu::FIN_THREADS);
+            fcfg.stream = stream;
+            fcfg.attrs = attr;
+            fcfg.numAttrs = 1;
+            st = launch_ex_status(cudaLaunchKernelEx(&fcfg, fin, f));
+            if (st != MOE_OK) return st;
+        }
         cudaLaunchConfig_t pcfg = {};
         pcfg.gridDim = dim3((unsigned)E);
         pcfg.blockDim = dim3(256);
         pcfg.stream = stream;
         pcfg.attrs = attr;
         pcfg.numAttrs = 1;
-        return launch_ex_status(cudaLaunchKernelEx(&pcfg, rfu::prob_sum_kernel, (const float*)psum, sh.grid, E,
+        return launch_ex_status(cudaLaunchKernelEx(&pcfg, rfu::prob_sum_kernel, (const float*)psum, rows, E,
                                                    prob_sum));
     }
     const int tpb = route_tokens_per_block(E);

@@ -1,5 +1,5 @@
 // Router of bf16 x on the tensor cores, fused: logits, softmax, top-k and the
-// per-block probability sums of one 128-token tile in one kernel.
+// per-CTA probability sums in one kernel.
 //
 // Expert-parallelism tutorial "专家并行：混合专家模型的分布式训练方案" §1.1 / §2.1
 // step 1 (a light linear layer scores the experts, each token keeps its
@@ -24,23 +24,40 @@
 // and the first x tiles overlap the split, and only the weight loads wait
 // for it.
 //
-// Work split.  A cluster of S CTAs shares one 128-token tile (S > 1 splits d
-// when there are too few tiles to fill the GPU); CTA s of the cluster covers
-// K blocks [s*nk/S, (s+1)*nk/S).  Each CTA has 6 warps:
-//   warp 0      TMA producer: per stage the x tile (128 tokens x 64 columns)
-//               and the three weight parts (E_pad rows x 64 columns each)
+// Work split.  A CTA owns TPB 128-token tiles (TPB = 2 while the TMEM columns
+// allow, so each weight block serves 256 tokens); a cluster of S CTAs shares
+// them (S > 1 splits d when there are too few tiles to fill the GPU): CTA s
+// covers K blocks [s*nk/S, (s+1)*nk/S).  Each CTA has 7 warps:
+//   warp 0      TMA producer of the x ring: per K block the TPB x tiles (128
+//               tokens x 64 columns each), as many blocks ahead as the ring
+//               holds (x comes from HBM: the ring is deep)
+//   warp 6      TMA producer of the weight ring: the three stacked parts (3
+//               E_pad rows x 64) per K block (they stay in L2: a short ring)
 //   warp 1      TMEM allocation and the single thread issuing tcgen05.mma
-//               (M = 128 tokens, N = E_pad experts, one MMA per part per K=16)
-//   warps 2-5   add each finished W0 chunk into the fp32 sum kept in TMEM;
-//               at the end, the partial logits of the tile's rows (thread =
-//               TMEM lane = token row)
-// TMEM columns: [W0 chunk, buffer 0 | W0 chunk, buffer 1 | W1 + W2 | W0 sum],
-// E_pad each.
-// The partial logits of the S CTAs meet in distributed shared memory: CTA s
-// finishes tokens [s*128/S, (s+1)*128/S) of the tile, adding the S partial rows
-// in split order plus the bias, then takes the softmax, the top-k (sorted
-// insertion per token on (logit desc, index asc)) and its per-expert sums of
-// p.  Every sum has a fixed order, so a call gives the same bits every run.
+//               (M = 128 tokens, K = 16 per instruction)
+//   warps 2-5   add each finished chunk into an fp32 sum (in TMEM, or in
+//               registers); at the end, the partial logits of the tiles'
+//               rows (thread = TMEM lane = token row)
+// Two accumulator layouts.  E_pad <= 32 (FUSED_PARTS): one MMA per tile and
+// K step covers all three parts (N = 3 E_pad), so each x tile is read once
+// per step; TMEM per tile [chunk buffer 0 (3 E_pad) | chunk buffer 1 (3 E_pad)
+// | sum (E_pad)], and a chunk adds W0 + (W1 + W2) into the sum.  Larger
+// E_pad: W0 (N = E_pad) into a chunk buffer and W1, W2 together (N = 2 E_pad)
+// into their own columns, TMEM per tile [W0 chunk buffer 0 | W0 chunk buffer
+// 1 | W1 | W2], E_pad each, the W0 sum in the accumulator warps' registers;
+// two tiles fit up to E_pad = 64 (they share each weight block, halving its
+// traffic).
+// The partial logits of the S CTAs meet in shared memory: CTA s takes tokens
+// [s*TPC, (s+1)*TPC), TPC = 128*TPB/S; every CTA pushes the rows of those
+// tokens to CTA s with one bulk copy into its shared memory (distributed
+// shared memory, completion counted on CTA s's mbarrier), and CTA s adds the
+// S partial logits in split order plus the bias.  For E <= 64 it then takes
+// the softmax, the top-k and its per-expert sums of p itself (finish_token:
+// four lanes per token); for larger E it writes the fp32 logits and
+// route_finish_kernel (a programmatic dependent, many blocks per SM to hide
+// the latency of the longer per-token chains) does that.  prob_sum_kernel
+// adds the per-CTA or per-block rows.  Every sum has a fixed order, so a call
+// gives the same bits every run.
 #pragma once
 #include "common.cuh"
 #include "ptx_sm103.cuh"
@@ -48,47 +65,69 @@
 namespace rfu {
 
 constexpr int BM = 128, BK = 64;
-constexpr int THREADS = 192;
-constexpr int MAX_STAGES = 8;
+constexpr int THREADS = 224;
+constexpr int WARPS = THREADS / 32;
+constexpr int MAX_XSTAGES = 12;             // x ring
+constexpr int MAX_WSTAGES = 12;             // weight-part ring
 constexpr int KC = 4;                       // K blocks per W0 accumulator chunk
 constexpr int X_BYTES = BM * BK * 2;        // one x tile, 16 KB
 constexpr int MAX_EPAD = 128;               // 4 * E_pad TMEM columns <= 512
-constexpr int MAX_SPLITS = 8;               // portable cluster size
+constexpr int MAX_SPLITS = 4;               // cluster size (larger clusters of one-SM CTAs may not all fit at once)
 constexpr int ACC_THREADS = 128;            // warps 2-5
 
 struct Args {
     int T, d, E, E_pad, k, renorm;
     int nk;             // K blocks of 64 over d
-    int S;              // CTAs per tile (cluster size)
-    int stages;
-    int stage_bytes;    // x tile + three weight parts
+    int S;              // CTAs per token group (cluster size)
+    int TPB;            // 128-token tiles per CTA (1 or 2)
+    int xstages;        // x ring: TPB tiles of 16 KB per stage
+    int wstages;        // weight ring: 3 E_pad x 64 bf16 per stage
     uint32_t tmem_cols;
     const float* bias;  // [E] or nullptr
-    int32_t* idx;       // [T, k]
+    int32_t* idx;       // [T, k]              (E <= 64: finished in this kernel)
     float* gate;        // [T, k]
-    float* psum;        // [gridDim.x, E]: per-CTA probability sums
-    RouteSel sel;
+    float* psum;        // [gridDim.x, E]      per-CTA probability sums
+    RouteSel sel;       // group-limited routing, lse and logits out
+    float* logits;      // [T, E] fp32 out (E > 64): the logits for route_finish_kernel
     unsigned long long wait_limit;
 };
 
-__host__ __device__ constexpr int red_bytes(int E_pad) { return BM * E_pad * 4; }
-__host__ __device__ constexpr int fin_bytes(int E_pad) { return BM * (E_pad + 1) * 4; }
+// Arguments of the finishing kernel.
+struct FinArgs {
+    int T, E, k, renorm;
+    const float* logits;  // [T, E]
+    int32_t* idx;         // [T, k]
+    float* gate;          // [T, k]
+    float* psum;          // [gridDim.x, E]: per-block probability sums
+    RouteSel sel;         // group-limited routing, lse out (its logits pointer is unused here)
+};
 
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
+// Shared memory after the main loop (reusing the stage ring): the partial
+// logits of the CTA's rows, [TPB * 128][E_pad + 1] (rows one float longer
+// than E_pad, so that threads reading one row each hit different banks); the
+// rows the other CTAs of the cluster push for the tokens this CTA finishes,
+// [S][TPC][E_pad + 1] (the same size); the per-warp probability sums are
+// not needed: one thread per expert sums the finished rows.
+__host__ __device__ constexpr int red_bytes(int TPB, int E_pad) { return TPB * BM * (E_pad + 1) * 4; }
+__host__ __device__ constexpr int finish_smem_bytes(int TPB, int E_pad) { return 2 * red_bytes(TPB, E_pad); }
+// TMEM columns of one 128-token tile in the two accumulator layouts.
+__host__ __device__ constexpr int tile_tmem_cols(bool fused_parts, int E_pad) { return fused_parts ? 7 * E_pad : 4 * E_pad; }
 
 // Programmatic dependent launch: the next kernel in the stream may start
 // (launch_dependents); wait until the kernel before this one has finished and
 // its memory is visible (wait).
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to the
+// shared memory of a CTA of the cluster (dst and bar: shared::cluster
+// addresses); completion is counted in bytes on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_push(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 
 // W (fp32 [E, d]) -> stacked bf16 [3*E_pad, d]: rows [0,E_pad) W0, [E_pad,2E_pad) W1,
 // [2E_pad,3E_pad) W2; rows of experts >= E are zero.  W0 = rn(W), W1 = rn(W - W0),
@@ -132,56 +171,231 @@ __global__ void __launch_bounds__(256) split_weight_kernel(const float* __restri
     }
 }
 
-// W0 chunk `buf` added into the W0 sum (or copied, for the first chunk), by
-// one accumulator warp (its 32 TMEM lanes).
-__device__ __forceinline__ void drain_chunk(uint32_t tb, int Ep, int buf, bool first)
+// FUSED_PARTS: chunk `buf` (W0 + (W1 + W2) from its three part blocks) of the
+// tile whose TMEM columns start at tb added into that tile's sum at column
+// 6 E_pad (or copied, for the first chunk), by one accumulator warp (its 32
+// TMEM lanes).
+__device__ __forceinline__ void drain_chunk_fp(uint32_t tb, int Ep, int buf, bool first)
 {
+    const uint32_t sum_col = (uint32_t)(6 * Ep), buf_col = (uint32_t)(buf * 3 * Ep);
     for (int e0 = 0; e0 < Ep; e0 += 16) {
-        uint32_t v[16], a[16];
-        ptx::tmem_ld16(tb + (uint32_t)(buf * Ep + e0), v);
-        if (!first) ptx::tmem_ld16(tb + (uint32_t)(3 * Ep + e0), a);
+        uint32_t v[16], v1[16], v2[16], a[16];
+        ptx::tmem_ld16(tb + buf_col + (uint32_t)e0, v);
+        ptx::tmem_ld16(tb + buf_col + (uint32_t)(Ep + e0), v1);
+        ptx::tmem_ld16(tb + buf_col + (uint32_t)(2 * Ep + e0), v2);
+        if (!first) ptx::tmem_ld16(tb + sum_col + (uint32_t)e0, a);
         ptx::tmem_ld_wait();
-        if (!first) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(a[u]) + __uint_as_float(v[u]));
+        for (int u = 0; u < 16; ++u) {
+            const float c = __uint_as_float(v[u]) + (__uint_as_float(v1[u]) + __uint_as_float(v2[u]));
+            v[u] = __float_as_uint(first ? c : __uint_as_float(a[u]) + c);
         }
-        ptx::tmem_st16(tb + (uint32_t)(3 * Ep + e0), v);
+        ptx::tmem_st16(tb + sum_col + (uint32_t)e0, v);
     }
     ptx::tmem_st_wait();
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(THREADS, 2)
+// Softmax and top-k of one token held by a group of four lanes (xor-1 and
+// xor-2 shuffles stay inside the group): lane sub holds the logits of experts
+// sub, sub + 4, ... in l[] (entries past E unused).  The maximum and the
+// softmax sum combine over the four lanes in a fixed order; each lane sorts
+// its candidates (logit desc, index asc) and k rounds of a four-lane argmax
+// of the list heads give the winners, in order.  On return l[] holds p
+// (softmax probabilities); lane 0 of a valid token has written idx, gate and
+// lse.  Every lane of the warp must call it (shuffles).
+template <int EPL, int KMAX>
+__device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, int k, int renorm, bool valid, int t,
+                                             const RouteSel& sel, int32_t* __restrict__ idx_out,
+                                             float* __restrict__ gate_out)
+{
+    constexpr int G = 4;
+    const bool grouped = sel.n_group > 1;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        if (sub + G * i < E) mx = fmaxf(mx, l[i]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // group-limited routing: keep the topk_group groups holding the best
+    // remaining logit, ordered by (logit desc, expert asc)
+    unsigned gkeep = 0xffffffffu;
+    if (grouped) {
+        gkeep = 0;
+        for (int rr = 0; rr < sel.topk_group; ++rr) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = sub + G * i;
+                if (e < E && !((gkeep >> (e / sel.gsz)) & 1u) && (l[i] > bv || (l[i] == bv && e < bi))) {
+                    bv = l[i];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < G; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (bi < E) gkeep |= 1u << (bi / sel.gsz);
+        }
+    }
+    // this lane's candidates, sorted: descending, an equal value keeps the
+    // lower expert ahead (experts ascend with i)
+    float tv[KMAX];
+    int ti[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        tv[j] = -INFINITY;
+        ti[j] = 0x7fffffff;
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = sub + G * i;
+        const float v = l[i];
+        if (e < E && v > tv[KMAX - 1] && (!grouped || ((gkeep >> (e / sel.gsz)) & 1u))) {
+#pragma unroll
+            for (int j = KMAX - 1; j > 0; --j) {
+                if (v > tv[j - 1]) {
+                    tv[j] = tv[j - 1];
+                    ti[j] = ti[j - 1];
+                } else if (v > tv[j]) {
+                    tv[j] = v;
+                    ti[j] = e;
+                }
+            }
+            if (v > tv[0]) {
+                tv[0] = v;
+                ti[0] = e;
+            }
+        }
+    }
+    // softmax over all E: this lane's terms in expert order, then the four
+    // lanes' sums in a fixed butterfly
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        if (sub + G * i < E) {
+            l[i] = expf(l[i] - mx);
+            s += l[i];
+        }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    const float inv = 1.f / s;
+    if (valid && sel.lse && sub == 0) sel.lse[t] = mx + logf(s);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) l[i] *= inv;
+    // the k winners: each round the best list head of the four lanes (logit
+    // desc, expert asc); the lane holding it drops it
+    int widx[KMAX];
+    float wp[KMAX];
+    float chosen = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+            float bv = tv[0];
+            int bi = ti[0];
+#pragma unroll
+            for (int o = 1; o < G; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (ti[0] == bi) {
+#pragma unroll
+                for (int u = 0; u + 1 < KMAX; ++u) {
+                    tv[u] = tv[u + 1];
+                    ti[u] = ti[u + 1];
+                }
+                tv[KMAX - 1] = -INFINITY;
+                ti[KMAX - 1] = 0x7fffffff;
+            }
+            wp[j] = expf(bv - mx) * inv;   // the winner's probability, as in l[]
+            widx[j] = bi;
+            chosen += wp[j];
+        }
+    }
+    if (valid && sub == 0) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            if (j < k) {
+                idx_out[(size_t)t * k + j] = widx[j];
+                gate_out[(size_t)t * k + j] = renorm ? wp[j] / chosen : wp[j];
+            }
+    }
+}
+
+// Per-expert sums of p over `n` rows (pitch P floats) of shared memory: eight
+// interleaved partial sums in row order, combined in a fixed order.
+__device__ __forceinline__ float column_sum(const float* rows, int n, int P, int e)
+{
+    float acc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+    int r = 0;
+    for (; r + 8 <= n; r += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] += rows[(size_t)(r + u) * P + e];
+    }
+    for (; r < n; ++r) acc[0] += rows[(size_t)r * P + e];
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+}
+
+template <int EMAX, int KMAX>
+__global__ void __launch_bounds__(THREADS, 1)
 route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Args g)
 {
+    constexpr bool FP = EMAX <= 32;
+    constexpr bool FINISH_HERE = EMAX <= 64;   // larger E: route_finish_kernel, at higher occupancy
     extern __shared__ uint8_t dsmem[];
-    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
-    __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], fin_bar;
+    __shared__ __align__(8) uint64_t xfull[MAX_XSTAGES], xempty[MAX_XSTAGES], wfull[MAX_WSTAGES], wempty[MAX_WSTAGES];
+    __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], fin_bar, recv_bar;
     __shared__ uint32_t tmem_base_sh;
+    __shared__ float bias_sh[MAX_EPAD];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem0 = (ptx::smem_u32(dsmem) + 1023u) & ~1023u;
     uint8_t* const gsmem = dsmem + (smem0 - ptx::smem_u32(dsmem));
-    const int S = g.S;
-    const int tile = blockIdx.x / S, split = blockIdx.x - tile * S;
+    const int S = g.S, TPB = g.TPB;
+    const int group = blockIdx.x / S, split = blockIdx.x - group * S;
+    const int row0 = group * TPB * BM;          // first token of this CTA's tiles
     const int kb0 = (int)((long long)split * g.nk / S), kb1 = (int)((long long)(split + 1) * g.nk / S);
     const int nkb = kb1 - kb0;
-    const int rot = nkb > 0 ? tile % nkb : 0;   // staggered walk: concurrent tiles read different W columns
+    const int rot = nkb > 0 ? group % nkb : 0;   // staggered walk: concurrent groups read different W columns
     const int nch = (nkb + KC - 1) / KC;
-    const int Ep = g.E_pad;
+    const int Ep = g.E_pad, P = Ep + 1;
+    const uint32_t tile_cols = (uint32_t)tile_tmem_cols(FP, Ep);
     const uint64_t limit = g.wait_limit;
+    const int TPC = TPB * BM / S;                 // tokens this CTA finishes
+    const uint32_t slice_bytes = (uint32_t)(TPC * P * 4);   // one CTA's partial rows of them
+    const uint32_t xstage_bytes = (uint32_t)(TPB * X_BYTES), wstage_bytes = (uint32_t)(3 * Ep * 128);
+    const uint32_t wring = smem0 + (uint32_t)g.xstages * xstage_bytes;   // weight ring after the x ring
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < g.stages; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+        for (int s = 0; s < g.xstages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&xfull[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&xempty[s]), 1);
+        }
+        for (int s = 0; s < g.wstages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&wfull[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&wempty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&accf_bar[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&acce_bar[b]), ACC_THREADS);
         }
         ptx::mbar_init(ptx::smem_u32(&fin_bar), 1);
+        ptx::mbar_init(ptx::smem_u32(&recv_bar), 1);
         ptx::fence_mbar_init();
+        // the other S-1 CTAs push their partial rows of this CTA's tokens
+        if (S > 1) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&recv_bar), (uint32_t)(S - 1) * slice_bytes);
         ptx::tma_prefetch_desc(&tmX);
         ptx::tma_prefetch_desc(&tmW);
     }
@@ -189,55 +403,59 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), g.tmem_cols);
         ptx::tmem_relinquish();
     }
+    for (int e = threadIdx.x; e < Ep; e += THREADS) bias_sh[e] = (g.bias && e < g.E) ? __ldg(g.bias + e) : 0.f;
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
+    // the stacked parts [W0; W1; W2] of a K block: one box of 3 E_pad rows when
+    // that is at most 256 rows, else one box per part
+    const bool w_one_box = 3 * Ep <= 256;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer: x and weight parts
+    if (warp == 0 || warp == 6) {
+        // ------------------------------------------------ TMA producers: x ring (warp 0), weight ring (warp 6)
         if (lane == 0) {
-            const int part_bytes = Ep * 128;
-            const uint32_t tx_bytes = (uint32_t)(X_BYTES + 3 * part_bytes);
-            auto kblock = [&](int i) { return kb0 + (i + rot) % nkb; };
-            auto load_parts = [&](int i, int stage) {
-                const uint32_t sb = smem0 + stage * g.stage_bytes + X_BYTES;
-                const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
-                for (int p = 0; p < 3; ++p) ptx::tma_load_2d(sb + p * part_bytes, &tmW, fb, kblock(i) * BK, p * Ep);
-            };
-            // the first stages' x tiles go out before the weight split has finished
-            const int pre = nkb < g.stages ? nkb : g.stages;
-            for (int i = 0; i < pre; ++i) {
-                const uint32_t fb = ptx::smem_u32(&full_bar[i]);
-                ptx::mbar_arrive_expect_tx(fb, tx_bytes);
-                ptx::tma_load_2d(smem0 + i * g.stage_bytes, &tmX, fb, kblock(i) * BK, tile * BM);
-            }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i) load_parts(i, i);
-            int stage = pre % g.stages;
-            uint32_t phase = pre == g.stages ? 1u : 0u;
-            int fills = pre;
+            const bool xring = warp == 0;
+            const int nst = xring ? g.xstages : g.wstages;
+            uint64_t* full = xring ? xfull : wfull;
+            uint64_t* empty = xring ? xempty : wempty;
+            const uint32_t sbytes = xring ? xstage_bytes : wstage_bytes;
+            const uint32_t base = xring ? smem0 : wring;
+            // the x ring fills before the weight split has finished; the
+            // weight producer waits for it (programmatic dependent launch)
+            if (!xring) pdl_wait();
+            int stage = 0;
+            uint32_t phase = 0;
+            int fills = 0;
             bool ok = true;
-            for (int i = pre; i < nkb; ++i) {
-                if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, limit)) {
+            int kb = kb0 + rot;                    // K blocks walked from kb0 + rot, wrapping at kb1
+            for (int i = 0; i < nkb; ++i) {
+                if (!ptx::mbar_wait(ptx::smem_u32(&empty[stage]), phase ^ 1u, limit)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
-                ptx::mbar_arrive_expect_tx(fb, tx_bytes);
-                ptx::tma_load_2d(smem0 + stage * g.stage_bytes, &tmX, fb, kblock(i) * BK, tile * BM);
-                load_parts(i, stage);
+                const uint32_t fb = ptx::smem_u32(&full[stage]);
+                const uint32_t dst = base + (uint32_t)stage * sbytes;
+                ptx::mbar_arrive_expect_tx(fb, sbytes);
+                if (xring) {
+                    ptx::tma_load_2d(dst, &tmX, fb, kb * BK, row0);
+                    if (TPB > 1) ptx::tma_load_2d(dst + X_BYTES, &tmX, fb, kb * BK, row0 + BM);
+                } else if (w_one_box) {
+                    ptx::tma_load_2d(dst, &tmW, fb, kb * BK, 0);
+                } else {
+                    for (int p = 0; p < 3; ++p) ptx::tma_load_2d(dst + p * Ep * 128, &tmW, fb, kb * BK, p * Ep);
+                }
                 ++fills;
-                if (++stage == g.stages) {
+                if (++kb == kb1) kb = kb0;
+                if (++stage == nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) moe_flag(MOE_DEV_TIMEOUT);
             // the last stages' copies must have landed before shared memory is reused or freed
-            for (int f = fills - 1; f >= 0 && f >= fills - g.stages; --f) {
-                const uint32_t bar = ptx::smem_u32(&full_bar[f % g.stages]);
-                if (!ptx::mbar_wait(bar, (uint32_t)((f / g.stages) & 1), limit)) {
+            for (int f = fills - 1; f >= 0 && f >= fills - nst; --f) {
+                if (!ptx::mbar_wait(ptx::smem_u32(&full[f % nst]), (uint32_t)((f / nst) & 1), limit)) {
                     moe_flag(MOE_DEV_TIMEOUT);
                     break;
                 }
@@ -247,11 +465,17 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_bf16_f32(BM, Ep);
-            const uint32_t t_w12 = tmem_base + (uint32_t)(2 * Ep);
-            const int part_bytes = Ep * 128;
-            int stage = 0;
-            uint32_t phase = 0;
+            // FUSED_PARTS: one MMA (N = 3 E_pad) per tile and K step into the
+            // chunk buffer; otherwise W0 (N = E_pad) into its chunk buffer and
+            // W1, W2 together (N = 2 E_pad, rows E_pad .. 3 E_pad of the weight
+            // block) into their own columns.  Descriptors advance by adding
+            // byte offsets / 16 to the start-address field.
+            const uint32_t idesc_a = ptx::idesc_bf16_f32(BM, FP ? 3 * Ep : Ep);
+            const uint32_t idesc_b = ptx::idesc_bf16_f32(BM, 2 * Ep);
+            const uint64_t xd0 = ptx::sdesc_kmajor_sw128(smem0), wd0 = ptx::sdesc_kmajor_sw128(wring);
+            const uint64_t w12_off = (uint64_t)(Ep * 128) >> 4;
+            int xs = 0, ws = 0;
+            uint32_t xph = 0, wph = 0;
             bool ok = true;
             for (int i = 0; i < nkb; ++i) {
                 const int c = i / KC, buf = c & 1;
@@ -262,27 +486,41 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                     ok = false;
                     break;
                 }
-                if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, limit)) {
+                if (!ptx::mbar_wait(ptx::smem_u32(&xfull[xs]), xph, limit) ||
+                    !ptx::mbar_wait(ptx::smem_u32(&wfull[ws]), wph, limit)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sa = smem0 + stage * g.stage_bytes, sb = sa + X_BYTES;
-                const uint32_t t_w0 = tmem_base + (uint32_t)(buf * Ep);
+                const uint64_t ad = xd0 + (((uint64_t)xs * xstage_bytes) >> 4);
+                const uint64_t bd = wd0 + (((uint64_t)ws * wstage_bytes) >> 4);
+                const uint32_t c0 = tmem_base + (uint32_t)(buf * (FP ? 3 : 1) * Ep);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t ad = ptx::sdesc_kmajor_sw128(sa + kk * 32);
-                    ptx::mma_bf16(t_w0, ad, ptx::sdesc_kmajor_sw128(sb + kk * 32), idesc, (!first || kk > 0) ? 1u : 0u);
-                    ptx::mma_bf16(t_w12, ad, ptx::sdesc_kmajor_sw128(sb + part_bytes + kk * 32), idesc,
-                                  (i > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_bf16(t_w12, ad, ptx::sdesc_kmajor_sw128(sb + 2 * part_bytes + kk * 32), idesc, 1u);
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        if (tt < TPB) {
+                            const uint64_t a = ad + (uint64_t)((tt * X_BYTES + kk * 32) >> 4);
+                            const uint64_t b = bd + (uint64_t)((kk * 32) >> 4);
+                            const uint32_t toff = (uint32_t)tt * tile_cols;
+                            ptx::mma_bf16(c0 + toff, a, b, idesc_a, (!first || kk > 0) ? 1u : 0u);
+                            if (!FP)
+                                ptx::mma_bf16(tmem_base + toff + (uint32_t)(2 * Ep), a, b + w12_off, idesc_b,
+                                              (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
                 }
-                ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+                ptx::mma_commit(ptx::smem_u32(&xempty[xs]));
+                ptx::mma_commit(ptx::smem_u32(&wempty[ws]));
                 const bool last = (i % KC) == KC - 1 || i == nkb - 1;
                 if (last && c < nch - 1) ptx::mma_commit(ptx::smem_u32(&accf_bar[buf]));
-                if (++stage == g.stages) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (++xs == g.xstages) {
+                    xs = 0;
+                    xph ^= 1u;
+                }
+                if (++ws == g.wstages) {
+                    ws = 0;
+                    wph ^= 1u;
                 }
             }
             if (!ok) moe_flag(MOE_DEV_TIMEOUT);
@@ -291,12 +529,20 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ warps 2-5: W0 sums, partial logits
+        // ------------------------------------------------ warps 2-5: chunk sums, partial logits
         const int q = warp & 3;                    // TMEM lanes 32q .. 32q+31
-        const int r = q * 32 + lane;               // token row of the tile
+        const int r = q * 32 + lane;               // token row of each tile
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+        // one CTA owns at most two tiles, and only when E_pad <= 64
+        constexpr int TMAX = EMAX <= 64 ? 2 : 1;
+        constexpr int SR = FP ? 1 : EMAX;          // the W0 sum lives in registers when not FUSED_PARTS
+        float sumr[TMAX][SR];
+#pragma unroll
+        for (int tt = 0; tt < TMAX; ++tt)
+#pragma unroll
+            for (int e = 0; e < SR; ++e) sumr[tt][e] = 0.f;
         bool ok = true;
-        for (int c = 0; c + 1 < nch; ++c) {        // every W0 chunk but the last into the sum
+        for (int c = 0; c + 1 < nch; ++c) {        // every chunk but the last into the sum
             const int buf = c & 1;
             const bool w = ptx::mbar_wait(ptx::smem_u32(&accf_bar[buf]), (uint32_t)((c >> 1) & 1), limit);
             if (!__all_sync(0xffffffffu, w)) {
@@ -304,7 +550,26 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                 break;
             }
             ptx::tc_fence_after();
-            drain_chunk(tb, Ep, buf, c == 0);
+#pragma unroll
+            for (int tt = 0; tt < TMAX; ++tt) {
+                if (tt < TPB) {
+                    const uint32_t tt_b = tb + (uint32_t)tt * tile_cols;
+                    if (FP) {
+                        drain_chunk_fp(tt_b, Ep, buf, c == 0);
+                    } else {
+#pragma unroll
+                        for (int e0 = 0; e0 < SR; e0 += 16) {
+                            if (e0 < Ep) {
+                                uint32_t v[16];
+                                ptx::tmem_ld16(tt_b + (uint32_t)(buf * Ep + e0), v);
+                                ptx::tmem_ld_wait();
+#pragma unroll
+                                for (int u = 0; u < 16; ++u) sumr[tt][e0 + u] += __uint_as_float(v[u]);
+                            }
+                        }
+                    }
+                }
+            }
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_u32(&acce_bar[buf]));
         }
@@ -312,160 +577,132 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         const bool fin = ptx::mbar_wait(ptx::smem_u32(&fin_bar), 0, limit);
         if (!__all_sync(0xffffffffu, fin)) moe_flag(MOE_DEV_TIMEOUT);
         ptx::tc_fence_after();
-        // partial logits: (W0 sum + last W0 chunk) + (W1 + W2)
+        // partial logits: (sum of the earlier chunks + the last chunk), and in
+        // the per-part layout + (W1 + W2) accumulated over the whole range
         const int lb = (nch - 1) & 1;
-        float* red = reinterpret_cast<float*>(gsmem) + (size_t)r * Ep;
-        for (int e0 = 0; e0 < Ep; e0 += 16) {
-            uint32_t a0[16], a1[16], as[16];
-            ptx::tmem_ld16(tb + (uint32_t)(lb * Ep + e0), a0);
-            ptx::tmem_ld16(tb + (uint32_t)(2 * Ep + e0), a1);
-            if (nch >= 2) ptx::tmem_ld16(tb + (uint32_t)(3 * Ep + e0), as);
-            ptx::tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; u += 4) {
-                float v[4];
+        for (int tt = 0; tt < TMAX; ++tt) {
+            if (tt < TPB) {
+                const uint32_t tt_b = tb + (uint32_t)tt * tile_cols;
+                float* red = reinterpret_cast<float*>(gsmem) + (size_t)(tt * BM + r) * P;
+                if (FP) {
+                    for (int e0 = 0; e0 < Ep; e0 += 16) {
+                        uint32_t a0[16], a1[16], a2[16], as[16];
+                        ptx::tmem_ld16(tt_b + (uint32_t)(lb * 3 * Ep + e0), a0);
+                        ptx::tmem_ld16(tt_b + (uint32_t)(lb * 3 * Ep + Ep + e0), a1);
+                        ptx::tmem_ld16(tt_b + (uint32_t)(lb * 3 * Ep + 2 * Ep + e0), a2);
+                        if (nch >= 2) ptx::tmem_ld16(tt_b + (uint32_t)(6 * Ep + e0), as);
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float s0 = nch >= 2 ? __uint_as_float(as[u + w]) + __uint_as_float(a0[u + w])
-                                              : __uint_as_float(a0[u + w]);
-                    v[w] = s0 + __uint_as_float(a1[u + w]);
+                        for (int u = 0; u < 16; ++u) {
+                            const float chunk = __uint_as_float(a0[u]) + (__uint_as_float(a1[u]) + __uint_as_float(a2[u]));
+                            red[e0 + u] = nch >= 2 ? __uint_as_float(as[u]) + chunk : chunk;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e0 = 0; e0 < SR; e0 += 16) {
+                        if (e0 < Ep) {
+                            uint32_t a0[16], a1[16], a2[16];
+                            ptx::tmem_ld16(tt_b + (uint32_t)(lb * Ep + e0), a0);
+                            ptx::tmem_ld16(tt_b + (uint32_t)(2 * Ep + e0), a1);
+                            ptx::tmem_ld16(tt_b + (uint32_t)(3 * Ep + e0), a2);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) {
+                                const float w0 = nch >= 2 ? sumr[tt][e0 + u] + __uint_as_float(a0[u]) : __uint_as_float(a0[u]);
+                                red[e0 + u] = w0 + (__uint_as_float(a1[u]) + __uint_as_float(a2[u]));
+                            }
+                        }
+                    }
                 }
-                *reinterpret_cast<float4*>(red + e0 + u) = make_float4(v[0], v[1], v[2], v[3]);
             }
         }
     }
 
-    pdl_launch_dependents();   // the probability-sum kernel may launch; it waits for this grid's results
-    // every CTA of the cluster has its partial rows in shared memory
+    pdl_launch_dependents();   // the finishing kernel may launch; it waits for this grid's results
+    // every CTA of the cluster has its partial rows in shared memory (the
+    // proxy fence makes them visible to the bulk copies)
+    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     if (S > 1) ptx2::cluster_sync();
     else __syncthreads();
 
-    // ---------------------------------------------------- gather the S partial rows
-    const int TPC = BM / S;                       // tokens this CTA finishes
-    const int tbase = split * TPC;
-    float* const L = reinterpret_cast<float*>(gsmem + red_bytes(Ep));   // [TPC][Ep + 1]
-    const int LP = Ep + 1;
-    {
-        const int g4n = Ep / 4;
-        const uint32_t red0 = smem0;
-        for (int it = threadIdx.x; it < TPC * g4n; it += THREADS) {
-            const int tau = it / g4n, e = (it - tau * g4n) * 4;
-            const uint32_t off = (uint32_t)(((tbase + tau) * Ep + e) * 4);
-            float4 s4;
-            if (S == 1) {
-                s4 = *reinterpret_cast<const float4*>(gsmem + off);
-            } else {
-                s4 = ld_cluster_f4(ptx2::mapa(red0 + off, 0));
-                for (int sp = 1; sp < S; ++sp) {
-                    const float4 v = ld_cluster_f4(ptx2::mapa(red0 + off, (uint32_t)sp));
-                    s4.x += v.x;
-                    s4.y += v.y;
-                    s4.z += v.z;
-                    s4.w += v.w;
+    // ---------------------------------------------------- exchange the partial rows, write the logits
+    const int E = g.E;
+    const int tbase = split * TPC;                // first token this CTA finishes, counted from row0
+    const uint32_t recv0 = smem0 + (uint32_t)red_bytes(TPB, Ep);   // [S][TPC][P]
+    if (S > 1 && threadIdx.x == 0) {
+        for (int j = 0; j < S; ++j)
+            if (j != split)
+                bulk_push(ptx2::mapa(recv0 + (uint32_t)split * slice_bytes, (uint32_t)j),
+                          smem0 + (uint32_t)j * slice_bytes, slice_bytes,
+                          ptx2::mapa(ptx::smem_u32(&recv_bar), (uint32_t)j));
+    }
+    if (S > 1) {
+        const bool w = ptx::mbar_wait(ptx::smem_u32(&recv_bar), 0, limit);
+        if (!__all_sync(0xffffffffu, w)) moe_flag(MOE_DEV_TIMEOUT);
+    }
+    float* const red = reinterpret_cast<float*>(gsmem);
+    const float* const recv = reinterpret_cast<const float*>(gsmem + red_bytes(TPB, Ep));
+    if constexpr (FINISH_HERE) {
+        // softmax / top-k of this CTA's tokens right here, four lanes per token
+        // (eight tokens per warp); p goes back into the token's own row
+        constexpr int G = 4, EPL = EMAX / G;
+        const int sub = lane & (G - 1);
+        for (int base = warp * (32 / G); base < TPC; base += WARPS * (32 / G)) {
+            const int tau = base + lane / G;
+            const int t = row0 + tbase + tau;
+            const bool in_cta = tau < TPC;
+            const bool valid = in_cta && t < g.T;
+            float* row = red + (size_t)(tbase + (in_cta ? tau : 0)) * P;   // this CTA's own partial row
+            // logits: the S partial rows added in split order, then the bias
+            float l[EPL];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) l[i] = 0.f;
+            if (valid) {
+                for (int sp = 0; sp < S; ++sp) {
+                    const float* src = sp == split ? row : recv + (size_t)(sp * TPC + tau) * P;
+#pragma unroll
+                    for (int i = 0; i < EPL; ++i)
+                        if (sub + G * i < E) l[i] += src[sub + G * i];
                 }
             }
-            const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float bb = (g.bias && e + u < g.E) ? __ldg(g.bias + e + u) : 0.f;
-                L[tau * LP + e + u] = vals[u] + bb;
+            for (int i = 0; i < EPL; ++i) {
+                const int e = sub + G * i;
+                if (e < E) {
+                    l[i] += bias_sh[e];
+                    if (valid && g.sel.logits) g.sel.logits[(size_t)t * E + e] = l[i];
+                }
+            }
+            finish_token<EPL, KMAX>(l, sub, E, g.k, g.renorm, valid, t, g.sel, g.idx, g.gate);
+            if (in_cta) {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if (sub + G * i < E) row[sub + G * i] = valid ? l[i] : 0.f;
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += THREADS)
+            g.psum[(size_t)blockIdx.x * E + e] = column_sum(red + (size_t)tbase * P, TPC, P, e);
+    } else {
+        // the logits of this CTA's tokens for the finishing kernel: the S
+        // partial rows added in split order, then the bias; one warp per token
+        for (int tau = warp; tau < TPC; tau += WARPS) {
+            const int t = row0 + tbase + tau;
+            if (t >= g.T) break;                  // tokens ascend with tau
+            for (int e = lane; e < E; e += 32) {
+                float acc = 0.f;
+                for (int sp = 0; sp < S; ++sp)
+                    acc += sp == split ? red[(size_t)(tbase + tau) * P + e] : recv[(size_t)(sp * TPC + tau) * P + e];
+                g.logits[(size_t)t * E + e] = acc + bias_sh[e];
             }
         }
     }
-    // no CTA reads another's partial rows after this point
+    // every push into this CTA has landed (waited above); the ones it sent
+    // have been read once every CTA is past this point
     if (S > 1) ptx2::cluster_sync();
-    else __syncthreads();
-
-    // ---------------------------------------------------- finish: one thread per token
-    // (the row of logits is read from shared memory in each pass; rows are
-    // E_pad + 1 floats apart, so the threads of a warp hit different banks)
-    if (threadIdx.x < TPC) {
-        const int tau = threadIdx.x;
-        const int t = tile * BM + tbase + tau;
-        float* row = L + tau * LP;
-        const int E = g.E;
-        if (t < g.T) {
-            const RouteSel& sel = g.sel;
-            // group-limited routing: keep the topk_group groups of largest max
-            // logit (strict > scanning up the index keeps the lower group on ties)
-            const bool grouped = sel.n_group > 1;
-            unsigned gkeep = 0xffffffffu;
-            if (grouped) {
-                gkeep = 0;
-                for (int rr = 0; rr < sel.topk_group; ++rr) {
-                    float bv = -INFINITY;
-                    int bg = -1;
-                    for (int e = 0; e < E; ++e) {
-                        const int ge = e / sel.gsz;
-                        const float v = row[e];
-                        if (!((gkeep >> ge) & 1u) && (bg < 0 || v > bv)) {
-                            bv = v;
-                            bg = ge;
-                        }
-                    }
-                    if (bg >= 0) gkeep |= 1u << bg;
-                }
-            }
-            // maximum and top-k (descending list; an equal value keeps the lower index ahead)
-            float tv[KMAX];
-            int ti[KMAX];
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                tv[j] = -INFINITY;
-                ti[j] = 0x7fffffff;
-            }
-            float mx = -INFINITY;
-            for (int e = 0; e < E; ++e) {
-                const float v = row[e];
-                mx = fmaxf(mx, v);
-                if (v > tv[KMAX - 1] && (!grouped || ((gkeep >> (e / sel.gsz)) & 1u))) {
-#pragma unroll
-                    for (int j = KMAX - 1; j > 0; --j) {
-                        if (v > tv[j - 1]) {
-                            tv[j] = tv[j - 1];
-                            ti[j] = ti[j - 1];
-                        } else if (v > tv[j]) {
-                            tv[j] = v;
-                            ti[j] = e;
-                        }
-                    }
-                    if (v > tv[0]) {
-                        tv[0] = v;
-                        ti[0] = e;
-                    }
-                }
-            }
-            float s = 0.f;
-            for (int e = 0; e < E; ++e) s += expf(row[e] - mx);
-            if (sel.lse) sel.lse[t] = mx + logf(s);
-            float chosen = 0.f;
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < g.k) chosen += expf(tv[j] - mx) / s;
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < g.k) {
-                    const float pj = expf(tv[j] - mx) / s;
-                    g.idx[(size_t)t * g.k + j] = ti[j];
-                    g.gate[(size_t)t * g.k + j] = g.renorm ? pj / chosen : pj;
-                }
-            for (int e = 0; e < E; ++e) {
-                const float v = row[e];
-                if (sel.logits) sel.logits[(size_t)t * E + e] = v;
-                row[e] = expf(v - mx) / s;
-            }
-        } else {
-            for (int e = 0; e < E; ++e) row[e] = 0.f;
-        }
-    }
-    __syncthreads();
-    // per-expert sums of p over this CTA's tokens, in token order
-    for (int e = threadIdx.x; e < g.E; e += THREADS) {
-        float v = 0.f;
-        for (int tau = 0; tau < TPC; ++tau) v += L[tau * LP + e];
-        g.psum[(size_t)blockIdx.x * g.E + e] = v;
-    }
 
     ptx::tc_fence_before();
     __syncthreads();
@@ -473,6 +710,42 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, g.tmem_cols);
     }
+}
+
+// Softmax, top-k and per-block probability sums from the logits [T, E] (for
+// E > 64, where the fused kernel leaves them to this one): four lanes per
+// token, FIN_TOKENS tokens per block.  Launched as a programmatic dependent
+// of the logits kernel; many blocks per SM hide the latency of the short
+// dependent chains of finish_token.
+constexpr int FIN_THREADS = 256;
+constexpr int FIN_TOKENS = FIN_THREADS / 4;
+
+template <int EMAX, int KMAX>
+__global__ void __launch_bounds__(FIN_THREADS)
+route_finish_kernel(const FinArgs g)
+{
+    constexpr int G = 4, EPL = EMAX / G;
+    __shared__ float pbuf[FIN_TOKENS][EMAX + 1];     // p of the block's tokens, for the per-expert sums
+    pdl_launch_dependents();
+    pdl_wait();                                      // the logits kernel has finished
+    const int lane = threadIdx.x & 31, sub = lane & (G - 1);
+    const int slot = threadIdx.x / G;                // token of the block handled by this group of four
+    const int t = blockIdx.x * FIN_TOKENS + slot;
+    const bool valid = t < g.T;
+    const int E = g.E;
+    float l[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = sub + G * i;
+        l[i] = (valid && e < E) ? __ldcg(g.logits + (size_t)t * E + e) : 0.f;
+    }
+    finish_token<EPL, KMAX>(l, sub, E, g.k, g.renorm, valid, t, g.sel, g.idx, g.gate);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        if (sub + G * i < E) pbuf[slot][sub + G * i] = valid ? l[i] : 0.f;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += FIN_THREADS)
+        g.psum[(size_t)blockIdx.x * E + e] = column_sum(&pbuf[0][0], FIN_TOKENS, EMAX + 1, e);
 }
 
 // prob_sum[e] = sum over the R rows of psum[:, e]: one block per expert, a
