@@ -440,9 +440,10 @@ moe_status moe_router_grads(const void* dx_perm, const int32_t* slot_row, const 
  * with a message on stderr and enqueue nothing.  It calls no cudaMalloc,
  * cudaFree or allocating library routine.
  *
- * The first call on a device looks up the array's device address with that
- * device current (once per device); make that first call before any stream
- * capture.  Every call shares the one array and the array keeps the last
+ * The first call on a device with more than 16384 assignments (T*k; smaller
+ * batches rank in one block and use no scratch) looks up the array's device
+ * address with that device current (once per device); make that first call
+ * before any stream capture.  Every call shares the one array and the array keeps the last
  * call's contents: each call overwrites every histogram cell it reads, so
  * nothing needs clearing, but calls that overlap on the GPU (different
  * streams, or different host threads, with no ordering between them) race on

@@ -35,10 +35,28 @@ def test_library_exports_every_declared_function():
     assert L.moe_abi_version() == 1
 
 
+def declared_parameter_counts():
+    """{name: number of parameters} of every function declared in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(moe_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
 def test_binding_declares_a_signature_for_every_function():
     src = open(os.path.join(ROOT, "top_routing_expert_02_b300", "__init__.py")).read()
     missing = [n for n in declared_functions() if f'"{n}"' not in src]
     assert not missing, missing
+
+
+def test_binding_signatures_match_the_header_parameter_counts():
+    """Each ctypes signature has as many arguments as the header declares."""
+    counts = declared_parameter_counts()
+    assert set(counts) == set(declared_functions())
+    wrong = {n: (c, len(moe._SIGS[n][1])) for n, c in counts.items() if len(moe._SIGS[n][1]) != c}
+    assert not wrong, wrong
 
 
 def _golden_caps():
@@ -62,7 +80,8 @@ def test_perm_rows_and_workspace():
     assert moe.perm_rows_max(10, 2, 8, -1) == -1
     assert moe.workspace_bytes("ffn", 4096, 4096, 8, 2, 14336) == 0
     assert moe.workspace_bytes("route", 4096, 4096, 8, 2, 14336) > 0
-    assert moe.workspace_bytes("dispatch", 4096, 4096, 8, 2, 14336) >= 8 * 4 * 8
+    assert moe.workspace_bytes("dispatch", 4096, 4096, 8, 2, 14336) == 0       # ranked in one block
+    assert moe.workspace_bytes("dispatch", 16384, 2048, 64, 2, 1408) == 32 * 64 * 4   # 32 chunk histograms
     assert moe.workspace_bytes("route", 0, 4096, 8, 2, 14336) == 0
 
 
@@ -101,7 +120,7 @@ def test_dispatch_ffn_combine_aux_argument_errors():
     assert L.moe_dispatch(*bad) == 1
     bad = list(args); bad[8] = 96
     assert L.moe_dispatch(*bad) == 2
-    bad = list(args); bad[18] = 8
+    bad = list(args); bad[2] = 20000; bad[18] = 8      # 40000 assignments: the two-kernel ranking needs a workspace
     assert L.moe_dispatch(*bad) == 3
     # ffn: F not a multiple of 64, bad act, null weights
     assert L.moe_expert_up(F_, F_, F_, 8, 128, 96, 0, 1, F_, 10, F_, None) == 2
@@ -191,6 +210,19 @@ def test_backward_argument_errors():
     assert L.moe_grad_x(FAKE, FAKE, FAKE, None, 16, 2, 8, 128, 1, FAKE, None) == 1
     assert L.moe_router_wgrad(FAKE, FAKE, 1, 0, 8, 128, FAKE, None, FAKE, 1 << 20, None) == 1
     assert L.moe_router_wgrad(FAKE, FAKE, 1, 64, 8, 128, FAKE, None, FAKE, 8, None) == 3    # workspace
+
+
+def test_d_must_be_a_multiple_of_64():
+    """d = 72 (16-byte rows, but not whole 64-element K blocks of the tensor-core
+    GEMMs and the router) is MOE_ERR_UNSUPPORTED on every call that takes d."""
+    L = moe.lib()
+    d = 72
+    assert L.moe_route(FAKE, 1, FAKE, None, 16, d, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 2
+    assert L.moe_dispatch(FAKE, FAKE, 16, 2, 8, 4, FAKE, 1, d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                          1 << 20, None) == 2
+    assert L.moe_expert_up(FAKE, FAKE, FAKE, 8, d, 128, 0, 1, FAKE, 10, FAKE, None) == 2
+    assert L.moe_expert_down(FAKE, FAKE, FAKE, 8, d, 128, 1, FAKE, FAKE, 10, FAKE, None) == 2
+    assert L.moe_combine(FAKE, FAKE, 16, 2, d, 1, FAKE, None) == 2
 
 
 def test_misaligned_buffers_are_refused_before_any_work():

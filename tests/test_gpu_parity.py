@@ -9,7 +9,8 @@ import oracle
 import top_routing_expert_02_b300 as moe
 from top_routing_expert_02_b300 import synth
 
-from moe_cases import compare_dispatch, compare_output, compare_routing, make_case, rel_fro, run_gpu, run_oracle
+from moe_cases import (Y_TOL, check_expert_rows_on_device, compare_dispatch, compare_output, compare_routing,
+                       make_case, rel_fro, run_gpu, run_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +41,9 @@ SMALL = {
     "min_d64_f64": C("min_d64_f64", 1, 64, 2, 1, 64, "gelu", 0.0, "bf16"),
     # fp32 layer with GELU and drops, two K blocks
     "f32_gelu_e4": C("f32_gelu_e4", 333, 128, 4, 2, 192, "gelu", 1.0, "f32"),
+    # more GEMM tiles than two per SM (up: 128 M-tiles x 6 N-tiles, down: 128 x 2), so the
+    # persistent blocks run several tiles each, through both TMEM accumulators; every token checked
+    "many_tiles": C("many_tiles", 8192, 512, 8, 2, 768, "swiglu", 0.0, "bf16"),
 }
 
 
@@ -65,6 +69,7 @@ def test_small_layers_full(name):
     cfg = SMALL[name]
     case = make_case(cfg)
     plan = run_gpu(case)
+    check_expert_rows_on_device(plan, case["x"], case["w1"], case["w2"], cfg.act, tol=Y_TOL[cfg.dtype])
     ref = run_oracle(case)
     compare_routing(plan, ref, cfg.dtype)
     compare_dispatch(plan, ref, case["x_h"])

@@ -165,7 +165,13 @@ inline size_t route_ws_bytes(long long T, int d, int E)
     return a > b ? a : b;
 }
 inline long long dispatch_chunks(long long T, int k) { return (T * k + dispatch::CHUNK - 1) / dispatch::CHUNK; }
-inline size_t dispatch_ws_bytes(long long T, int k, int E) { return (size_t)dispatch_chunks(T, k) * E * sizeof(int); }
+// Per-chunk expert histograms of the two-kernel ranking; a batch of at most
+// SMALL_MAX assignments ranks in one block and needs none.
+inline size_t dispatch_ws_bytes(long long T, int k, int E)
+{
+    if (T * k <= dispatch::SMALL_MAX) return 0;
+    return (size_t)dispatch_chunks(T, k) * E * sizeof(int);
+}
 
 
 // Opt a kernel into `bytes` of dynamic shared memory once per device (the
@@ -1387,7 +1393,7 @@ extern "C" moe_status moe_dispatch_noalloc(const int32_t* topk_idx, const float*
                      (long long)T * k, E, need, NOALLOC_SCRATCH_BYTES);
         return MOE_ERR_WORKSPACE;
     }
-    void* scratch = nullptr;
+    void* scratch = nullptr;   // only a batch ranked by the two-kernel path reads it
     if (need > 0) {
         const moe_status st = noalloc_scratch(&scratch);
         if (st != MOE_OK) return st;
