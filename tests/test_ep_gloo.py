@@ -94,7 +94,7 @@ def _tokens(rank):
     return torch.randn(40 + 9 * rank, D, generator=g)
 
 
-def _worker(rank, world, port, out_dir):
+def _worker(rank, world, port, out_dir, host_exchange=False):
     import oracle
     from top_routing_expert_02_b300.ep import ep_forward, expert_block
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -104,16 +104,19 @@ def _worker(rank, world, port, out_dir):
     lo, hi = expert_block(E, world, rank)
     cap = oracle.capacity(x.shape[0], E, 1.0)
     res = ep_forward(x, W, None, w1[lo:hi].contiguous(), w2[lo:hi].contiguous(), k=K, cap=cap, act=ACT,
-                     ops=OracleOps())
+                     ops=OracleOps(), host_exchange=host_exchange)
     np.save(os.path.join(out_dir, f"y{rank}.npy"), res.y.numpy())
     np.save(os.path.join(out_dir, f"m{rank}.npy"), np.array([float(res.loss), res.recv_rows]))
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 4])
-def test_expert_parallel_forward_matches_the_layer_on_each_shard(world, tmp_path):
+@pytest.mark.parametrize("world,host_exchange", [(2, False), (4, False), (2, True)])
+def test_expert_parallel_forward_matches_the_layer_on_each_shard(world, host_exchange, tmp_path):
+    """host_exchange=True stages the exchanges as raw bytes through host
+    tensors (the path the two-rank GPU test takes over gloo)."""
     import oracle
-    mp.start_processes(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, start_method="spawn")
+    mp.start_processes(_worker, args=(world, _free_port(), str(tmp_path), host_exchange), nprocs=world,
+                       start_method="spawn")
     W, w1, w2 = _weights()
     xs = [_tokens(r) for r in range(world)]
     whole = torch.cat(xs)

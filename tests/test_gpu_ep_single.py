@@ -1,7 +1,8 @@
 """The expert-parallel layer (top_routing_expert_02_b300.ep) through the CUDA
 library on one GPU: a one-rank NCCL group, where the exchange is a copy and
-the regrouping an identity permutation, must reproduce MoEPlan bit for bit;
-and moe_permute_rows against torch indexing."""
+the regrouping an identity permutation, must reproduce MoEPlan bit for bit
+and the oracle's layer within the bf16 bar; and moe_permute_rows against
+torch indexing."""
 import pytest
 import torch
 import torch.distributed as dist
@@ -10,7 +11,7 @@ import top_routing_expert_02_b300 as moe
 from top_routing_expert_02_b300 import synth
 from top_routing_expert_02_b300.ep import ep_forward
 
-from moe_cases import make_case
+from moe_cases import compare_output, make_case, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -45,3 +46,6 @@ def test_one_rank_expert_parallel_layer_equals_the_plan():
     assert torch.equal(res.y, plan.y)
     assert abs(float(res.loss) - float(plan.loss.item())) <= 1e-6 * float(plan.loss.item())
     assert res.recv_rows == int(plan.disp.offsets[-1].item())
+    ref = run_oracle(case)                       # and directly against the oracle's layer
+    assert res.recv_rows == int(ref["kept"].sum())
+    compare_output(plan, ref, cfg.dtype)

@@ -23,9 +23,15 @@ The local steps go through an ``ops`` object (route, dispatch, permute_rows,
 expert_ffn, combine, aux_loss): :class:`LibraryOps` runs the CUDA library;
 tests may supply another implementation of the same six calls.  Host synchronisation
 happens once per layer, to turn the received counts into split sizes.
+
+``host_exchange=True`` stages every exchange through host memory (device
+tensors are copied to the host, exchanged, and copied back), for process
+groups whose backend moves host tensors only (gloo); the device-side steps
+are unchanged.
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass
 
 import torch
@@ -84,12 +90,24 @@ class EPResult:
     recv_rows: int             # rows this rank's experts processed
 
 
-def _a2a(out, inp, out_splits, in_splits, group):
-    dist.all_to_all_single(out, inp, out_splits, in_splits, group=group)
+def _bytes_view(t: torch.Tensor) -> torch.Tensor:
+    """Rows of t as raw bytes [rows, row_bytes] (keeps the row split sizes)."""
+    row_bytes = t.element_size() * (math.prod(t.shape[1:]) if t.dim() > 1 else 1)
+    return t.contiguous().view(torch.uint8).reshape(t.shape[0], row_bytes)
+
+
+def _a2a(out, inp, out_splits, in_splits, group, host=False):
+    if not host:
+        dist.all_to_all_single(out, inp, out_splits, in_splits, group=group)
+        return
+    src = _bytes_view(inp).cpu()
+    dst = torch.empty((out.shape[0], src.shape[1]), dtype=torch.uint8)
+    dist.all_to_all_single(dst, src, out_splits, in_splits, group=group)
+    out.copy_(dst.view(out.dtype).reshape(out.shape))
 
 
 def ep_forward(x, W, b, w1_local, w2_local, *, k: int, cap: int, act: str, renorm: bool = True, alpha: float = 0.01,
-               group=None, ops=None) -> EPResult:
+               group=None, ops=None, host_exchange: bool = False) -> EPResult:
     """One expert-parallel layer forward (module docstring).  x [T_local, d] is
     this rank's tokens; W [E, d] (and b) the router, the same on every rank;
     w1_local / w2_local this rank's expert block of w1 [E, N1, d] / w2 [E, d, F]."""
@@ -111,10 +129,14 @@ def ep_forward(x, W, b, w1_local, w2_local, *, k: int, cap: int, act: str, renor
     offsets = D["offsets"].to("cpu", torch.int64)
 
     # exchange 1: how many rows of each of its experts every rank receives from us
-    send_counts = kept.view(G, El).to(dev)
-    recv_dev = torch.empty_like(send_counts)
-    dist.all_to_all_single(recv_dev, send_counts, group=group)   # equal splits: El counts per rank
-    recv_counts = recv_dev.to("cpu")                              # [source rank, local expert]
+    if host_exchange:
+        recv_counts = torch.empty((G, El), dtype=torch.int64)
+        dist.all_to_all_single(recv_counts, kept.view(G, El).contiguous(), group=group)
+    else:
+        send_counts = kept.view(G, El).to(dev)
+        recv_dev = torch.empty_like(send_counts)
+        dist.all_to_all_single(recv_dev, send_counts, group=group)   # equal splits: El counts per rank
+        recv_counts = recv_dev.to("cpu")                              # [source rank, local expert]
 
     in_splits = [int(offsets[(r + 1) * El] - offsets[r * El]) for r in range(G)]
     out_splits = [int(recv_counts[s].sum()) for s in range(G)]
@@ -128,8 +150,8 @@ def ep_forward(x, W, b, w1_local, w2_local, *, k: int, cap: int, act: str, renor
     rdt = x_send.dtype
     x_recv = torch.empty((n_recv, d), dtype=rdt, device=dev)
     g_recv = torch.empty((n_recv,), dtype=g_send.dtype, device=dev)
-    _a2a(x_recv, x_send, out_splits, in_splits, group)
-    _a2a(g_recv, g_send, out_splits, in_splits, group)
+    _a2a(x_recv, x_send, out_splits, in_splits, group, host_exchange)
+    _a2a(g_recv, g_send, out_splits, in_splits, group, host_exchange)
 
     # regroup: received [src][local expert] blocks -> [local expert][src] segments;
     # every received row gets the key (local expert, src) of its block, and a
@@ -157,10 +179,14 @@ def ep_forward(x, W, b, w1_local, w2_local, *, k: int, cap: int, act: str, renor
 
     # reverse exchange: every row returns to its sender, in the order it was sent
     y_perm = torch.empty((max(A, 1), d), dtype=y_back.dtype, device=dev)
-    _a2a(y_perm[:A], y_back.contiguous(), in_splits, out_splits, group)
+    _a2a(y_perm[:A], y_back.contiguous(), in_splits, out_splits, group, host_exchange)
     y = ops.combine(y_perm, D["slot_row"])
 
     # global aux loss over every rank's tokens
-    c, p, t = global_aux_inputs(D["counts"], prob_sum, T, group)
+    if host_exchange:
+        c, p, t = global_aux_inputs(D["counts"].cpu(), prob_sum.cpu(), T, group)
+        c, p = c.to(D["counts"].device), p.to(prob_sum.device)
+    else:
+        c, p, t = global_aux_inputs(D["counts"], prob_sum, T, group)
     loss = ops.aux_loss(c, p, t, alpha)
     return EPResult(y=y, loss=loss, counts=D["counts"], recv_rows=n_recv)
