@@ -435,13 +435,13 @@ moe_status moe_router_grads(const void* dx_perm, const int32_t* slot_row, const 
  * Its scratch (the per-chunk expert histograms) is a fixed 256 KiB array in
  * the library's device memory, which every GPU that loads the library holds
  * until the process exits.  Limit: moe_workspace_bytes(MOE_CALL_DISPATCH,
- * T, d, E, k, ...) <= 262144, i.e. ceil(T*k / 1024) * E <= 65536 (for
- * example T*k <= 262144 at E = 256); larger calls return MOE_ERR_WORKSPACE
- * with a message on stderr and enqueue nothing.  It calls no cudaMalloc,
- * cudaFree or allocating library routine.
+ * T, d, E, k, ...) <= 262144, i.e. ceil(T*k / c) * E <= 65536 with chunks of
+ * c = 256 assignments up to T*k = 65536 and c = 1024 above (for example
+ * T*k <= 262144 at E = 256); larger calls return MOE_ERR_WORKSPACE with a
+ * message on stderr and enqueue nothing.  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.
  *
- * The first call on a device with more than 16384 assignments (T*k; smaller
- * batches rank in one block and use no scratch) looks up the array's device
+ * The first call on a device with T*k > 0 looks up the array's device
  * address with that device current (once per device); make that first call
  * before any stream capture.  Every call shares the one array and the array keeps the last
  * call's contents: each call overwrites every histogram cell it reads, so

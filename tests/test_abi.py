@@ -80,8 +80,11 @@ def test_perm_rows_and_workspace():
     assert moe.perm_rows_max(10, 2, 8, -1) == -1
     assert moe.workspace_bytes("ffn", 4096, 4096, 8, 2, 14336) == 0
     assert moe.workspace_bytes("route", 4096, 4096, 8, 2, 14336) > 0
-    assert moe.workspace_bytes("dispatch", 4096, 4096, 8, 2, 14336) == 0       # ranked in one block
-    assert moe.workspace_bytes("dispatch", 16384, 2048, 64, 2, 1408) == 32 * 64 * 4   # 32 chunk histograms
+    # per-chunk expert histograms: chunks of 256 assignments up to T*k = 65536, of 1024 above
+    assert moe.workspace_bytes("dispatch", 4096, 4096, 8, 2, 14336) == 32 * 8 * 4
+    assert moe.workspace_bytes("dispatch", 16384, 2048, 64, 2, 1408) == 128 * 64 * 4
+    assert moe.workspace_bytes("dispatch", 32768, 4096, 128, 8, 1536) == 256 * 128 * 4
+    assert moe.workspace_bytes("dispatch", 0, 4096, 8, 2, 14336) == 0
     assert moe.workspace_bytes("route", 0, 4096, 8, 2, 14336) == 0
 
 
@@ -120,7 +123,7 @@ def test_dispatch_ffn_combine_aux_argument_errors():
     assert L.moe_dispatch(*bad) == 1
     bad = list(args); bad[8] = 96
     assert L.moe_dispatch(*bad) == 2
-    bad = list(args); bad[2] = 20000; bad[18] = 8      # 40000 assignments: the two-kernel ranking needs a workspace
+    bad = list(args); bad[18] = 8                       # 32 assignments: one chunk histogram of 8 experts (32 bytes)
     assert L.moe_dispatch(*bad) == 3
     # ffn: F not a multiple of 64, bad act, null weights
     assert L.moe_expert_up(F_, F_, F_, 8, 128, 96, 0, 1, F_, 10, F_, None) == 2

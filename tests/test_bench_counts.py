@@ -1,10 +1,9 @@
 """bench.py's launch-count claim (`gpu_launches`) against the launch lists
-captured with ncu on the same workloads: eight library kernels per e8_swiglu
-forward step (router 3, one-block dispatch ranks + row scatter 2, up and down
-GEMMs, combine with the aux loss) and 20 per training step; the two-kernel
-dispatch above 16384 assignments; one more finishing kernel of the router
-above 64 experts; one more for the global aux loss of token-sharded
-replicas."""
+captured with ncu on the same workloads: nine library kernels per e8_swiglu
+forward step (router 3, dispatch histograms + ranks + row scatter 3, up and
+down GEMMs, combine with the aux loss) and 21 per training step; one more
+finishing kernel of the router above 64 experts; one more for the global aux
+loss of token-sharded replicas."""
 import argparse
 import importlib.util
 import os
@@ -29,13 +28,13 @@ def test_forward_and_training_launch_counts(monkeypatch):
     b = _bench()
     monkeypatch.delenv("WORLD_SIZE", raising=False)
     e8 = b.synth.workload("e8_swiglu")
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 8
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(train=True)) == 20
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(gather=True)) == 7          # no row scatter
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(z_beta=1e-3)) == 9         # + z-loss
-    e64 = b.synth.workload("e64_zipf")                                     # T*k = 32768: hist + rank
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 9
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(train=True)) == 21
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(gather=True)) == 8          # no row scatter
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(z_beta=1e-3)) == 10        # + z-loss
+    e64 = b.synth.workload("e64_zipf")
     assert b.KERNELS_PER_STEP_TOTAL(e64, _args()) == 9
     e128 = b.synth.workload("e128_top8_T32768")                           # E > 64: + finishing kernel
     assert b.KERNELS_PER_STEP_TOTAL(e128, _args()) == 10
     monkeypatch.setenv("WORLD_SIZE", "2")                                  # replicas: + global aux loss
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 9
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 10

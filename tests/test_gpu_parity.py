@@ -180,10 +180,11 @@ def test_identity_experts_return_x_bf16():
 
 
 @pytest.mark.parametrize("T,k,E,cap", [(8192, 2, 64, 160), (8193, 2, 64, 160), (2048, 8, 128, 100),
-                                       (4097, 8, 128, 300), (1, 1, 8, 1), (33, 16, 256, 2)])
+                                       (4097, 8, 128, 300), (1, 1, 8, 1), (33, 16, 256, 2),
+                                       (32768, 2, 8, 9000), (9001, 8, 128, 700), (70001, 1, 16, 5000)])
 def test_dispatch_both_rank_paths_against_oracle(T, k, E, cap):
-    """The one-block rank kernel (T*k <= 16384) and the histogram + rank pair
-    (larger T*k) against the oracle's queue simulation: counts, kept,
+    """The histogram + rank kernels with chunks of 256 assignments (T*k <=
+    65536) and of 1024 (larger T*k) against the oracle's queue simulation: counts, kept,
     n_dropped, offsets (exclusive scan of kept) and every slot's row, bit for
     bit, on skewed expert choices (distinct experts per token)."""
     g = torch.Generator().manual_seed(T * 31 + k)

@@ -46,18 +46,17 @@ def _check_against_workspace_path(T, E, k, d, cap, seed):
 
 
 def test_noalloc_dispatch_matches_workspace_dispatch_twice_in_a_row():
-    # Both calls have T*k above 16384, where the dispatch keeps its per-chunk
-    # histograms in the scratch array (smaller batches rank in one block and
-    # need none).
-    # first call: 18 chunks of 1024 assignments, 64 experts, drops
+    # The dispatch keeps its per-chunk histograms in the scratch array.
+    # first call: 71 chunks of 256 assignments, 64 experts, drops
     d1 = _check_against_workspace_path(T=9000, E=64, k=2, d=256, cap=150, seed=11)
-    # second call: other shape; leftover histogram cells of the first call remain in the array
-    d2 = _check_against_workspace_path(T=20000, E=8, k=2, d=128, cap=3000, seed=12)
+    # second call: other shape and chunk size (79 chunks of 1024); leftover
+    # histogram cells of the first call remain in the array
+    d2 = _check_against_workspace_path(T=40000, E=8, k=2, d=128, cap=6000, seed=12)
     assert d1 > 0 and d2 > 0
 
 
-def test_noalloc_dispatch_small_batch_needs_no_scratch():
-    # T*k <= 16384: the one-block path, same results as the workspace call
+def test_noalloc_dispatch_small_batch():
+    # a few chunks of 256 assignments, same results as the workspace call
     assert _check_against_workspace_path(T=1000, E=8, k=2, d=128, cap=200, seed=13) > 0
 
 

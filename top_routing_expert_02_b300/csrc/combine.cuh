@@ -29,7 +29,9 @@ __device__ __forceinline__ void aux_loss_warp(const int32_t* __restrict__ counts
 }
 
 // Optional auxiliary loss computed by the first warp of a combine launch
-// (saves the aux-loss launch; loss == nullptr: none).
+// (saves the aux-loss launch; loss == nullptr: none).  Its inputs (counts,
+// prob_sum) come from routing and dispatch, which have finished before the
+// expert GEMMs, so it runs before the wait for y_perm.
 struct AuxArgs {
     const int32_t* counts;
     const float* prob_sum;
@@ -39,68 +41,83 @@ struct AuxArgs {
     float* loss;
 };
 
-// One warp per token; each lane sums 16-byte vectors of the token's k rows
-// in j order (fp32) and rounds once.  Dropped slots (-1) are skipped; a token
-// with none kept gets zeros.  Each lane works on four vectors at a time, so
-// 4·k loads are in flight before the first sum.
+// One warp per (token, chunk of 128 16-byte vectors of its row): each lane
+// sums four vectors of the token's k rows in j order (fp32) and rounds once.
+// The rows go in pairs whose eight loads are all issued before their sums,
+// unconditionally: a dropped slot (-1) reads row 0 and adds -0.0, which is
+// an exact identity for every fp32 value (x + -0 = x, also for x = +0 and
+// -0), so the result has the bits of skipping it.  A token with no kept slot
+// gets zeros.  The slot rows of the token are loaded once per task, one per
+// lane, and handed out by shuffles.
+constexpr int CHUNK_VEC = 128;   // 16-byte vectors per chunk (4 per lane)
+constexpr int ROWS_PER_BATCH = 2;
+
 template <bool BF16>
 __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ slot_row, int T, int k,
                int vec16, uint4* __restrict__ y, AuxArgs aux)
 {
+    constexpr int V = CHUNK_VEC / 32, KB = ROWS_PER_BATCH;
     const int lane = threadIdx.x & 31;
     if (aux.loss && blockIdx.x == 0 && threadIdx.x < 32)
         aux_loss_warp(aux.counts, aux.prob_sum, aux.T, aux.E, aux.alpha, aux.loss, lane);
-    const int warps_total = gridDim.x * WARPS;
-    for (int t = blockIdx.x * WARPS + (threadIdx.x >> 5); t < T; t += warps_total) {
-        int rows[16];
+    pdl_wait();   // launched as a programmatic dependent of the kernel writing y_perm
+    const int nchunk = (vec16 + CHUNK_VEC - 1) / CHUNK_VEC;
+    const long long tasks = (long long)T * nchunk;
+    const long long warps_total = (long long)gridDim.x * WARPS;
+    for (long long task = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5); task < tasks; task += warps_total) {
+        const int t = (int)(task / nchunk);
+        const int v0 = (int)(task - (long long)t * nchunk) * CHUNK_VEC + lane;
+        const int my_row = lane < k ? __ldg(slot_row + (size_t)t * k + lane) : -1;   // k <= 16
+        float acc[V][8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) rows[j] = j < k ? __ldg(slot_row + (size_t)t * k + j) : -1;
-        for (int v0 = lane; v0 < vec16; v0 += 128) {
-            float acc[4][8];
+        for (int u = 0; u < V; ++u)
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+        for (int j0 = 0; j0 < k; j0 += KB) {
+            uint4 q[KB][V];
+            bool ok[KB];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+            for (int jj = 0; jj < KB; ++jj) {
+                const int r = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
+                ok[jj] = j0 + jj < k && r >= 0;
+                const uint4* src = y_perm + (size_t)(ok[jj] ? r : 0) * vec16;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (rows[j] < 0) continue;
-                const uint4* src = y_perm + (size_t)rows[j] * vec16;
-                uint4 q[4];
+                for (int u = 0; u < V; ++u)
+                    q[jj][u] = v0 + 32 * u < vec16 ? ldg_nc_v4(src + v0 + 32 * u) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    q[u] = (v0 + 32 * u < vec16) ? ldg_nc_v4(src + v0 + 32 * u) : make_uint4(0, 0, 0, 0);
+            for (int jj = 0; jj < KB; ++jj)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < V; ++u) {
                     if (BF16) {
                         float f[8];
-                        unpack_bf16x8(q[u], f);
+                        unpack_bf16x8(q[jj][u], f);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[u][i] += f[i];
+                        for (int i = 0; i < 8; ++i) acc[u][i] += ok[jj] ? f[i] : -0.0f;
                     } else {
-                        acc[u][0] += __uint_as_float(q[u].x);
-                        acc[u][1] += __uint_as_float(q[u].y);
-                        acc[u][2] += __uint_as_float(q[u].z);
-                        acc[u][3] += __uint_as_float(q[u].w);
+                        acc[u][0] += ok[jj] ? __uint_as_float(q[jj][u].x) : -0.0f;
+                        acc[u][1] += ok[jj] ? __uint_as_float(q[jj][u].y) : -0.0f;
+                        acc[u][2] += ok[jj] ? __uint_as_float(q[jj][u].z) : -0.0f;
+                        acc[u][3] += ok[jj] ? __uint_as_float(q[jj][u].w) : -0.0f;
                     }
                 }
-            }
+        }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int v = v0 + 32 * u;
-                if (v >= vec16) break;
-                uint4 o;
-                if (BF16) {
-                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-                } else {
-                    o = make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]), __float_as_uint(acc[u][2]),
-                                   __float_as_uint(acc[u][3]));
-                }
-                y[(size_t)t * vec16 + v] = o;
+        for (int u = 0; u < V; ++u) {
+            const int v = v0 + 32 * u;
+            if (v >= vec16) break;
+            uint4 o;
+            if (BF16) {
+                o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+            } else {
+                o = make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]), __float_as_uint(acc[u][2]),
+                               __float_as_uint(acc[u][3]));
             }
+            y[(size_t)t * vec16 + v] = o;
         }
     }
 }

@@ -17,6 +17,13 @@ __device__ unsigned int g_moe_status;
 
 __device__ __forceinline__ void moe_flag(unsigned bits) { atomicOr(&g_moe_status, bits); }
 
+// Programmatic dependent launch: the next kernel in the stream may start
+// (launch_dependents); wait until the kernel before this one has finished and
+// its memory is visible (wait).  Both are no-ops for a kernel launched
+// without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t u16) { return __uint_as_float(u16 << 16); }
 
 // Eight bf16 (one 16-byte vector) -> eight floats.

@@ -65,6 +65,40 @@ inline moe_status launch_ex_status(cudaError_t e)
     return launch_status();
 }
 
+// Launch configuration of a kernel that is a programmatic dependent of the
+// kernel before it in the stream (it may start once that kernel has called
+// griddepcontrol.launch_dependents; it calls griddepcontrol.wait before it
+// reads that kernel's results).
+struct PdlLaunch {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg;
+    PdlLaunch(int grid, int threads, cudaStream_t stream, size_t smem = 0)
+    {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    PdlLaunch(const PdlLaunch&) = delete;
+};
+
+// Blocks of `kern` (no dynamic shared memory) that fit on one SM at once (at least 1).
+template <typename K>
+int resident_blocks(K kern, int threads)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    return n > 0 ? n : 1;
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;
@@ -164,14 +198,13 @@ inline size_t route_ws_bytes(long long T, int d, int E)
     const size_t a = route_ws_bytes_simt(T, E), b = route_ws_bytes_tc(T, d, E);
     return a > b ? a : b;
 }
-inline long long dispatch_chunks(long long T, int k) { return (T * k + dispatch::CHUNK - 1) / dispatch::CHUNK; }
-// Per-chunk expert histograms of the two-kernel ranking; a batch of at most
-// SMALL_MAX assignments ranks in one block and needs none.
-inline size_t dispatch_ws_bytes(long long T, int k, int E)
+inline long long dispatch_chunks(long long T, int k)
 {
-    if (T * k <= dispatch::SMALL_MAX) return 0;
-    return (size_t)dispatch_chunks(T, k) * E * sizeof(int);
+    const int ch = dispatch::chunk_size(T * k);
+    return (T * k + ch - 1) / ch;
 }
+// Per-chunk expert histograms of the ranking.
+inline size_t dispatch_ws_bytes(long long T, int k, int E) { return (size_t)dispatch_chunks(T, k) * E * sizeof(int); }
 
 
 // Opt a kernel into `bytes` of dynamic shared memory once per device (the
@@ -690,25 +723,39 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     const int nchunk = (int)dispatch_chunks(T, k);
     const int cap32 = cap > INT_MAX ? INT_MAX : (int)cap;
     int* hist = (int*)ws;
-    if (T * k <= dispatch::SMALL_MAX) {   // one block: no histogram round trip through global memory
-        dispatch::dispatch_small_kernel<<<1, dispatch::SMALL_THREADS, 0, stream>>>(
-            topk_idx, topk_gate, (int)T, k, E, cap32, counts, kept, offsets, slot_row, row_token, row_gate, n_dropped);
-    } else {
-        dispatch::hist_kernel<<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T, k, E, hist);
-        const moe_status st = launch_status();
-        if (st != MOE_OK) return st;
-        dispatch::rank_kernel<<<nchunk, dispatch::THREADS, 0, stream>>>(
-            topk_idx, topk_gate, (int)T, k, E, cap32, hist, nchunk, counts, kept, offsets, slot_row, row_token,
-            row_gate, n_dropped);
+    // hist -> rank -> scatter, each a programmatic dependent of the one before
+    // (T = 0: no histograms; one rank block writes the zero counts)
+    const bool small = dispatch::chunk_size(T * k) == dispatch::SMALL_CHUNK;
+    if (nchunk > 0) {
+        if (small)
+            dispatch::hist_kernel<dispatch::SMALL_CHUNK><<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T,
+                                                                                                  k, E, hist);
+        else
+            dispatch::hist_kernel<dispatch::LARGE_CHUNK><<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T,
+                                                                                                  k, E, hist);
+        const moe_status st0 = launch_status();
+        if (st0 != MOE_OK) return st0;
+    }
+    {
+        PdlLaunch rl(nchunk > 0 ? nchunk : 1, dispatch::THREADS, stream);
+        const moe_status st1 = launch_ex_status(cudaLaunchKernelEx(
+            &rl.cfg, small ? dispatch::rank_kernel<dispatch::SMALL_CHUNK> : dispatch::rank_kernel<dispatch::LARGE_CHUNK>,
+            topk_idx, topk_gate, (int)T, k, E, cap32, (const int*)hist, nchunk, counts, kept, offsets, slot_row,
+            row_token, row_gate, n_dropped));
+        if (st1 != MOE_OK) return st1;
     }
     moe_status st = launch_status();
     if (st != MOE_OK || rows_max == 0 || !x_perm) return st;   // x_perm NULL: the up GEMM gathers from x
     const int vec16 = d * esize(xdt) / 16;
-    long long grid = (T + dispatch::WARPS - 1) / dispatch::WARPS;
-    if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
-    dispatch::scatter_tokens_kernel<<<(int)grid, dispatch::THREADS, 0, stream>>>(slot_row, (int)T, k, (const uint4*)x,
-                                                                                 (uint4*)x_perm, vec16);
-    return launch_status();
+    const long long tasks = T * ((vec16 + dispatch::CHUNK_VEC - 1) / dispatch::CHUNK_VEC);
+    long long grid = (tasks + dispatch::WARPS - 1) / dispatch::WARPS;
+    // only resident blocks preload before the ranking ends: one wave of them, grid-striding
+    static const int per_sm = resident_blocks(dispatch::scatter_tokens_kernel, dispatch::THREADS);
+    if (grid > (long long)sm_count() * per_sm) grid = (long long)sm_count() * per_sm;
+    // a programmatic dependent of the ranking: x loads start before slot_row is final
+    PdlLaunch sl((int)grid, dispatch::THREADS, stream);
+    return launch_ex_status(cudaLaunchKernelEx(&sl.cfg, dispatch::scatter_tokens_kernel, slot_row, (int)T, k,
+                                               (const uint4*)x, (uint4*)x_perm, vec16));
 }
 
 moe_status moe_permute_rows(const void* src, const int32_t* index, int64_t n, int d, moe_dtype dtype, void* dst,
@@ -910,15 +957,21 @@ moe_status combine_impl(const void* y_perm, const int32_t* slot_row, int64_t T, 
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     const int vec16 = d * esize(dtype) / 16;
-    long long grid = (T + combine::WARPS - 1) / combine::WARPS;
-    if (grid > (long long)sm_count() * 8) grid = (long long)sm_count() * 8;
+    const long long tasks = T * ((vec16 + combine::CHUNK_VEC - 1) / combine::CHUNK_VEC);
+    long long grid = (tasks + combine::WARPS - 1) / combine::WARPS;
+    // one wave of resident blocks, grid-striding over the (token, chunk) tasks
+    static const int per_sm_bf16 = resident_blocks(combine::combine_kernel<true>, combine::THREADS);
+    static const int per_sm_f32 = resident_blocks(combine::combine_kernel<false>, combine::THREADS);
+    const long long wave = (long long)sm_count() * (dtype == MOE_BF16 ? per_sm_bf16 : per_sm_f32);
+    if (grid > wave) grid = wave;
+    // a programmatic dependent of the kernel writing y_perm: it launches while that kernel's last blocks
+    // run and waits (griddepcontrol.wait) before reading y_perm
+    PdlLaunch cl((int)grid, combine::THREADS, stream);
     if (dtype == MOE_BF16)
-        combine::combine_kernel<true><<<(int)grid, combine::THREADS, 0, stream>>>((const uint4*)y_perm, slot_row,
-                                                                                  (int)T, k, vec16, (uint4*)y, aux);
-    else
-        combine::combine_kernel<false><<<(int)grid, combine::THREADS, 0, stream>>>((const uint4*)y_perm, slot_row,
-                                                                                   (int)T, k, vec16, (uint4*)y, aux);
-    return launch_status();
+        return launch_ex_status(cudaLaunchKernelEx(&cl.cfg, combine::combine_kernel<true>, (const uint4*)y_perm,
+                                                   slot_row, (int)T, k, vec16, (uint4*)y, aux));
+    return launch_ex_status(cudaLaunchKernelEx(&cl.cfg, combine::combine_kernel<false>, (const uint4*)y_perm,
+                                               slot_row, (int)T, k, vec16, (uint4*)y, aux));
 }
 }  // namespace
 
@@ -1393,7 +1446,7 @@ extern "C" moe_status moe_dispatch_noalloc(const int32_t* topk_idx, const float*
                      (long long)T * k, E, need, NOALLOC_SCRATCH_BYTES);
         return MOE_ERR_WORKSPACE;
     }
-    void* scratch = nullptr;   // only a batch ranked by the two-kernel path reads it
+    void* scratch = nullptr;   // an empty batch (T*k = 0) reads no histogram
     if (need > 0) {
         const moe_status st = noalloc_scratch(&scratch);
         if (st != MOE_OK) return st;

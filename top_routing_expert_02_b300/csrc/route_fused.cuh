@@ -113,12 +113,6 @@ __host__ __device__ constexpr int finish_smem_bytes(int TPB, int E_pad) { return
 // TMEM columns of one 128-token tile in the two accumulator layouts.
 __host__ __device__ constexpr int tile_tmem_cols(bool fused_parts, int E_pad) { return fused_parts ? 7 * E_pad : 4 * E_pad; }
 
-// Programmatic dependent launch: the next kernel in the stream may start
-// (launch_dependents); wait until the kernel before this one has finished and
-// its memory is visible (wait).
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to the
 // shared memory of a CTA of the cluster (dst and bar: shared::cluster
 // addresses); completion is counted in bytes on that CTA's mbarrier.
@@ -203,19 +197,19 @@ __device__ __forceinline__ void drain_chunk_fp(uint32_t tb, int Ep, int buf, boo
 // of the list heads give the winners, in order.  On return l[] holds p
 // (softmax probabilities); lane 0 of a valid token has written idx, gate and
 // lse.  Every lane of the warp must call it (shuffles).
-template <int EPL, int KMAX>
+template <int G, int EPL, int KMAX>
 __device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, int k, int renorm, bool valid, int t,
                                              const RouteSel& sel, int32_t* __restrict__ idx_out,
                                              float* __restrict__ gate_out)
 {
-    constexpr int G = 4;
+    static_assert(G == 4 || G == 8 || G == 16, "G consecutive lanes share a token");
     const bool grouped = sel.n_group > 1;
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
         if (sub + G * i < E) mx = fmaxf(mx, l[i]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     // group-limited routing: keep the topk_group groups holding the best
     // remaining logit, ordered by (logit desc, expert asc)
     unsigned gkeep = 0xffffffffu;
@@ -274,7 +268,7 @@ __device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, in
             }
         }
     }
-    // softmax over all E: this lane's terms in expert order, then the four
+    // softmax over all E: this lane's terms in expert order, then the G
     // lanes' sums in a fixed butterfly
     float s = 0.f;
 #pragma unroll
@@ -283,13 +277,13 @@ __device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, in
             l[i] = expf(l[i] - mx);
             s += l[i];
         }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const float inv = 1.f / s;
     if (valid && sel.lse && sub == 0) sel.lse[t] = mx + logf(s);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) l[i] *= inv;
-    // the k winners: each round the best list head of the four lanes (logit
+    // the k winners: each round the best list head of the G lanes (logit
     // desc, expert asc); the lane holding it drops it
     int widx[KMAX];
     float wp[KMAX];
@@ -676,7 +670,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                     if (valid && g.sel.logits) g.sel.logits[(size_t)t * E + e] = l[i];
                 }
             }
-            finish_token<EPL, KMAX>(l, sub, E, g.k, g.renorm, valid, t, g.sel, g.idx, g.gate);
+            finish_token<4, EPL, KMAX>(l, sub, E, g.k, g.renorm, valid, t, g.sel, g.idx, g.gate);
             if (in_cta) {
 #pragma unroll
                 for (int i = 0; i < EPL; ++i)
@@ -713,23 +707,25 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 }
 
 // Softmax, top-k and per-block probability sums from the logits [T, E] (for
-// E > 64, where the fused kernel leaves them to this one): four lanes per
-// token, FIN_TOKENS tokens per block.  Launched as a programmatic dependent
-// of the logits kernel; many blocks per SM hide the latency of the short
-// dependent chains of finish_token.
+// E > 64, where the fused kernel leaves them to this one): FIN_G lanes per
+// token (16 logits per lane at E = 128: short per-lane candidate lists and a
+// three-step butterfly per winner), FIN_TOKENS tokens per block.  Launched as
+// a programmatic dependent of the logits kernel; many blocks per SM hide the
+// latency of the dependent chains of finish_token.
 constexpr int FIN_THREADS = 256;
-constexpr int FIN_TOKENS = FIN_THREADS / 4;
+constexpr int FIN_G = 8;
+constexpr int FIN_TOKENS = FIN_THREADS / FIN_G;
 
 template <int EMAX, int KMAX>
-__global__ void __launch_bounds__(FIN_THREADS)
+__global__ void __launch_bounds__(FIN_THREADS, KMAX <= 8 ? 4 : 2)
 route_finish_kernel(const FinArgs g)
 {
-    constexpr int G = 4, EPL = EMAX / G;
+    constexpr int G = FIN_G, EPL = EMAX / G;
     __shared__ float pbuf[FIN_TOKENS][EMAX + 1];     // p of the block's tokens, for the per-expert sums
     pdl_launch_dependents();
     pdl_wait();                                      // the logits kernel has finished
     const int lane = threadIdx.x & 31, sub = lane & (G - 1);
-    const int slot = threadIdx.x / G;                // token of the block handled by this group of four
+    const int slot = threadIdx.x / G;                // token of the block handled by this group of G lanes
     const int t = blockIdx.x * FIN_TOKENS + slot;
     const bool valid = t < g.T;
     const int E = g.E;
@@ -739,7 +735,7 @@ route_finish_kernel(const FinArgs g)
         const int e = sub + G * i;
         l[i] = (valid && e < E) ? __ldcg(g.logits + (size_t)t * E + e) : 0.f;
     }
-    finish_token<EPL, KMAX>(l, sub, E, g.k, g.renorm, valid, t, g.sel, g.idx, g.gate);
+    finish_token<G, EPL, KMAX>(l, sub, E, g.k, g.renorm, valid, t, g.sel, g.idx, g.gate);
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
         if (sub + G * i < E) pbuf[slot][sub + G * i] = valid ? l[i] : 0.f;

@@ -104,6 +104,12 @@ WORKLOADS["prof_e8_swiglu_F2048"] = _mk("prof_e8_swiglu_F2048", 4096, 4096, 8, 2
 WORKLOADS["prof_route_e8_T32768"] = _mk("prof_route_e8_T32768", 32768, 4096, 8, 2, 128, "swiglu", 1.25, "bf16")
 WORKLOADS["prof_route_e128_T16384"] = _mk("prof_route_e128_T16384", 16384, 4096, 128, 8, 128, "swiglu", 1.25,
                                           "bf16")
+# profiling cases of the many-expert layer: the e128 per-token shape with tiny
+# experts (route, dispatch and combine bytes per token as at full size, a few
+# GB on the device), and 32 experts at 2048 rows each (the per-expert GEMM
+# shape of T=32768, top-8 over 128 experts)
+WORKLOADS["prof_e128_T16384_F128"] = _mk("prof_e128_T16384_F128", 16384, 4096, 128, 8, 128, "swiglu", 0.0, "bf16")
+WORKLOADS["prof_e32_top8_T8192"] = _mk("prof_e32_top8_T8192", 8192, 4096, 32, 8, 1536, "swiglu", 0.0, "bf16")
 for _T in (512, 2048, 8192, 32768):
     WORKLOADS[f"e128_top8_T{_T}"] = _mk(f"e128_top8_T{_T}", _T, 4096, 128, 8, 1536,
                                         "swiglu", 0.0, "bf16")
