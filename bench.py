@@ -86,7 +86,9 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     # weight split + logits (+ softmax/top-k for E > 64) + prob sums | CUDA-core router + sums
     route = (3 if cfg.E <= 64 else 4) if tc_router else 2
     gather = bool(args and args.gather)
-    ranks = 2 if cfg.T * cfg.k > 0 else 1        # chunk histograms + ranks (T*k = 0: the rank kernel alone)
+    n = cfg.T * cfg.k
+    # chunk histograms (+ per-expert scan above 65536 assignments) + ranks; T*k = 0: the rank kernel alone
+    ranks = 1 if n == 0 else (2 if n <= 65536 else 3)
     dispatch = ranks + (0 if gather else 1)      # (+ row copy)
     z = 1 if (args and args.z_beta is not None) else 0
     bwd = BWD_KERNELS if (args and args.train) else 0
@@ -358,24 +360,31 @@ def hbm_rooflines(cfg, A, T_used, esz, part, hbm_gbs, peak_src, gather=False) ->
 
 def traffic_from_profile(kernel_src: str, workload: str):
     """DRAM bytes per launch of the up-projection GEMM from the committed ncu
-    summary, only for the workload it was captured for and only while the
-    kernel source is unchanged since the capture."""
+    summary: one `workload = ...` block per captured workload; a block counts
+    only for its own workload and only while the kernel source is unchanged
+    since the capture."""
     p = os.path.join(ROOT, "profiles", "expert_up_gemm_traffic.txt")
     if not os.path.exists(p):
         return None
     with open(kernel_src, "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    vals = {}
+    blocks, cur = [], None
     for line in open(p):
-        if "=" in line and not line.startswith("#"):
-            k, v = line.split("=", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != sha or vals.get("workload") != workload:
-        return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+        if "=" not in line or line.startswith("#"):
+            continue
+        k, v = (x.strip() for x in line.split("=", 1))
+        if k == "workload":
+            cur = {}
+            blocks.append(cur)
+        if cur is not None:
+            cur[k] = v
+    for vals in blocks:
+        if vals.get("workload") == workload and vals.get("kernel_source_sha256_16") == sha:
+            try:
+                return float(vals["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
 
 
 # -------------------------------------------------------------------- ours --

@@ -4,10 +4,12 @@ path through the C ABI, run the oracle, compare.
 Bars (written here once, used by every parity test):
   routing indices, counts, kept, offsets, slot places, drops: bit-exact
   gates, prob sums, aux loss:         relative error <= 1e-5 for fp32 x (router logits are
-                                      one fp32 FMA chain each), <= 2e-4 for bf16 x (tensor-core
-                                      router: d/16 accumulation steps of at most 2^-23 relative
-                                      error each, about 1e-4 absolute on a logit of size ~1.5 at
-                                      d = 4096; a gate inherits at most twice that relatively)
+                                      one fp32 FMA chain each) and for bf16 x (tensor-core
+                                      router: exact bf16 products of the three weight parts;
+                                      the large part accumulates over at most 4 K blocks of 64
+                                      columns in the tensor core before an fp32 add into the
+                                      running sum, which bounds the accumulator's drift to
+                                      about 16 steps of 2^-23 of a chunk sum)
   layer output y:                     relative Frobenius error <= 1e-5 (fp32 layer),
                                       <= 2e-2 (bf16 layer), pooled over the compared tokens
                                       and for every token on its own (a token whose every

@@ -19,20 +19,21 @@ C = synth.MoEConfig
 
 # name: (config, n_group, topk_group, post-drop aux)
 CASES = {
-    # tensor-core router, lane finisher (E <= 16): 2 groups of 4, one kept
+    # fused tensor-core router, finished in the logits kernel (E <= 64): 2 groups of 4, one kept
     "e8_g2m1": (C("e8_g2m1", 2000, 256, 8, 2, 384, "swiglu", 1.25, "bf16"), 2, 1, False),
-    # lane finisher at E = 32, one group of 4 kept, no renormalisation, post-drop aux
+    # E = 32 (one MMA for the three weight parts), one group of 4 kept, no renormalisation, post-drop aux
     "e32_g8m1": (C("e32_g8m1", 1500, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False), 8, 1, True),
-    # warp finisher (E = 64), Zipf skew, 3 of 32 groups of 2, k = 6 (every kept expert chosen)
+    # E = 64 (two MMAs per K step, still finished in the logits kernel), Zipf skew, 3 of 32 groups of 2,
+    # k = 6 (every kept expert chosen)
     "e64_g32m3_zipf": (C("e64_g32m3_zipf", 3000, 128, 64, 6, 192, "swiglu", 1.25, "bf16", bias="zipf"), 32, 3,
                        True),
-    # warp finisher (E = 128), 4 of 8 groups, top-8, dropless
+    # E = 128: logits kernel + the separate finishing kernel, 4 of 8 groups, top-8, dropless
     "e128_g8m4": (C("e128_g8m4", 600, 256, 128, 8, 128, "swiglu", 0.0, "bf16"), 8, 4, False),
-    # warp finisher at E = 160: 32 groups of 5, 4 kept, top-16
+    # E = 160 (above the tensor-core router: CUDA-core router), 32 groups of 5, 4 kept, top-16
     "e160_g32m4": (C("e160_g32m4", 300, 192, 160, 16, 128, "swiglu", 0.0, "bf16", renorm=False), 32, 4, False),
     # fused CUDA-core router, fp32 x: 4 groups of 16, 2 kept
     "f32_e64_g4m2": (C("f32_e64_g4m2", 700, 128, 64, 4, 128, "gelu", 1.25, "f32"), 4, 2, True),
-    # fused CUDA-core router, bf16 x with E = 200 > 160: 8 groups of 25, 3 kept
+    # CUDA-core router, bf16 x with E = 200: 8 groups of 25, 3 kept
     "bf16_e200_g8m3": (C("bf16_e200_g8m3", 400, 128, 200, 4, 128, "gelu", 2.0, "bf16"), 8, 3, False),
 }
 

@@ -12,8 +12,10 @@
 // dependent of the one before (it launches while that one runs, and waits
 // for it only where it reads its results):
 //   hist    per chunk of CH assignments, a histogram over experts
+//   scan    (large chunks only) per expert, the exclusive prefix of the
+//           histograms over chunks, in place, and the totals
 //   rank    per chunk: base of every expert from the earlier chunks and the
-//           totals (threads split the chunks of an expert), then the stable
+//           totals (small chunks: threads split the chunks of an expert), then the stable
 //           rank of each assignment inside the chunk (warp match + per-warp
 //           counts), giving its place in the expert's queue; kept slots get a
 //           row of the permuted buffer; chunk 0 also writes counts, kept,
@@ -38,7 +40,10 @@ template <int CH>
 __global__ void __launch_bounds__(THREADS)
 hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int* __restrict__ hist)
 {
-    pdl_launch_dependents();   // the rank kernel preloads its chunk, then waits for this grid
+    // idx is final once the router has finished; only then may the rank
+    // kernel launch (it preloads idx and gate before its own wait)
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int R = CH / THREADS;
     __shared__ int h[MAX_E];
     for (int e = threadIdx.x; e < E; e += THREADS) h[e] = 0;
@@ -65,6 +70,46 @@ hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int* __restric
     if (bad) moe_flag(MOE_DEV_BAD_EXPERT);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += THREADS) hist[(size_t)blockIdx.x * E + e] = h[e];
+}
+
+// Large chunks: per expert, the exclusive prefix of the chunk histograms
+// over chunks, in place (hist[c][e] becomes the assignments to e in chunks
+// before c), and the total into counts[e].  One warp per expert, windows of
+// 256 chunks: lane l loads its run of 8 at once, a warp scan orders the runs.
+constexpr int SCAN_PER = 8;   // chunks per lane in one window of 256
+
+__global__ void __launch_bounds__(THREADS)
+scan_kernel(int* __restrict__ hist, int nchunk, int E, int32_t* __restrict__ counts)
+{
+    pdl_launch_dependents();   // the rank kernel preloads its chunk meanwhile
+    pdl_wait();                // every histogram is written
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * WARPS + (threadIdx.x >> 5);
+    if (e >= E) return;
+    int carry = 0;   // assignments to e in the windows before
+    for (int w0 = 0; w0 < nchunk; w0 += 32 * SCAN_PER) {
+        const int c0 = w0 + lane * SCAN_PER;
+        int v[SCAN_PER], run = 0;
+#pragma unroll
+        for (int i = 0; i < SCAN_PER; ++i) v[i] = c0 + i < nchunk ? __ldcg(hist + (size_t)(c0 + i) * E + e) : 0;
+#pragma unroll
+        for (int i = 0; i < SCAN_PER; ++i) run += v[i];
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int acc = carry + incl - run;   // before this lane's run of chunks
+#pragma unroll
+        for (int i = 0; i < SCAN_PER; ++i)
+            if (c0 + i < nchunk) {
+                hist[(size_t)(c0 + i) * E + e] = acc;
+                acc += v[i];
+            }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) counts[e] = carry;
 }
 
 template <int CH>
@@ -101,14 +146,23 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
     pdl_wait();   // every histogram is written
 
     // 1. per expert: the assignments of earlier chunks (base) and in all
-    //    chunks (total).  P threads (consecutive lanes, P a power of two)
-    //    share an expert, each summing every P-th chunk; a butterfly over the
-    //    P lanes adds their sums.
+    //    chunks (total).  Large chunks: scan_kernel has turned hist into that
+    //    exclusive prefix over chunks and written the totals to counts.
+    //    Small chunks: P threads (consecutive lanes, P a power of two) share
+    //    an expert, each summing every P-th chunk; a butterfly over the P
+    //    lanes adds their sums.
+    constexpr bool SCANNED = CH == LARGE_CHUNK;
     int P = 32;
     while (P > 1 && P * E > THREADS) P >>= 1;
+    if (SCANNED) P = 1;
     const int e1 = tid / P, s1 = tid & (P - 1);
     int before = 0, total = 0;
-    if (e1 < E) {
+    if (SCANNED) {
+        if (e1 < E) {
+            before = __ldcg(hist + (size_t)chunk * E + e1);
+            total = __ldcg(counts + e1);
+        }
+    } else if (e1 < E) {
         const int* col = hist + e1;
         int c = s1;
         for (; c + 3 * P < nchunk; c += 4 * P) {
@@ -136,7 +190,7 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
         off[e1] = kp;
         dr = total - kp;
         if (chunk == 0) {
-            counts[e1] = total;
+            if (!SCANNED) counts[e1] = total;
             kept[e1] = kp;
         }
     }

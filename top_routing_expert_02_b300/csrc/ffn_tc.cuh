@@ -208,6 +208,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // launched as a programmatic dependent: the kernel before it (which wrote
+    // kept[], the A rows, row_gate) has finished once this returns
+    pdl_wait();
     if (warp == 2) {
         if (WGRAD) {
             for (int e = lane; e <= g.E; e += 32) mstart[e] = e * g.m_tiles;

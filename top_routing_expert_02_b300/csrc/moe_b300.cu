@@ -158,7 +158,9 @@ inline bool route_fu_shape(long long T, int d, int E, RouteFuShape* s)
     while (c < (uint32_t)(s->TPB * tcols)) c <<= 1;
     s->tmem_cols = c;
     // one CTA per SM: x and weight rings of the same depth in K blocks, as
-    // deep as the 227 KB (less alignment and static use) allow
+    // deep as the 227 KB (less alignment and static use) allow.  (A shorter
+    // weight ring with a deeper x ring measured slower: at small E the
+    // weight boxes' L2 latency then shows, and at E = 128 it gained nothing.)
     const int xbytes = s->TPB * rfu::X_BYTES, wbytes = 3 * s->E_pad * 128;
     int st = (232448 - 1024 - 1536) / (xbytes + wbytes);
     if (st > rfu::MAX_XSTAGES) st = rfu::MAX_XSTAGES;
@@ -174,8 +176,8 @@ inline bool route_fu_shape(long long T, int d, int E, RouteFuShape* s)
 }
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 // Workspace of the tensor-core router: the three bf16 parts of the weight
-// [3 E_pad, d], the fp32 logits [T, E], one row of E probability sums per
-// finishing block.
+// [3 E_pad, d], the fp32 logits [T, E] (E > 64), one row of E probability
+// sums per finishing CTA or block.
 inline size_t route_parts_bytes(int d, const RouteFuShape& sh) { return align256((size_t)3 * sh.E_pad * d * 2); }
 inline long long route_fin_blocks(long long T) { return (T + rfu::FIN_TOKENS - 1) / rfu::FIN_TOKENS; }
 // E <= 64: the logits kernel finishes its own tokens (one probability-sum row
@@ -344,8 +346,9 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
                                     : ((rows_max + tcg::BM - 1) / tcg::BM + args.E) * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
-    tcg::grouped_gemm_kernel<EPI, BN, MODE><<<grid, tcg::THREADS, smem, stream>>>(ta, tb, tc, args);
-    return launch_status();
+    // a programmatic dependent of the kernel before it: launch and set-up overlap that kernel's end
+    PdlLaunch gl(grid, tcg::THREADS, stream, (size_t)smem);
+    return launch_ex_status(cudaLaunchKernelEx(&gl.cfg, tcg::grouped_gemm_kernel<EPI, BN, MODE>, ta, tb, tc, args));
 }
 
 // Output-tile width of the tensor-core GEMMs.  Measured in SM cycles on the
@@ -553,10 +556,11 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
     RouteFuShape sh;
     if (xdt == MOE_BF16 && route_fu_shape(T, d, E, &sh)) {
         // the weight split into three bf16 parts; the tensor-core logits
-        // kernel; the softmax / top-k / per-block probability sums; the
-        // fixed-order sums over blocks.  Each launch after the first is a
-        // programmatic dependent of the one before, so its set-up overlaps
-        // that kernel's tail.
+        // kernel, which for E <= 64 also takes the softmax, top-k and
+        // per-CTA probability sums; for larger E the finishing kernel does
+        // that; prob_sum_kernel adds the per-CTA / per-block rows.  Each
+        // launch after the first is a programmatic dependent of the one
+        // before, so its set-up overlaps that kernel's tail.
         const bool here = route_finish_here(sh);
         uint4* parts = (uint4*)ws;
         float* logits = here ? nullptr
@@ -603,6 +607,7 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         a.sel = sel;
         a.logits = logits;
         a.wait_limit = g_wait_limit.load();
+        const int rows = here ? sh.grid : (int)route_fin_blocks(T);
         rfu::FinArgs f{};
         f.T = (int)T;
         f.E = E;
@@ -613,7 +618,6 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         f.gate = topk_gate;
         f.psum = psum;
         f.sel = sel;
-        const int rows = here ? sh.grid : (int)route_fin_blocks(T);
 
         const long long n8 = (long long)sh.E_pad * (d / 8);
         long long sg = (n8 + 255) / 256;
@@ -723,18 +727,21 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     const int nchunk = (int)dispatch_chunks(T, k);
     const int cap32 = cap > INT_MAX ? INT_MAX : (int)cap;
     int* hist = (int*)ws;
-    // hist -> rank -> scatter, each a programmatic dependent of the one before
+    // hist -> (scan) -> rank -> scatter, each a programmatic dependent of the one before
     // (T = 0: no histograms; one rank block writes the zero counts)
     const bool small = dispatch::chunk_size(T * k) == dispatch::SMALL_CHUNK;
     if (nchunk > 0) {
-        if (small)
-            dispatch::hist_kernel<dispatch::SMALL_CHUNK><<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T,
-                                                                                                  k, E, hist);
-        else
-            dispatch::hist_kernel<dispatch::LARGE_CHUNK><<<nchunk, dispatch::THREADS, 0, stream>>>(topk_idx, (int)T,
-                                                                                                  k, E, hist);
-        const moe_status st0 = launch_status();
+        PdlLaunch hl(nchunk, dispatch::THREADS, stream);   // waits for the router's last kernel
+        const moe_status st0 = launch_ex_status(cudaLaunchKernelEx(
+            &hl.cfg, small ? dispatch::hist_kernel<dispatch::SMALL_CHUNK> : dispatch::hist_kernel<dispatch::LARGE_CHUNK>,
+            topk_idx, (int)T, k, E, hist));
         if (st0 != MOE_OK) return st0;
+        if (!small) {   // per-expert prefix over the chunks, and counts
+            PdlLaunch sl((E + dispatch::WARPS - 1) / dispatch::WARPS, dispatch::THREADS, stream);
+            const moe_status st_s = launch_ex_status(
+                cudaLaunchKernelEx(&sl.cfg, dispatch::scan_kernel, hist, nchunk, E, counts));
+            if (st_s != MOE_OK) return st_s;
+        }
     }
     {
         PdlLaunch rl(nchunk > 0 ? nchunk : 1, dispatch::THREADS, stream);

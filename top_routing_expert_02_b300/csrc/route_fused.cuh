@@ -751,6 +751,7 @@ __global__ void __launch_bounds__(256) prob_sum_kernel(const float* __restrict__
                                                        float* __restrict__ prob_sum)
 {
     __shared__ double sh[256];
+    pdl_launch_dependents();   // the next step's first kernel may launch; it waits for this grid
     pdl_wait();   // launched as a programmatic dependent of the kernel writing psum
     const int e = blockIdx.x;
     double acc = 0.0;
