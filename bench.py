@@ -87,8 +87,9 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     route = (3 if cfg.E <= 64 else 4) if tc_router else 2
     gather = bool(args and args.gather)
     n = cfg.T * cfg.k
-    # chunk histograms (+ per-expert scan above 65536 assignments) + ranks; T*k = 0: the rank kernel alone
-    ranks = 1 if n == 0 else (2 if n <= 65536 else 3)
+    # chunk histograms (+ a per-expert scan of them above 65536 assignments) + ranks; T*k = 0: the rank
+    # kernel alone
+    ranks = 1 if n == 0 else (3 if n > 65536 else 2)
     dispatch = ranks + (0 if gather else 1)      # (+ row copy)
     z = 1 if (args and args.z_beta is not None) else 0
     bwd = BWD_KERNELS if (args and args.train) else 0

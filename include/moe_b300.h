@@ -479,6 +479,13 @@ moe_status moe_set_gemm_kernel(int kind);
  * any other value. */
 moe_status moe_set_gemm_tile_n(int bn);
 
+/* Tile order of the forward and data-gradient bf16 expert GEMMs inside each
+ * expert: 0 (default) automatic (M-fastest: the blocks running together
+ * share a weight tile), 1 M-fastest, 2 N-fastest (they share a row tile).
+ * The results do not depend on it.  Process-wide; for tests and tuning.
+ * MOE_ERR_INVALID_ARG otherwise. */
+moe_status moe_set_gemm_order(int order);
+
 /* Tile order of the weight-gradient GEMMs (moe_expert_wgrad,
  * moe_expert_wgrad_rows) inside each expert: 0 (default) automatic
  * (N-fastest), 1 M-fastest, 2 N-fastest.  The results do not depend on it.

@@ -116,6 +116,27 @@ def test_every_gemm_tile_width(name, bn):
     compare_output(plan, ref, cfg.dtype)
 
 
+@pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot", "swiglu_e128_top8", "many_tiles"])
+def test_gemm_tile_order_changes_no_bit(name):
+    """N-fastest tiles inside each expert (the blocks running together share a
+    row tile instead of a weight tile) give the same bits as the default
+    M-fastest order, and the oracle's layer."""
+    cfg = SMALL[name]
+    case = make_case(cfg)
+    base = run_gpu(case)
+    moe.set_gemm_order(2)
+    try:
+        plan = run_gpu(case)
+    finally:
+        moe.set_gemm_order(0)
+    moe.check()
+    A = int(base.disp.offsets[-1].item())
+    assert torch.equal(plan.h[:A], base.h[:A])
+    assert torch.equal(plan.y_perm[:A], base.y_perm[:A])
+    assert torch.equal(plan.y, base.y)
+    compare_output(plan, run_oracle(case), cfg.dtype)
+
+
 @pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot", "swiglu_e64_zipf", "swiglu_e128_top8", "small_T",
                                   "gelu_e32_norenorm"])
 def test_cta_pair_gemm_kernel(name):

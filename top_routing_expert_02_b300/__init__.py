@@ -89,6 +89,7 @@ _SIGS = {
     "moe_check": (_I32, [_P]),
     "moe_set_wait_limit": (None, [_U64]),
     "moe_set_gemm_tile_n": (_I32, [_I32]),
+    "moe_set_gemm_order": (_I32, [_I32]),
     "moe_set_wgrad_order": (_I32, [_I32]),
     "moe_set_gemm_kernel": (_I32, [_I32]),
     "moe_selftest_wait_timeout": (_I32, [_P]),
@@ -190,6 +191,11 @@ def set_wait_limit(cycles: int):
 def set_gemm_tile_n(bn: int):
     """Force the bf16 expert GEMM tile width (128, 192, 256) or 0 for automatic."""
     _ok("moe_set_gemm_tile_n", lib().moe_set_gemm_tile_n(int(bn)))
+
+
+def set_gemm_order(order: int):
+    """Forward / data-gradient GEMM tile order: 0 automatic, 1 M-fastest, 2 N-fastest (results unchanged)."""
+    _ok("moe_set_gemm_order", lib().moe_set_gemm_order(int(order)))
 
 
 def set_wgrad_order(order: int):

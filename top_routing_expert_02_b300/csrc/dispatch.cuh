@@ -12,10 +12,10 @@
 // dependent of the one before (it launches while that one runs, and waits
 // for it only where it reads its results):
 //   hist    per chunk of CH assignments, a histogram over experts
-//   scan    (large chunks only) per expert, the exclusive prefix of the
+//   scan    (large chunks) per expert, the exclusive prefix of the
 //           histograms over chunks, in place, and the totals
 //   rank    per chunk: base of every expert from the earlier chunks and the
-//           totals (small chunks: threads split the chunks of an expert), then the stable
+//           totals (without the scan: threads split the chunks of an expert), then the stable
 //           rank of each assignment inside the chunk (warp match + per-warp
 //           counts), giving its place in the expert's queue; kept slots get a
 //           row of the permuted buffer; chunk 0 also writes counts, kept,
@@ -25,6 +25,7 @@
 // spread the latency-bound ranking over the GPU), else 1024.
 #pragma once
 #include "common.cuh"
+#include "ptx_sm103.cuh"
 
 namespace dispatch {
 
@@ -72,7 +73,19 @@ hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int* __restric
     for (int e = threadIdx.x; e < E; e += THREADS) hist[(size_t)blockIdx.x * E + e] = h[e];
 }
 
-// Large chunks: per expert, the exclusive prefix of the chunk histograms
+// Lanes that share an expert's chunk sums in rank_kernel (no scan): the
+// largest power of two P <= 32 with P * E <= THREADS.
+__host__ __device__ constexpr int rank_lanes_per_expert(int E)
+{
+    return E <= 8 ? 32 : E <= 16 ? 16 : E <= 32 ? 8 : E <= 64 ? 4 : E <= 128 ? 2 : 1;
+}
+// The per-expert scan runs for large chunks (up to 2M chunks, where the rank
+// blocks' own sums would grow with the chunk count).  With chunks of 256 (at
+// most 256 chunks) the rank kernel sums them itself: a scan launch measured
+// no faster even at 128 chunks of 64 experts.
+__host__ __device__ constexpr bool use_chunk_scan(int, int, bool large) { return large; }
+
+// Per expert, the exclusive prefix of the chunk histograms
 // over chunks, in place (hist[c][e] becomes the assignments to e in chunks
 // before c), and the total into counts[e].  One warp per expert, windows of
 // 256 chunks: lane l loads its run of 8 at once, a warp scan orders the runs.
@@ -115,9 +128,9 @@ scan_kernel(int* __restrict__ hist, int nchunk, int E, int32_t* __restrict__ cou
 template <int CH>
 __global__ void __launch_bounds__(THREADS)
 rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int T, int k, int E, int cap,
-            const int* __restrict__ hist, int nchunk, int32_t* __restrict__ counts, int32_t* __restrict__ kept,
-            int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row, int32_t* __restrict__ row_token,
-            float* __restrict__ row_gate, int32_t* __restrict__ n_dropped)
+            const int* __restrict__ hist, int nchunk, int scanned, int32_t* __restrict__ counts,
+            int32_t* __restrict__ kept, int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+            int32_t* __restrict__ row_token, float* __restrict__ row_gate, int32_t* __restrict__ n_dropped)
 {
     constexpr int R = CH / THREADS;
     __shared__ int base[MAX_E], off[MAX_E + 1], running[MAX_E];
@@ -146,14 +159,13 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
     pdl_wait();   // every histogram is written
 
     // 1. per expert: the assignments of earlier chunks (base) and in all
-    //    chunks (total).  Large chunks: scan_kernel has turned hist into that
-    //    exclusive prefix over chunks and written the totals to counts.
-    //    Small chunks: P threads (consecutive lanes, P a power of two) share
-    //    an expert, each summing every P-th chunk; a butterfly over the P
-    //    lanes adds their sums.
-    constexpr bool SCANNED = CH == LARGE_CHUNK;
-    int P = 32;
-    while (P > 1 && P * E > THREADS) P >>= 1;
+    //    chunks (total).  scanned: scan_kernel has turned hist into that
+    //    exclusive prefix over chunks and written the totals to counts (many
+    //    chunks per expert).  Otherwise P threads (consecutive lanes, P a power
+    //    of two) share an expert, each summing every P-th chunk; a butterfly
+    //    over the P lanes adds their sums.
+    const bool SCANNED = scanned != 0;
+    int P = rank_lanes_per_expert(E);
     if (SCANNED) P = 1;
     const int e1 = tid / P, s1 = tid & (P - 1);
     int before = 0, total = 0;
@@ -278,43 +290,66 @@ rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int
 }
 
 // Row permutation, token-major: one warp per (token, 2 KB chunk of its row)
-// reads that chunk of x[t] once (four 16-byte vectors per lane, all in
-// flight together) and writes it to every kept slot row of the token
-// (slot_row[t, j] >= 0), so a token routed to k experts costs one read and
-// k writes instead of k of each, and a whole row's chunks run in separate
-// warps at once.
+// reads that chunk of x[t] once and writes it to every kept slot row of the
+// token (slot_row[t, j] >= 0), so a token routed to k experts costs one read
+// and k writes instead of k of each, and a whole row's chunks run in separate
+// warps at once.  One wave of resident blocks grid-strides over the tasks.
 // Launched as a programmatic dependent of the ranking kernel: x does not
-// depend on it, so every warp loads the chunks of its first PRE tasks before
-// waiting for the ranks (the loads overlap the ranking); later chunks of a
-// token whose slots were all dropped are not read.
-constexpr int CHUNK_VEC = 128;   // 16-byte vectors per chunk
-constexpr int PRE = 2;           // tasks per warp whose chunk is loaded before the wait
-
-__device__ __forceinline__ void load_chunk(const uint4* __restrict__ x, int vec16, int nchunk, long long task,
-                                           int lane, uint4 (&a)[4])
-{
-    const int t = (int)(task / nchunk);
-    const int v0 = (int)(task - (long long)t * nchunk) * CHUNK_VEC + lane;
-    const uint4* src = x + (size_t)t * vec16;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-        if (v0 + 32 * u < vec16) a[u] = ldg_nc_v4(src + v0 + 32 * u);
-}
+// depend on it, so before waiting for the ranks every warp starts bulk copies
+// of the x chunks of its first SLOTS tasks into its own shared-memory slots
+// (one mbarrier per warp counts their bytes); those chunks are written from
+// shared memory once the ranks are final, later ones are loaded directly
+// (four 16-byte vectors per lane, all in flight together), and skipped when
+// every slot of the token was dropped.
+constexpr int CHUNK_VEC = 128;                   // 16-byte vectors per chunk
+constexpr int CHUNK_BYTES = CHUNK_VEC * 16;      // 2 KB
+constexpr int SLOTS = 4;                         // staged chunks per warp
+constexpr int SCATTER_SMEM = WARPS * SLOTS * CHUNK_BYTES;   // 64 KB of dynamic shared memory
 
 __global__ void __launch_bounds__(THREADS)
 scatter_tokens_kernel(const int32_t* __restrict__ slot_row, int T, int k, const uint4* __restrict__ x,
-                      uint4* __restrict__ x_perm, int vec16)
+                      uint4* __restrict__ x_perm, int vec16, unsigned long long wait_limit)
 {
-    const int lane = threadIdx.x & 31;
+    extern __shared__ __align__(128) uint8_t sbuf[];
+    __shared__ __align__(8) uint64_t bar[WARPS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nchunk = (vec16 + CHUNK_VEC - 1) / CHUNK_VEC;
     const long long tasks = (long long)T * nchunk;
     const long long warps_total = (long long)gridDim.x * WARPS;
-    const long long first = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
-    uint4 pre[PRE][4];
+    const long long first = (long long)blockIdx.x * WARPS + warp;
+    const uint32_t wbar = ptx::smem_u32(&bar[warp]);
+    const uint32_t wbuf = ptx::smem_u32(sbuf) + (uint32_t)(warp * SLOTS * CHUNK_BYTES);
+    auto chunk_vecs = [&](long long task) {
+        const int c = (int)(task % nchunk);
+        return min(CHUNK_VEC, vec16 - c * CHUNK_VEC);
+    };
+    int nst = 0;   // staged tasks of this warp
 #pragma unroll
-    for (int p = 0; p < PRE; ++p)
-        if (first + p * warps_total < tasks) load_chunk(x, vec16, nchunk, first + p * warps_total, lane, pre[p]);
+    for (int p = 0; p < SLOTS; ++p)
+        if (first + p * warps_total < tasks) ++nst;
+    if (lane == 0) {
+        ptx::mbar_init(wbar, 1);
+        ptx::fence_mbar_init();
+        if (nst > 0) {
+            uint32_t bytes = 0;
+            for (int p = 0; p < nst; ++p) bytes += (uint32_t)chunk_vecs(first + p * warps_total) * 16u;
+            ptx::mbar_arrive_expect_tx(wbar, bytes);
+            for (int p = 0; p < nst; ++p) {
+                const long long task = first + p * warps_total;
+                const int t = (int)(task / nchunk), c = (int)(task - (long long)t * nchunk);
+                ptx::bulk_load(wbuf + (uint32_t)(p * CHUNK_BYTES), x + (size_t)t * vec16 + (size_t)c * CHUNK_VEC,
+                               (uint32_t)chunk_vecs(task) * 16u, wbar);
+            }
+        }
+    }
+    __syncwarp();
     pdl_wait();   // slot_row is final
+    if (nst > 0 && !ptx::mbar_wait(wbar, 0, wait_limit)) {
+        moe_flag(MOE_DEV_TIMEOUT);
+        // the copies into this warp's slots must land before the block exits
+        ptx::mbar_wait(wbar, 0, wait_limit);
+        return;
+    }
     int p = 0;
     for (long long task = first; task < tasks; task += warps_total, ++p) {
         const int t = (int)(task / nchunk);
@@ -324,14 +359,16 @@ scatter_tokens_kernel(const int32_t* __restrict__ slot_row, int T, int k, const 
         for (int j = 0; j < k; ++j) any |= __ldg(sr + j) >= 0;
         if (!any) continue;
         uint4 a[4];
-        if (p == 0) {
+        if (p < nst) {
+            const uint32_t slot = wbuf + (uint32_t)(p * CHUNK_BYTES) + (uint32_t)lane * 16u;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = pre[0][u];
-        } else if (p == 1) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = pre[1][u];
+            for (int u = 0; u < 4; ++u)
+                if (v0 + 32 * u < vec16) a[u] = ptx::ld_shared_v4(slot + (uint32_t)(u * 512));
         } else {
-            load_chunk(x, vec16, nchunk, task, lane, a);
+            const uint4* src = x + (size_t)t * vec16;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v0 + 32 * u < vec16) a[u] = ldg_nc_v4(src + v0 + 32 * u);
         }
         for (int j = 0; j < k; ++j) {
             const int row = __ldg(sr + j);
@@ -343,7 +380,6 @@ scatter_tokens_kernel(const int32_t* __restrict__ slot_row, int T, int k, const 
         }
     }
 }
-static_assert(PRE == 2, "scatter_tokens_kernel selects the preloaded chunks by hand");
 
 // dst[i] = src[index[i]] for i < n: one warp per row, 16-byte vectors (the
 // regrouping of received rows in the expert-parallel exchange).

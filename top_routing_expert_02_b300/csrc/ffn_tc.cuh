@@ -88,7 +88,7 @@ struct Args {
     int m_tiles;                // weight gradient: M-tiles per expert, ceil(m_rows / BM)
     int m_rows;                 // weight gradient: rows M of each expert's gradient
     int lda;                    // MODE_WGRAD_ROWS: row stride of A in elements (>= m_rows)
-    int n_fastest;              // weight-gradient modes: tile order N-fastest inside an expert
+    int n_fastest;              // tile order N-fastest inside an expert (default: M-fastest)
     unsigned long long wait_limit;
 };
 
@@ -142,7 +142,7 @@ template <int N>
 __device__ __forceinline__ void gather_offsets(const Args& g, const int* mstart, int tile, int lane, uint32_t (&off)[N])
 {
     int e, m, n;
-    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n);
+    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, g.n_fastest != 0);
     const int rowA = __ldg(g.offsets + e) + m * BM;
     const int rows_valid = __ldg(g.kept + e) - m * BM;
     const int first = __ldg(g.row_token + rowA);
@@ -237,7 +237,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t roff[GATHER ? 32 : 1];   // gathered rows: this lane's 32 offsets in x
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 int e, m, n;
-                decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, WGRAD && g.n_fastest);
+                decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, g.n_fastest != 0);
                 const int rowA = WGRAD ? m * BM : __ldg(g.offsets + e) + m * BM;
                 const int rowB0 = (WGRAD ? 0 : e * g.b_rows) + n * g.n_step;
                 const int rowB1 = rowB0 + g.half_off;
@@ -333,7 +333,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 int nkt = nk, kept_e = 0;
                 if (WGRAD) {
                     int e, m, n;
-                    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, WGRAD && g.n_fastest);
+                    decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, g.n_fastest != 0);
                     nkt = kstart[e + 1] - kstart[e];   // 0: nothing accumulates, the epilogue writes zeros
                     if (WGR) kept_e = __ldg(g.kept + e);
                 }
@@ -393,7 +393,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t aphase = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             int e, m, n;
-            decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, WGRAD && g.n_fastest);
+            decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, g.n_fastest != 0);
             const int rows_valid = WGRAD ? g.m_rows - m * BM : __ldg(g.kept + e) - m * BM;
             const int row = WGRAD ? e * g.m_rows + m * BM + r_in : __ldg(g.offsets + e) + m * BM + r_in;
             const bool rv = r_in < rows_valid;

@@ -29,6 +29,7 @@ constexpr unsigned long long DEFAULT_WAIT_LIMIT = 4000000000ull;   // ~2 s of SM
 std::atomic<unsigned long long> g_wait_limit{DEFAULT_WAIT_LIMIT};
 std::atomic<int> g_forced_bn{0};   // 0: pick the GEMM tile width per call
 std::atomic<int> g_wgrad_order{0};  // weight-gradient tile order: 0 automatic, 1 M-fastest, 2 N-fastest
+std::atomic<int> g_gemm_order{0};   // forward / data-gradient tile order: 0 automatic (M-fastest), 1 M-fastest, 2 N-fastest
 
 // Weight-gradient tile order.  N-fastest (the blocks running together share
 // the A tile and write neighbouring column blocks of the same output rows)
@@ -87,12 +88,12 @@ struct PdlLaunch {
     PdlLaunch(const PdlLaunch&) = delete;
 };
 
-// Blocks of `kern` (no dynamic shared memory) that fit on one SM at once (at least 1).
+// Blocks of `kern` that fit on one SM at once (at least 1).
 template <typename K>
-int resident_blocks(K kern, int threads)
+int resident_blocks(K kern, int threads, size_t dyn_smem = 0)
 {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, dyn_smem) != cudaSuccess) {
         cudaGetLastError();
         n = 1;
     }
@@ -346,6 +347,7 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
                                     : ((rows_max + tcg::BM - 1) / tcg::BM + args.E) * args.n_tiles;
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
+    if (!wg) args.n_fastest = g_gemm_order.load() == 2;
     // a programmatic dependent of the kernel before it: launch and set-up overlap that kernel's end
     PdlLaunch gl(grid, tcg::THREADS, stream, (size_t)smem);
     return launch_ex_status(cudaLaunchKernelEx(&gl.cfg, tcg::grouped_gemm_kernel<EPI, BN, MODE>, ta, tb, tc, args));
@@ -730,13 +732,14 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     // hist -> (scan) -> rank -> scatter, each a programmatic dependent of the one before
     // (T = 0: no histograms; one rank block writes the zero counts)
     const bool small = dispatch::chunk_size(T * k) == dispatch::SMALL_CHUNK;
+    const bool scanned = nchunk > 0 && dispatch::use_chunk_scan(nchunk, E, !small);
     if (nchunk > 0) {
         PdlLaunch hl(nchunk, dispatch::THREADS, stream);   // waits for the router's last kernel
         const moe_status st0 = launch_ex_status(cudaLaunchKernelEx(
             &hl.cfg, small ? dispatch::hist_kernel<dispatch::SMALL_CHUNK> : dispatch::hist_kernel<dispatch::LARGE_CHUNK>,
             topk_idx, (int)T, k, E, hist));
         if (st0 != MOE_OK) return st0;
-        if (!small) {   // per-expert prefix over the chunks, and counts
+        if (scanned) {   // per-expert prefix over the chunks, and counts
             PdlLaunch sl((E + dispatch::WARPS - 1) / dispatch::WARPS, dispatch::THREADS, stream);
             const moe_status st_s = launch_ex_status(
                 cudaLaunchKernelEx(&sl.cfg, dispatch::scan_kernel, hist, nchunk, E, counts));
@@ -747,8 +750,8 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
         PdlLaunch rl(nchunk > 0 ? nchunk : 1, dispatch::THREADS, stream);
         const moe_status st1 = launch_ex_status(cudaLaunchKernelEx(
             &rl.cfg, small ? dispatch::rank_kernel<dispatch::SMALL_CHUNK> : dispatch::rank_kernel<dispatch::LARGE_CHUNK>,
-            topk_idx, topk_gate, (int)T, k, E, cap32, (const int*)hist, nchunk, counts, kept, offsets, slot_row,
-            row_token, row_gate, n_dropped));
+            topk_idx, topk_gate, (int)T, k, E, cap32, (const int*)hist, nchunk, (int)scanned, counts, kept, offsets,
+            slot_row, row_token, row_gate, n_dropped));
         if (st1 != MOE_OK) return st1;
     }
     moe_status st = launch_status();
@@ -756,13 +759,15 @@ moe_status moe_dispatch(const int32_t* topk_idx, const float* topk_gate, int64_t
     const int vec16 = d * esize(xdt) / 16;
     const long long tasks = T * ((vec16 + dispatch::CHUNK_VEC - 1) / dispatch::CHUNK_VEC);
     long long grid = (tasks + dispatch::WARPS - 1) / dispatch::WARPS;
-    // only resident blocks preload before the ranking ends: one wave of them, grid-striding
-    static const int per_sm = resident_blocks(dispatch::scatter_tokens_kernel, dispatch::THREADS);
+    if (!ensure_dyn_smem((const void*)dispatch::scatter_tokens_kernel, dispatch::SCATTER_SMEM)) return launch_status();
+    // only resident blocks stage x before the ranking ends: one wave of them, grid-striding
+    static const int per_sm = resident_blocks(dispatch::scatter_tokens_kernel, dispatch::THREADS,
+                                              (size_t)dispatch::SCATTER_SMEM);
     if (grid > (long long)sm_count() * per_sm) grid = (long long)sm_count() * per_sm;
-    // a programmatic dependent of the ranking: x loads start before slot_row is final
-    PdlLaunch sl((int)grid, dispatch::THREADS, stream);
+    // a programmatic dependent of the ranking: x copies start before slot_row is final
+    PdlLaunch sl((int)grid, dispatch::THREADS, stream, (size_t)dispatch::SCATTER_SMEM);
     return launch_ex_status(cudaLaunchKernelEx(&sl.cfg, dispatch::scatter_tokens_kernel, slot_row, (int)T, k,
-                                               (const uint4*)x, (uint4*)x_perm, vec16));
+                                               (const uint4*)x, (uint4*)x_perm, vec16, g_wait_limit.load()));
 }
 
 moe_status moe_permute_rows(const void* src, const int32_t* index, int64_t n, int d, moe_dtype dtype, void* dst,
@@ -1034,6 +1039,13 @@ moe_status moe_set_wgrad_order(int order)
 {
     if (order < 0 || order > 2) return MOE_ERR_INVALID_ARG;
     g_wgrad_order.store(order);
+    return MOE_OK;
+}
+
+moe_status moe_set_gemm_order(int order)
+{
+    if (order < 0 || order > 2) return MOE_ERR_INVALID_ARG;
+    g_gemm_order.store(order);
     return MOE_OK;
 }
 
