@@ -83,8 +83,9 @@ def KERNELS_PER_STEP_TOTAL(cfg, args=None) -> int:
     """Library kernels launched by one layer forward of this workload (the
     device-timed region launches exactly these, K times)."""
     tc_router = cfg.dtype == "bf16" and cfg.E <= 128
-    # weight split + logits (+ softmax/top-k for E > 64) + prob sums | CUDA-core router + sums
-    route = (3 if cfg.E <= 64 else 4) if tc_router else 2
+    # weight split + logits (E <= 64: with softmax/top-k and the prob sums, written by its last CTA;
+    # E > 64: + finishing kernel + prob sums) | CUDA-core router + sums
+    route = (2 if cfg.E <= 64 else 4) if tc_router else 2
     gather = bool(args and args.gather)
     n = cfg.T * cfg.k
     # chunk histograms (+ a per-expert scan of them above 65536 assignments) + ranks; T*k = 0: the rank

@@ -1,9 +1,10 @@
 """bench.py's launch-count claim (`gpu_launches`) against the launch lists
-captured with ncu on the same workloads: nine library kernels per e8_swiglu
-forward step (router 3: weight split, the fused logits/softmax/top-k kernel
-and the probability sums; dispatch histograms + ranks + row scatter 3; up and
-down GEMMs; combine with the aux loss) and 21 per training step; one more
-router kernel (the finishing kernel) above 64 experts; one more dispatch kernel (the
+captured with ncu on the same workloads: eight library kernels per e8_swiglu
+forward step (router 2: weight split and the fused logits/softmax/top-k
+kernel, whose last CTA writes the probability sums; dispatch histograms +
+ranks + row scatter 3; up and down GEMMs; combine with the aux loss) and 20
+per training step; two more router kernels above 64 experts (the finishing
+kernel and the probability sums); one more dispatch kernel (the
 per-expert scan of the chunk histograms) above 65536 assignments; one more for
 the global aux loss of token-sharded replicas."""
 import argparse
@@ -30,13 +31,13 @@ def test_forward_and_training_launch_counts(monkeypatch):
     b = _bench()
     monkeypatch.delenv("WORLD_SIZE", raising=False)
     e8 = b.synth.workload("e8_swiglu")
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 9
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(train=True)) == 21
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(gather=True)) == 8          # no row scatter
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(z_beta=1e-3)) == 10        # + z-loss
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 8
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(train=True)) == 20
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(gather=True)) == 7          # no row scatter
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args(z_beta=1e-3)) == 9         # + z-loss
     e64 = b.synth.workload("e64_zipf")
-    assert b.KERNELS_PER_STEP_TOTAL(e64, _args()) == 9
+    assert b.KERNELS_PER_STEP_TOTAL(e64, _args()) == 8
     e128 = b.synth.workload("e128_top8_T32768")       # E > 64: + finishing kernel; T*k > 65536: + chunk scan
     assert b.KERNELS_PER_STEP_TOTAL(e128, _args()) == 11
     monkeypatch.setenv("WORLD_SIZE", "2")                                  # replicas: + global aux loss
-    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 10
+    assert b.KERNELS_PER_STEP_TOTAL(e8, _args()) == 9

@@ -178,7 +178,9 @@ inline bool route_fu_shape(long long T, int d, int E, RouteFuShape* s)
 inline size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 // Workspace of the tensor-core router: the three bf16 parts of the weight
 // [3 E_pad, d], the fp32 logits [T, E] (E > 64), one row of E probability
-// sums per finishing CTA or block.
+// sums per finishing block (E > 64; space for one per CTA at E <= 64), and
+// the E fixed-point probability-sum accumulators with the count of finished
+// CTAs (E <= 64).
 inline size_t route_parts_bytes(int d, const RouteFuShape& sh) { return align256((size_t)3 * sh.E_pad * d * 2); }
 inline long long route_fin_blocks(long long T) { return (T + rfu::FIN_TOKENS - 1) / rfu::FIN_TOKENS; }
 // E <= 64: the logits kernel finishes its own tokens (one probability-sum row
@@ -194,7 +196,9 @@ inline size_t route_ws_bytes_tc(long long T, int d, int E)
     RouteFuShape sh;
     if (!route_fu_shape(T, d, E, &sh)) return 0;
     const long long rows = route_finish_here(sh) ? sh.grid : route_fin_blocks(T);
-    return route_parts_bytes(d, sh) + route_logits_bytes(T, E, sh) + align256((size_t)rows * E * sizeof(float));
+    // + the fixed-point probability-sum accumulators [E] and the count of finished CTAs
+    return route_parts_bytes(d, sh) + route_logits_bytes(T, E, sh) + align256((size_t)rows * E * sizeof(float)) +
+           align256((size_t)E * 8 + 4);
 }
 inline size_t route_ws_bytes(long long T, int d, int E)
 {
@@ -559,10 +563,10 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
     if (xdt == MOE_BF16 && route_fu_shape(T, d, E, &sh)) {
         // the weight split into three bf16 parts; the tensor-core logits
         // kernel, which for E <= 64 also takes the softmax, top-k and
-        // per-CTA probability sums; for larger E the finishing kernel does
-        // that; prob_sum_kernel adds the per-CTA / per-block rows.  Each
-        // launch after the first is a programmatic dependent of the one
-        // before, so its set-up overlaps that kernel's tail.
+        // probability sums (its last CTA writes prob_sum); for larger E the
+        // finishing kernel does that and prob_sum_kernel adds its per-block
+        // rows.  Each launch after the first is a programmatic dependent of
+        // the one before, so its set-up overlaps that kernel's tail.
         const bool here = route_finish_here(sh);
         uint4* parts = (uint4*)ws;
         float* logits = here ? nullptr
@@ -610,6 +614,12 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         a.logits = logits;
         a.wait_limit = g_wait_limit.load();
         const int rows = here ? sh.grid : (int)route_fin_blocks(T);
+        unsigned long long* psum_fx =
+            (unsigned long long*)((char*)psum + align256((size_t)rows * E * sizeof(float)));
+        unsigned* done = (unsigned*)(psum_fx + E);
+        a.psum_fx = psum_fx;
+        a.done = done;
+        a.prob_sum = prob_sum;
         rfu::FinArgs f{};
         f.T = (int)T;
         f.E = E;
@@ -624,7 +634,8 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         const long long n8 = (long long)sh.E_pad * (d / 8);
         long long sg = (n8 + 255) / 256;
         if (sg > 4LL * sm_count()) sg = 4LL * sm_count();
-        rfu::split_weight_kernel<<<(int)sg, 256, 0, stream>>>(w_router, E, sh.E_pad, d, parts);
+        rfu::split_weight_kernel<<<(int)sg, 256, 0, stream>>>(w_router, E, sh.E_pad, d, parts,
+                                                               here ? psum_fx : nullptr, done);
         moe_status st = launch_status();
         if (st != MOE_OK) return st;
         cudaLaunchAttribute attr[2];
@@ -653,6 +664,7 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
             st = launch_ex_status(cudaLaunchKernelEx(&fcfg, fin, f));
             if (st != MOE_OK) return st;
         }
+        if (here) return MOE_OK;   // prob_sum: written by the logits kernel's last CTA
         cudaLaunchConfig_t pcfg = {};
         pcfg.gridDim = dim3((unsigned)E);
         pcfg.blockDim = dim3(256);

@@ -55,9 +55,11 @@
 // the softmax, the top-k and its per-expert sums of p itself (finish_token:
 // four lanes per token); for larger E it writes the fp32 logits and
 // route_finish_kernel (a programmatic dependent, many blocks per SM to hide
-// the latency of the longer per-token chains) does that.  prob_sum_kernel
-// adds the per-CTA or per-block rows.  Every sum has a fixed order, so a call
-// gives the same bits every run.
+// the latency of the longer per-token chains) does that.  For E <= 64 each
+// CTA adds its probability sums into 64-bit fixed-point accumulators and the
+// CTA that finishes last writes prob_sum (integer adds: the bits do not
+// depend on the order); for larger E prob_sum_kernel adds the per-block rows
+// in a fixed order.  A call gives the same bits every run.
 #pragma once
 #include "common.cuh"
 #include "ptx_sm103.cuh"
@@ -89,8 +91,18 @@ struct Args {
     float* psum;        // [gridDim.x, E]      per-CTA probability sums
     RouteSel sel;       // group-limited routing, lse and logits out
     float* logits;      // [T, E] fp32 out (E > 64): the logits for route_finish_kernel
+    // E <= 64: the per-CTA probability sums go into E 64-bit fixed-point
+    // accumulators (zeroed by the split kernel, like the count of CTAs done);
+    // the CTA that counts itself in last writes prob_sum
+    unsigned long long* psum_fx;
+    unsigned* done;
+    float* prob_sum;
     unsigned long long wait_limit;
 };
+// Fixed-point scale of the probability-sum accumulators: integer adds are
+// exact and associative, so the result does not depend on which CTA adds
+// first; per CTA the rounding error is at most 2^-33, and T * 2^32 < 2^63.
+constexpr double PSUM_FX_SCALE = 4294967296.0;
 
 // Arguments of the finishing kernel.
 struct FinArgs {
@@ -126,10 +138,18 @@ __device__ __forceinline__ void bulk_push(uint32_t dst, uint32_t src, uint32_t b
 // W (fp32 [E, d]) -> stacked bf16 [3*E_pad, d]: rows [0,E_pad) W0, [E_pad,2E_pad) W1,
 // [2E_pad,3E_pad) W2; rows of experts >= E are zero.  W0 = rn(W), W1 = rn(W - W0),
 // W2 = rn(W - W0 - W1); both differences are exact in fp32.  Eight columns per thread.
+// It also zeroes the fixed-point probability-sum accumulators of the call.
 __global__ void __launch_bounds__(256) split_weight_kernel(const float* __restrict__ W, int E, int E_pad, int d,
-                                                           uint4* __restrict__ Ws)
+                                                           uint4* __restrict__ Ws, unsigned long long* __restrict__ psum_fx,
+                                                           unsigned* __restrict__ done)
 {
     pdl_launch_dependents();
+    // the router's probability-sum accumulators and its count of finished CTAs
+    // (every later kernel of the call starts its use of them after this grid)
+    if (psum_fx && blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) psum_fx[e] = 0ull;
+        if (threadIdx.x == 0) *done = 0u;
+    }
     const int d8 = d / 8;
     const long long n8 = (long long)E_pad * d8;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
@@ -678,8 +698,25 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             }
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < E; e += THREADS)
-            g.psum[(size_t)blockIdx.x * E + e] = column_sum(red + (size_t)tbase * P, TPC, P, e);
+        // this CTA's probability sums into the fixed-point accumulators; the
+        // CTA that finishes last converts them into prob_sum
+        __shared__ int is_last;
+        for (int e = threadIdx.x; e < E; e += THREADS) {
+            const float v = column_sum(red + (size_t)tbase * P, TPC, P, e);
+            atomicAdd(g.psum_fx + e, (unsigned long long)__double2ll_rn((double)v * PSUM_FX_SCALE));
+            __threadfence();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            pdl_wait();   // the split kernel (which zeroed the accumulators) has finished
+            is_last = atomicAdd(g.done, 1u) == gridDim.x - 1;
+        }
+        __syncthreads();
+        if (is_last) {
+            __threadfence();
+            for (int e = threadIdx.x; e < E; e += THREADS)
+                g.prob_sum[e] = (float)((double)(long long)__ldcg(g.psum_fx + e) * (1.0 / PSUM_FX_SCALE));
+        }
     } else {
         // the logits of this CTA's tokens for the finishing kernel: the S
         // partial rows added in split order, then the bias; one warp per token
