@@ -115,12 +115,16 @@ struct FinArgs {
 };
 
 // Shared memory after the main loop (reusing the stage ring): the partial
-// logits of the CTA's rows, [TPB * 128][E_pad + 1] (rows one float longer
-// than E_pad, so that threads reading one row each hit different banks); the
-// rows the other CTAs of the cluster push for the tokens this CTA finishes,
-// [S][TPC][E_pad + 1] (the same size); the per-warp probability sums are
-// not needed: one thread per expert sums the finished rows.
-__host__ __device__ constexpr int red_bytes(int TPB, int E_pad) { return TPB * BM * (E_pad + 1) * 4; }
+// logits of the CTA's rows, [TPB * 128][E_pad + 4]; the rows the other CTAs
+// of the cluster push for the tokens this CTA finishes, [S][TPC][E_pad + 4]
+// (the same size).  Rows are RPITCH = E_pad + 4 floats long (4 times an odd
+// number, since E_pad is a multiple of 16): the accumulator threads write
+// their rows with 16-byte stores (eight lanes per 128 bytes hit eight
+// different 16-byte bank groups), the finishing lanes read with a stride of
+// four floats (the four lanes of eight tokens hit 32 different banks), and a
+// thread per expert summing a column hits its own bank.
+__host__ __device__ constexpr int rpitch(int E_pad) { return E_pad + 4; }
+__host__ __device__ constexpr int red_bytes(int TPB, int E_pad) { return TPB * BM * rpitch(E_pad) * 4; }
 __host__ __device__ constexpr int finish_smem_bytes(int TPB, int E_pad) { return 2 * red_bytes(TPB, E_pad); }
 // TMEM columns of one 128-token tile in the two accumulator layouts.
 __host__ __device__ constexpr int tile_tmem_cols(bool fused_parts, int E_pad) { return fused_parts ? 7 * E_pad : 4 * E_pad; }
@@ -216,7 +220,10 @@ __device__ __forceinline__ void drain_chunk_fp(uint32_t tb, int Ep, int buf, boo
 // its candidates (logit desc, index asc) and k rounds of a four-lane argmax
 // of the list heads give the winners, in order.  On return l[] holds p
 // (softmax probabilities); lane 0 of a valid token has written idx, gate and
-// lse.  Every lane of the warp must call it (shuffles).
+// lse.  Every lane of the warp must call it (shuffles).  The exponentials use
+// the hardware approximation (__expf): its relative error on arguments in
+// [-30, 0] is a few units in the last place, far inside the 1e-5 bar of the
+// gates and probability sums, and the top-k decision uses the logits alone.
 template <int G, int EPL, int KMAX>
 __device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, int k, int renorm, bool valid, int t,
                                              const RouteSel& sel, int32_t* __restrict__ idx_out,
@@ -294,7 +301,7 @@ __device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, in
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
         if (sub + G * i < E) {
-            l[i] = expf(l[i] - mx);
+            l[i] = __expf(l[i] - mx);
             s += l[i];
         }
 #pragma unroll
@@ -331,7 +338,7 @@ __device__ __forceinline__ void finish_token(float (&l)[EPL], int sub, int E, in
                 tv[KMAX - 1] = -INFINITY;
                 ti[KMAX - 1] = 0x7fffffff;
             }
-            wp[j] = expf(bv - mx) * inv;   // the winner's probability, as in l[]
+            wp[j] = __expf(bv - mx) * inv;   // the winner's probability, as in l[]
             widx[j] = bi;
             chosen += wp[j];
         }
@@ -384,7 +391,7 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const int nkb = kb1 - kb0;
     const int rot = nkb > 0 ? group % nkb : 0;   // staggered walk: concurrent groups read different W columns
     const int nch = (nkb + KC - 1) / KC;
-    const int Ep = g.E_pad, P = Ep + 1;
+    const int Ep = g.E_pad, P = rpitch(Ep);
     const uint32_t tile_cols = (uint32_t)tile_tmem_cols(FP, Ep);
     const uint64_t limit = g.wait_limit;
     const int TPC = TPB * BM / S;                 // tokens this CTA finishes
@@ -607,11 +614,15 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         ptx::tmem_ld16(tt_b + (uint32_t)(lb * 3 * Ep + 2 * Ep + e0), a2);
                         if (nch >= 2) ptx::tmem_ld16(tt_b + (uint32_t)(6 * Ep + e0), as);
                         ptx::tmem_ld_wait();
+                        float o[16];
 #pragma unroll
                         for (int u = 0; u < 16; ++u) {
                             const float chunk = __uint_as_float(a0[u]) + (__uint_as_float(a1[u]) + __uint_as_float(a2[u]));
-                            red[e0 + u] = nch >= 2 ? __uint_as_float(as[u]) + chunk : chunk;
+                            o[u] = nch >= 2 ? __uint_as_float(as[u]) + chunk : chunk;
                         }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            reinterpret_cast<float4*>(red + e0)[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
                     }
                 } else {
 #pragma unroll
@@ -622,11 +633,16 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                             ptx::tmem_ld16(tt_b + (uint32_t)(2 * Ep + e0), a1);
                             ptx::tmem_ld16(tt_b + (uint32_t)(3 * Ep + e0), a2);
                             ptx::tmem_ld_wait();
+                            float o[16];
 #pragma unroll
                             for (int u = 0; u < 16; ++u) {
                                 const float w0 = nch >= 2 ? sumr[tt][e0 + u] + __uint_as_float(a0[u]) : __uint_as_float(a0[u]);
-                                red[e0 + u] = w0 + (__uint_as_float(a1[u]) + __uint_as_float(a2[u]));
+                                o[u] = w0 + (__uint_as_float(a1[u]) + __uint_as_float(a2[u]));
                             }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                reinterpret_cast<float4*>(red + e0)[u] =
+                                    make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
                         }
                     }
                 }
