@@ -8,19 +8,20 @@
 // contiguous.
 //
 // Assignments are numbered a = j*T + t (k-rank major, token minor): that is
-// the order in which slots are granted.  Three kernels, each a programmatic
-// dependent of the one before (it launches while that one runs, and waits
-// for it only where it reads its results):
+// the order in which slots are granted.  Three or four kernels, each a
+// programmatic dependent of the one before (it launches while that one runs,
+// and waits for it only where it reads its results):
 //   hist    per chunk of CH assignments, a histogram over experts
 //   scan    (large chunks) per expert, the exclusive prefix of the
 //           histograms over chunks, in place, and the totals
 //   rank    per chunk: base of every expert from the earlier chunks and the
-//           totals (without the scan: threads split the chunks of an expert), then the stable
-//           rank of each assignment inside the chunk (warp match + per-warp
-//           counts), giving its place in the expert's queue; kept slots get a
-//           row of the permuted buffer; chunk 0 also writes counts, kept,
-//           offsets and n_dropped
-//   scatter x_perm[row] = x[token] with 16-byte vector moves
+//           totals (without the scan: threads split the chunks of an
+//           expert), then the stable rank of each assignment inside the
+//           chunk (warp match + per-warp counts), giving its place in the
+//           expert's queue; kept slots get a row of the permuted buffer;
+//           chunk 0 also writes counts, kept, offsets and n_dropped
+//   scatter x_perm[row] = x[token] with 16-byte vector moves, x staged in
+//           shared memory while the ranks are computed
 // CH = 256 while T*k <= SMALL_CHUNK_MAX (many short chunks: enough blocks to
 // spread the latency-bound ranking over the GPU), else 1024.
 #pragma once
