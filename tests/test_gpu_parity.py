@@ -202,7 +202,8 @@ def test_identity_experts_return_x_bf16():
 
 @pytest.mark.parametrize("T,k,E,cap", [(8192, 2, 64, 160), (8193, 2, 64, 160), (2048, 8, 128, 100),
                                        (4097, 8, 128, 300), (1, 1, 8, 1), (33, 16, 256, 2),
-                                       (32768, 2, 8, 9000), (9001, 8, 128, 700), (70001, 1, 16, 5000)])
+                                       (32768, 2, 8, 9000), (9001, 8, 128, 700), (70001, 1, 16, 5000),
+                                       (32768, 2, 16, 3000), (65537, 1, 16, 3000)])
 def test_dispatch_both_rank_paths_against_oracle(T, k, E, cap):
     """The histogram + rank kernels with chunks of 256 assignments (T*k <=
     65536) and of 1024 (larger T*k) against the oracle's queue simulation: counts, kept,
@@ -228,6 +229,26 @@ def test_dispatch_both_rank_paths_against_oracle(T, k, E, cap):
     tok = np.nonzero(sr >= 0)[0]
     assert np.array_equal(D.row_token.cpu().numpy()[rows], tok)
     assert np.array_equal(D.row_gate.cpu().numpy()[rows], gate.numpy()[sr >= 0])
+    assert torch.equal(D.x_perm[torch.as_tensor(rows, dtype=torch.long).cuda()].cpu(), x[torch.as_tensor(tok)])
+
+
+@pytest.mark.parametrize("d", [2112, 192])
+def test_dispatch_rows_of_partial_chunks(d):
+    """The row scatter moves rows in 2 KB chunks staged by bulk copies; rows of
+    2112 bf16 (4224 bytes: chunks of 2048, 2048 and 128 bytes) and 192 bf16
+    (384 bytes, one partial chunk) land bit for bit, every kept slot row."""
+    T, k, E, cap = 3000, 2, 16, 300
+    g = torch.Generator().manual_seed(d)
+    w = torch.arange(E, 0, -1, dtype=torch.float64)
+    idx = torch.multinomial(w.expand(T, E), k, replacement=False, generator=g).to(torch.int32)
+    gate = torch.rand(T, k, generator=g)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    D = moe.dispatch(idx.cuda(), gate.cuda(), x.cuda(), E, cap)
+    moe.check()
+    sr = D.slot_row.cpu().numpy()
+    rows = sr[sr >= 0]
+    tok = np.nonzero(sr >= 0)[0]
+    assert len(rows) > 0 and int(D.n_dropped.item()) > 0
     assert torch.equal(D.x_perm[torch.as_tensor(rows, dtype=torch.long).cuda()].cpu(), x[torch.as_tensor(tok)])
 
 
