@@ -397,6 +397,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int rows_valid = WGRAD ? g.m_rows - m * BM : __ldg(g.kept + e) - m * BM;
             const int row = WGRAD ? e * g.m_rows + m * BM + r_in : __ldg(g.offsets + e) + m * BM + r_in;
             const bool rv = r_in < rows_valid;
+            // the row's gate does not depend on the MMAs: its load is in flight during the wait
+            const float gate_pre = (EPI == EPI_GATE && rv) ? __ldg(g.row_gate + row) : 0.f;
             const bool waited = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), aphase, limit);
             if (!__all_sync(0xffffffffu, waited)) {
                 moe_flag(MOE_DEV_TIMEOUT);
@@ -495,7 +497,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             } else {
-                const float gate = (EPI == EPI_GATE && rv) ? __ldg(g.row_gate + row) : 0.f;
+                const float gate = gate_pre;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t av[32];
