@@ -131,8 +131,10 @@ int moe_abi_version(void);
  *                      ties go to the lower expert index; j is the k-rank
  *   topk_gate  [T, k]  fp32: p[t, idx]; divided by sum_j p[t, idx[t,j]] when
  *                      renorm != 0
- *   prob_sum   [E]     fp32: sum_t p[t,e], reduced in a fixed order
- *                      (bitwise reproducible run to run)
+ *   prob_sum   [E]     fp32: sum_t p[t,e], bitwise reproducible run to run:
+ *                      a fixed-order sum, or (bf16 x, E <= 64) per-block
+ *                      sums added as 64-bit fixed point (resolution 2^-32,
+ *                      integer adds, so the order does not matter)
  *   ws         >= moe_workspace_bytes(MOE_CALL_ROUTE, T, d, E, k, ...) bytes
  * T == 0 is allowed (prob_sum becomes zeros). */
 moe_status moe_route(const void* x, moe_dtype xdt, const float* w_router, const float* b_router,
