@@ -398,6 +398,8 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const uint32_t slice_bytes = (uint32_t)(TPC * P * 4);   // one CTA's partial rows of them
     const uint32_t xstage_bytes = (uint32_t)(TPB * X_BYTES), wstage_bytes = (uint32_t)(3 * Ep * 128);
     const uint32_t wring = smem0 + (uint32_t)g.xstages * xstage_bytes;   // weight ring after the x ring
+    // x fills issued by the x producer before the block-wide barrier below
+    const int xpre = nkb < g.xstages ? nkb : g.xstages;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < g.xstages; ++s) {
@@ -419,6 +421,17 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         if (S > 1) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&recv_bar), (uint32_t)(S - 1) * slice_bytes);
         ptx::tma_prefetch_desc(&tmX);
         ptx::tma_prefetch_desc(&tmW);
+        // the first pass of the x ring needs no free slot: it starts here, while
+        // the other warps allocate TMEM and load the bias
+        int kb = kb0 + rot;
+        for (int i = 0; i < xpre; ++i) {
+            const uint32_t fb = ptx::smem_u32(&xfull[i]);
+            const uint32_t dst = smem0 + (uint32_t)i * xstage_bytes;
+            ptx::mbar_arrive_expect_tx(fb, xstage_bytes);
+            ptx::tma_load_2d(dst, &tmX, fb, kb * BK, row0);
+            if (TPB > 1) ptx::tma_load_2d(dst + X_BYTES, &tmX, fb, kb * BK, row0 + BM);
+            if (++kb == kb1) kb = kb0;
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), g.tmem_cols);
@@ -445,12 +458,13 @@ route_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             // the x ring fills before the weight split has finished; the
             // weight producer waits for it (programmatic dependent launch)
             if (!xring) pdl_wait();
-            int stage = 0;
-            uint32_t phase = 0;
-            int fills = 0;
+            const int i0 = xring ? xpre : 0;       // the x ring's first fills went out before the barrier
+            int stage = i0 % nst;
+            uint32_t phase = (uint32_t)((i0 / nst) & 1);
+            int fills = i0;
             bool ok = true;
-            int kb = kb0 + rot;                    // K blocks walked from kb0 + rot, wrapping at kb1
-            for (int i = 0; i < nkb; ++i) {
+            int kb = kb0 + (rot + i0) % (nkb > 0 ? nkb : 1);   // K blocks walked from kb0 + rot, wrapping at kb1
+            for (int i = i0; i < nkb; ++i) {
                 if (!ptx::mbar_wait(ptx::smem_u32(&empty[stage]), phase ^ 1u, limit)) {
                     ok = false;
                     break;
