@@ -488,6 +488,15 @@ moe_status moe_set_gemm_tile_n(int bn);
  * MOE_ERR_INVALID_ARG otherwise. */
 moe_status moe_set_gemm_order(int order);
 
+/* Last wave of the forward bf16 expert GEMMs with 256-column tiles (GELU,
+ * identity and gate epilogues): 1 (default) lets a launch whose tiles end in
+ * a wave that would leave at least half of the SMs idle run that wave's R
+ * tiles as 2R units of 128 columns, one per SM; 0 keeps whole tiles.  The
+ * results do not depend on it (every output is the same dot product in the
+ * same K order).  Process-wide; for tests and tuning.  MOE_ERR_INVALID_ARG
+ * for any other value. */
+moe_status moe_set_gemm_tail_halves(int on);
+
 /* Tile order of the weight-gradient GEMMs (moe_expert_wgrad,
  * moe_expert_wgrad_rows) inside each expert: 0 (default) automatic
  * (N-fastest), 1 M-fastest, 2 N-fastest.  The results do not depend on it.

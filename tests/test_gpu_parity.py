@@ -137,6 +137,46 @@ def test_gemm_tile_order_changes_no_bit(name):
     compare_output(plan, run_oracle(case), cfg.dtype)
 
 
+def _halves_apply(plan, n_out, sms):
+    """Whether a forward GEMM of n_out columns (256-column tiles) runs its last
+    wave as half-width units: its tiles end in a wave that uses at most half
+    of the blocks (the launch's grid is min(SMs, the host's tile bound))."""
+    kept = plan.disp.kept.cpu().numpy().astype(np.int64)
+    n_tiles = -(-n_out // 256)
+    tiles = int(sum(-(-int(c) // 128) for c in kept)) * n_tiles
+    grid = min(sms, (-(-plan.rows_max // 128) + len(kept)) * n_tiles)
+    tail = tiles % grid
+    return 0 < tail and 2 * tail <= grid
+
+
+@pytest.mark.parametrize("name", ["gelu_e8_tail", "gelu_e16_hot"])
+def test_gemm_half_width_last_wave_changes_no_bit(name):
+    """A last wave of R <= SMs/2 tiles run as 2R half-width units (GELU up
+    and gate-scaled down GEMMs) gives the same bits as whole tiles, and the
+    oracle's layer.  gelu_e8_tail is sized so that both GEMMs take that path
+    on 148 SMs (~1375 rows = 11 M tiles per expert, 2 N tiles: ~176 tiles,
+    a last wave of ~28), with a ragged last N tile in both (F = 384: the
+    second half of the second up tile is past F; d = 448: the second half of
+    the second down tile holds 64 columns)."""
+    cfg = C("gelu_e8_tail", 5500, 448, 8, 2, 384, "gelu", 4.0, "bf16") if name == "gelu_e8_tail" else SMALL[name]
+    case = make_case(cfg)
+    base = run_gpu(case)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if name == "gelu_e8_tail" and sms >= 128:
+        assert _halves_apply(base, cfg.F, sms) and _halves_apply(base, cfg.d, sms)
+    moe.set_gemm_tail_halves(False)
+    try:
+        plan = run_gpu(case)
+    finally:
+        moe.set_gemm_tail_halves(True)
+    moe.check()
+    A = int(base.disp.offsets[-1].item())
+    assert torch.equal(plan.h[:A], base.h[:A])
+    assert torch.equal(plan.y_perm[:A], base.y_perm[:A])
+    assert torch.equal(plan.y, base.y)
+    compare_output(base, run_oracle(case), cfg.dtype)
+
+
 @pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot", "swiglu_e64_zipf", "swiglu_e128_top8", "small_T",
                                   "gelu_e32_norenorm"])
 def test_cta_pair_gemm_kernel(name):

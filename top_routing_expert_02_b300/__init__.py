@@ -90,6 +90,7 @@ _SIGS = {
     "moe_set_wait_limit": (None, [_U64]),
     "moe_set_gemm_tile_n": (_I32, [_I32]),
     "moe_set_gemm_order": (_I32, [_I32]),
+    "moe_set_gemm_tail_halves": (_I32, [_I32]),
     "moe_set_wgrad_order": (_I32, [_I32]),
     "moe_set_gemm_kernel": (_I32, [_I32]),
     "moe_selftest_wait_timeout": (_I32, [_P]),
@@ -196,6 +197,11 @@ def set_gemm_tile_n(bn: int):
 def set_gemm_order(order: int):
     """Forward / data-gradient GEMM tile order: 0 automatic, 1 M-fastest, 2 N-fastest (results unchanged)."""
     _ok("moe_set_gemm_order", lib().moe_set_gemm_order(int(order)))
+
+
+def set_gemm_tail_halves(on: bool):
+    """Let a short last wave of the forward GEMMs run as half-width units (default on; results unchanged)."""
+    _ok("moe_set_gemm_tail_halves", lib().moe_set_gemm_tail_halves(int(bool(on))))
 
 
 def set_wgrad_order(order: int):

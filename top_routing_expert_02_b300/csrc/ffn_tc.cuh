@@ -89,6 +89,7 @@ struct Args {
     int m_rows;                 // weight gradient: rows M of each expert's gradient
     int lda;                    // MODE_WGRAD_ROWS: row stride of A in elements (>= m_rows)
     int n_fastest;              // tile order N-fastest inside an expert (default: M-fastest)
+    int tail_halves;            // let a short last wave run as 128-column units (see unit_tile)
     unsigned long long wait_limit;
 };
 
@@ -134,6 +135,24 @@ __device__ __forceinline__ void decode_tile(const int* mstart, int E, int n_tile
 }
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+// Units of work of a launch.  The tiles are dealt to the blocks round-robin,
+// so a launch of W whole waves plus R < grid tiles ends with a wave in which
+// grid - R blocks idle for a whole tile time.  When R <= grid / 2, those R
+// tiles run instead as 2R units of half the columns (BN/2), one per block:
+// the last wave takes about half as long.  Units [0, full) are whole tiles
+// (hv = -1); unit full + 2i + h is half h of tile full + i.  A half computes
+// the same dot products over the same K order as the whole tile, so the
+// output bits do not change.
+__device__ __forceinline__ int unit_tile(int u, int full, int& hv)
+{
+    if (u < full) {
+        hv = -1;
+        return u;
+    }
+    hv = (u - full) & 1;
+    return full + ((u - full) >> 1);
+}
 
 // Byte offsets in x of the 32 rows lane `lane` copies for `tile` (rows
 // 4i + lane/8, plus its 16-byte chunk lane%8); rows past the expert's segment
@@ -225,6 +244,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     const uint32_t tmem_base = tmem_base_sh;
     const int total_tiles = mstart[g.E] * g.n_tiles;
+    // half-width units for a short last wave: plain x_perm rows, 256-column
+    // tiles whose columns are independent outputs (not the SwiGLU pairing)
+    constexpr bool HALVES = MODE == MODE_ROWS && BN == 256 && (EPI == EPI_GATE || EPI == EPI_GELU || EPI == EPI_IDENT);
+    const int tail = total_tiles % (int)gridDim.x;
+    const bool halves = HALVES && g.tail_halves != 0 && tail > 0 && 2 * tail <= (int)gridDim.x;
+    const int full_units = total_tiles - (halves ? tail : 0);
+    const int total_units = full_units + (halves ? 2 * tail : 0);
+    constexpr uint32_t IDESC_HALF = ptx::idesc_bf16_f32(128, BN / 2);
     const int nk = (g.K + BK - 1) / BK;
     const uint64_t limit = g.wait_limit;
 
@@ -235,7 +262,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             long long fills = 0;
             bool ok = true;
             uint32_t roff[GATHER ? 32 : 1];   // gathered rows: this lane's 32 offsets in x
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+                int hv;
+                const int tile = unit_tile(u, full_units, hv);
                 int e, m, n;
                 decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, g.n_fastest != 0);
                 const int rowA = WGRAD ? m * BM : __ldg(g.offsets + e) + m * BM;
@@ -256,7 +285,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
                     const uint32_t sa = smem0 + stage * STAGE_BYTES;
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(fb, GATHER ? 2 * BH_BYTES : STAGE_BYTES);
+                        ptx::mbar_arrive_expect_tx(fb, GATHER ? 2 * BH_BYTES : hv < 0 ? STAGE_BYTES : A_BYTES + BH_BYTES);
                         const int kx = (kb0 + kb) * BK;
                         if (WGR) {
                             // rows rowK0 + 64 kb.. (K); A columns m*128.. (M), B columns n*256.. (N)
@@ -274,9 +303,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                 for (int j = 0; j < 4; ++j)
                                     ptx::tma_load_2d(sa + A_BYTES + j * BOX_BYTES, &tmB, fb, n * BN + 64 * j,
                                                      e * g.K + kx);
-                            } else {
+                            } else if (hv < 0) {
                                 ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, rowB0);
                                 ptx::tma_load_2d(sa + A_BYTES + BH_BYTES, &tmB, fb, kx, rowB1);
+                            } else {
+                                // half unit: the BN/2 weight rows of its columns, first in the stage
+                                ptx::tma_load_2d(sa + A_BYTES, &tmB, fb, kx, hv ? rowB1 : rowB0);
                             }
                         }
                     }
@@ -323,7 +355,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+                int hv;
+                const int tile = unit_tile(u, full_units, hv);
+                const uint32_t idesc = hv < 0 ? IDESC : IDESC_HALF;
                 if (!wait(&tempty_bar[acc], aphase ^ 1u)) {
                     ok = false;
                     break;
@@ -364,7 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                                        : ptx::sdesc_kmajor_sw128(sa + kk * 32);
                             const uint64_t bdesc = (BMN || WGR) ? ptx::sdesc_mnmajor_sw128(sb + kk * 2048, BOX_BYTES)
                                                                 : ptx::sdesc_kmajor_sw128(sb + kk * 32);
-                            ptx::mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
+                            ptx::mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
                         }
                         ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
                     }
@@ -391,7 +426,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int r_in = q * 32 + lane;    // row of the tile owned by this thread
         int acc = 0;
         uint32_t aphase = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+            int hv;
+            const int tile = unit_tile(u, full_units, hv);
             int e, m, n;
             decode_tile(mstart, g.E, g.n_tiles, tile, e, m, n, g.n_fastest != 0);
             const int rows_valid = WGRAD ? g.m_rows - m * BM : __ldg(g.kept + e) - m * BM;
@@ -498,11 +535,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             } else {
                 const float gate = gate_pre;
+                // a half unit: BN/2 columns from accumulator column 0
+                const int ncols = hv < 0 ? BN : BN / 2;
+                const int col0 = n * BN + (hv > 0 ? BN / 2 : 0);
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 0; c < ncols; c += 32) {
                     uint32_t av[32];
                     ptx::tmem_ld32(tb + c, av);
-                    const int col = n * BN + c;
+                    const int col = col0 + c;
                     if (EPI == EPI_DGELU || EPI == EPI_DSWIGLU) {
                         // z loads issued before the TMEM wait; 32 columns of this row
                         uint4 zg[4], zu[4];

@@ -30,6 +30,7 @@ std::atomic<unsigned long long> g_wait_limit{DEFAULT_WAIT_LIMIT};
 std::atomic<int> g_forced_bn{0};   // 0: pick the GEMM tile width per call
 std::atomic<int> g_wgrad_order{0};  // weight-gradient tile order: 0 automatic, 1 M-fastest, 2 N-fastest
 std::atomic<int> g_gemm_order{0};   // forward / data-gradient tile order: 0 automatic (M-fastest), 1 M-fastest, 2 N-fastest
+std::atomic<int> g_gemm_tail{1};    // a short last wave of forward tiles runs as half-width units: 1 on, 0 off
 
 // Weight-gradient tile order.  N-fastest (the blocks running together share
 // the A tile and write neighbouring column blocks of the same output rows)
@@ -352,6 +353,7 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     if (grid <= 0) return MOE_OK;
     if (!wg) args.n_fastest = g_gemm_order.load() == 2;
+    args.tail_halves = g_gemm_tail.load();
     // a programmatic dependent of the kernel before it: launch and set-up overlap that kernel's end
     PdlLaunch gl(grid, tcg::THREADS, stream, (size_t)smem);
     return launch_ex_status(cudaLaunchKernelEx(&gl.cfg, tcg::grouped_gemm_kernel<EPI, BN, MODE>, ta, tb, tc, args));
@@ -1058,6 +1060,13 @@ moe_status moe_set_gemm_order(int order)
 {
     if (order < 0 || order > 2) return MOE_ERR_INVALID_ARG;
     g_gemm_order.store(order);
+    return MOE_OK;
+}
+
+moe_status moe_set_gemm_tail_halves(int on)
+{
+    if (on != 0 && on != 1) return MOE_ERR_INVALID_ARG;
+    g_gemm_tail.store(on);
     return MOE_OK;
 }
 
