@@ -497,6 +497,15 @@ moe_status moe_set_gemm_order(int order);
  * for any other value. */
 moe_status moe_set_gemm_tail_halves(int on);
 
+/* Programmatic dependent launch between the library's kernels: 1 (default)
+ * launches each kernel after the first of a call as a programmatic dependent
+ * of the one before it (its set-up overlaps that kernel's end; it waits for
+ * that kernel's results before reading them), 0 plain stream order.  The
+ * results do not depend on it.  Process-wide, read at each launch (a CUDA
+ * graph keeps what was set when it was captured); for tests and tuning.
+ * MOE_ERR_INVALID_ARG for any other value. */
+moe_status moe_set_launch_overlap(int on);
+
 /* Tile order of the weight-gradient GEMMs (moe_expert_wgrad,
  * moe_expert_wgrad_rows) inside each expert: 0 (default) automatic
  * (N-fastest), 1 M-fastest, 2 N-fastest.  The results do not depend on it.

@@ -91,6 +91,7 @@ _SIGS = {
     "moe_set_gemm_tile_n": (_I32, [_I32]),
     "moe_set_gemm_order": (_I32, [_I32]),
     "moe_set_gemm_tail_halves": (_I32, [_I32]),
+    "moe_set_launch_overlap": (_I32, [_I32]),
     "moe_set_wgrad_order": (_I32, [_I32]),
     "moe_set_gemm_kernel": (_I32, [_I32]),
     "moe_selftest_wait_timeout": (_I32, [_P]),
@@ -202,6 +203,11 @@ def set_gemm_order(order: int):
 def set_gemm_tail_halves(on: bool):
     """Let a short last wave of the forward GEMMs run as half-width units (default on; results unchanged)."""
     _ok("moe_set_gemm_tail_halves", lib().moe_set_gemm_tail_halves(int(bool(on))))
+
+
+def set_launch_overlap(on: bool):
+    """Programmatic dependent launch between the library's kernels (default on; results unchanged)."""
+    _ok("moe_set_launch_overlap", lib().moe_set_launch_overlap(int(bool(on))))
 
 
 def set_wgrad_order(order: int):

@@ -71,13 +71,14 @@ inline moe_status launch_ex_status(cudaError_t e)
 // kernel before it in the stream (it may start once that kernel has called
 // griddepcontrol.launch_dependents; it calls griddepcontrol.wait before it
 // reads that kernel's results).
+std::atomic<int> g_pdl{1};   // programmatic dependent launches: 1 on, 0 plain stream order
 struct PdlLaunch {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg;
     PdlLaunch(int grid, int threads, cudaStream_t stream, size_t smem = 0)
     {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[0].val.programmaticStreamSerializationAllowed = g_pdl.load();
         cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3((unsigned)threads);
@@ -642,7 +643,7 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
         if (st != MOE_OK) return st;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[0].val.programmaticStreamSerializationAllowed = g_pdl.load();
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)sh.S;
         attr[1].val.clusterDim.y = 1;
@@ -1060,6 +1061,13 @@ moe_status moe_set_gemm_order(int order)
 {
     if (order < 0 || order > 2) return MOE_ERR_INVALID_ARG;
     g_gemm_order.store(order);
+    return MOE_OK;
+}
+
+moe_status moe_set_launch_overlap(int on)
+{
+    if (on != 0 && on != 1) return MOE_ERR_INVALID_ARG;
+    g_pdl.store(on);
     return MOE_OK;
 }
 
