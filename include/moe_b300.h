@@ -506,6 +506,16 @@ moe_status moe_set_gemm_tail_halves(int on);
  * MOE_ERR_INVALID_ARG for any other value. */
 moe_status moe_set_launch_overlap(int on);
 
+/* Router kernel for bf16 x: 0 (default) automatic (the tensor-core router
+ * for E <= 128), 1 the tensor-core router wherever it applies, 2 the
+ * CUDA-core router for E <= 8 (d a multiple of 256, at most 4096: one fused
+ * kernel for logits, softmax, top-k and per-block probability sums, then the
+ * fixed-order sum of the blocks' rows) wherever it applies.  Both give the
+ * routing the pages define within fp32 rounding (identical selections away
+ * from near-ties).  Process-wide; for tests and tuning.  MOE_ERR_INVALID_ARG
+ * for any other value. */
+moe_status moe_set_router_kernel(int kind);
+
 /* Tile order of the weight-gradient GEMMs (moe_expert_wgrad,
  * moe_expert_wgrad_rows) inside each expert: 0 (default) automatic
  * (N-fastest), 1 M-fastest, 2 N-fastest.  The results do not depend on it.

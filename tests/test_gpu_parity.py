@@ -320,6 +320,45 @@ def test_capacity_zero_drops_everything():
     assert abs(plan.loss.item() - ref["loss"]) <= 2e-4 * ref["loss"]
 
 
+SMALL_E_ROUTER = {
+    # E = 1 (every token to the one expert), the smallest d
+    "r_e1": C("r_e1", 257, 256, 1, 1, 128, "gelu", 1.0, "bf16"),
+    # E = 3, d = 768 (three warps), two hot experts over capacity
+    "r_e3_k2_hot": C("r_e3_k2_hot", 1001, 768, 3, 2, 128, "swiglu", 1.25, "bf16", bias="hot2"),
+    # E = 5, k = 4, no renormalisation, an odd token count
+    "r_e5_k4": C("r_e5_k4", 333, 256, 5, 4, 128, "gelu", 2.0, "bf16", renorm=False),
+    # E = k = 8 at the largest d (512 threads per block), dropless
+    "r_e8_k8_d4096": C("r_e8_k8_d4096", 600, 4096, 8, 8, 128, "swiglu", 0.0, "bf16"),
+    # one token
+    "r_e8_T1": C("r_e8_T1", 1, 512, 8, 2, 128, "gelu", 1.0, "bf16"),
+    # more than one wave of 64-token blocks, a ragged odd last block
+    "r_e7_two_waves": C("r_e7_two_waves", 148 * 64 + 37, 256, 7, 2, 128, "gelu", 1.25, "bf16"),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL_E_ROUTER))
+def test_small_e_router_against_oracle_and_tensor_core_router(name):
+    """The CUDA-core router for E <= 8 and the tensor-core router (the
+    default) on the same inputs: both against the oracle's routing, dispatch
+    and layer; their top-k indices are identical (near-ties are conditioned
+    away)."""
+    cfg = SMALL_E_ROUTER[name]
+    case = make_case(cfg)
+    ref = run_oracle(case)
+    plans = []
+    for kind in (2, 1):
+        moe.set_router_kernel(kind)
+        try:
+            plan = run_gpu(case)
+        finally:
+            moe.set_router_kernel(0)
+        compare_routing(plan, ref, cfg.dtype)
+        compare_dispatch(plan, ref)
+        compare_output(plan, ref, cfg.dtype)
+        plans.append(plan.topk_idx.clone())
+    assert torch.equal(plans[0], plans[1])
+
+
 def test_single_expert_dense_layer():
     cfg = C("dense", 300, 128, 1, 1, 256, "gelu", 0.0, "bf16")
     case = make_case(cfg)

@@ -1,8 +1,9 @@
 """GPU parity of the routing variants against the oracle: group-limited
-top-k (every router kernel: the fused CUDA-core router for fp32 x and for
-more than 160 experts, the tensor-core router's lane-per-token finisher for
-E <= 32 and warp-per-token finisher above), the per-token log-sum-exp and the
-router z-loss, and the post-drop f_i aux loss.  Bars are in moe_cases."""
+top-k (every router kernel: the tensor-core router finished in its logits
+kernel for E <= 64 and by the finishing kernel above, the CUDA-core E <= 8
+router for bf16 x on request, the fused CUDA-core router for fp32 x and for
+more than 128 experts), the per-token log-sum-exp and the router z-loss,
+and the post-drop f_i aux loss.  Bars are in moe_cases."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +20,8 @@ C = synth.MoEConfig
 
 # name: (config, n_group, topk_group, post-drop aux)
 CASES = {
-    # fused tensor-core router, finished in the logits kernel (E <= 64): 2 groups of 4, one kept
+    # E = 8: the tensor-core router finished in the logits kernel (and the CUDA-core E <= 8 router:
+    # test_e8_variants_on_both_router_kernels), 2 groups of 4, one kept
     "e8_g2m1": (C("e8_g2m1", 2000, 256, 8, 2, 384, "swiglu", 1.25, "bf16"), 2, 1, False),
     # E = 32 (one MMA for the three weight parts), one group of 4 kept, no renormalisation, post-drop aux
     "e32_g8m1": (C("e32_g8m1", 1500, 128, 32, 4, 256, "gelu", 1.5, "bf16", renorm=False), 8, 1, True),
@@ -67,6 +69,24 @@ def test_routing_variant_layer(name):
     # the restriction really bites: some token's choice differs from plain top-k
     plain = run_oracle(case, tokens=[0])
     assert not np.array_equal(plain["idx"], ref["idx"])
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+def test_e8_variants_on_both_router_kernels(kind):
+    """The E = 8 group-limited case (with the log-sum-exp and the z-loss) on the
+    tensor-core router (1) and on the CUDA-core E <= 8 router (2)."""
+    cfg, G, M, post = CASES["e8_g2m1"]
+    case = make_case(cfg, n_group=G, topk_group=M)
+    moe.set_router_kernel(kind)
+    try:
+        plan = run_gpu(case, _plan(case, G, M, post))
+    finally:
+        moe.set_router_kernel(0)
+    ref = run_oracle(case, n_group=G, topk_group=M, z_beta=Z_BETA, aux_post_drop=post)
+    compare_routing(plan, ref, cfg.dtype)
+    compare_dispatch(plan, ref, case["x_h"])
+    compare_output(plan, ref, cfg.dtype)
+    compare_z_loss(plan, ref, cfg.dtype)
 
 
 def test_one_group_equals_moe_route_bitwise():

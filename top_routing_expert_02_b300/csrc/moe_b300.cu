@@ -20,6 +20,7 @@
 #include "ffn_tc2.cuh"
 #include "route.cuh"
 #include "route_fused.cuh"
+#include "route_small.cuh"
 
 namespace {
 
@@ -72,6 +73,7 @@ inline moe_status launch_ex_status(cudaError_t e)
 // griddepcontrol.launch_dependents; it calls griddepcontrol.wait before it
 // reads that kernel's results).
 std::atomic<int> g_pdl{1};   // programmatic dependent launches: 1 on, 0 plain stream order
+std::atomic<int> g_router_kind{0};   // bf16 router: 0 automatic (tensor cores), 1 tensor cores, 2 CUDA cores for E <= 8
 struct PdlLaunch {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg;
@@ -202,10 +204,35 @@ inline size_t route_ws_bytes_tc(long long T, int d, int E)
     return route_parts_bytes(d, sh) + route_logits_bytes(T, E, sh) + align256((size_t)rows * E * sizeof(float)) +
            align256((size_t)E * 8 + 4);
 }
+// CUDA-core router for E <= 8 (bf16 x): d / 8 threads per block (whole
+// warps, at most 512), tokens spread evenly over one wave of blocks, at most
+// TPC_MAX per block (an even count: tokens go through the butterfly in pairs).
+struct RouteSmShape {
+    int tpc, grid, threads;
+    size_t smem;
+};
+inline bool route_small_shape(long long T, int d, int E, RouteSmShape* s)
+{
+    if (E > rsm::EMAX || T <= 0 || d % 256 || d < 256 || d > 8 * rsm::MAX_THREADS) return false;
+    const long long sms = (long long)sm_count();
+    long long tpc = (T + sms - 1) / sms;
+    tpc = (tpc + rsm::NT - 1) / rsm::NT * rsm::NT;
+    if (tpc > rsm::TPC_MAX) tpc = rsm::TPC_MAX;
+    s->tpc = (int)tpc;
+    s->grid = (int)((T + tpc - 1) / tpc);
+    s->threads = d / 8;
+    s->smem = rsm::smem_bytes(d, s->tpc);
+    return s->smem <= 227 * 1024;
+}
+inline size_t route_ws_bytes_small(long long T, int d, int E)
+{
+    RouteSmShape sh;
+    return route_small_shape(T, d, E, &sh) ? (size_t)sh.grid * E * sizeof(float) : 0;
+}
 inline size_t route_ws_bytes(long long T, int d, int E)
 {
-    const size_t a = route_ws_bytes_simt(T, E), b = route_ws_bytes_tc(T, d, E);
-    return a > b ? a : b;
+    const size_t a = route_ws_bytes_simt(T, E), b = route_ws_bytes_tc(T, d, E), c = route_ws_bytes_small(T, d, E);
+    return a > b ? (a > c ? a : c) : (b > c ? b : c);
 }
 inline long long dispatch_chunks(long long T, int k)
 {
@@ -562,8 +589,41 @@ static moe_status route_impl(const void* x, moe_dtype xdt, const float* w_router
     if (d % 64) return MOE_ERR_UNSUPPORTED;
     const size_t need = route_ws_bytes(T, d, E);
     if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+    const int rk = g_router_kind.load();
+    RouteSmShape ss;
+    if (xdt == MOE_BF16 && rk == 2 && route_small_shape(T, d, E, &ss)) {
+        // on request, few experts: one CUDA-core kernel (logits, softmax,
+        // top-k, per-block probability sums), then prob_sum_kernel adds the
+        // blocks' rows.  On the B300 it takes as long as the tensor-core
+        // router at E = 8 (its FMAs and butterflies are issue-bound), so the
+        // automatic choice stays with the tensor cores.
+        const int kmax = k <= 2 ? 2 : k <= 4 ? 4 : 8;
+        void (*kern)(const rsm::Args) = kmax == 2 ? rsm::route_small_kernel<2>
+                                        : kmax == 4 ? rsm::route_small_kernel<4> : rsm::route_small_kernel<8>;
+        if (!ensure_dyn_smem((const void*)kern, (int)ss.smem)) return launch_status();
+        rsm::Args a{};
+        a.x = (const uint16_t*)x;
+        a.W = w_router;
+        a.bias = b_router;
+        a.T = (int)T;
+        a.d = d;
+        a.E = E;
+        a.k = k;
+        a.renorm = renorm;
+        a.tpc = ss.tpc;
+        a.idx = topk_idx;
+        a.gate = topk_gate;
+        a.psum = (float*)ws;
+        a.sel = sel;
+        PdlLaunch rl(ss.grid, ss.threads, stream, ss.smem);
+        moe_status st = launch_ex_status(cudaLaunchKernelEx(&rl.cfg, kern, a));
+        if (st != MOE_OK) return st;
+        PdlLaunch pl(E, 256, stream);
+        return launch_ex_status(cudaLaunchKernelEx(&pl.cfg, rfu::prob_sum_kernel, (const float*)ws, ss.grid, E,
+                                                   prob_sum));
+    }
     RouteFuShape sh;
-    if (xdt == MOE_BF16 && route_fu_shape(T, d, E, &sh)) {
+    if (xdt == MOE_BF16 && rk != 2 && route_fu_shape(T, d, E, &sh)) {
         // the weight split into three bf16 parts; the tensor-core logits
         // kernel, which for E <= 64 also takes the softmax, top-k and
         // probability sums (its last CTA writes prob_sum); for larger E the
@@ -1061,6 +1121,13 @@ moe_status moe_set_gemm_order(int order)
 {
     if (order < 0 || order > 2) return MOE_ERR_INVALID_ARG;
     g_gemm_order.store(order);
+    return MOE_OK;
+}
+
+moe_status moe_set_router_kernel(int kind)
+{
+    if (kind < 0 || kind > 2) return MOE_ERR_INVALID_ARG;
+    g_router_kind.store(kind);
     return MOE_OK;
 }
 
