@@ -137,6 +137,26 @@ def test_gemm_tile_order_changes_no_bit(name):
     compare_output(plan, run_oracle(case), cfg.dtype)
 
 
+@pytest.mark.parametrize("name", ["swiglu_e8", "swiglu_e128_top8"])
+def test_launch_overlap_off_changes_no_bit(name):
+    """Plain stream order instead of programmatic dependent launches between
+    the library's kernels gives the same bits (the overlap only moves launch
+    and set-up work)."""
+    cfg = SMALL[name]
+    case = make_case(cfg)
+    base = run_gpu(case)
+    y0, h0 = base.y.clone(), base.h.clone()
+    moe.set_launch_overlap(False)
+    try:
+        plan = run_gpu(case)
+    finally:
+        moe.set_launch_overlap(True)
+    moe.check()
+    A = int(plan.disp.offsets[-1].item())
+    assert torch.equal(plan.h[:A], h0[:A])
+    assert torch.equal(plan.y, y0)
+
+
 def _halves_apply(plan, n_out, sms):
     """Whether a forward GEMM of n_out columns (256-column tiles) runs its last
     wave as half-width units: its tiles end in a wave that uses at most half

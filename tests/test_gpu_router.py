@@ -85,3 +85,36 @@ def test_router_bitwise_run_to_run_and_logits_output():
     print(f"[router] logits max abs err / max |l| {err:.3e}")
     assert err <= 1e-6
     np.testing.assert_allclose(lse.cpu().numpy(), oracle.logsumexp(L), rtol=GATE_RTOL["bf16"], atol=1e-6)
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+def test_small_e_logits_and_lse_outputs_on_both_router_kernels(kind):
+    """At E = 8 (with a bias) the tensor-core router (1) and the CUDA-core
+    E <= 8 router (2) both write logits within 1e-6 of max |l| of the oracle's
+    fp64 logits and the log-sum-exp within the gate bar, and repeat their
+    bits run to run."""
+    cfg = synth.MoEConfig("e8_logits", 1000, 512, 8, 2, 128, "gelu", 1.25, "bf16", bias="hot2")
+    ri = synth.condition_near_ties(cfg, synth.make_routing_inputs(cfg), oracle.router_logits)
+    x, W, b = ri.x.cuda(), ri.W.cuda(), ri.b.cuda()
+    T, E = cfg.T, cfg.E
+    moe.set_router_kernel(kind)
+    try:
+        outs = []
+        for _ in range(2):
+            logits = torch.empty(T, E, device="cuda")
+            lse = torch.empty(T, device="cuda")
+            r = moe.route(x, W, b, cfg.k, True, logits=logits, lse=lse)
+            outs.append([t.clone() for t in r] + [logits, lse])
+        moe.check()
+    finally:
+        moe.set_router_kernel(0)
+    for u, v in zip(outs[0], outs[1]):
+        assert torch.equal(u, v)
+    L = oracle.router_logits(ri.x, ri.W, ri.b)
+    got = outs[0][3].cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(got - L)) / np.max(np.abs(L))
+    print(f"[router] kind {kind}: logits max abs err / max |l| {err:.3e}")
+    assert err <= 1e-6
+    np.testing.assert_allclose(outs[0][4].cpu().numpy(), oracle.logsumexp(L), rtol=GATE_RTOL["bf16"], atol=1e-6)
+    ref_idx, ref_gate, _ = oracle.route(L, cfg.k, True)
+    assert np.array_equal(outs[0][0].cpu().numpy(), ref_idx)
