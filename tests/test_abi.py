@@ -154,6 +154,8 @@ def test_gemm_tile_width_setter_validates():
     assert L.moe_set_launch_overlap(1) == 0
     assert L.moe_set_router_kernel(3) == 1
     assert L.moe_set_router_kernel(0) == 0
+    assert L.moe_set_gemm_tma_store(2) == 1
+    assert L.moe_set_gemm_tma_store(1) == 0
 
 
 def test_binding_rejects_unsupported_dtype():

@@ -92,6 +92,7 @@ _SIGS = {
     "moe_set_gemm_order": (_I32, [_I32]),
     "moe_set_gemm_tail_halves": (_I32, [_I32]),
     "moe_set_launch_overlap": (_I32, [_I32]),
+    "moe_set_gemm_tma_store": (_I32, [_I32]),
     "moe_set_router_kernel": (_I32, [_I32]),
     "moe_set_wgrad_order": (_I32, [_I32]),
     "moe_set_gemm_kernel": (_I32, [_I32]),
@@ -214,6 +215,11 @@ def set_launch_overlap(on: bool):
 def set_router_kernel(kind: int):
     """bf16 router kernel: 0 automatic (tensor cores), 1 tensor cores, 2 CUDA cores for E <= 8 (where each applies)."""
     _ok("moe_set_router_kernel", lib().moe_set_router_kernel(int(kind)))
+
+
+def set_gemm_tma_store(on: bool):
+    """Down-projection output blocks by TMA stores (default on) or per-thread stores (results unchanged)."""
+    _ok("moe_set_gemm_tma_store", lib().moe_set_gemm_tma_store(int(bool(on))))
 
 
 def set_wgrad_order(order: int):

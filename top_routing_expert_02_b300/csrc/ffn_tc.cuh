@@ -90,6 +90,7 @@ struct Args {
     int lda;                    // MODE_WGRAD_ROWS: row stride of A in elements (>= m_rows)
     int n_fastest;              // tile order N-fastest inside an expert (default: M-fastest)
     int tail_halves;            // let a short last wave run as 128-column units (see unit_tile)
+    int tma_store;              // gate epilogue: output tiles through shared memory and TMA stores
     unsigned long long wait_limit;
 };
 
@@ -196,7 +197,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int BOX_BYTES = BK * 128;   // one 64x64 bf16 box
     // fp32 output tiles of the MN-major identity GEMM go out through the same
     // shared-memory staging and TMA stores as the weight gradients
-    constexpr bool TMA_OUT_OK = WGRAD || (BMN && EPI == EPI_IDENT);
+    // the down projection (gate epilogue, bf16 rows of y_perm): whole 32-row blocks go out by TMA
+    // stores as well -- per-thread stores of 32 different rows per warp instruction measured
+    // 12-14% of the kernel at the many-expert shapes, where each tile has only 24 K blocks
+    constexpr bool FWD_TMA = MODE == MODE_ROWS && EPI == EPI_GATE;
+    constexpr bool TMA_OUT_OK = WGRAD || (BMN && EPI == EPI_IDENT) || FWD_TMA;
     constexpr uint32_t IDESC = WGR ? ptx::idesc_bf16_f32(128, BN, true, true)
                                : BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
     extern __shared__ uint8_t dsmem[];
@@ -443,8 +448,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr)) {
+            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || (FWD_TMA && g.tma_store != 0))) {
                 const bool empty = WGRAD && kstart[e + 1] == kstart[e];
+                const float gsc = gate_pre;   // gate epilogue: the row's gate
                 // this warp's 32 rows all inside the expert's M rows: stage each block of
                 // 32 rows x 128 bytes in shared memory (128-byte swizzle) and store it with
                 // TMA; otherwise (a ragged last M-tile) masked per-thread stores
@@ -452,8 +458,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const bool f32_out = g.out_f32 != nullptr;
                 const uint32_t stg = smem0 + STAGES * STAGE_BYTES + q * SH::WG_STAGE_OUT;
                 const int step = f32_out ? 32 : 64;   // output columns per 128-byte row block
+                // a half-width unit: BN/2 columns from accumulator column 0
+                const int ncols = hv < 0 ? BN : BN / 2;
+                const int col0 = n * BN + (hv > 0 ? BN / 2 : 0);
 #pragma unroll 1
-                for (int c = 0; c < BN; c += step) {
+                for (int c = 0; c < ncols; c += step) {
                     uint32_t av[32], bv[32];
                     if (!empty) {
                         ptx::tmem_ld32(tb + c, av);
@@ -463,7 +472,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                         for (int i = 0; i < 32; ++i) av[i] = bv[i] = 0u;
                     }
-                    const int col = n * BN + c;
+                    if (EPI == EPI_GATE) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            av[i] = __float_as_uint(f32(av[i]) * gsc);
+                            bv[i] = __float_as_uint(f32(bv[i]) * gsc);
+                        }
+                    }
+                    const int col = col0 + c;
                     if (col >= g.out_cols) continue;
                     uint32_t w[32];   // this thread's 128 output bytes
                     if (f32_out) {
@@ -640,7 +656,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
-        if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr) && lane == 0)
+        if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || (FWD_TMA && g.tma_store != 0)) && lane == 0)
             ptx::bulk_wait_group<0>();   // every output store has completed
     }
 

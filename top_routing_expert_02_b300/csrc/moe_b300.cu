@@ -32,6 +32,7 @@ std::atomic<int> g_forced_bn{0};   // 0: pick the GEMM tile width per call
 std::atomic<int> g_wgrad_order{0};  // weight-gradient tile order: 0 automatic, 1 M-fastest, 2 N-fastest
 std::atomic<int> g_gemm_order{0};   // forward / data-gradient tile order: 0 automatic (M-fastest), 1 M-fastest, 2 N-fastest
 std::atomic<int> g_gemm_tail{1};    // a short last wave of forward tiles runs as half-width units: 1 on, 0 off
+std::atomic<int> g_gemm_tma_store{1};   // down-projection output tiles by TMA stores: 1 on, 0 per-thread stores
 
 // Weight-gradient tile order.  N-fastest (the blocks running together share
 // the A tile and write neighbouring column blocks of the same output rows)
@@ -373,7 +374,13 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
         if (!make_tmap_f32_out(&tc, args.out_f32, (unsigned long long)rows_max, (unsigned long long)args.out_cols))
             return MOE_ERR_CUDA;
     }
-    const int smem = (wg || MODE == tcg::MODE_BMN) ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
+    // the down projection: bf16 [rows_max, out_cols] 32-row x 64-column output blocks by TMA stores
+    constexpr bool fwd_tma = MODE == tcg::MODE_ROWS && EPI == tcg::EPI_GATE;
+    args.tma_store = fwd_tma ? g_gemm_tma_store.load() : 0;
+    if (fwd_tma && args.tma_store &&
+        !make_tmap_bf16_box(&tc, args.out, (unsigned long long)rows_max, (unsigned long long)args.out_cols, 32))
+        return MOE_ERR_CUDA;
+    const int smem = (wg || MODE == tcg::MODE_BMN || fwd_tma) ? SH::WG_SMEM_DYN : SH::SMEM_DYN;
     if (!ensure_dyn_smem((const void*)tcg::grouped_gemm_kernel<EPI, BN, MODE>, smem)) return launch_status();
     const long long max_tiles = wg
                                     ? (long long)args.E * args.m_tiles * args.n_tiles
@@ -1128,6 +1135,13 @@ moe_status moe_set_router_kernel(int kind)
 {
     if (kind < 0 || kind > 2) return MOE_ERR_INVALID_ARG;
     g_router_kind.store(kind);
+    return MOE_OK;
+}
+
+moe_status moe_set_gemm_tma_store(int on)
+{
+    if (on != 0 && on != 1) return MOE_ERR_INVALID_ARG;
+    g_gemm_tma_store.store(on);
     return MOE_OK;
 }
 
