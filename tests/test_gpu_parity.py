@@ -159,9 +159,10 @@ def test_launch_overlap_off_changes_no_bit(name):
 
 @pytest.mark.parametrize("name", ["swiglu_e8", "gelu_e16_hot", "swiglu_e64_zipf", "swiglu_e128_top8", "many_tiles",
                                   "gelu_e8_tail"])
-def test_down_gemm_tma_store_changes_no_bit(name):
-    """The down projection's output blocks written by TMA stores (the default)
-    and by per-thread stores give the same y_perm and y bits, and the oracle's
+def test_forward_gemm_tma_store_changes_no_bit(name):
+    """The forward GEMMs' output blocks written by TMA stores (the default)
+    and by per-thread stores give the same h, y_perm and y bits (SwiGLU and
+    GELU up projections, gate-scaled down projection), and the oracle's
     layer: ragged last M tiles (per-thread rows), several tiles per block,
     and (gelu_e8_tail) half-width last-wave units with a ragged N tile."""
     cfg = C("gelu_e8_tail", 5500, 448, 8, 2, 384, "gelu", 4.0, "bf16") if name == "gelu_e8_tail" else SMALL[name]
@@ -174,6 +175,7 @@ def test_down_gemm_tma_store_changes_no_bit(name):
         moe.set_gemm_tma_store(True)
     moe.check()
     A = int(base.disp.offsets[-1].item())
+    assert torch.equal(plan.h[:A], base.h[:A])
     assert torch.equal(plan.y_perm[:A], base.y_perm[:A])
     assert torch.equal(plan.y, base.y)
     compare_output(base, run_oracle(case), cfg.dtype)

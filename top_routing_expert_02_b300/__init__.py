@@ -218,7 +218,7 @@ def set_router_kernel(kind: int):
 
 
 def set_gemm_tma_store(on: bool):
-    """Down-projection output blocks by TMA stores (default on) or per-thread stores (results unchanged)."""
+    """Forward GEMM output blocks by TMA stores (default on) or per-thread stores (results unchanged)."""
     _ok("moe_set_gemm_tma_store", lib().moe_set_gemm_tma_store(int(bool(on))))
 
 

@@ -197,10 +197,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int BOX_BYTES = BK * 128;   // one 64x64 bf16 box
     // fp32 output tiles of the MN-major identity GEMM go out through the same
     // shared-memory staging and TMA stores as the weight gradients
-    // the down projection (gate epilogue, bf16 rows of y_perm): whole 32-row blocks go out by TMA
+    // the forward projections (bf16 rows of y_perm or h): whole 32-row blocks go out by TMA
     // stores as well -- per-thread stores of 32 different rows per warp instruction measured
-    // 12-14% of the kernel at the many-expert shapes, where each tile has only 24 K blocks
-    constexpr bool FWD_TMA = MODE == MODE_ROWS && EPI == EPI_GATE;
+    // 12-14% of the down GEMM at the many-expert shapes, where each tile has only 24 K blocks.
+    // FWD_TMA: the column-wise epilogues (gate, GELU, identity) through the path below;
+    // FWD_TMA_SW: SwiGLU, whose 64-column output blocks pair 64 gate and 64 up columns
+    constexpr bool FWD_TMA = MODE == MODE_ROWS && (EPI == EPI_GATE || EPI == EPI_GELU || EPI == EPI_IDENT);
+    constexpr bool FWD_TMA_SW = MODE == MODE_ROWS && EPI == EPI_SWIGLU && BN % 128 == 0;
     constexpr bool TMA_OUT_OK = WGRAD || (BMN && EPI == EPI_IDENT) || FWD_TMA;
     constexpr uint32_t IDESC = WGR ? ptx::idesc_bf16_f32(128, BN, true, true)
                                : BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
@@ -478,6 +481,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             av[i] = __float_as_uint(f32(av[i]) * gsc);
                             bv[i] = __float_as_uint(f32(bv[i]) * gsc);
                         }
+                    } else if (EPI == EPI_GELU) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            av[i] = __float_as_uint(gelu_f32(f32(av[i])));
+                            bv[i] = __float_as_uint(gelu_f32(f32(bv[i])));
+                        }
                     }
                     const int col = col0 + c;
                     if (col >= g.out_cols) continue;
@@ -509,6 +518,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     } else if (rv) {
                         uint4* dst = f32_out ? reinterpret_cast<uint4*>(g.out_f32 + (size_t)row * g.out_cols + col)
                                              : reinterpret_cast<uint4*>(g.out + (size_t)row * g.out_cols + col);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                    }
+                }
+            } else if (FWD_TMA_SW && g.tma_store != 0) {
+                // SwiGLU outputs in blocks of 64 columns (gate columns c.., up columns BN/2 + c..),
+                // whole 32-row blocks staged in shared memory and stored by TMA
+                const bool whole = rows_valid >= q * 32 + 32;
+                const uint32_t stg = smem0 + STAGES * STAGE_BYTES + q * SH::WG_STAGE_OUT;
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 64) {
+                    uint32_t w[32];   // this thread's 64 outputs
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t gv[32], uv[32];
+                        ptx::tmem_ld32(tb + c + 32 * h2, gv);
+                        ptx::tmem_ld32(tb + BN / 2 + c + 32 * h2, uv);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[16 * h2 + i] = pack_bf16x2(silu_f32(f32(gv[2 * i])) * f32(uv[2 * i]),
+                                                         silu_f32(f32(gv[2 * i + 1])) * f32(uv[2 * i + 1]));
+                    }
+                    const int col = n * (BN / 2) + c;
+                    if (col >= g.out_cols) continue;
+                    if (whole) {
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();   // the previous block has left smem
+                        __syncwarp();
+                        const uint32_t rb = stg + lane * 128;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            ptx::st_shared_v4(rb + ((v ^ (lane & 7)) << 4), w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                                              w[4 * v + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&tmC, stg, col, row - lane);
+                            ptx::bulk_commit_group();
+                        }
+                    } else if (rv) {
+                        uint4* dst = reinterpret_cast<uint4*>(g.out + (size_t)row * g.out_cols + col);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                     }
@@ -656,7 +706,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aphase ^= 1u;
         }
-        if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || (FWD_TMA && g.tma_store != 0)) && lane == 0)
+        if ((TMA_OUT_OK || FWD_TMA_SW) &&
+            (WGRAD || g.out_f32 != nullptr || ((FWD_TMA || FWD_TMA_SW) && g.tma_store != 0)) && lane == 0)
             ptx::bulk_wait_group<0>();   // every output store has completed
     }
 

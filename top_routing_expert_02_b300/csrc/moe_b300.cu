@@ -374,9 +374,12 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
         if (!make_tmap_f32_out(&tc, args.out_f32, (unsigned long long)rows_max, (unsigned long long)args.out_cols))
             return MOE_ERR_CUDA;
     }
-    // the down projection: bf16 [rows_max, out_cols] 32-row x 64-column output blocks by TMA stores
-    constexpr bool fwd_tma = MODE == tcg::MODE_ROWS && EPI == tcg::EPI_GATE;
-    args.tma_store = fwd_tma ? g_gemm_tma_store.load() : 0;
+    // the forward projections: bf16 [rows_max, out_cols] 32-row x 64-column output blocks by TMA
+    // stores (not while the up projection also keeps the pre-activation z for the backward)
+    constexpr bool fwd_tma = MODE == tcg::MODE_ROWS &&
+                             (EPI == tcg::EPI_GATE || EPI == tcg::EPI_GELU || EPI == tcg::EPI_IDENT ||
+                              (EPI == tcg::EPI_SWIGLU && BN % 128 == 0));
+    args.tma_store = (fwd_tma && args.out_z == nullptr && args.out_f32 == nullptr) ? g_gemm_tma_store.load() : 0;
     if (fwd_tma && args.tma_store &&
         !make_tmap_bf16_box(&tc, args.out, (unsigned long long)rows_max, (unsigned long long)args.out_cols, 32))
         return MOE_ERR_CUDA;
