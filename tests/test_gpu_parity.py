@@ -164,7 +164,10 @@ def test_forward_gemm_tma_store_changes_no_bit(name):
     and by per-thread stores give the same h, y_perm and y bits (SwiGLU and
     GELU up projections, gate-scaled down projection), and the oracle's
     layer: ragged last M tiles (per-thread rows), several tiles per block,
-    and (gelu_e8_tail) half-width last-wave units with a ragged N tile."""
+    and (gelu_e8_tail) half-width last-wave units with a ragged N tile.  The
+    TMA stores apply from 3 row tiles per expert on average (swiglu_e8,
+    many_tiles, gelu_e8_tail); the other cases check that the weight-bound
+    launches keep the per-thread stores."""
     cfg = C("gelu_e8_tail", 5500, 448, 8, 2, 384, "gelu", 4.0, "bf16") if name == "gelu_e8_tail" else SMALL[name]
     case = make_case(cfg)
     base = run_gpu(case)

@@ -260,6 +260,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int full_units = total_tiles - (halves ? tail : 0);
     const int total_units = full_units + (halves ? 2 * tail : 0);
     constexpr uint32_t IDESC_HALF = ptx::idesc_bf16_f32(128, BN / 2);
+    // TMA stores of the forward output only where the GEMM is not bound by streaming its weights:
+    // with fewer than 3 M-tiles per expert on average each weight tile serves at most ~2 row
+    // tiles, the loads keep the TMA unit busy, and the stores measured slower there (e64_zipf up
+    // GEMM 127 -> 148 us); per-thread stores then
+    const bool tma_rows = g.tma_store != 0 && mstart[g.E] >= 3 * g.E;
     const int nk = (g.K + BK - 1) / BK;
     const uint64_t limit = g.wait_limit;
 
@@ -451,7 +456,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || (FWD_TMA && g.tma_store != 0))) {
+            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || (FWD_TMA && tma_rows))) {
                 const bool empty = WGRAD && kstart[e + 1] == kstart[e];
                 const float gsc = gate_pre;   // gate epilogue: the row's gate
                 // this warp's 32 rows all inside the expert's M rows: stage each block of
@@ -522,7 +527,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int v = 0; v < 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                     }
                 }
-            } else if (FWD_TMA_SW && g.tma_store != 0) {
+            } else if (FWD_TMA_SW && tma_rows) {
                 // SwiGLU outputs in blocks of 64 columns (gate columns c.., up columns BN/2 + c..),
                 // whole 32-row blocks staged in shared memory and stored by TMA
                 const bool whole = rows_valid >= q * 32 + 32;
@@ -707,7 +712,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (acc == 0) aphase ^= 1u;
         }
         if ((TMA_OUT_OK || FWD_TMA_SW) &&
-            (WGRAD || g.out_f32 != nullptr || ((FWD_TMA || FWD_TMA_SW) && g.tma_store != 0)) && lane == 0)
+            (WGRAD || g.out_f32 != nullptr || ((FWD_TMA || FWD_TMA_SW) && tma_rows)) && lane == 0)
             ptx::bulk_wait_group<0>();   // every output store has completed
     }
 
