@@ -508,8 +508,9 @@ moe_status moe_set_launch_overlap(int on);
 
 /* Output of the forward expert GEMMs (moe_expert_up, moe_expert_down,
  * moe_expert_ffn; the up projection of moe_expert_up_z keeps per-thread
- * stores): 1 (default) writes each whole block of 32 rows x 64 columns of h
- * or y_perm through shared memory with one TMA store when the launch has at
+ * stores) and of moe_expert_dgrad: 1 (default) writes each whole block of 32
+ * rows x 64 columns of h, y_perm or dx_perm through shared memory with one
+ * TMA store when the launch has at
  * least 3 row tiles of 128 per expert on average (below that the GEMM streams
  * its weights and keeps per-thread stores), 0 always per-thread 16-byte
  * stores.  The results do not depend on it.  Process-wide; for tests and

@@ -322,19 +322,29 @@ def test_kept_pre_activation_equals_recompute(name):
     assert torch.equal(plan.h[:A], h2[:A])
 
 
-def test_expert_dgrad_mn_major_against_torch():
+@pytest.mark.parametrize("kept_list", [[150, 0, 7, 300], [1000, 777, 0, 1300]])
+def test_expert_dgrad_mn_major_against_torch(kept_list):
     """out[r] = a[r] . w[e] with w [E, K, N] read MN-major, against torch fp32
-    per expert: ragged segments, an empty expert, N not a multiple of 256."""
+    per expert: ragged segments, an empty expert, N not a multiple of 256;
+    the second segment list has >= 3 row tiles per expert on average, so its
+    output blocks go by TMA stores, and they match the per-thread stores bit
+    for bit."""
     g = torch.Generator(device="cuda").manual_seed(7)
     E, K, N = 4, 192, 320
-    kept = torch.tensor([150, 0, 7, 300], dtype=torch.int32, device="cuda")
+    kept = torch.tensor(kept_list, dtype=torch.int32, device="cuda")
     offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
     offsets[1:] = torch.cumsum(kept, 0)
     R = int(offsets[-1])
     a = torch.randn(R, K, device="cuda", generator=g).to(torch.bfloat16)
     w = (torch.randn(E, K, N, device="cuda", generator=g) / 8).to(torch.bfloat16)
     out = moe.expert_dgrad(a, offsets, kept, w, R)
+    moe.set_gemm_tma_store(False)
+    try:
+        out2 = moe.expert_dgrad(a, offsets, kept, w, R)
+    finally:
+        moe.set_gemm_tma_store(True)
     moe.check()
+    assert torch.equal(out, out2)
     for e in range(E):
         o, n = int(offsets[e]), int(kept[e])
         ref = a[o:o + n].float() @ w[e].float()

@@ -204,6 +204,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // FWD_TMA_SW: SwiGLU, whose 64-column output blocks pair 64 gate and 64 up columns
     constexpr bool FWD_TMA = MODE == MODE_ROWS && (EPI == EPI_GATE || EPI == EPI_GELU || EPI == EPI_IDENT);
     constexpr bool FWD_TMA_SW = MODE == MODE_ROWS && EPI == EPI_SWIGLU && BN % 128 == 0;
+    // the data-gradient GEMM dx_perm = dz . w1[e] (MN-major weights, bf16 output) likewise
+    constexpr bool BMN_TMA = BMN && EPI == EPI_IDENT;
     constexpr bool TMA_OUT_OK = WGRAD || (BMN && EPI == EPI_IDENT) || FWD_TMA;
     constexpr uint32_t IDESC = WGR ? ptx::idesc_bf16_f32(128, BN, true, true)
                                : BMN ? ptx::idesc_bf16_f32(128, BN, true) : SH::IDESC;
@@ -456,7 +458,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || (FWD_TMA && tma_rows))) {
+            if (TMA_OUT_OK && (WGRAD || g.out_f32 != nullptr || ((FWD_TMA || BMN_TMA) && tma_rows))) {
                 const bool empty = WGRAD && kstart[e + 1] == kstart[e];
                 const float gsc = gate_pre;   // gate epilogue: the row's gate
                 // this warp's 32 rows all inside the expert's M rows: stage each block of
@@ -712,7 +714,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (acc == 0) aphase ^= 1u;
         }
         if ((TMA_OUT_OK || FWD_TMA_SW) &&
-            (WGRAD || g.out_f32 != nullptr || ((FWD_TMA || FWD_TMA_SW) && tma_rows)) && lane == 0)
+            (WGRAD || g.out_f32 != nullptr || ((FWD_TMA || FWD_TMA_SW || BMN_TMA) && tma_rows)) && lane == 0)
             ptx::bulk_wait_group<0>();   // every output store has completed
     }
 

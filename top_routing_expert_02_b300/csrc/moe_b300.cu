@@ -376,9 +376,10 @@ moe_status launch_tc_bn(const void* A, long long rows_max, int K, const void* W,
     }
     // the forward projections: bf16 [rows_max, out_cols] 32-row x 64-column output blocks by TMA
     // stores (not while the up projection also keeps the pre-activation z for the backward)
-    constexpr bool fwd_tma = MODE == tcg::MODE_ROWS &&
-                             (EPI == tcg::EPI_GATE || EPI == tcg::EPI_GELU || EPI == tcg::EPI_IDENT ||
-                              (EPI == tcg::EPI_SWIGLU && BN % 128 == 0));
+    constexpr bool fwd_tma = (MODE == tcg::MODE_ROWS &&
+                              (EPI == tcg::EPI_GATE || EPI == tcg::EPI_GELU || EPI == tcg::EPI_IDENT ||
+                               (EPI == tcg::EPI_SWIGLU && BN % 128 == 0))) ||
+                             (MODE == tcg::MODE_BMN && EPI == tcg::EPI_IDENT);   // + dx_perm (bf16 out)
     args.tma_store = (fwd_tma && args.out_z == nullptr && args.out_f32 == nullptr) ? g_gemm_tma_store.load() : 0;
     if (fwd_tma && args.tma_store &&
         !make_tmap_bf16_box(&tc, args.out, (unsigned long long)rows_max, (unsigned long long)args.out_cols, 32))
